@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark of the double-double GEMM on GB300: dd-GFLOP/s (2MNK/s) at 4096^3.
+
+One step = one whole product C = A*B (split into 13-bit parts, slice-pair
+GEMM on the FP64 tensor pipe, recombination) over the seeded synthetic
+4096x4096x4096 wide-range workload (hi = U[-1,1] * 2^e, e ~ U{-20..20}).
+Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timed regions (CUDA events on the launching stream, synchronised on both
+sides, max over ranks):
+  * value:  K calls of dd_gemm_ws with inputs resident in HBM;
+  * per-kernel durations (roofline): K more passes through the step entry
+    points (split rows/cols, slice GEMM, recombine) with events between them;
+  * e2e:    K calls of dd_gemm_host (host buffers, copies inside the region).
+Inputs (512 MB) and the part planes (2 GB) are larger than the 126 MB L2, so
+no flush is needed between steps.
+
+--impl reference times the oracle (exact superaccumulator, all host cores) on
+a bounded sample of the same workload per step.
+N > 1 (torchrun): every rank multiplies its own copy of the workload (weak
+scaling, no collective on the data path); value = all ranks' work / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import workloads  # noqa: E402
+
+METRIC = "double-double GEMM dd-GFLOPS (2MNK/s) at 4096^3; % of FP64 tensor-pipe roof"
+UNIT = "dd-GFLOP/s"
+DEFAULT_WORKLOAD = 2
+PAIRS = 36          # slice pairs with index sum <= 7 (8 parts per double double)
+SPLIT_BYTES = 80    # per input element: 16 B read (hi, lo) + 8 parts * 8 B written
+RECOMB_BYTES = 80   # per output element: 8 part sums * 8 B read + 16 B written
+FP64_NOMINAL_TF = 1.25
+BF16_NOMINAL_TF = 2250.0
+FALLBACK_BF16_TF = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = ROOT / "profiles" / "slice_gemm_kernel_dram_traffic.txt"
+KERNEL_SOURCES = ["extended_precision_gemm_gb300/csrc/slice_gemm.cu",
+                  "extended_precision_gemm_gb300/csrc/common.cuh", "include/ddgemm.h"]
+
+
+# ----------------------------------------------------------------------------
+# multi-process plumbing (torchrun); single process when WORLD_SIZE is unset
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def allreduce_max(dist, x: float, device=None) -> float:
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def allreduce_sum(dist, x: float, device=None) -> float:
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(dist, elapsed_s: float, units: float, device=None):
+    """Whole-job (total units, slowest rank's time) for weak scaling."""
+    return allreduce_sum(dist, units, device), allreduce_max(dist, elapsed_s, device)
+
+
+# ----------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ----------------------------------------------------------------------------
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TF, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per slice-GEMM launch from a committed ncu summary, or None
+    when the kernel's sources changed since the capture."""
+    if not TRAFFIC_FILE.exists():
+        return None
+    fields = {}
+    for line in TRAFFIC_FILE.read_text().splitlines():
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    if fields.get("workload") != workload_name:
+        return None
+    try:
+        return float(fields["bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in pathlib.Path(self.path).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample (rows of C)
+# ----------------------------------------------------------------------------
+
+def oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, rows):
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    C_hi, C_lo = oracle.exact_dd_gemm(A_hi, A_lo, B_hi, B_lo, rows=np.asarray(rows))
+    return time.perf_counter() - t0, C_hi, C_lo
+
+
+def cpu_baseline(w, A_hi, A_lo, B_hi, B_lo, target_s: float = 12.0):
+    import oracle
+    t1, _, _ = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, [0])
+    nrows = max(1, min(w.M, int(target_s / max(t1, 1e-3))))
+    rows = list(range(nrows))
+    t, C_hi, C_lo = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, rows)
+    value = 2.0 * nrows * w.N * w.K / t / 1e9
+    return {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"rows 0..{nrows - 1} of C ({nrows} x {w.N} outputs, K = {w.K}), exact "
+                      f"superaccumulator, {t:.1f} s"}, rows, C_hi, C_lo
+
+
+# ----------------------------------------------------------------------------
+# the two arms
+# ----------------------------------------------------------------------------
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    A_hi, A_lo, B_hi, B_lo = workloads.make_workload(args.workload)
+    t1, _, _ = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, [0])
+    rows_per_step = max(1, int(2.0 / max(t1, 1e-3)))
+    rows = list(range(rows_per_step))
+    for _ in range(args.warmup):
+        oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, rows)
+    total = 0.0
+    for _ in range(args.steps):
+        t, _, _ = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, rows)
+        total += t
+    value = args.steps * 2.0 * rows_per_step * w.N * w.K / total / 1e9
+    sample = (f"per step rows 0..{rows_per_step - 1} of C ({rows_per_step} x {w.N} outputs, "
+              f"K = {w.K}) of {w.name}")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, world, None),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_of(w, world, splits):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dist": w.dist, "seed": w.seed,
+            "slices": 8, "pairs": PAIRS, "k_splits": splits,
+            "parallelism": f"independent problem per GPU x{world}",
+            "l2": "no flush: inputs 512 MB and part planes 2 GB exceed the 126 MB L2"}
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    import extended_precision_gemm_gb300 as ddg
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dist = dist_init("nccl")
+    dev = torch.device("cuda", local)
+    M, N, K = w.M, w.N, w.K
+
+    A_hi, A_lo, B_hi, B_lo = workloads.make_workload(args.workload)
+    pinned = [torch.from_numpy(x).pin_memory() for x in (A_hi, A_lo, B_hi, B_lo)]
+    dA_hi, dA_lo, dB_hi, dB_lo = (t.to(dev, non_blocking=True) for t in pinned)
+    C_hi = torch.empty((M, N), dtype=torch.float64, device=dev)
+    C_lo = torch.empty((M, N), dtype=torch.float64, device=dev)
+    Mp, Np, Kp, splits = ddg.layout(M, N, K)
+    ws = torch.empty(ddg.workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    dmma_tf = ddg.fp64_tensor_roof()
+
+    def step():
+        ddg.dd_gemm_ws(dA_hi, dA_lo, dB_hi, dB_lo, ws, C_hi, C_lo, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: the whole product, inputs resident in HBM ----
+    clocks = ClockSampler(local)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    clock_info = clocks.stop()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    units, t_max = aggregate(dist, elapsed, args.steps * w.dd_flops, dev)
+    assert ddg.wait_timeouts() == 0
+
+    # ---- per-kernel durations through the step entry points ----
+    e_buf = torch.empty(M, dtype=torch.int32, device=dev)
+    f_buf = torch.empty(N, dtype=torch.int32, device=dev)
+    pA = torch.empty(8 * Mp * Kp, dtype=torch.float64, device=dev)
+    pB = torch.empty(8 * Np * Kp, dtype=torch.float64, device=dev)
+    P = torch.empty((splits, 8, Mp, Np), dtype=torch.float64, device=dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        ddg.split_rows(dA_hi, dA_lo, pA, e_buf, stream=stream)
+        ddg.split_cols(dB_hi, dB_lo, pB, f_buf, stream=stream)
+        evs[i][1].record(stream)
+        ddg.slice_gemm(M, N, K, pA, pB, splits, P, stream=stream)
+        evs[i][2].record(stream)
+        ddg.recombine(M, N, P, e_buf, f_buf, splits, C_hi, C_lo, stream=stream)
+        evs[i][3].record(stream)
+    torch.cuda.synchronize(dev)
+    t_split = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1e3
+    t_gemm = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1e3
+    t_recomb = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1e3
+    t_gemm = allreduce_max(dist, t_gemm, dev)
+    t_split = allreduce_max(dist, t_split, dev)
+    t_recomb = allreduce_max(dist, t_recomb, dev)
+
+    # ---- end to end through the C ABI with host buffers ----
+    h_C_hi = torch.empty((M, N), dtype=torch.float64).pin_memory()
+    h_C_lo = torch.empty((M, N), dtype=torch.float64).pin_memory()
+    ddg.dd_gemm_host(*pinned, h_C_hi, h_C_lo, stream=stream)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ddg.dd_gemm_host(*pinned, h_C_hi, h_C_lo, stream=stream)
+    t_e2e = time.perf_counter() - t0
+    e2e_units, t_e2e = aggregate(dist, t_e2e, args.steps * w.dd_flops, dev)
+    same = bool(torch.equal(h_C_hi, C_hi.cpu()) and torch.equal(h_C_lo, C_lo.cpu()))
+
+    if rank != 0:
+        return None
+
+    hbm_gbs, bf16_tf, peak_src = load_peaks()
+    fp64_peak = bf16_tf * FP64_NOMINAL_TF / BF16_NOMINAL_TF
+    gemm_flops = PAIRS * 2.0 * M * N * K
+    achieved_tf = gemm_flops / t_gemm / 1e12
+    traffic = recorded_traffic(w.name)
+    split_gbs = SPLIT_BYTES * (M * K + K * N) / t_split / 1e9
+    recomb_gbs = RECOMB_BYTES * M * N / t_recomb / 1e9
+
+    cpu, rows, R_hi, R_lo = cpu_baseline(w, A_hi, A_lo, B_hi, B_lo)
+    G_hi = C_hi[rows].cpu().numpy()
+    G_lo = C_lo[rows].cpu().numpy()
+    d = (G_hi - R_hi) + (G_lo - R_lo)
+    normwise = float(np.linalg.norm(d) / (np.linalg.norm(A_hi[rows] + A_lo[rows])
+                                          * np.linalg.norm(B_hi + B_lo)))
+
+    value = units / t_max / 1e9
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, world, splits),
+        "roofline": {"bound": "tensor", "kernel": "slice_gemm_kernel (FP64 mma.sync m8n8k4)",
+                     "achieved": achieved_tf, "peak": fp64_peak, "unit": "TFLOP/s",
+                     "frac": achieved_tf / fp64_peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 burst {bf16_tf} TF/s x nominal FP64/bf16 "
+                                    f"{FP64_NOMINAL_TF}/{BF16_NOMINAL_TF}",
+                     "flops_per_launch": gemm_flops, "ms_per_launch": 1e3 * t_gemm,
+                     "fp64_tensor_loop_measured_tflops": dmma_tf,
+                     "frac_of_measured_loop": achieved_tf / dmma_tf},
+        "roofline_split": {"bound": "hbm", "achieved": split_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                           "frac": split_gbs / hbm_gbs, "bytes_per_step": SPLIT_BYTES * (M * K + K * N),
+                           "ms": 1e3 * t_split, "kernels": "exponents + split_rows + split_cols"},
+        "roofline_recombine": {"bound": "hbm", "achieved": recomb_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                               "frac": recomb_gbs / hbm_gbs, "ms": 1e3 * t_recomb},
+        "frac_of_fp64_tensor_roof_end_to_end": (units / t_max * PAIRS) / (fp64_peak * 1e12),
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_units / t_e2e / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": 16 * (M * K + K * N), "d2h_bytes_per_step": 16 * M * N,
+                "matches_device_result": same},
+        "accuracy": {"normwise_vs_exact_oracle": normwise, "rows_checked": len(rows), "bound": 1e-26},
+        "gpu_launches": 7 * args.steps,
+        "clocks": clock_info,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    args = ap.parse_args(argv)
+    w = workloads.WORKLOADS[args.workload]
+    out = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,275 @@
+"""Double-double GEMM on the GB300 FP64 tensor pipe: Python binding.
+
+A thin ctypes layer over ``libddgemm.so`` (declared in ``include/ddgemm.h``):
+argument marshalling only.  Every step of the product runs in the library's
+CUDA kernels; there is no CPU path.  PyTorch supplies device memory and the
+current CUDA stream.  Importing works without a GPU (the library loads without
+touching the device); calling a compute function without the built library or
+without a GPU raises.
+
+Method ("Multiple Double Arithmetic on NVIDIA Tensor Cores", Section 2): each
+double double is cut into 8 parts of 13 bits on a grid shared by its row of A
+or column of B, the 36 part-pair products with index sum <= 7 run as exact
+FP64 matrix products (mma.sync m8n8k4 f64), and the parts of the product are
+added back into a double double.
+"""
+from __future__ import annotations
+
+import ctypes
+import pathlib
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "DDGemmError", "SLICES", "MAX_K", "TILE_M", "TILE_N", "CHUNK_K", "STATUS",
+    "load", "library_path", "exported_symbols",
+    "dd_gemm", "dd_gemm_ws", "dd_gemm_host", "layout", "workspace_size",
+    "split_rows", "split_cols", "slice_gemm", "recombine", "wait_timeouts", "fp64_tensor_roof",
+]
+
+SLICES = 8
+MAX_K = 1 << 24
+TILE_M = 32
+TILE_N = 32
+CHUNK_K = 8
+STATUS = {0: "DDGEMM_OK", 1: "DDGEMM_ERR_INVALID_ARG", 2: "DDGEMM_ERR_UNSUPPORTED",
+          3: "DDGEMM_ERR_ALLOC", 4: "DDGEMM_ERR_CUDA"}
+
+
+class DDGemmError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+_i64, _ptr, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+_SIGNATURES = {
+    "dd_status_string": ([_int], ctypes.c_char_p),
+    "dd_gemm_layout": ([_i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr], _int),
+    "dd_gemm_workspace_size": ([_i64, _i64, _i64, _ptr], _int),
+    "dd_gemm_ws": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64,
+                    _ptr, ctypes.c_size_t, _ptr], _int),
+    "dd_gemm": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
+    "dd_gemm_host": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
+    "dd_split_rows": ([_i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr], _int),
+    "dd_split_cols": ([_i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr], _int),
+    "dd_slice_gemm": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
+    "dd_recombine": ([_i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _ptr, _i64, _ptr], _int),
+    "dd_wait_timeouts": ([_ptr], _int),
+    "dd_fp64_tensor_roof": ([_ptr, _ptr], _int),
+}
+
+
+def library_path() -> pathlib.Path:
+    return _build.LIB
+
+
+def exported_symbols():
+    """Names of the C-ABI entry points this binding expects."""
+    return sorted(_SIGNATURES)
+
+
+def load(build_if_missing: bool = True):
+    """Load libddgemm.so (building it with nvcc first if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not _build.up_to_date():
+                if not build_if_missing and not path.exists():
+                    raise RuntimeError(f"{path} is not built")
+                _build.build()
+            lib = ctypes.CDLL(str(path))
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise DDGemmError(fn, status)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _mat(t, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float64 or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D float64 torch tensor")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be on a CUDA device")
+    if t.stride(1) != 1 and t.numel() > 0:
+        raise ValueError(f"{name} must be row-major with unit column stride")
+    return t
+
+
+def _ld(t):
+    return max(t.stride(0), t.shape[1], 1) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def layout(M: int, N: int, K: int):
+    """(Mp, Np, Kp, splits) chosen for this shape on the current device."""
+    lib = load()
+    Mp, Np, Kp, sp = _i64(), _i64(), _i64(), _int()
+    _check("dd_gemm_layout", lib.dd_gemm_layout(M, N, K, ctypes.byref(Mp), ctypes.byref(Np),
+                                                ctypes.byref(Kp), ctypes.byref(sp)))
+    return Mp.value, Np.value, Kp.value, sp.value
+
+
+def workspace_size(M: int, N: int, K: int) -> int:
+    lib = load()
+    n = ctypes.c_size_t()
+    _check("dd_gemm_workspace_size", lib.dd_gemm_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo):
+    torch = _torch()
+    for t, n in ((A_hi, "A_hi"), (A_lo, "A_lo"), (B_hi, "B_hi"), (B_lo, "B_lo")):
+        _mat(t, n)
+    M, K = A_hi.shape
+    K2, N = B_hi.shape
+    if A_lo.shape != (M, K) or B_lo.shape != (K2, N) or K2 != K:
+        raise ValueError("shape mismatch")
+    if C_hi is None:
+        C_hi = torch.empty((M, N), dtype=torch.float64, device=A_hi.device)
+    if C_lo is None:
+        C_lo = torch.empty((M, N), dtype=torch.float64, device=A_hi.device)
+    _mat(C_hi, "C_hi"), _mat(C_lo, "C_lo")
+    if A_hi.stride() != A_lo.stride() or B_hi.stride() != B_lo.stride() or C_hi.stride() != C_lo.stride():
+        raise ValueError("hi and lo planes must share strides")
+    return M, N, K, C_hi, C_lo
+
+
+def dd_gemm(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, stream=None):
+    """(C_hi, C_lo) = (A_hi + A_lo) @ (B_hi + B_lo) on the GPU (workspace from the
+    stream-ordered allocator)."""
+    M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
+    _check("dd_gemm", load().dd_gemm(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                     B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                     C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi), _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def dd_gemm_ws(A_hi, A_lo, B_hi, B_lo, workspace, C_hi=None, C_lo=None, stream=None):
+    """dd_gemm with a caller-provided device workspace (a uint8 tensor of at
+    least workspace_size(M, N, K) bytes)."""
+    M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
+    _check("dd_gemm_ws", load().dd_gemm_ws(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                           B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                           C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi),
+                                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                           _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def dd_gemm_host(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, stream=None):
+    """The product with HOST operands and result (C-contiguous float64 numpy
+    arrays or CPU torch tensors, ideally pinned); returns when C is written."""
+    def ptr(x):
+        return x.data_ptr() if hasattr(x, "data_ptr") else x.ctypes.data
+    M, K = A_hi.shape
+    K2, N = B_hi.shape
+    if K2 != K or tuple(C_hi.shape) != (M, N) or tuple(C_lo.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _check("dd_gemm_host", load().dd_gemm_host(M, N, K, ptr(A_hi), ptr(A_lo), max(K, 1),
+                                               ptr(B_hi), ptr(B_lo), max(N, 1),
+                                               ptr(C_hi), ptr(C_lo), max(N, 1), _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def split_rows(A_hi, A_lo, planes=None, e=None, stream=None):
+    """Step 1a: (planes, e) for the rows of A; planes in the tiled layout of
+    dd_split_rows (8 * Mp * Kp doubles), e int32 of length M."""
+    torch = _torch()
+    _mat(A_hi, "A_hi"), _mat(A_lo, "A_lo")
+    M, K = A_hi.shape
+    Mp, Kp = -(-M // TILE_M) * TILE_M, -(-K // CHUNK_K) * CHUNK_K
+    if planes is None:
+        planes = torch.empty(SLICES * Mp * Kp, dtype=torch.float64, device=A_hi.device)
+    if e is None:
+        e = torch.empty(M, dtype=torch.int32, device=A_hi.device)
+    if planes.numel() < SLICES * Mp * Kp or e.numel() < M:
+        raise ValueError("output buffers too small")
+    _check("dd_split_rows", load().dd_split_rows(M, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                                 planes.data_ptr(), e.data_ptr(), _stream_handle(stream)))
+    return planes, e
+
+
+def split_cols(B_hi, B_lo, planes=None, f=None, stream=None):
+    """Step 1b: (planes, f) for the columns of B (8 * Np * Kp doubles, f int32 N)."""
+    torch = _torch()
+    _mat(B_hi, "B_hi"), _mat(B_lo, "B_lo")
+    K, N = B_hi.shape
+    Np, Kp = -(-N // TILE_N) * TILE_N, -(-K // CHUNK_K) * CHUNK_K
+    if planes is None:
+        planes = torch.empty(SLICES * Np * Kp, dtype=torch.float64, device=B_hi.device)
+    if f is None:
+        f = torch.empty(N, dtype=torch.int32, device=B_hi.device)
+    if planes.numel() < SLICES * Np * Kp or f.numel() < N:
+        raise ValueError("output buffers too small")
+    _check("dd_split_cols", load().dd_split_cols(K, N, B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                                 planes.data_ptr(), f.data_ptr(), _stream_handle(stream)))
+    return planes, f
+
+
+def slice_gemm(M: int, N: int, K: int, planesA, planesB, splits: int, P=None, stream=None):
+    """Step 2: P (splits x 8 x Mp x Np) from the part planes of A and B."""
+    torch = _torch()
+    Mp, Np = -(-M // TILE_M) * TILE_M, -(-N // TILE_N) * TILE_N
+    if P is None:
+        P = torch.empty((splits, SLICES, Mp, Np), dtype=torch.float64, device=planesA.device)
+    if P.numel() < splits * SLICES * Mp * Np:
+        raise ValueError("output buffer too small")
+    _check("dd_slice_gemm", load().dd_slice_gemm(M, N, K, planesA.data_ptr(), planesB.data_ptr(), splits,
+                                                 P.data_ptr(), _stream_handle(stream)))
+    return P
+
+
+def recombine(M: int, N: int, P, e, f, splits=None, C_hi=None, C_lo=None, stream=None):
+    """Step 3: (C_hi, C_lo) from the split planes P and the exponents e, f."""
+    torch = _torch()
+    splits = P.shape[0] if splits is None else splits
+    if C_hi is None:
+        C_hi = torch.empty((M, N), dtype=torch.float64, device=P.device)
+    if C_lo is None:
+        C_lo = torch.empty((M, N), dtype=torch.float64, device=P.device)
+    _mat(C_hi, "C_hi"), _mat(C_lo, "C_lo")
+    if C_hi.stride() != C_lo.stride():
+        raise ValueError("hi and lo planes must share strides")
+    _check("dd_recombine", load().dd_recombine(M, N, P.data_ptr(), splits, e.data_ptr(), f.data_ptr(),
+                                               C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi),
+                                               _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def wait_timeouts() -> int:
+    """Slice-GEMM blocks that gave up on a bounded wait since the last call
+    (synchronises the device; 0 in normal operation)."""
+    n = ctypes.c_uint()
+    _check("dd_wait_timeouts", load().dd_wait_timeouts(ctypes.byref(n)))
+    return n.value
+
+
+def fp64_tensor_roof(stream=None) -> float:
+    """Measured FP64 tensor-pipe rate of the current device (TFLOP/s)."""
+    t = ctypes.c_double()
+    _check("dd_fp64_tensor_roof", load().dd_fp64_tensor_roof(ctypes.byref(t), _stream_handle(stream)))
+    return t.value

@@ -1,0 +1,339 @@
+// api.cu -- the C ABI of the dd GEMM library (declarations in ddgemm.h).
+//
+// Argument checking, the workspace layout, and the launch sequence of the
+// three steps: split (exponents + part planes), slice-pair GEMM, recombine.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.cuh"
+
+using namespace ddg;
+
+namespace {
+
+constexpr int64_t kAlign = 256;
+constexpr int kMaxSplits = 64;
+constexpr int64_t kMaxRowTiles = 65535;  // grid.y of the slice GEMM
+
+struct Layout {
+    int64_t Mp, Np, Kp, KC;
+    int splits;
+    // byte offsets inside the workspace
+    int64_t off_e, off_f, off_A, off_B, off_P, total;
+};
+
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return 152;
+    return sms;
+}
+
+// k-split of the slice GEMM: the smallest split count whose waves of blocks
+// fill the GPU best (tiles * splits over whole waves of resident blocks),
+// keeping at least 4 k-chunks per split.
+int choose_splits(int64_t Mp, int64_t Np, int64_t KC) {
+    const int64_t tiles = (Mp / TM) * (Np / TN);
+    if (tiles == 0 || KC <= 1) return 1;
+    const int64_t slots = (int64_t)device_sms() * slice_gemm_ctas_per_sm();
+    int best = 1;
+    double best_score = -1.0;
+    const int64_t max_s = std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, KC / 4));
+    for (int64_t s = 1; s <= max_s; ++s) {
+        const int64_t blocks = tiles * s;
+        const int64_t waves = (blocks + slots - 1) / slots;
+        const double eff = (double)blocks / (double)(waves * slots);
+        const double score = eff - 0.002 * (double)s;
+        if (score > best_score + 1e-12) { best_score = score; best = (int)s; }
+    }
+    return best;
+}
+
+Layout make_layout(int64_t M, int64_t N, int64_t K) {
+    Layout L;
+    L.Mp = round_up(M, TM);
+    L.Np = round_up(N, TN);
+    L.Kp = round_up(K, BK);
+    L.KC = L.Kp / BK;
+    L.splits = choose_splits(L.Mp, L.Np, L.KC);
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) { int64_t o = off; off = round_up(off + bytes, kAlign); return o; };
+    L.off_e = take(L.Mp * 4);
+    L.off_f = take(L.Np * 4);
+    L.off_A = take(S * L.Mp * L.Kp * 8);
+    L.off_B = take(S * L.Np * L.Kp * 8);
+    L.off_P = take((int64_t)L.splits * S * L.Mp * L.Np * 8);
+    L.total = off;
+    return L;
+}
+
+bool ranges_overlap(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+    if (a == nullptr || b == nullptr || abytes <= 0 || bbytes <= 0) return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+// Bytes spanned by a rows x cols row-major matrix with leading dimension ld.
+int64_t span_bytes(int64_t rows, int64_t cols, int64_t ld) {
+    if (rows == 0 || cols == 0) return 0;
+    return ((rows - 1) * ld + cols) * 8;
+}
+
+ddgemm_status check_shapes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc) {
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) || ldc < std::max<int64_t>(1, N))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (round_up(M, TM) / TM > kMaxRowTiles) return DDGEMM_ERR_UNSUPPORTED;
+    return DDGEMM_OK;
+}
+
+ddgemm_status check_gemm_args(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                              int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb,
+                              const double* C_hi, const double* C_lo, int64_t ldc) {
+    ddgemm_status s = check_shapes(M, N, K, lda, ldb, ldc);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;  // empty product: no pointer is read
+    if (C_hi == nullptr || C_lo == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    if (M > 0 && K > 0 && (A_hi == nullptr || A_lo == nullptr)) return DDGEMM_ERR_INVALID_ARG;
+    if (N > 0 && K > 0 && (B_hi == nullptr || B_lo == nullptr)) return DDGEMM_ERR_INVALID_ARG;
+    const int64_t a = span_bytes(M, K, lda), b = span_bytes(K, N, ldb), c = span_bytes(M, N, ldc);
+    const void* ins[4] = {A_hi, A_lo, B_hi, B_lo};
+    const int64_t insz[4] = {a, a, b, b};
+    const void* outs[2] = {C_hi, C_lo};
+    for (int o = 0; o < 2; ++o) {
+        for (int i = 0; i < 4; ++i)
+            if (ranges_overlap(outs[o], c, ins[i], insz[i])) return DDGEMM_ERR_INVALID_ARG;
+    }
+    if (ranges_overlap(C_hi, c, C_lo, c)) return DDGEMM_ERR_INVALID_ARG;
+    return DDGEMM_OK;
+}
+
+ddgemm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DDGEMM_OK : DDGEMM_ERR_CUDA; }
+
+#define DDG_TRY(call)                                   \
+    do {                                                \
+        cudaError_t err_ = (call);                      \
+        if (err_ != cudaSuccess) return DDGEMM_ERR_CUDA; \
+    } while (0)
+
+// The launch sequence on a workspace laid out by make_layout.
+ddgemm_status run_gemm(const Layout& L, int64_t M, int64_t N, int64_t K, const double* A_hi,
+                       const double* A_lo, int64_t lda, const double* B_hi, const double* B_lo,
+                       int64_t ldb, double* C_hi, double* C_lo, int64_t ldc, char* ws,
+                       cudaStream_t st) {
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    int32_t* e = reinterpret_cast<int32_t*>(ws + L.off_e);
+    int32_t* f = reinterpret_cast<int32_t*>(ws + L.off_f);
+    double* pA = reinterpret_cast<double*>(ws + L.off_A);
+    double* pB = reinterpret_cast<double*>(ws + L.off_B);
+    double* P = reinterpret_cast<double*>(ws + L.off_P);
+    DDG_TRY(launch_init_exponents(e, M, f, N, K, st));
+    DDG_TRY(launch_row_exponents(A_hi, lda, M, K, e, st));
+    DDG_TRY(launch_col_exponents(B_hi, ldb, K, N, f, st));
+    DDG_TRY(launch_split_rows(A_hi, A_lo, lda, M, K, L.Kp, e, pA, st));
+    DDG_TRY(launch_split_cols(B_hi, B_lo, ldb, K, N, L.Kp, f, pB, st));
+    DDG_TRY(launch_slice_gemm(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_TRY(launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
+    return DDGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dd_status_string(int status) {
+    switch (status) {
+        case DDGEMM_OK: return "DDGEMM_OK";
+        case DDGEMM_ERR_INVALID_ARG: return "DDGEMM_ERR_INVALID_ARG";
+        case DDGEMM_ERR_UNSUPPORTED: return "DDGEMM_ERR_UNSUPPORTED";
+        case DDGEMM_ERR_ALLOC: return "DDGEMM_ERR_ALLOC";
+        case DDGEMM_ERR_CUDA: return "DDGEMM_ERR_CUDA";
+        default: return "DDGEMM_UNKNOWN_STATUS";
+    }
+}
+
+ddgemm_status dd_gemm_layout(int64_t M, int64_t N, int64_t K, int64_t* Mp, int64_t* Np, int64_t* Kp,
+                             int* splits) {
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    Layout L = make_layout(M, N, K);
+    if (Mp) *Mp = L.Mp;
+    if (Np) *Np = L.Np;
+    if (Kp) *Kp = L.Kp;
+    if (splits) *splits = L.splits;
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    if (bytes == nullptr || M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    *bytes = (size_t)make_layout(M, N, K).total;
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_gemm_ws(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                         int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb,
+                         double* C_hi, double* C_lo, int64_t ldc, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    Layout L = make_layout(M, N, K);
+    if (workspace == nullptr || (uintptr_t)workspace % kAlign != 0 || workspace_bytes < (size_t)L.total)
+        return DDGEMM_ERR_INVALID_ARG;
+    const int64_t c = span_bytes(M, N, ldc);
+    if (ranges_overlap(workspace, L.total, C_hi, c) || ranges_overlap(workspace, L.total, C_lo, c))
+        return DDGEMM_ERR_INVALID_ARG;
+    return run_gemm(L, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc,
+                    static_cast<char*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+ddgemm_status dd_gemm(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                      int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb, double* C_hi,
+                      double* C_lo, int64_t ldc, void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Layout L = make_layout(M, N, K);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    s = run_gemm(L, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc, static_cast<char*>(ws), st);
+    cudaError_t fe = cudaFreeAsync(ws, st);
+    if (s == DDGEMM_OK && fe != cudaSuccess) s = DDGEMM_ERR_CUDA;
+    return s;
+}
+
+ddgemm_status dd_gemm_host(int64_t M, int64_t N, int64_t K, const double* h_A_hi,
+                           const double* h_A_lo, int64_t lda, const double* h_B_hi,
+                           const double* h_B_lo, int64_t ldb, double* h_C_hi, double* h_C_lo,
+                           int64_t ldc, void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, h_A_hi, h_A_lo, lda, h_B_hi, h_B_lo, ldb, h_C_hi,
+                                      h_C_lo, ldc);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Layout L = make_layout(M, N, K);
+    // One device block: A_hi, A_lo (M x K dense), B_hi, B_lo (K x N), C_hi,
+    // C_lo (M x N), then the workspace.
+    const int64_t a = round_up(M * K * 8, kAlign), b = round_up(K * N * 8, kAlign),
+                  c = round_up(M * N * 8, kAlign);
+    const int64_t total = 2 * a + 2 * b + 2 * c + L.total;
+    char* dev = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&dev), (size_t)total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    double* dA_hi = reinterpret_cast<double*>(dev);
+    double* dA_lo = reinterpret_cast<double*>(dev + a);
+    double* dB_hi = reinterpret_cast<double*>(dev + 2 * a);
+    double* dB_lo = reinterpret_cast<double*>(dev + 2 * a + b);
+    double* dC_hi = reinterpret_cast<double*>(dev + 2 * a + 2 * b);
+    double* dC_lo = reinterpret_cast<double*>(dev + 2 * a + 2 * b + c);
+    char* ws = dev + 2 * a + 2 * b + 2 * c;
+    cudaError_t err = cudaSuccess;
+    auto copy_in = [&](double* dst, const double* src, int64_t rows, int64_t cols, int64_t ld) {
+        if (err != cudaSuccess || rows == 0 || cols == 0) return;
+        err = cudaMemcpy2DAsync(dst, (size_t)cols * 8, src, (size_t)ld * 8, (size_t)cols * 8, (size_t)rows,
+                                cudaMemcpyHostToDevice, st);
+    };
+    copy_in(dA_hi, h_A_hi, M, K, lda);
+    copy_in(dA_lo, h_A_lo, M, K, lda);
+    copy_in(dB_hi, h_B_hi, K, N, ldb);
+    copy_in(dB_lo, h_B_lo, K, N, ldb);
+    if (err == cudaSuccess)
+        s = run_gemm(L, M, N, K, dA_hi, dA_lo, std::max<int64_t>(K, 1), dB_hi, dB_lo, N, dC_hi, dC_lo, N, ws, st);
+    else
+        s = DDGEMM_ERR_CUDA;
+    if (s == DDGEMM_OK) {
+        err = cudaMemcpy2DAsync(h_C_hi, (size_t)ldc * 8, dC_hi, (size_t)N * 8, (size_t)N * 8, (size_t)M,
+                                cudaMemcpyDeviceToHost, st);
+        if (err == cudaSuccess)
+            err = cudaMemcpy2DAsync(h_C_lo, (size_t)ldc * 8, dC_lo, (size_t)N * 8, (size_t)N * 8, (size_t)M,
+                                    cudaMemcpyDeviceToHost, st);
+        if (err != cudaSuccess) s = DDGEMM_ERR_CUDA;
+    }
+    cudaError_t fe = cudaFreeAsync(dev, st);
+    cudaError_t se = cudaStreamSynchronize(st);
+    if (s == DDGEMM_OK && (fe != cudaSuccess || se != cudaSuccess)) s = DDGEMM_ERR_CUDA;
+    return s;
+}
+
+ddgemm_status dd_split_rows(int64_t M, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
+                            double* planes, int32_t* e, void* stream) {
+    if (M < 0 || K < 0 || lda < std::max<int64_t>(1, K)) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (M == 0) return DDGEMM_OK;
+    if (e == nullptr || (K > 0 && (A_hi == nullptr || A_lo == nullptr || planes == nullptr)))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planes % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t Kp = round_up(K, BK);
+    DDG_TRY(launch_init_exponents(e, M, nullptr, 0, K, st));
+    DDG_TRY(launch_row_exponents(A_hi, lda, M, K, e, st));
+    DDG_TRY(launch_split_rows(A_hi, A_lo, lda, M, K, Kp, e, planes, st));
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_split_cols(int64_t K, int64_t N, const double* B_hi, const double* B_lo, int64_t ldb,
+                            double* planes, int32_t* f, void* stream) {
+    if (N < 0 || K < 0 || ldb < std::max<int64_t>(1, N)) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (N == 0) return DDGEMM_OK;
+    if (f == nullptr || (K > 0 && (B_hi == nullptr || B_lo == nullptr || planes == nullptr)))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planes % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t Kp = round_up(K, BK);
+    DDG_TRY(launch_init_exponents(nullptr, 0, f, N, K, st));
+    DDG_TRY(launch_col_exponents(B_hi, ldb, K, N, f, st));
+    DDG_TRY(launch_split_cols(B_hi, B_lo, ldb, K, N, Kp, f, planes, st));
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_slice_gemm(int64_t M, int64_t N, int64_t K, const double* planesA,
+                            const double* planesB, int splits, double* P, void* stream) {
+    ddgemm_status s = check_shapes(M, N, K, std::max<int64_t>(1, K), std::max<int64_t>(1, N),
+                                   std::max<int64_t>(1, N));
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    const int64_t Mp = round_up(M, TM), Np = round_up(N, TN), Kp = round_up(K, BK), KC = Kp / BK;
+    if (splits < 1 || splits > kMaxSplits || (KC > 0 && splits > KC) || (KC == 0 && splits != 1))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (P == nullptr || (K > 0 && (planesA == nullptr || planesB == nullptr))) return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0 || (uintptr_t)P % 16 != 0)
+        return DDGEMM_ERR_INVALID_ARG;
+    return from_cuda(launch_slice_gemm(planesA, planesB, Mp, Np, Kp, splits, P,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status dd_recombine(int64_t M, int64_t N, const double* P, int splits, const int32_t* e,
+                           const int32_t* f, double* C_hi, double* C_lo, int64_t ldc, void* stream) {
+    if (M < 0 || N < 0 || ldc < std::max<int64_t>(1, N)) return DDGEMM_ERR_INVALID_ARG;
+    if (splits < 1 || splits > kMaxSplits) return DDGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    if (P == nullptr || e == nullptr || f == nullptr || C_hi == nullptr || C_lo == nullptr)
+        return DDGEMM_ERR_INVALID_ARG;
+    const int64_t Mp = round_up(M, TM), Np = round_up(N, TN);
+    return from_cuda(launch_recombine(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status dd_fp64_tensor_roof(double* tflops, void* stream) {
+    if (tflops == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    return from_cuda(measure_dmma_roof(tflops, static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status dd_wait_timeouts(unsigned int* count) {
+    if (count == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    return from_cuda(read_and_reset_wait_timeouts(count));
+}
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// launch.cuh -- host-side launchers of the dd GEMM kernels (one per step).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ddg {
+
+// Step 1: exponents and part planes.  Exponent arrays are accumulated with
+// atomicMax and must be reset by launch_init_exponents first.
+cudaError_t launch_init_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int64_t K,
+                                  cudaStream_t st);
+cudaError_t launch_row_exponents(const double* A_hi, int64_t lda, int64_t M, int64_t K,
+                                 int32_t* e, cudaStream_t st);
+cudaError_t launch_col_exponents(const double* B_hi, int64_t ldb, int64_t K, int64_t N,
+                                 int32_t* f, cudaStream_t st);
+cudaError_t launch_split_rows(const double* A_hi, const double* A_lo, int64_t lda, int64_t M,
+                              int64_t K, int64_t Kp, int32_t* e, double* planes, cudaStream_t st);
+cudaError_t launch_split_cols(const double* B_hi, const double* B_lo, int64_t ldb, int64_t K,
+                              int64_t N, int64_t Kp, int32_t* f, double* planes, cudaStream_t st);
+
+// Step 2: slice-pair GEMM into `splits` partial sets of 8 planes Mp x Np.
+cudaError_t launch_slice_gemm(const double* planesA, const double* planesB, int64_t Mp,
+                              int64_t Np, int64_t Kp, int splits, double* P, cudaStream_t st);
+int slice_gemm_ctas_per_sm();
+
+// Step 3: recombination of the (split) planes into C = C_hi + C_lo.
+cudaError_t launch_recombine(const double* P, int splits, int64_t Mp, int64_t Np,
+                             const int32_t* e, const int32_t* f, int64_t M, int64_t N,
+                             double* C_hi, double* C_lo, int64_t ldc, cudaStream_t st);
+
+// Rate of a register-only mma.sync.m8n8k4.f64 loop over the whole device
+// (TFLOP/s); synchronises `st`.
+cudaError_t measure_dmma_roof(double* tflops, cudaStream_t st);
+
+// Diagnostics of the bounded waits inside the slice GEMM.
+cudaError_t read_and_reset_wait_timeouts(unsigned int* count);
+
+}  // namespace ddg

@@ -1,0 +1,81 @@
+// recombine.cu -- step 3 of the dd GEMM: the parts of the product summed into
+// one double double and scaled back.
+//
+// "Multiple Double Arithmetic on NVIDIA Tensor Cores", Section 2, steps 4-5:
+// extract the parts of the product and add them in double-double arithmetic
+// (massively parallel, on the regular cores).  For output (i, j):
+//     P_d   = sum over k-splits (exact: integers below 2^53)
+//     (h,l) = P_7 2^-117, then for d = 6 .. 0:
+//             (s, err) = two_sum(h, P_d 2^(-13(d+2)));  err += l;
+//             (h, l)   = quick_two_sum(s, err)
+//     C_hi  = ldexp(h, e_i + f_j),  C_lo = ldexp(l, e_i + f_j)   (+0 for zero)
+// The weights 2^(-13(d+2)) are exact powers of two: part d of the product of
+// two digit expansions x = sum_s D_s 2^(-13(s+1)) carries 2^(-13(d+2)).
+// Every addition is an explicit round-to-nearest FP64 operation (the
+// error-free transformations must not be contracted or reassociated).
+#include "common.cuh"
+#include "launch.cuh"
+
+namespace ddg {
+namespace {
+
+__device__ __forceinline__ void two_sum(double a, double b, double& s, double& e) {
+    s = __dadd_rn(a, b);
+    double bb = __dsub_rn(s, a);
+    e = __dadd_rn(__dsub_rn(a, __dsub_rn(s, bb)), __dsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void quick_two_sum(double a, double b, double& s, double& e) {
+    s = __dadd_rn(a, b);
+    e = __dsub_rn(b, __dsub_rn(s, a));
+}
+
+// 2^(-13 (d + 2)), d = 0..7: the weight of part d of the product.
+__device__ __constant__ double kPartWeight[S] = {0x1p-26, 0x1p-39, 0x1p-52, 0x1p-65,
+                                                 0x1p-78, 0x1p-91, 0x1p-104, 0x1p-117};
+
+__global__ void __launch_bounds__(256) recombine_kernel(const double* __restrict__ P, int splits,
+                                                        int64_t Mp, int64_t Np,
+                                                        const int32_t* __restrict__ e,
+                                                        const int32_t* __restrict__ f, int64_t M,
+                                                        int64_t N, double* __restrict__ C_hi,
+                                                        double* __restrict__ C_lo, int64_t ldc) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= N) return;
+    const int64_t plane = Mp * Np;
+    const int fj = effective_exponent(f[j]);
+    for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
+        const double* p = P + i * Np + j;
+        double part[S];
+#pragma unroll
+        for (int d = 0; d < S; ++d) part[d] = __ldg(p + d * plane);
+        for (int z = 1; z < splits; ++z)
+#pragma unroll
+            for (int d = 0; d < S; ++d) part[d] = __dadd_rn(part[d], __ldg(p + ((int64_t)z * S + d) * plane));
+        double h = __dmul_rn(part[S - 1], kPartWeight[S - 1]), l = 0.0;
+#pragma unroll
+        for (int d = S - 2; d >= 0; --d) {
+            double s, err;
+            two_sum(h, __dmul_rn(part[d], kPartWeight[d]), s, err);
+            err = __dadd_rn(err, l);
+            quick_two_sum(s, err, h, l);
+        }
+        const int sc = effective_exponent(e[i]) + fj;
+        C_hi[i * ldc + j] = __dadd_rn(ldexp(h, sc), 0.0);
+        C_lo[i * ldc + j] = __dadd_rn(ldexp(l, sc), 0.0);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_recombine(const double* P, int splits, int64_t Mp, int64_t Np,
+                             const int32_t* e, const int32_t* f, int64_t M, int64_t N,
+                             double* C_hi, double* C_lo, int64_t ldc, cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    const unsigned gx = (unsigned)((N + 255) / 256);
+    const unsigned gy = (unsigned)(M < 65535 ? M : 65535);
+    recombine_kernel<<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc);
+    return cudaGetLastError();
+}
+
+}  // namespace ddg

@@ -1,0 +1,201 @@
+/*
+ * ddgemm.h -- double-double matrix product on the FP64 tensor pipe of GB300.
+ *
+ * C = A * B for double-double matrices (A = A_hi + A_lo, M x K; B = B_hi +
+ * B_lo, K x N; C = C_hi + C_lo, M x N), following "Multiple Double Arithmetic
+ * on NVIDIA Tensor Cores" (arXiv 2607.06881v1), Section 2: every double
+ * double is split into 8 parts of 13 bits ("quarters": 4 of the high double,
+ * 4 of the low double), the products of the parts run as ordinary FP64 matrix
+ * products that are exact, and the parts of the product are added back into a
+ * double double.  Here the 13-bit parts of a row of A (a column of B) share
+ * one exponent, so that every part of the row lies on one grid (the balancing
+ * goal of Section 3, Problems 3.2 and 3.4).
+ *
+ * Conventions shared by every entry point below:
+ *   - Matrices are row-major.  lda, ldb, ldc are leading dimensions in
+ *     elements: lda >= K, ldb >= N, ldc >= N (and >= 1).
+ *   - Pointers named d_* / A_hi ... are DEVICE pointers on the current device,
+ *     owned by the caller; the library keeps no reference after the call.
+ *     Pointers named h_* are host pointers.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) unless stated otherwise.  Argument errors are returned
+ *     before anything is launched.  Errors raised by the device surface at the
+ *     next synchronising call, as with any CUDA work.
+ *   - Inputs must be finite, normalised double doubles (|lo| <= ulp(hi)/2 and
+ *     lo = 0 where hi = 0).  Other inputs give unspecified values (no fault,
+ *     no hang); they are not checked.
+ *   - K <= DDGEMM_MAX_K (2^24): every slice-pair sum then stays below 2^53 and
+ *     is exact (the argument of eq. (5) of the paper, for 13-bit parts and
+ *     8 index sums).  Larger K returns DDGEMM_ERR_UNSUPPORTED.
+ *   - M, N or K = 0 is valid; K = 0 writes C = +0.
+ */
+#ifndef DDGEMM_H
+#define DDGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DDGEMM_SLICES 8          /* parts per double double (4 + 4 quarters) */
+#define DDGEMM_DIGIT_BITS 13     /* bits per quarter */
+#define DDGEMM_MAX_K (1 << 24)   /* exactness bound on the inner dimension */
+#define DDGEMM_TILE_M 32         /* row tile of the part planes of A / of P */
+#define DDGEMM_TILE_N 32         /* column tile of the part planes of B / of P */
+#define DDGEMM_CHUNK_K 8         /* k-chunk of the part planes */
+
+typedef enum {
+    DDGEMM_OK = 0,
+    DDGEMM_ERR_INVALID_ARG = 1,  /* bad size, leading dimension, pointer or overlap */
+    DDGEMM_ERR_UNSUPPORTED = 2,  /* K beyond DDGEMM_MAX_K */
+    DDGEMM_ERR_ALLOC = 3,        /* device allocation failed */
+    DDGEMM_ERR_CUDA = 4          /* a CUDA call or launch failed */
+} ddgemm_status;
+
+/* Human-readable name of a status code (static string). */
+const char* dd_status_string(int status);
+
+/* ------------------------------------------------------------------ */
+/* Whole product                                                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Padded extents and the k-split of the slice GEMM chosen for this shape on
+ * the current device: Mp = M rounded up to DDGEMM_TILE_M, Np = N rounded up to
+ * DDGEMM_TILE_N, Kp = K rounded up to DDGEMM_CHUNK_K; splits >= 1.  Any output
+ * pointer may be NULL.
+ */
+ddgemm_status dd_gemm_layout(int64_t M, int64_t N, int64_t K,
+                             int64_t* Mp, int64_t* Np, int64_t* Kp, int* splits);
+
+/* Bytes of device workspace dd_gemm_ws needs for this shape on the current
+ * device (written to *bytes). */
+ddgemm_status dd_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/*
+ * C = A * B (double double), caller-provided workspace.
+ * The paper's five steps (Section 2): split into 8 parts, rewrite, multiply on
+ * the tensor cores, extract, add the parts into a double double; here run as
+ * seven kernels on `stream`: exponent init, row / column exponents, row /
+ * column split into part planes, the slice-pair GEMM (FP64 mma.sync), and the
+ * recombination.  `workspace` is a device buffer of at least
+ * dd_gemm_workspace_size() bytes, 256-byte aligned; its contents on entry do
+ * not matter and it must not be used by anything else until the work on
+ * `stream` completes.  C must not overlap A, B or the workspace.
+ */
+ddgemm_status dd_gemm_ws(int64_t M, int64_t N, int64_t K,
+                         const double* A_hi, const double* A_lo, int64_t lda,
+                         const double* B_hi, const double* B_lo, int64_t ldb,
+                         double* C_hi, double* C_lo, int64_t ldc,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * C = A * B (double double).  As dd_gemm_ws, with the workspace taken from the
+ * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * Returns DDGEMM_ERR_ALLOC when the allocation fails.
+ */
+ddgemm_status dd_gemm(int64_t M, int64_t N, int64_t K,
+                      const double* A_hi, const double* A_lo, int64_t lda,
+                      const double* B_hi, const double* B_lo, int64_t ldb,
+                      double* C_hi, double* C_lo, int64_t ldc, void* stream);
+
+/*
+ * C = A * B with HOST operands and result: copies A and B to the current
+ * device, runs dd_gemm, copies C back, frees what it allocated, and returns
+ * only after the result is in h_C_hi / h_C_lo (it synchronises `stream`).
+ * Host buffers are read and written as dense row-major arrays with the given
+ * leading dimensions; page-locked (pinned) buffers make the copies faster.
+ */
+ddgemm_status dd_gemm_host(int64_t M, int64_t N, int64_t K,
+                           const double* h_A_hi, const double* h_A_lo, int64_t lda,
+                           const double* h_B_hi, const double* h_B_lo, int64_t ldb,
+                           double* h_C_hi, double* h_C_lo, int64_t ldc, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* The steps of the path, one entry point each                          */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Step 1a (rows of A): shared exponents and part planes.
+ *   e[i] = smallest integer with max_k |A_hi[i,k]| < 2^e[i]; 0 for a zero row.
+ *   The parts of x = A_hi[i,k] + A_lo[i,k] are the 8 truncating base-2^13
+ *   digits of |x| * 2^-e[i], most significant first, with the sign of x:
+ *       x * 2^-e[i] = sum_s D_s 2^(-13 (s+1)) + r,   |r| < 2^-104,
+ *   each D_s an integer in (-2^13, 2^13) stored as a double (the quarters of
+ *   Section 2 of the paper, on a grid shared by the row).  When hi and lo
+ *   have opposite signs the truncation of their sum borrows from the higher
+ *   digits, the value-preserving move of Problem 3.3, eq. (7).
+ * Output layout (tiled for the slice GEMM; entries outside M x K are 0):
+ *   planes[((((mt * KC + kc) * 8 + s) * 2 + q) * 32 + mi) * 4 + r]
+ *     holds D_s of element (i, k) with mt = i / 32, mi = i % 32,
+ *     kc = k / 8, q = (k % 8) / 4, r = k % 4, KC = Kp / 8
+ *   (8 * Mp * Kp doubles; Mp, Kp from dd_gemm_layout).  e: M int32.
+ */
+ddgemm_status dd_split_rows(int64_t M, int64_t K,
+                            const double* A_hi, const double* A_lo, int64_t lda,
+                            double* planes, int32_t* e, void* stream);
+
+/*
+ * Step 1b (columns of B): as dd_split_rows, for the columns of B (K x N,
+ * row-major, leading dimension ldb): f[j] from max_k |B_hi[k,j]|, and
+ *   planes[((((nt * KC + kc) * 8 + t) * 2 + q) * 32 + ni) * 4 + r]
+ *     holds D_t of element (k, j) with nt = j / 32, ni = j % 32
+ *   (8 * Np * Kp doubles).  f: N int32.
+ */
+ddgemm_status dd_split_cols(int64_t K, int64_t N,
+                            const double* B_hi, const double* B_lo, int64_t ldb,
+                            double* planes, int32_t* f, void* stream);
+
+/*
+ * Step 2 (slice-pair GEMM, eqs. (3)-(4) of the paper grouped by index sum):
+ *   P[z][d][i][j] = sum_{s+t=d} sum_{k in split z} A_s[i,k] * B_t[k,j],
+ *   d = 0..7, for the 36 pairs s + t <= 7, on the FP64 tensor pipe
+ *   (mma.sync m8n8k4 f64), with every sum an exact integer below 2^53.
+ * planesA / planesB: the outputs of dd_split_rows / dd_split_cols for the same
+ * M, N, K.  P: splits x 8 x Mp x Np doubles, row-major per plane; split z
+ * covers the k-chunks [z * KC / splits, (z + 1) * KC / splits).  splits must
+ * be in [1, KC] (or 1 when KC = 0); dd_gemm_layout gives the automatic choice.
+ */
+ddgemm_status dd_slice_gemm(int64_t M, int64_t N, int64_t K,
+                            const double* planesA, const double* planesB,
+                            int splits, double* P, void* stream);
+
+/*
+ * Step 3 (recombination, steps 4-5 of the paper's algorithm):
+ *   P_d = sum_z P[z][d][i][j] (exact), then, from d = 7 down to 0,
+ *   (h, l) <- quick_two_sum(two_sum(h, P_d 2^(-13(d+2))) with l added to its
+ *   error), starting from h = P_7 2^-117, l = 0; finally
+ *   C_hi = h * 2^(e[i] + f[j]), C_lo = l * 2^(e[i] + f[j]) (ldexp, correctly
+ *   rounded; +0 for zero).  P as produced by dd_slice_gemm.
+ */
+ddgemm_status dd_recombine(int64_t M, int64_t N, const double* P, int splits,
+                           const int32_t* e, const int32_t* f,
+                           double* C_hi, double* C_lo, int64_t ldc, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* Diagnostics                                                          */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Measured rate of the FP64 tensor pipe on the current device, in TFLOP/s
+ * (2 * 8 * 8 * 4 flops per mma.sync.m8n8k4.f64): a register-only loop of
+ * that instruction on every SM, timed with CUDA events on `stream`.  This is
+ * the roof of the slice-pair GEMM.  Synchronises `stream`.
+ */
+ddgemm_status dd_fp64_tensor_roof(double* tflops, void* stream);
+
+/*
+ * Number of times a slice-GEMM thread block gave up waiting for its operand
+ * copies on the current device (each wait is bounded in time; a block that
+ * gives up stops early and its P tile is incomplete).  Synchronises the
+ * device, reads the counter and resets it to 0.  Zero in normal operation.
+ */
+ddgemm_status dd_wait_timeouts(unsigned int* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDGEMM_H */

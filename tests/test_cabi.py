@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/ddgemm.h declares; argument errors are caught on the host before any
+launch (no GPU needed for any of these checks)."""
+import ctypes
+import pathlib
+import re
+
+import pytest
+
+import extended_precision_gemm_gb300 as ddg
+
+HEADER = pathlib.Path(__file__).resolve().parent.parent / "include" / "ddgemm.h"
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dd_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ddg.load()
+
+
+def test_header_matches_binding():
+    assert declared_functions() == ddg.exported_symbols()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and they are C symbols (no C++ mangling)
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", str(ddg.library_path())],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, name
+
+
+def test_status_strings(lib):
+    assert lib.dd_status_string(0) == b"DDGEMM_OK"
+    assert lib.dd_status_string(2) == b"DDGEMM_ERR_UNSUPPORTED"
+    assert lib.dd_status_string(99) == b"DDGEMM_UNKNOWN_STATUS"
+
+
+def _gemm(lib, M, N, K, A=1 << 20, B=1 << 30, C=1 << 40, lda=None, ldb=None, ldc=None):
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    big = 1 << 36
+    return lib.dd_gemm(M, N, K, A, A + big, max(lda, 1), B, B + big, max(ldb, 1),
+                       C, C + big, max(ldc, 1), None)
+
+
+def test_argument_errors_are_host_side(lib):
+    # negative sizes, short leading dimensions, null pointers, overlaps
+    assert _gemm(lib, -1, 4, 4) == 1
+    assert _gemm(lib, 4, 4, 4, lda=3) == 1
+    assert _gemm(lib, 4, 4, 4, ldc=2) == 1
+    assert lib.dd_gemm(4, 4, 4, None, None, 4, 1 << 30, 1 << 31, 4, 1 << 40, 1 << 41, 4, None) == 1
+    # C overlapping A
+    assert lib.dd_gemm(4, 4, 4, 1 << 20, 1 << 30, 4, 1 << 32, 1 << 33, 4, (1 << 20) + 8, 1 << 41, 4, None) == 1
+    # C_hi overlapping C_lo
+    assert lib.dd_gemm(4, 4, 4, 1 << 20, 1 << 30, 4, 1 << 32, 1 << 33, 4, 1 << 40, (1 << 40) + 64, 4, None) == 1
+    # K beyond the exactness bound
+    assert _gemm(lib, 4, 4, ddg.MAX_K + 1) == 2
+    assert lib.dd_gemm_workspace_size(4, 4, ddg.MAX_K + 1, ctypes.byref(ctypes.c_size_t())) == 2
+    # empty products need no pointers at all
+    assert lib.dd_gemm(0, 5, 7, None, None, 7, None, None, 5, None, None, 5, None) == 0
+    assert lib.dd_gemm(5, 0, 7, None, None, 7, None, None, 1, None, None, 1, None) == 0
+    # step entry points validate too
+    assert lib.dd_split_rows(-1, 4, None, None, 4, None, None, None) == 1
+    assert lib.dd_slice_gemm(32, 32, 64, 1 << 20, 1 << 30, 0, 1 << 40, None) == 1   # splits = 0
+    assert lib.dd_slice_gemm(32, 32, 64, 1 << 20, 1 << 30, 9, 1 << 40, None) == 1   # splits > KC
+    assert lib.dd_recombine(4, 4, None, 1, None, None, None, None, 4, None) == 1
+    assert lib.dd_wait_timeouts(None) == 1
+    # workspace: bad alignment / too small
+    assert lib.dd_gemm_ws(4, 4, 4, 1 << 20, 1 << 30, 4, 1 << 32, 1 << 33, 4, 1 << 40, 1 << 41, 4,
+                          (1 << 42) + 8, 1 << 30, None) == 1
+    assert lib.dd_gemm_ws(4, 4, 4, 1 << 20, 1 << 30, 4, 1 << 32, 1 << 33, 4, 1 << 40, 1 << 41, 4,
+                          1 << 42, 16, None) == 1
+
+
+def test_layout_padding(lib):
+    Mp, Np, Kp, sp = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int()
+    assert lib.dd_gemm_layout(33, 1, 9, ctypes.byref(Mp), ctypes.byref(Np), ctypes.byref(Kp), ctypes.byref(sp)) == 0
+    assert (Mp.value, Np.value, Kp.value) == (64, 32, 16)
+    assert sp.value >= 1
+    n = ctypes.c_size_t()
+    assert lib.dd_gemm_workspace_size(33, 1, 9, ctypes.byref(n)) == 0
+    # exponents + both plane sets + split P planes, each 256-byte aligned
+    need = 256 + 256 + 8 * 64 * 16 * 8 + 8 * 32 * 16 * 8 + sp.value * 8 * 64 * 32 * 8
+    assert n.value == need

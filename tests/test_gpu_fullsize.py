@@ -1,0 +1,80 @@
+"""The full-size workloads, in the launch configuration bench.py times
+(dd_gemm_ws with the automatic layout), checked on samples the oracle can
+afford: a block of sampled rows x columns bit for bit against the oracle's
+model of the method (row / column exponents depend only on that row /
+column, so the block is the model's product of the sampled rows and
+columns), and whole sampled rows against the exact product (normwise bound
+1e-26 on those rows).  Plus the maximum inner dimension K = 2^24 with the
+largest digits, whose part sums sit just below 2^53 and have a closed form."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import extended_precision_gemm_gb300 as ddg
+import oracle
+import workloads
+from oracle import slices
+from tests.gpu_util import dev, host, normwise
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_full_size_workload(idx):
+    import torch
+    w = workloads.WORKLOADS[idx]
+    A_hi, A_lo, B_hi, B_lo = workloads.make_workload(idx)
+    tA_hi, tA_lo, tB_hi, tB_lo = dev(A_hi), dev(A_lo), dev(B_hi), dev(B_lo)
+    ws = torch.empty(ddg.workspace_size(w.M, w.N, w.K), dtype=torch.uint8, device="cuda")
+    C_hi, C_lo = ddg.dd_gemm_ws(tA_hi, tA_lo, tB_hi, tB_lo, ws)
+    torch.cuda.synchronize()
+    assert ddg.wait_timeouts() == 0
+    rng = np.random.default_rng(100 + idx)
+    rows = np.unique(np.concatenate([[0, w.M // 2, w.M - 1], rng.integers(0, w.M, 3)]))
+    cols = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, 14)]))
+    G_hi = host(C_hi[torch.from_numpy(rows).cuda()])
+    G_lo = host(C_lo[torch.from_numpy(rows).cuda()])
+    # bit-exact block against the model of the method
+    M_hi, M_lo, *_ = slices.sliced_dd_gemm(A_hi[rows], A_lo[rows], B_hi[:, cols], B_lo[:, cols])
+    assert np.array_equal(G_hi[:, cols].view(np.int64), M_hi.view(np.int64))
+    assert np.array_equal(G_lo[:, cols].view(np.int64), M_lo.view(np.int64))
+    # exact product on two whole rows
+    r2 = rows[:2]
+    R_hi, R_lo = oracle.exact_dd_gemm(A_hi, A_lo, B_hi, B_lo, rows=r2)
+    err = normwise(G_hi[:2], G_lo[:2], R_hi, R_lo, A_hi[r2], A_lo[r2], B_hi, B_lo)
+    assert err <= 1e-26, err
+
+
+def test_maximum_k_closed_form():
+    import torch
+    K = ddg.MAX_K
+    # x = 1 - 2^-104 as a normalised double double: (1, -2^-104).  With the
+    # shared exponent 1, x/2 = 0.0111...1 (104 fraction bits): parts
+    # D_0 = 4095 and D_1..7 = 8191, the largest a row can hold.
+    A_hi = torch.ones((1, K), dtype=torch.float64, device="cuda")
+    A_lo = torch.full((1, K), -2.0**-104, dtype=torch.float64, device="cuda")
+    B_hi = torch.ones((K, 1), dtype=torch.float64, device="cuda")
+    B_lo = torch.full((K, 1), -2.0**-104, dtype=torch.float64, device="cuda")
+    Mp, Np, Kp, splits = ddg.layout(1, 1, K)
+    pA, e = ddg.split_rows(A_hi, A_lo)
+    pB, f = ddg.split_cols(B_hi, B_lo)
+    P = ddg.slice_gemm(1, 1, K, pA, pB, splits)
+    D = [4095] + [8191] * 7
+    P_sum = host(P.sum(dim=0))[:, 0, 0]
+    for d in range(8):
+        exact = K * sum(D[s] * D[d - s] for s in range(d + 1))
+        assert exact < 2**53
+        assert P_sum[d] == exact, (d, P_sum[d], exact)
+    del pA, pB
+    C_hi, C_lo = ddg.recombine(1, 1, P, e, f)
+    assert host(e)[0] == 1 and host(f)[0] == 1
+    x = Fraction(1) - Fraction(1, 2**104)
+    exact = K * x * x
+    got = Fraction(float(host(C_hi)[0, 0])) + Fraction(float(host(C_lo)[0, 0]))
+    # per k: truncation of both factors (< 2^-104 each) plus the dropped pairs
+    # of index sum 8..14 (sum of (15-d) 2^26 2^(-13(d+2)) < 7.01 2^-104), all
+    # times 2^(e+f) = 4; the double-double rounding adds far less
+    assert abs(got - exact) <= K * 4 * Fraction(10, 2**104)
+    assert got < exact  # truncation toward zero of positive parts
+    assert ddg.wait_timeouts() == 0
