@@ -214,8 +214,9 @@ def oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, rows):
 
 def cpu_baseline(w, A_hi, A_lo, B_hi, B_lo, target_s: float = 12.0):
     import oracle
-    t1, _, _ = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, [0])
-    nrows = max(1, min(w.M, int(target_s / max(t1, 1e-3))))
+    r0 = list(range(min(16, w.M)))   # one row per core or so: calibrates the parallel rate
+    t1, _, _ = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, r0)
+    nrows = max(1, min(w.M, int(target_s * len(r0) / max(t1, 1e-3))))
     rows = list(range(nrows))
     t, C_hi, C_lo = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, rows)
     value = 2.0 * nrows * w.N * w.K / t / 1e9
@@ -233,8 +234,9 @@ def run_reference(args, w):
     if rank != 0:
         return None
     import oracle
-    A_hi, A_lo, B_hi, B_lo = workloads.make_workload(args.workload)
-    t1, _, _ = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, [0])
+    A_hi, A_lo, B_hi, B_lo = workloads.make_dd(w.M, w.N, w.K, w.dist, w.seed)
+    t1, _, _ = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, list(range(min(16, w.M))))
+    t1 /= min(16, w.M)
     rows_per_step = max(1, int(2.0 / max(t1, 1e-3)))
     rows = list(range(rows_per_step))
     for _ in range(args.warmup):
@@ -277,7 +279,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     M, N, K = w.M, w.N, w.K
 
-    A_hi, A_lo, B_hi, B_lo = workloads.make_workload(args.workload)
+    A_hi, A_lo, B_hi, B_lo = workloads.make_dd(M, N, K, w.dist, w.seed)
     pinned = [torch.from_numpy(x).pin_memory() for x in (A_hi, A_lo, B_hi, B_lo)]
     dA_hi, dA_lo, dB_hi, dB_lo = (t.to(dev, non_blocking=True) for t in pinned)
     C_hi = torch.empty((M, N), dtype=torch.float64, device=dev)
@@ -406,8 +408,14 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--shape", type=int, nargs=3, metavar=("M", "N", "K"),
+                    help="profiling only: the workload's distribution and seed at another shape")
     args = ap.parse_args(argv)
     w = workloads.WORKLOADS[args.workload]
+    if args.shape:
+        M, N, K = args.shape
+        w = workloads.Workload(w.index, f"dd_gemm_{M}x{N}x{K}_{w.dist}", M, N, K, w.dist, w.seed)
+    args.w = w
     out = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if out is not None:
         print(json.dumps(out), flush=True)
