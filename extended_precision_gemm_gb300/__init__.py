@@ -24,7 +24,7 @@ from . import build as _build
 __all__ = [
     "DDGemmError", "SLICES", "MAX_K", "TILE_M", "TILE_N", "CHUNK_K", "STATUS",
     "load", "library_path", "exported_symbols",
-    "dd_gemm", "dd_gemm_ws", "dd_gemm_host", "layout", "workspace_size",
+    "dd_gemm", "dd_gemm_ws", "dd_gemm_host", "dd_gemm_noalloc", "layout", "workspace_size",
     "split_rows", "split_cols", "slice_gemm", "recombine", "wait_timeouts", "fp64_tensor_roof",
 ]
 
@@ -34,7 +34,8 @@ TILE_M = 32
 TILE_N = 32
 CHUNK_K = 8
 STATUS = {0: "DDGEMM_OK", 1: "DDGEMM_ERR_INVALID_ARG", 2: "DDGEMM_ERR_UNSUPPORTED",
-          3: "DDGEMM_ERR_ALLOC", 4: "DDGEMM_ERR_CUDA"}
+          3: "DDGEMM_ERR_ALLOC", 4: "DDGEMM_ERR_CUDA", 5: "DDGEMM_ERR_TOO_LARGE"}
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class DDGemmError(RuntimeError):
@@ -61,6 +62,7 @@ _SIGNATURES = {
     "dd_recombine": ([_i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _ptr, _i64, _ptr], _int),
     "dd_wait_timeouts": ([_ptr], _int),
     "dd_fp64_tensor_roof": ([_ptr, _ptr], _int),
+    "dd_gemm_noalloc": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
 }
 
 
@@ -177,6 +179,22 @@ def dd_gemm_ws(A_hi, A_lo, B_hi, B_lo, workspace, C_hi=None, C_lo=None, stream=N
                                            C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi),
                                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                            _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def dd_gemm_noalloc(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, stream=None):
+    """The product for callers that cannot allocate device memory while they
+    run: the library's fixed 64 MiB scratch buffer replaces the workspace, and
+    C_hi / C_lo must be given.  Shapes needing more scratch raise
+    DDGemmError(DDGEMM_ERR_TOO_LARGE).  Calls that overlap on the GPU share the
+    buffer and race: order them."""
+    if C_hi is None or C_lo is None:
+        raise ValueError("dd_gemm_noalloc writes into caller-provided C_hi and C_lo")
+    M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
+    _check("dd_gemm_noalloc", load().dd_gemm_noalloc(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                                     B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                                     C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi),
+                                                     _stream_handle(stream)))
     return C_hi, C_lo
 
 

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.cuh"
@@ -152,6 +153,7 @@ const char* dd_status_string(int status) {
         case DDGEMM_ERR_UNSUPPORTED: return "DDGEMM_ERR_UNSUPPORTED";
         case DDGEMM_ERR_ALLOC: return "DDGEMM_ERR_ALLOC";
         case DDGEMM_ERR_CUDA: return "DDGEMM_ERR_CUDA";
+        case DDGEMM_ERR_TOO_LARGE: return "DDGEMM_ERR_TOO_LARGE";
         default: return "DDGEMM_UNKNOWN_STATUS";
     }
 }
@@ -337,3 +339,57 @@ ddgemm_status dd_wait_timeouts(unsigned int* count) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dd_gemm_noalloc: the product with a fixed, library-owned scratch buffer, for
+// callers that cannot allocate device memory while they run.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// The scratch buffer.  In host code this name only stands in for the device
+// array: its device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DDGEMM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch buffer on the current device (looked up on
+// the first call for that device).
+ddgemm_status noalloc_scratch(char** addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DDGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return DDGEMM_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = p;
+    }
+    *addr = static_cast<char*>(g_noalloc_addr[dev]);
+    return DDGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" ddgemm_status dd_gemm_noalloc(int64_t M, int64_t N, int64_t K, const double* A_hi,
+                                         const double* A_lo, int64_t lda, const double* B_hi,
+                                         const double* B_lo, int64_t ldb, double* C_hi, double* C_lo,
+                                         int64_t ldc, void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    Layout L = make_layout(M, N, K);
+    if (L.total > (int64_t)DDGEMM_NOALLOC_SCRATCH_BYTES) return DDGEMM_ERR_TOO_LARGE;
+    char* ws = nullptr;
+    s = noalloc_scratch(&ws);
+    if (s != DDGEMM_OK) return s;
+    // Every region of the workspace is written before it is read within the
+    // call (exponents by their init kernel, part planes including padding by
+    // the split kernels, P by the slice GEMM), so no clearing is needed.
+    return run_gemm(L, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc, ws,
+                    static_cast<cudaStream_t>(stream));
+}

@@ -51,7 +51,8 @@ typedef enum {
     DDGEMM_ERR_INVALID_ARG = 1,  /* bad size, leading dimension, pointer or overlap */
     DDGEMM_ERR_UNSUPPORTED = 2,  /* K beyond DDGEMM_MAX_K */
     DDGEMM_ERR_ALLOC = 3,        /* device allocation failed */
-    DDGEMM_ERR_CUDA = 4          /* a CUDA call or launch failed */
+    DDGEMM_ERR_CUDA = 4,         /* a CUDA call or launch failed */
+    DDGEMM_ERR_TOO_LARGE = 5     /* needs more scratch than dd_gemm_noalloc's fixed buffer */
 } ddgemm_status;
 
 /* Human-readable name of a status code (static string). */
@@ -112,6 +113,37 @@ ddgemm_status dd_gemm_host(int64_t M, int64_t N, int64_t K,
                            const double* h_A_hi, const double* h_A_lo, int64_t lda,
                            const double* h_B_hi, const double* h_B_lo, int64_t ldb,
                            double* h_C_hi, double* h_C_lo, int64_t ldc, void* stream);
+
+/*
+ * C = A * B (double double) without allocating any memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that must not allocate device memory while they run: an application that
+ * hands all GPU memory to its own allocator at start-up, a plug-in whose host
+ * forbids allocations, or a latency-critical loop where cudaMalloc / cudaFree
+ * could wait for the whole device.  Instead of a workspace it uses one fixed
+ * scratch buffer of DDGEMM_NOALLOC_SCRATCH_BYTES (64 MiB), a static device
+ * array of the library; every GPU on which the library's device code is
+ * loaded holds that buffer until the process exits.
+ *
+ * Same arguments and results as dd_gemm.  Shapes whose workspace
+ * (dd_gemm_workspace_size) exceeds the buffer return DDGEMM_ERR_TOO_LARGE
+ * before anything runs; M = N = K = 256 fits, for example.
+ * The first call on a device looks up the buffer's device address
+ * (cudaGetSymbolAddress, which may also make the driver load the module that
+ * holds it); make that first call on each device before any stream capture.
+ * All calls on a device share the one buffer, which keeps whatever the last
+ * call left in it.  Each call writes every part of the buffer it reads before
+ * reading it, so leftovers never change a result and nothing needs clearing;
+ * but calls whose work can overlap on the same GPU (issued on different
+ * streams, or from different host threads) race on the buffer: order them,
+ * for example by issuing them on one stream.
+ */
+#define DDGEMM_NOALLOC_SCRATCH_BYTES (64u << 20)
+ddgemm_status dd_gemm_noalloc(int64_t M, int64_t N, int64_t K,
+                              const double* A_hi, const double* A_lo, int64_t lda,
+                              const double* B_hi, const double* B_lo, int64_t ldb,
+                              double* C_hi, double* C_lo, int64_t ldc, void* stream);
 
 /* ------------------------------------------------------------------ */
 /* The steps of the path, one entry point each                          */
