@@ -16,7 +16,7 @@ namespace {
 
 constexpr int64_t kAlign = 256;
 constexpr int kMaxSplits = 64;
-constexpr int64_t kMaxRowTiles = 65535;  // grid.y of the slice GEMM
+constexpr int64_t kMaxTiles = 0x7FFFFFFF;  // grid.x of the slice GEMM
 
 struct Layout {
     int64_t Mp, Np, Kp, KC;
@@ -88,7 +88,7 @@ ddgemm_status check_shapes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t
     if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) || ldc < std::max<int64_t>(1, N))
         return DDGEMM_ERR_INVALID_ARG;
     if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
-    if (round_up(M, TM) / TM > kMaxRowTiles) return DDGEMM_ERR_UNSUPPORTED;
+    if ((round_up(M, TM) / TM) * (round_up(N, TN) / TN) > kMaxTiles) return DDGEMM_ERR_UNSUPPORTED;
     return DDGEMM_OK;
 }
 

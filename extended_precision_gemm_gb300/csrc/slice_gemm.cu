@@ -11,14 +11,16 @@
 // compute them exactly and in any order (the argument of eq. (5)).
 //
 // GB300 mapping:
-//  * one 128-thread block per 32x32 tile of P (all 8 index sums) and k-split;
+//  * one 128-thread block per 32x32 tile of P (all 8 index sums) and k-split,
+//    tiles walked in groups of 16 tile rows so resident blocks share operands;
 //  * operands arrive by bulk asynchronous copies (TMA engine, no tensor map
 //    needed: the part planes are stored tile-contiguous) into a 3-stage
 //    shared-memory ring, one mbarrier per stage; 16 KB of A and 16 KB of B
 //    parts per stage;
-//  * the four warps share the 36 pairs evenly: warp w owns index sums w and
-//    7 - w, i.e. (w + 1) + (8 - w) = 9 pairs, over the whole 32x32 tile
-//    (16 m8n8 accumulator tiles per index sum);
+//  * each of the four warps owns a 16x16 quadrant of the tile and issues all
+//    36 pairs for it (4 m8n8 blocks x 8 index sums = 32 accumulators); all
+//    warps run one instruction stream, which keeps the unrolled loop small
+//    enough for the instruction cache;
 //  * mma.sync.m8n8k4.f64 fragments are read straight from the stage: the
 //    layout [part][k4][row][k%4] makes each fragment 32 consecutive doubles.
 // Every wait on an mbarrier is bounded in time; a block that gives up counts
@@ -37,6 +39,7 @@ constexpr int STAGE_DOUBLES = 2 * CHUNK_DOUBLES;            // A block + B block
 constexpr uint32_t COPY_BYTES = CHUNK_DOUBLES * sizeof(double);  // 16 KB per operand
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_DOUBLES * sizeof(double) + 64;
 constexpr unsigned long long WAIT_BUDGET_NS = 2000000000ULL;  // 2 s per wait
+constexpr int64_t TILE_GROUP = 16;
 
 static_assert(COPY_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 
@@ -116,33 +119,34 @@ __device__ __forceinline__ void dmma(double& c0, double& c1, double a, double b)
         : "d"(a), "d"(b));
 }
 
-// One k-chunk (8 values of k) of the pairs owned by warp W: index sums W and
-// 7 - W.  acc[g][mb][nb][2]: g = 0 for index sum W, 1 for 7 - W.
-template <int W>
+// One k-chunk (8 values of k) of all 36 pairs for the warp's 16x16 quadrant
+// of the tile: rows mq*16 + {0..15}, columns nq*16 + {0..15}, i.e. m8n8
+// blocks mb in {2mq, 2mq+1} and nb in {2nq, 2nq+1}.  acc[d][i][j][2] holds
+// index sum d of block (2mq+i, 2nq+j).  Every warp runs the same instruction
+// stream.  Within a k4 step the B fragments of all 8 parts are loaded once;
+// then for each part s of A the 8-s pairs (s, t) are issued, so consecutive
+// updates of one accumulator are at least 4 * (8 - s) >= 4 MMAs apart.
 __device__ __forceinline__ void chunk_products(const double* __restrict__ As,
-                                               const double* __restrict__ Bs, int lane,
-                                               double (&acc)[2][4][4][2]) {
+                                               const double* __restrict__ Bs, int lane, int mq,
+                                               int nq, double (&acc)[S][2][2][2]) {
 #pragma unroll
     for (int q = 0; q < BK / 4; ++q) {
+        double b[S][2];
+#pragma unroll
+        for (int t = 0; t < S; ++t)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) b[t][j] = Bs[((t * (BK / 4) + q) * TN + (2 * nq + j) * 8) * 4 + lane];
 #pragma unroll
         for (int s = 0; s < S; ++s) {
-            constexpr int D0 = W, D1 = S - 1 - W;
-            if (s > D1) continue;  // no pair of this warp uses A_s
-            double a[4];
+            double a[2];
 #pragma unroll
-            for (int mb = 0; mb < 4; ++mb) a[mb] = As[((s * (BK / 4) + q) * TM + mb * 8) * 4 + lane];
+            for (int i = 0; i < 2; ++i) a[i] = As[((s * (BK / 4) + q) * TM + (2 * mq + i) * 8) * 4 + lane];
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const int t = (g == 0 ? D0 : D1) - s;
-                if (t < 0) continue;
-                double b[4];
+            for (int t = 0; t + s < S; ++t)
 #pragma unroll
-                for (int nb = 0; nb < 4; ++nb) b[nb] = Bs[((t * (BK / 4) + q) * TN + nb * 8) * 4 + lane];
+                for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int mb = 0; mb < 4; ++mb)
-#pragma unroll
-                    for (int nb = 0; nb < 4; ++nb) dmma(acc[g][mb][nb][0], acc[g][mb][nb][1], a[mb], b[nb]);
-            }
+                    for (int j = 0; j < 2; ++j) dmma(acc[s + t][i][j][0], acc[s + t][i][j][1], a[i], b[t][j]);
         }
     }
 }
@@ -154,8 +158,16 @@ __global__ void __launch_bounds__(THREADS, 2)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_DOUBLES);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t nt = blockIdx.x, mt = blockIdx.y;
-    const int z = blockIdx.z;
+    // Tile order: groups of TILE_GROUP row tiles, column-major inside a group,
+    // so the blocks resident at one time share few A and B blocks (L2 reuse).
+    const int64_t MT = Mp / TM, NT = Np / TN;
+    const int64_t t = blockIdx.x;
+    const int64_t group = t / (TILE_GROUP * NT);
+    const int64_t first = group * TILE_GROUP;
+    const int64_t rows = min((int64_t)TILE_GROUP, MT - first);
+    const int64_t local = t - group * TILE_GROUP * NT;
+    const int64_t mt = first + local % rows, nt = local / rows;
+    const int z = blockIdx.y;
     const int64_t kc0 = (int64_t)z * KC / splits, kc1 = (int64_t)(z + 1) * KC / splits;
     const int nk = (int)(kc1 - kc0);
     const double* srcA = planesA + (mt * KC + kc0) * CHUNK_DOUBLES;
@@ -171,13 +183,14 @@ __global__ void __launch_bounds__(THREADS, 2)
             issue_stage(smem_addr(&bars[i]), smem + i * STAGE_DOUBLES, srcA + (int64_t)i * CHUNK_DOUBLES,
                         srcB + (int64_t)i * CHUNK_DOUBLES);
 
-    double acc[2][4][4][2];
+    const int mq = warp >> 1, nq = warp & 1;
+    double acc[S][2][2][2];
 #pragma unroll
-    for (int g = 0; g < 2; ++g)
+    for (int d = 0; d < S; ++d)
 #pragma unroll
-        for (int mb = 0; mb < 4; ++mb)
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int nb = 0; nb < 4; ++nb) acc[g][mb][nb][0] = acc[g][mb][nb][1] = 0.0;
+            for (int j = 0; j < 2; ++j) acc[d][i][j][0] = acc[d][i][j][1] = 0.0;
 
     for (int it = 0; it < nk; ++it) {
         const int st = it % STAGES;
@@ -202,29 +215,22 @@ __global__ void __launch_bounds__(THREADS, 2)
                         srcA + (int64_t)nxt * CHUNK_DOUBLES, srcB + (int64_t)nxt * CHUNK_DOUBLES);
         }
         const double* As = smem + st * STAGE_DOUBLES;
-        const double* Bs = As + CHUNK_DOUBLES;
-        switch (warp) {
-            case 0: chunk_products<0>(As, Bs, lane, acc); break;
-            case 1: chunk_products<1>(As, Bs, lane, acc); break;
-            case 2: chunk_products<2>(As, Bs, lane, acc); break;
-            default: chunk_products<3>(As, Bs, lane, acc); break;
-        }
+        chunk_products(As, As + CHUNK_DOUBLES, lane, mq, nq, acc);
     }
 
-    // Epilogue: thread (lane) holds rows mb*8 + lane/4, columns nb*8 + 2(lane%4) + {0,1}.
+    // Epilogue: for block (mb, nb) the thread holds row mb*8 + lane/4 and
+    // columns nb*8 + 2(lane%4) + {0, 1}.
     const int64_t plane = Mp * Np;
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        const int d = (g == 0) ? warp : S - 1 - warp;
+    for (int d = 0; d < S; ++d) {
         double* out = P + ((int64_t)z * S + d) * plane;
 #pragma unroll
-        for (int mb = 0; mb < 4; ++mb) {
-            const int64_t row = mt * TM + mb * 8 + (lane >> 2);
+        for (int i = 0; i < 2; ++i) {
+            const int64_t row = mt * TM + (2 * mq + i) * 8 + (lane >> 2);
 #pragma unroll
-            for (int nb = 0; nb < 4; ++nb) {
-                const int64_t col = nt * TN + nb * 8 + 2 * (lane & 3);
-                *reinterpret_cast<double2*>(out + row * Np + col) =
-                    make_double2(acc[g][mb][nb][0], acc[g][mb][nb][1]);
+            for (int j = 0; j < 2; ++j) {
+                const int64_t col = nt * TN + (2 * nq + j) * 8 + 2 * (lane & 3);
+                *reinterpret_cast<double2*>(out + row * Np + col) = make_double2(acc[d][i][j][0], acc[d][i][j][1]);
             }
         }
     }
@@ -295,7 +301,7 @@ cudaError_t launch_slice_gemm(const double* planesA, const double* planesB, int6
     cudaError_t err = cudaFuncSetAttribute(slice_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    dim3 grid((unsigned)(Np / TN), (unsigned)(Mp / TM), (unsigned)splits);
+    dim3 grid((unsigned)((Mp / TM) * (Np / TN)), (unsigned)splits);
     slice_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(planesA, planesB, Kp / BK, splits, P, Mp, Np);
     return cudaGetLastError();
 }

@@ -160,102 +160,137 @@ __device__ __forceinline__ void split_digits(double hi, double lo, int e, double
     }
 }
 
-// Offset of part s of element (row-in-tile ti, k) inside the plane array:
-// [tile][k-chunk][s][k4 group in chunk][row in tile][k % 4].
-__device__ __forceinline__ int64_t plane_offset(int64_t tile, int64_t KC, int64_t k, int s, int ti) {
-    int64_t kc = k / BK;
-    int q = (int)((k % BK) >> 2);
-    return ((((tile * KC + kc) * S + s) * (BK / 4) + q) * TM + ti) * 4;
+// Each split block covers one 32-row (A) or 32-column (B) tile and 32
+// consecutive k (4 k-chunks).  Its parts form one contiguous 64 KB block of
+// the plane array ([chunk][part][k4 group][row in tile][k % 4]); the block is
+// assembled in shared memory and written with one bulk asynchronous copy
+// (TMA engine), so every DRAM line is written whole.
+constexpr int SPLIT_THREADS = 256;
+constexpr int SPLIT_CHUNKS = 32 / BK;                              // k-chunks per block
+constexpr size_t SPLIT_SMEM = (size_t)SPLIT_CHUNKS * CHUNK_DOUBLES * sizeof(double);  // 64 KB
+constexpr int PART_STRIDE = (BK / 4) * TM * 4;                     // doubles between parts s, s+1
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Parts of 4 consecutive elements (k0 .. k0+3) of one row or column into the
+// staging block, two elements per 16-byte shared-memory store.
+__device__ __forceinline__ void stage_parts(const double (&hi)[4], const double (&lo)[4], int ex,
+                                            double* dst) {
+#pragma unroll
+    for (int r = 0; r < 4; r += 2) {
+        double d0[S], d1[S];
+        split_digits(hi[r], lo[r], ex, d0);
+        split_digits(hi[r + 1], lo[r + 1], ex, d1);
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+            *reinterpret_cast<double2*>(dst + s * PART_STRIDE + r) = make_double2(d0[s], d1[s]);
+    }
+}
+
+// Write the staged block (`chunks` k-chunks) to global memory and wait until
+// the copy has read shared memory, so the stage can be refilled.
+__device__ __forceinline__ void flush_stage(double* stage, double* gdst, int chunks) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)chunks * CHUNK_DOUBLES * sizeof(double);
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                     "r"(smem_u32(stage)), "r"(bytes)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
+    __syncthreads();
 }
 
 // Rows of A.  Block = 32 rows (lanes) x 8 groups of 4 consecutive k (warps);
 // blockIdx.x walks k in steps of 32, blockIdx.y strides over the row tiles.
 // Each thread reads 4 hi and 4 lo values of its row (two 128-bit loads each
-// when VEC == 2) and writes 4 consecutive doubles to each of the 8 planes;
-// the 32 lanes of a warp write 1 KB contiguous per plane.
+// when VEC == 2) and stages its 32 parts.
 template <int VEC>
-__global__ void __launch_bounds__(256) split_rows_kernel(const double* __restrict__ A_hi,
-                                                         const double* __restrict__ A_lo,
-                                                         int64_t lda, int64_t M, int64_t K,
-                                                         int64_t Kp, int32_t* e,
-                                                         double* __restrict__ planes) {
+__global__ void __launch_bounds__(SPLIT_THREADS, 3) split_rows_kernel(const double* __restrict__ A_hi,
+                                                                   const double* __restrict__ A_lo,
+                                                                   int64_t lda, int64_t M, int64_t K,
+                                                                   int64_t Kp, int32_t* e,
+                                                                   double* __restrict__ planes) {
+    extern __shared__ __align__(128) double stage[];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t k0 = (int64_t)blockIdx.x * 32 + 4 * w;
-    if (k0 >= Kp) return;
     const int64_t KC = Kp / BK;
+    const int64_t kc0 = (int64_t)blockIdx.x * SPLIT_CHUNKS;
+    const int chunks = (int)min((int64_t)SPLIT_CHUNKS, KC - kc0);
+    const int64_t k0 = kc0 * BK + 4 * w;
+    const bool active = (w >> 1) < chunks;  // this warp's k-chunk exists
+    double* dst = stage + (((w >> 1) * S * (BK / 4) + (w & 1)) * TM + lane) * 4;
     const int64_t tiles = (M + TM - 1) / TM;
     for (int64_t mt = blockIdx.y; mt < tiles; mt += gridDim.y) {
-    const int64_t i = mt * TM + lane;
-    double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-    int ex = 0;
-    if (i < M) {
-        const int32_t er = e[i];
-        ex = effective_exponent(er);
-        if (blockIdx.x == 0 && w == 0 && er == EXP_NONE) e[i] = 0;
-        const double* ph = A_hi + i * lda + k0;
-        const double* pl = A_lo + i * lda + k0;
-        if (VEC == 2 && k0 + 3 < K) {
-            double2 h0 = __ldg(reinterpret_cast<const double2*>(ph));
-            double2 h1 = __ldg(reinterpret_cast<const double2*>(ph + 2));
-            double2 l0 = __ldg(reinterpret_cast<const double2*>(pl));
-            double2 l1 = __ldg(reinterpret_cast<const double2*>(pl + 2));
-            hi[0] = h0.x; hi[1] = h0.y; hi[2] = h1.x; hi[3] = h1.y;
-            lo[0] = l0.x; lo[1] = l0.y; lo[2] = l1.x; lo[3] = l1.y;
-        } else {
+        if (active) {
+            const int64_t i = mt * TM + lane;
+            double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+            int ex = 0;
+            if (i < M) {
+                const int32_t er = e[i];
+                ex = effective_exponent(er);
+                if (blockIdx.x == 0 && w == 0 && er == EXP_NONE) e[i] = 0;
+                const double* ph = A_hi + i * lda + k0;
+                const double* pl = A_lo + i * lda + k0;
+                if (VEC == 2 && k0 + 3 < K) {
+                    double2 h0 = __ldg(reinterpret_cast<const double2*>(ph));
+                    double2 h1 = __ldg(reinterpret_cast<const double2*>(ph + 2));
+                    double2 l0 = __ldg(reinterpret_cast<const double2*>(pl));
+                    double2 l1 = __ldg(reinterpret_cast<const double2*>(pl + 2));
+                    hi[0] = h0.x; hi[1] = h0.y; hi[2] = h1.x; hi[3] = h1.y;
+                    lo[0] = l0.x; lo[1] = l0.y; lo[2] = l1.x; lo[3] = l1.y;
+                } else {
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (k0 + r < K) { hi[r] = __ldg(ph + r); lo[r] = __ldg(pl + r); }
+                    for (int r = 0; r < 4; ++r)
+                        if (k0 + r < K) { hi[r] = __ldg(ph + r); lo[r] = __ldg(pl + r); }
+                }
+            }
+            stage_parts(hi, lo, ex, dst);
         }
-    }
-    double d[4][S];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) split_digits(hi[r], lo[r], ex, d[r]);
-#pragma unroll
-    for (int s = 0; s < S; ++s) {
-        double2* dst = reinterpret_cast<double2*>(planes + plane_offset(mt, KC, k0, s, lane));
-        dst[0] = make_double2(d[0][s], d[1][s]);
-        dst[1] = make_double2(d[2][s], d[3][s]);
-    }
+        flush_stage(stage, planes + (mt * KC + kc0) * CHUNK_DOUBLES, chunks);
     }
 }
 
 // Columns of B (K x N row-major).  Block = 32 columns (lanes) x 8 groups of 4
-// consecutive k (warps), grid as split_rows_kernel; every load of a warp reads 32 consecutive columns of
-// one row.  Writes as split_rows_kernel, in B's plane layout.
-__global__ void __launch_bounds__(256) split_cols_kernel(const double* __restrict__ B_hi,
-                                                         const double* __restrict__ B_lo,
-                                                         int64_t ldb, int64_t K, int64_t N,
-                                                         int64_t Kp, int32_t* f,
-                                                         double* __restrict__ planes) {
+// consecutive k (warps), grid as split_rows_kernel; every load of a warp
+// reads 32 consecutive columns of one row.  Stages and writes as
+// split_rows_kernel, in B's plane layout.
+__global__ void __launch_bounds__(SPLIT_THREADS, 3) split_cols_kernel(const double* __restrict__ B_hi,
+                                                                   const double* __restrict__ B_lo,
+                                                                   int64_t ldb, int64_t K, int64_t N,
+                                                                   int64_t Kp, int32_t* f,
+                                                                   double* __restrict__ planes) {
+    extern __shared__ __align__(128) double stage[];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t k0 = (int64_t)blockIdx.x * 32 + 4 * w;
-    if (k0 >= Kp) return;
     const int64_t KC = Kp / BK;
+    const int64_t kc0 = (int64_t)blockIdx.x * SPLIT_CHUNKS;
+    const int chunks = (int)min((int64_t)SPLIT_CHUNKS, KC - kc0);
+    const int64_t k0 = kc0 * BK + 4 * w;
+    const bool active = (w >> 1) < chunks;
+    double* dst = stage + (((w >> 1) * S * (BK / 4) + (w & 1)) * TN + lane) * 4;
     const int64_t tiles = (N + TN - 1) / TN;
     for (int64_t nt = blockIdx.y; nt < tiles; nt += gridDim.y) {
-    const int64_t j = nt * TN + lane;
-    double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-    int ex = 0;
-    if (j < N) {
-        const int32_t fr = f[j];
-        ex = effective_exponent(fr);
-        if (blockIdx.x == 0 && w == 0 && fr == EXP_NONE) f[j] = 0;
+        if (active) {
+            const int64_t j = nt * TN + lane;
+            double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+            int ex = 0;
+            if (j < N) {
+                const int32_t fr = f[j];
+                ex = effective_exponent(fr);
+                if (blockIdx.x == 0 && w == 0 && fr == EXP_NONE) f[j] = 0;
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-            if (k0 + r < K) {
-                hi[r] = __ldg(B_hi + (k0 + r) * ldb + j);
-                lo[r] = __ldg(B_lo + (k0 + r) * ldb + j);
+                for (int r = 0; r < 4; ++r)
+                    if (k0 + r < K) {
+                        hi[r] = __ldg(B_hi + (k0 + r) * ldb + j);
+                        lo[r] = __ldg(B_lo + (k0 + r) * ldb + j);
+                    }
             }
-    }
-    double d[4][S];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) split_digits(hi[r], lo[r], ex, d[r]);
-#pragma unroll
-    for (int s = 0; s < S; ++s) {
-        double2* dst = reinterpret_cast<double2*>(planes + plane_offset(nt, KC, k0, s, lane));
-        dst[0] = make_double2(d[0][s], d[1][s]);
-        dst[1] = make_double2(d[2][s], d[3][s]);
-    }
+            stage_parts(hi, lo, ex, dst);
+        }
+        flush_stage(stage, planes + (nt * KC + kc0) * CHUNK_DOUBLES, chunks);
     }
 }
 
@@ -312,10 +347,18 @@ cudaError_t launch_split_rows(const double* A_hi, const double* A_lo, int64_t ld
                               int64_t K, int64_t Kp, int32_t* e, double* planes, cudaStream_t st) {
     const int64_t Mp = round_up(M, TM);
     if (Mp == 0 || Kp == 0) return cudaSuccess;
-    dim3 grid((unsigned)((Kp + 31) / 32), (unsigned)std::min<int64_t>(Mp / TM, 65535));
+    dim3 grid((unsigned)((Kp / BK + SPLIT_CHUNKS - 1) / SPLIT_CHUNKS), (unsigned)std::min<int64_t>(Mp / TM, 65535));
     const bool vec = ((uintptr_t)A_hi % 16 == 0) && ((uintptr_t)A_lo % 16 == 0) && (lda % 2 == 0);
-    if (vec) split_rows_kernel<2><<<grid, 256, 0, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
-    else split_rows_kernel<1><<<grid, 256, 0, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
+    cudaError_t err;
+    if (vec) {
+        err = cudaFuncSetAttribute(split_rows_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
+        if (err != cudaSuccess) return err;
+        split_rows_kernel<2><<<grid, SPLIT_THREADS, SPLIT_SMEM, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
+    } else {
+        err = cudaFuncSetAttribute(split_rows_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
+        if (err != cudaSuccess) return err;
+        split_rows_kernel<1><<<grid, SPLIT_THREADS, SPLIT_SMEM, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
+    }
     return cudaGetLastError();
 }
 
@@ -323,8 +366,10 @@ cudaError_t launch_split_cols(const double* B_hi, const double* B_lo, int64_t ld
                               int64_t N, int64_t Kp, int32_t* f, double* planes, cudaStream_t st) {
     const int64_t Np = round_up(N, TN);
     if (Np == 0 || Kp == 0) return cudaSuccess;
-    dim3 grid((unsigned)((Kp + 31) / 32), (unsigned)std::min<int64_t>(Np / TN, 65535));
-    split_cols_kernel<<<grid, 256, 0, st>>>(B_hi, B_lo, ldb, K, N, Kp, f, planes);
+    dim3 grid((unsigned)((Kp / BK + SPLIT_CHUNKS - 1) / SPLIT_CHUNKS), (unsigned)std::min<int64_t>(Np / TN, 65535));
+    cudaError_t err = cudaFuncSetAttribute(split_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
+    if (err != cudaSuccess) return err;
+    split_cols_kernel<<<grid, SPLIT_THREADS, SPLIT_SMEM, st>>>(B_hi, B_lo, ldb, K, N, Kp, f, planes);
     return cudaGetLastError();
 }
 

@@ -222,3 +222,50 @@ def test_identity_returns_truncated_parts():
 
 def test_no_wait_timeouts():
     assert ddg.wait_timeouts() == 0
+
+
+def test_extreme_scales_match_model():
+    # rows and columns scaled towards the ends of the exponent range: shared
+    # exponents near +-1000, products that land in the subnormal range and
+    # near the overflow threshold; the GPU must follow the model bit for bit
+    # (including the correctly rounded final scaling)
+    rng = np.random.default_rng(13)
+    M, N, K = 12, 10, 33
+    A_hi, A_lo, B_hi, B_lo = workloads.make_dd(M, N, K, "normal", 77)
+    ra = np.array([-600, -520, -300, 0, 300, 500, 900, -1000, 1000, 10, -10, 0])
+    cb = np.array([-500, -560, 100, 0, -300, 20, 100, 40, -1040, 0])
+    A_hi, A_lo = np.ldexp(A_hi, ra[:, None]), np.ldexp(A_lo, ra[:, None])
+    B_hi, B_lo = np.ldexp(B_hi, cb[None, :]), np.ldexp(B_lo, cb[None, :])
+    assert np.all(np.isfinite(A_lo)) and np.all(np.isfinite(B_lo))
+    C_hi, C_lo = ddg.dd_gemm(dev(A_hi), dev(A_lo), dev(B_hi), dev(B_lo))
+    M_hi, M_lo, *_ = slices.sliced_dd_gemm(A_hi, A_lo, B_hi, B_lo)
+    assert np.array_equal(host(C_hi).view(np.int64), M_hi.view(np.int64))
+    assert np.array_equal(host(C_lo).view(np.int64), M_lo.view(np.int64))
+    # entries whose scale stays in the normal range are within the bound of
+    # the exact product, entry by entry relative to |A||B|
+    R_hi, R_lo = oracle.exact_dd_gemm(A_hi, A_lo, B_hi, B_lo)
+    mag = np.abs(A_hi) @ np.abs(B_hi)
+    ok = (mag > 2.0**-900) & (mag < 2.0**900)
+    err = np.abs((host(C_hi) - R_hi) + (host(C_lo) - R_lo))
+    assert np.all(err[ok] <= 1e-28 * mag[ok])
+
+
+def test_many_row_tiles():
+    # more than 65535 row tiles (a grid-dimension limit the kernels must not
+    # inherit) and a ragged last tile
+    import torch
+    M, N, K = 65536 * 32 + 7, 40, 24
+    rng = np.random.default_rng(14)
+    A_hi = rng.uniform(-1, 1, (M, K))
+    A_lo = A_hi * 2.0**-54 * rng.uniform(-1, 1, (M, K))
+    s = A_hi + A_lo
+    A_lo = A_lo - (s - A_hi)
+    A_hi = s
+    _, _, B_hi, B_lo = workloads.make_dd(1, N, K, "uniform", 15)
+    C_hi, C_lo = ddg.dd_gemm(dev(A_hi), dev(A_lo), dev(B_hi), dev(B_lo))
+    rows = np.array([0, 1, 31, 32, M // 2, M - 33, M - 1])
+    G_hi = host(C_hi[torch.from_numpy(rows).cuda()])
+    G_lo = host(C_lo[torch.from_numpy(rows).cuda()])
+    M_hi, M_lo, *_ = slices.sliced_dd_gemm(A_hi[rows], A_lo[rows], B_hi, B_lo)
+    assert np.array_equal(G_hi.view(np.int64), M_hi.view(np.int64))
+    assert np.array_equal(G_lo.view(np.int64), M_lo.view(np.int64))
