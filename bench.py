@@ -52,9 +52,13 @@ FP64_NOMINAL_TF = 1.25
 BF16_NOMINAL_TF = 2250.0
 FALLBACK_BF16_TF = 1900.0
 FALLBACK_HBM_GBS = 6800.0
+IMAD_PER_CLK_SM = 64   # 32-bit integer multiply-add (also 32x32->64 wide) per clock per SM
+SM_COUNT = 152
+SM_MAX_GHZ = 2.07
 TRAFFIC_FILE = ROOT / "profiles" / "slice_gemm_kernel_dram_traffic.txt"
 KERNEL_SOURCES = ["extended_precision_gemm_gb300/csrc/slice_gemm.cu",
-                  "extended_precision_gemm_gb300/csrc/common.cuh", "include/ddgemm.h"]
+                  "extended_precision_gemm_gb300/csrc/common.cuh",
+                  "extended_precision_gemm_gb300/csrc/async_copy.cuh"]
 
 
 # ----------------------------------------------------------------------------
@@ -353,6 +357,47 @@ def run_ours(args, w):
     e2e_units, t_e2e = aggregate(dist, t_e2e, args.steps * w.dd_flops, dev)
     same = bool(torch.equal(h_C_hi, C_hi.cpu()) and torch.equal(h_C_lo, C_lo.cpu()))
 
+    # ---- the integer-pipe variant of the slice GEMM (same parts, exact int64 sums) ----
+    ws_i = torch.empty(ddg.workspace_size_i64(M, N, K), dtype=torch.uint8, device=dev)
+    I_hi = torch.empty_like(C_hi)
+    I_lo = torch.empty_like(C_lo)
+
+    def step_i64():
+        ddg.dd_gemm_i64(dA_hi, dA_lo, dB_hi, dB_lo, I_hi, I_lo, workspace=ws_i, stream=stream)
+
+    for _ in range(args.warmup):
+        step_i64()
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step_i64()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    units_i, t_i = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    same_i = bool(torch.equal(I_hi, C_hi) and torch.equal(I_lo, C_lo))
+    splits_i = ddg.layout_i64(M, N, K)
+    pA16 = torch.empty(8 * Mp * Kp, dtype=torch.int16, device=dev)
+    pB16 = torch.empty(8 * Np * Kp, dtype=torch.int16, device=dev)
+    Pi = torch.empty((splits_i, 8, Mp, Np), dtype=torch.float64, device=dev)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        ddg.split_rows_i16(dA_hi, dA_lo, pA16, e_buf, stream=stream)
+        ddg.split_cols_i16(dB_hi, dB_lo, pB16, f_buf, stream=stream)
+        evs[i][1].record(stream)
+        ddg.slice_gemm_i64(M, N, K, pA16, pB16, splits_i, Pi, stream=stream)
+        evs[i][2].record(stream)
+        ddg.recombine(M, N, Pi, e_buf, f_buf, splits_i, I_hi, I_lo, stream=stream)
+        evs[i][3].record(stream)
+    torch.cuda.synchronize(dev)
+    ti_split = allreduce_max(dist, sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1e3, dev)
+    ti_gemm = allreduce_max(dist, sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1e3, dev)
+    ti_recomb = allreduce_max(dist, sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1e3, dev)
+    del ws_i, pA16, pB16, Pi
+    assert ddg.wait_timeouts() == 0
+
     if rank != 0:
         return None
 
@@ -398,6 +443,20 @@ def run_ours(args, w):
         "accuracy": {"normwise_vs_exact_oracle": normwise, "rows_checked": len(rows), "bound": 1e-26},
         "gpu_launches": 7 * args.steps,
         "clocks": clock_info,
+        "int_pipe_variant": {
+            "what": "same 13-bit parts and 36 pairs; products as IMAD.WIDE (32x32->64) into exact int64 "
+                    "sums; C identical bit for bit to the FP64 tensor-pipe path",
+            "value": units_i / t_i / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_i / args.steps,
+            "identical_to_fp64_path": same_i, "k_splits": splits_i,
+            "roofline": {"bound": "alu", "kernel": "slice_gemm_i64_kernel (mad.wide.s32)",
+                         "achieved": PAIRS * M * N * K / ti_gemm / 1e12,
+                         "peak": IMAD_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3, "unit": "Tops/s",
+                         "frac": (PAIRS * M * N * K / ti_gemm / 1e12) / (IMAD_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3),
+                         "peak_source": f"{IMAD_PER_CLK_SM} int32 multiply-adds/clk/SM x {SM_COUNT} SMs x "
+                                        f"{SM_MAX_GHZ} GHz", "ms_per_launch": 1e3 * ti_gemm,
+                         "ops_per_launch": PAIRS * M * N * K},
+            "ms_split_int16": 1e3 * ti_split, "ms_recombine": 1e3 * ti_recomb,
+        },
     }
 
 

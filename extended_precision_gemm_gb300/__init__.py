@@ -26,6 +26,7 @@ __all__ = [
     "load", "library_path", "exported_symbols",
     "dd_gemm", "dd_gemm_ws", "dd_gemm_host", "dd_gemm_noalloc", "layout", "workspace_size",
     "split_rows", "split_cols", "slice_gemm", "recombine", "wait_timeouts", "fp64_tensor_roof",
+    "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
 ]
 
 SLICES = 8
@@ -63,6 +64,13 @@ _SIGNATURES = {
     "dd_wait_timeouts": ([_ptr], _int),
     "dd_fp64_tensor_roof": ([_ptr, _ptr], _int),
     "dd_gemm_noalloc": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
+    "dd_gemm_i64_layout": ([_i64, _i64, _i64, _ptr], _int),
+    "dd_gemm_i64_workspace_size": ([_i64, _i64, _i64, _ptr], _int),
+    "dd_gemm_i64": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64,
+                     _ptr, ctypes.c_size_t, _ptr], _int),
+    "dd_split_rows_i16": ([_i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr], _int),
+    "dd_split_cols_i16": ([_i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr], _int),
+    "dd_slice_gemm_i64": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
 }
 
 
@@ -291,3 +299,79 @@ def fp64_tensor_roof(stream=None) -> float:
     t = ctypes.c_double()
     _check("dd_fp64_tensor_roof", load().dd_fp64_tensor_roof(ctypes.byref(t), _stream_handle(stream)))
     return t.value
+
+
+# ---- integer-pipe variant of the slice-pair GEMM ----
+
+def layout_i64(M: int, N: int, K: int) -> int:
+    """k-split the integer-pipe slice GEMM uses for this shape."""
+    sp = _int()
+    _check("dd_gemm_i64_layout", load().dd_gemm_i64_layout(M, N, K, ctypes.byref(sp)))
+    return sp.value
+
+
+def workspace_size_i64(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check("dd_gemm_i64_workspace_size", load().dd_gemm_i64_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def dd_gemm_i64(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, workspace=None, stream=None):
+    """The product with the slice-pair GEMM on the integer pipe (int16 parts,
+    exact int64 sums); identical results to dd_gemm.  `workspace` (uint8
+    tensor of workspace_size_i64 bytes) is optional."""
+    M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("dd_gemm_i64", load().dd_gemm_i64(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                             B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                             C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi), wp, wn,
+                                             _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def split_rows_i16(A_hi, A_lo, planes=None, e=None, stream=None):
+    """Step 1a for the integer pipe: (int16 planes, e)."""
+    torch = _torch()
+    _mat(A_hi, "A_hi"), _mat(A_lo, "A_lo")
+    M, K = A_hi.shape
+    Mp, Kp = -(-M // TILE_M) * TILE_M, -(-K // CHUNK_K) * CHUNK_K
+    if planes is None:
+        planes = torch.empty(SLICES * Mp * Kp, dtype=torch.int16, device=A_hi.device)
+    if e is None:
+        e = torch.empty(M, dtype=torch.int32, device=A_hi.device)
+    if planes.numel() < SLICES * Mp * Kp or e.numel() < M:
+        raise ValueError("output buffers too small")
+    _check("dd_split_rows_i16", load().dd_split_rows_i16(M, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                                         planes.data_ptr(), e.data_ptr(), _stream_handle(stream)))
+    return planes, e
+
+
+def split_cols_i16(B_hi, B_lo, planes=None, f=None, stream=None):
+    """Step 1b for the integer pipe: (int16 planes, f)."""
+    torch = _torch()
+    _mat(B_hi, "B_hi"), _mat(B_lo, "B_lo")
+    K, N = B_hi.shape
+    Np, Kp = -(-N // TILE_N) * TILE_N, -(-K // CHUNK_K) * CHUNK_K
+    if planes is None:
+        planes = torch.empty(SLICES * Np * Kp, dtype=torch.int16, device=B_hi.device)
+    if f is None:
+        f = torch.empty(N, dtype=torch.int32, device=B_hi.device)
+    if planes.numel() < SLICES * Np * Kp or f.numel() < N:
+        raise ValueError("output buffers too small")
+    _check("dd_split_cols_i16", load().dd_split_cols_i16(K, N, B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                                         planes.data_ptr(), f.data_ptr(), _stream_handle(stream)))
+    return planes, f
+
+
+def slice_gemm_i64(M: int, N: int, K: int, planesA, planesB, splits: int, P=None, stream=None):
+    """Step 2 on the integer pipe: P (splits x 8 x Mp x Np doubles)."""
+    torch = _torch()
+    Mp, Np = -(-M // TILE_M) * TILE_M, -(-N // TILE_N) * TILE_N
+    if P is None:
+        P = torch.empty((splits, SLICES, Mp, Np), dtype=torch.float64, device=planesA.device)
+    if P.numel() < splits * SLICES * Mp * Np:
+        raise ValueError("output buffer too small")
+    _check("dd_slice_gemm_i64", load().dd_slice_gemm_i64(M, N, K, planesA.data_ptr(), planesB.data_ptr(), splits,
+                                                         P.data_ptr(), _stream_handle(stream)))
+    return P

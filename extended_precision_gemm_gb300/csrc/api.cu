@@ -33,13 +33,18 @@ int device_sms() {
     return sms;
 }
 
+// Which slice GEMM a layout is for: FP64 parts for mma.sync f64, or int16
+// parts for the integer pipe.
+enum class Engine { kFp64Tensor, kInt64Pipe };
+
 // k-split of the slice GEMM: the smallest split count whose waves of blocks
 // fill the GPU best (tiles * splits over whole waves of resident blocks),
 // keeping at least 4 k-chunks per split.
-int choose_splits(int64_t Mp, int64_t Np, int64_t KC) {
+int choose_splits(int64_t Mp, int64_t Np, int64_t KC, Engine eng) {
     const int64_t tiles = (Mp / TM) * (Np / TN);
     if (tiles == 0 || KC <= 1) return 1;
-    const int64_t slots = (int64_t)device_sms() * slice_gemm_ctas_per_sm();
+    const int per_sm = eng == Engine::kFp64Tensor ? slice_gemm_ctas_per_sm() : slice_gemm_i64_ctas_per_sm();
+    const int64_t slots = (int64_t)device_sms() * per_sm;
     int best = 1;
     double best_score = -1.0;
     const int64_t max_s = std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, KC / 4));
@@ -53,19 +58,20 @@ int choose_splits(int64_t Mp, int64_t Np, int64_t KC) {
     return best;
 }
 
-Layout make_layout(int64_t M, int64_t N, int64_t K) {
+Layout make_layout(int64_t M, int64_t N, int64_t K, Engine eng = Engine::kFp64Tensor) {
     Layout L;
     L.Mp = round_up(M, TM);
     L.Np = round_up(N, TN);
     L.Kp = round_up(K, BK);
     L.KC = L.Kp / BK;
-    L.splits = choose_splits(L.Mp, L.Np, L.KC);
+    L.splits = choose_splits(L.Mp, L.Np, L.KC, eng);
+    const int64_t part_bytes = eng == Engine::kFp64Tensor ? 8 : 2;
     int64_t off = 0;
     auto take = [&](int64_t bytes) { int64_t o = off; off = round_up(off + bytes, kAlign); return o; };
     L.off_e = take(L.Mp * 4);
     L.off_f = take(L.Np * 4);
-    L.off_A = take(S * L.Mp * L.Kp * 8);
-    L.off_B = take(S * L.Np * L.Kp * 8);
+    L.off_A = take(S * L.Mp * L.Kp * part_bytes);
+    L.off_B = take(S * L.Np * L.Kp * part_bytes);
     L.off_P = take((int64_t)L.splits * S * L.Mp * L.Np * 8);
     L.total = off;
     return L;
@@ -138,6 +144,27 @@ ddgemm_status run_gemm(const Layout& L, int64_t M, int64_t N, int64_t K, const d
     DDG_TRY(launch_split_rows(A_hi, A_lo, lda, M, K, L.Kp, e, pA, st));
     DDG_TRY(launch_split_cols(B_hi, B_lo, ldb, K, N, L.Kp, f, pB, st));
     DDG_TRY(launch_slice_gemm(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_TRY(launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
+    return DDGEMM_OK;
+}
+
+// The launch sequence of the integer-pipe variant (int16 parts, int64 sums).
+ddgemm_status run_gemm_i64(const Layout& L, int64_t M, int64_t N, int64_t K, const double* A_hi,
+                           const double* A_lo, int64_t lda, const double* B_hi, const double* B_lo,
+                           int64_t ldb, double* C_hi, double* C_lo, int64_t ldc, char* ws,
+                           cudaStream_t st) {
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    int32_t* e = reinterpret_cast<int32_t*>(ws + L.off_e);
+    int32_t* f = reinterpret_cast<int32_t*>(ws + L.off_f);
+    int16_t* pA = reinterpret_cast<int16_t*>(ws + L.off_A);
+    int16_t* pB = reinterpret_cast<int16_t*>(ws + L.off_B);
+    double* P = reinterpret_cast<double*>(ws + L.off_P);
+    DDG_TRY(launch_init_exponents(e, M, f, N, K, st));
+    DDG_TRY(launch_row_exponents(A_hi, lda, M, K, e, st));
+    DDG_TRY(launch_col_exponents(B_hi, ldb, K, N, f, st));
+    DDG_TRY(launch_split_rows_i16(A_hi, A_lo, lda, M, K, L.Kp, e, pA, st));
+    DDG_TRY(launch_split_cols_i16(B_hi, B_lo, ldb, K, N, L.Kp, f, pB, st));
+    DDG_TRY(launch_slice_gemm_i64(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
     DDG_TRY(launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
     return DDGEMM_OK;
 }
@@ -335,7 +362,102 @@ ddgemm_status dd_fp64_tensor_roof(double* tflops, void* stream) {
 
 ddgemm_status dd_wait_timeouts(unsigned int* count) {
     if (count == nullptr) return DDGEMM_ERR_INVALID_ARG;
-    return from_cuda(read_and_reset_wait_timeouts(count));
+    unsigned int a = 0, b = 0;
+    ddgemm_status s = from_cuda(read_and_reset_wait_timeouts(&a));
+    if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_i64(&b));
+    *count = a + b;
+    return s;
+}
+
+// ---- integer-pipe variant ----
+
+ddgemm_status dd_gemm_i64_layout(int64_t M, int64_t N, int64_t K, int* splits) {
+    if (M < 0 || N < 0 || K < 0 || splits == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    *splits = make_layout(M, N, K, Engine::kInt64Pipe).splits;
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_gemm_i64_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    if (bytes == nullptr || M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    *bytes = (size_t)make_layout(M, N, K, Engine::kInt64Pipe).total;
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_gemm_i64(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                          int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb, double* C_hi,
+                          double* C_lo, int64_t ldc, void* workspace, size_t workspace_bytes, void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Layout L = make_layout(M, N, K, Engine::kInt64Pipe);
+    const int64_t c = span_bytes(M, N, ldc);
+    if (workspace != nullptr) {
+        if ((uintptr_t)workspace % kAlign != 0 || workspace_bytes < (size_t)L.total) return DDGEMM_ERR_INVALID_ARG;
+        if (ranges_overlap(workspace, L.total, C_hi, c) || ranges_overlap(workspace, L.total, C_lo, c))
+            return DDGEMM_ERR_INVALID_ARG;
+        return run_gemm_i64(L, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc,
+                            static_cast<char*>(workspace), st);
+    }
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    s = run_gemm_i64(L, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc, static_cast<char*>(ws), st);
+    cudaError_t fe = cudaFreeAsync(ws, st);
+    if (s == DDGEMM_OK && fe != cudaSuccess) s = DDGEMM_ERR_CUDA;
+    return s;
+}
+
+ddgemm_status dd_split_rows_i16(int64_t M, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
+                                int16_t* planes, int32_t* e, void* stream) {
+    if (M < 0 || K < 0 || lda < std::max<int64_t>(1, K)) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (M == 0) return DDGEMM_OK;
+    if (e == nullptr || (K > 0 && (A_hi == nullptr || A_lo == nullptr || planes == nullptr)))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planes % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t Kp = round_up(K, BK);
+    DDG_TRY(launch_init_exponents(e, M, nullptr, 0, K, st));
+    DDG_TRY(launch_row_exponents(A_hi, lda, M, K, e, st));
+    DDG_TRY(launch_split_rows_i16(A_hi, A_lo, lda, M, K, Kp, e, planes, st));
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_split_cols_i16(int64_t K, int64_t N, const double* B_hi, const double* B_lo, int64_t ldb,
+                                int16_t* planes, int32_t* f, void* stream) {
+    if (N < 0 || K < 0 || ldb < std::max<int64_t>(1, N)) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (N == 0) return DDGEMM_OK;
+    if (f == nullptr || (K > 0 && (B_hi == nullptr || B_lo == nullptr || planes == nullptr)))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planes % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t Kp = round_up(K, BK);
+    DDG_TRY(launch_init_exponents(nullptr, 0, f, N, K, st));
+    DDG_TRY(launch_col_exponents(B_hi, ldb, K, N, f, st));
+    DDG_TRY(launch_split_cols_i16(B_hi, B_lo, ldb, K, N, Kp, f, planes, st));
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_slice_gemm_i64(int64_t M, int64_t N, int64_t K, const int16_t* planesA,
+                                const int16_t* planesB, int splits, double* P, void* stream) {
+    ddgemm_status s = check_shapes(M, N, K, std::max<int64_t>(1, K), std::max<int64_t>(1, N),
+                                   std::max<int64_t>(1, N));
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    const int64_t Mp = round_up(M, TM), Np = round_up(N, TN), Kp = round_up(K, BK), KC = Kp / BK;
+    if (splits < 1 || splits > kMaxSplits || (KC > 0 && splits > KC) || (KC == 0 && splits != 1))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (P == nullptr || (K > 0 && (planesA == nullptr || planesB == nullptr))) return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0 || (uintptr_t)P % 16 != 0)
+        return DDGEMM_ERR_INVALID_ARG;
+    return from_cuda(launch_slice_gemm_i64(planesA, planesB, Mp, Np, Kp, splits, P,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -19,10 +19,23 @@ cudaError_t launch_split_rows(const double* A_hi, const double* A_lo, int64_t ld
 cudaError_t launch_split_cols(const double* B_hi, const double* B_lo, int64_t ldb, int64_t K,
                               int64_t N, int64_t Kp, int32_t* f, double* planes, cudaStream_t st);
 
+// Step 1, int16 parts for the integer-pipe slice GEMM (layout
+// [tile][k-chunk][k in chunk][row in tile][part]).
+cudaError_t launch_split_rows_i16(const double* A_hi, const double* A_lo, int64_t lda, int64_t M,
+                                  int64_t K, int64_t Kp, int32_t* e, int16_t* planes, cudaStream_t st);
+cudaError_t launch_split_cols_i16(const double* B_hi, const double* B_lo, int64_t ldb, int64_t K,
+                                  int64_t N, int64_t Kp, int32_t* f, int16_t* planes, cudaStream_t st);
+
 // Step 2: slice-pair GEMM into `splits` partial sets of 8 planes Mp x Np.
 cudaError_t launch_slice_gemm(const double* planesA, const double* planesB, int64_t Mp,
                               int64_t Np, int64_t Kp, int splits, double* P, cudaStream_t st);
 int slice_gemm_ctas_per_sm();
+
+// Step 2 on the integer pipe: the same P from int16 parts, exact int64 sums.
+cudaError_t launch_slice_gemm_i64(const int16_t* planesA, const int16_t* planesB, int64_t Mp,
+                                  int64_t Np, int64_t Kp, int splits, double* P, cudaStream_t st);
+int slice_gemm_i64_ctas_per_sm();
+cudaError_t read_and_reset_wait_timeouts_i64(unsigned int* count);
 
 // Step 3: recombination of the (split) planes into C = C_hi + C_lo.
 cudaError_t launch_recombine(const double* P, int splits, int64_t Mp, int64_t Np,

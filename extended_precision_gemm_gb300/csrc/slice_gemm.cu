@@ -27,6 +27,7 @@
 // itself in a device counter (see dd_wait_timeouts) and stops.
 #include <algorithm>
 
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 
@@ -45,72 +46,13 @@ static_assert(COPY_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 __device__ unsigned int g_wait_timeouts = 0;
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ unsigned long long global_timer_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n"
-        " .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Wait for phase `parity` of the barrier to complete, for at most `budget` ns.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  unsigned long long budget) {
-    for (int i = 0; i < 32; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > budget) return false;
-    }
-}
-
 // Post the expected byte count on the stage barrier and start the two bulk
 // copies (A block, B block) that complete it.
 __device__ __forceinline__ void issue_stage(uint32_t bar, double* dst, const double* srcA,
                                             const double* srcB) {
-    asm volatile(
-        "{\n"
-        " .reg .b64 st;\n"
-        " mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n"
-        "}\n" ::"r"(bar),
-        "r"(2u * COPY_BYTES)
-        : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(srcA), "r"(COPY_BYTES), "r"(bar)
-        : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst + CHUNK_DOUBLES)),
-        "l"(srcB), "r"(COPY_BYTES), "r"(bar)
-        : "memory");
+    mbar_expect_tx(bar, 2u * COPY_BYTES);
+    bulk_load(dst, srcA, COPY_BYTES, bar);
+    bulk_load(dst + CHUNK_DOUBLES, srcB, COPY_BYTES, bar);
 }
 
 __device__ __forceinline__ void dmma(double& c0, double& c1, double a, double b) {

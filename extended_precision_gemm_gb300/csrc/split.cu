@@ -45,7 +45,20 @@ __global__ void __launch_bounds__(256) row_exponents_kernel(const double* __rest
     const double* p = A_hi + row * lda;
     uint64_t m = 0;
     if (VEC == 2) {
-        for (int64_t k = k0 + 2 * lane; k < k1; k += 64) {
+        // four independent 128-bit loads in flight per lane
+        uint64_t m1 = 0, m2 = 0, m3 = 0;
+        int64_t k = k0 + 2 * lane;
+        for (; k + 193 < k1; k += 256) {
+            const double2 v0 = __ldg(reinterpret_cast<const double2*>(p + k));
+            const double2 v1 = __ldg(reinterpret_cast<const double2*>(p + k + 64));
+            const double2 v2 = __ldg(reinterpret_cast<const double2*>(p + k + 128));
+            const double2 v3 = __ldg(reinterpret_cast<const double2*>(p + k + 192));
+            m = max(m, max(abs_bits(v0.x), abs_bits(v0.y)));
+            m1 = max(m1, max(abs_bits(v1.x), abs_bits(v1.y)));
+            m2 = max(m2, max(abs_bits(v2.x), abs_bits(v2.y)));
+            m3 = max(m3, max(abs_bits(v3.x), abs_bits(v3.y)));
+        }
+        for (; k < k1; k += 64) {
             if (k + 1 < k1) {
                 double2 v = __ldg(reinterpret_cast<const double2*>(p + k));
                 m = max(m, max(abs_bits(v.x), abs_bits(v.y)));
@@ -53,6 +66,7 @@ __global__ void __launch_bounds__(256) row_exponents_kernel(const double* __rest
                 m = max(m, abs_bits(__ldg(p + k)));
             }
         }
+        m = max(max(m, m1), max(m2, m3));
     } else {
         for (int64_t k = k0 + lane; k < k1; k += 32) m = max(m, abs_bits(__ldg(p + k)));
     }
@@ -73,11 +87,15 @@ __global__ void __launch_bounds__(128) col_exponents_kernel(const double* __rest
     const double* p = B_hi + col;
     uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
     int64_t k = k0;
-    for (; k + 3 < k1; k += 4) {
-        m0 = max(m0, abs_bits(__ldg(p + (k + 0) * ldb)));
-        m1 = max(m1, abs_bits(__ldg(p + (k + 1) * ldb)));
-        m2 = max(m2, abs_bits(__ldg(p + (k + 2) * ldb)));
-        m3 = max(m3, abs_bits(__ldg(p + (k + 3) * ldb)));
+    for (; k + 7 < k1; k += 8) {  // eight loads in flight per thread
+        const double x0 = __ldg(p + (k + 0) * ldb), x1 = __ldg(p + (k + 1) * ldb);
+        const double x2 = __ldg(p + (k + 2) * ldb), x3 = __ldg(p + (k + 3) * ldb);
+        const double x4 = __ldg(p + (k + 4) * ldb), x5 = __ldg(p + (k + 5) * ldb);
+        const double x6 = __ldg(p + (k + 6) * ldb), x7 = __ldg(p + (k + 7) * ldb);
+        m0 = max(m0, max(abs_bits(x0), abs_bits(x4)));
+        m1 = max(m1, max(abs_bits(x1), abs_bits(x5)));
+        m2 = max(m2, max(abs_bits(x2), abs_bits(x6)));
+        m3 = max(m3, max(abs_bits(x3), abs_bits(x7)));
     }
     for (; k < k1; ++k) m0 = max(m0, abs_bits(__ldg(p + k * ldb)));
     uint64_t m = max(max(m0, m1), max(m2, m3));
@@ -131,7 +149,8 @@ __device__ __forceinline__ bool scaled_frac_zero(uint64_t m, int sh) {
     return (m & ((1ULL << (-sh)) - 1)) == 0;
 }
 
-__device__ __forceinline__ void split_digits(double hi, double lo, int e, double out[S]) {
+// X = floor(|hi + lo| * 2^(104 - e)) and the sign of the element.
+__device__ __forceinline__ unsigned __int128 fixed_point(double hi, double lo, int e, uint64_t& sign_out) {
     uint64_t hb = (uint64_t)__double_as_longlong(hi);
     uint64_t lb = (uint64_t)__double_as_longlong(lo);
     if ((hb & ABS_MASK) == 0) { hb = lb; lb = 0; }  // hi = 0: the element is lo alone
@@ -153,11 +172,35 @@ __device__ __forceinline__ void split_digits(double hi, double lo, int e, double
             }
         }
     }
+    sign_out = sign;
+    return X;
+}
+
+// 13-bit field s of X, most significant first.
+__device__ __forceinline__ uint32_t digit_field(unsigned __int128 X, int s) {
+    return (uint32_t)(X >> (DIGIT * (S - 1 - s))) & ((1u << DIGIT) - 1);
+}
+
+// The 8 parts as doubles (exact small integers).
+__device__ __forceinline__ void split_digits(double hi, double lo, int e, double out[S]) {
+    uint64_t sign;
+    const unsigned __int128 X = fixed_point(hi, lo, e, sign);
 #pragma unroll
-    for (int s = 0; s < S; ++s) {
-        uint32_t v = (uint32_t)(X >> (DIGIT * (S - 1 - s))) & ((1u << DIGIT) - 1);
-        out[s] = small_int_to_double(v, sign);
+    for (int s = 0; s < S; ++s) out[s] = small_int_to_double(digit_field(X, s), sign);
+}
+
+// The 8 parts as int16, packed two per 32-bit word (part 2j in the low half).
+__device__ __forceinline__ uint4 split_digits_i16(double hi, double lo, int e) {
+    uint64_t sign;
+    const unsigned __int128 X = fixed_point(hi, lo, e, sign);
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t d0 = digit_field(X, 2 * j), d1 = digit_field(X, 2 * j + 1);
+        if (sign) { d0 = (uint32_t)(-(int32_t)d0); d1 = (uint32_t)(-(int32_t)d1); }
+        w[j] = (d0 & 0xFFFFu) | (d1 << 16);
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Each split block covers one 32-row (A) or 32-column (B) tile and 32
@@ -294,6 +337,88 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 3) split_cols_kernel(const doub
     }
 }
 
+// ---------------------------------------------------------------------------
+// Part planes as int16 for the integer-pipe slice GEMM.  Layout
+// [tile][k-chunk][k in chunk][row in tile][part]: the 8 parts of one element
+// are 16 contiguous bytes, so one 128-bit load brings all of them.  A warp
+// (32 rows or columns of a tile, one k) writes 512 contiguous bytes.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int64_t i16_offset(int64_t tile, int64_t KC, int64_t k, int ti) {
+    return (((tile * KC + k / BK) * BK + k % BK) * TM + ti) * S;
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(256, 4) split_rows_i16_kernel(const double* __restrict__ A_hi,
+                                                              const double* __restrict__ A_lo,
+                                                              int64_t lda, int64_t M, int64_t K,
+                                                              int64_t Kp, int32_t* e,
+                                                              int16_t* __restrict__ planes) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t k0 = (int64_t)blockIdx.x * 32 + 4 * w;
+    if (k0 >= Kp) return;
+    const int64_t KC = Kp / BK;
+    const int64_t tiles = (M + TM - 1) / TM;
+    for (int64_t mt = blockIdx.y; mt < tiles; mt += gridDim.y) {
+        const int64_t i = mt * TM + lane;
+        double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+        int ex = 0;
+        if (i < M) {
+            const int32_t er = e[i];
+            ex = effective_exponent(er);
+            if (blockIdx.x == 0 && w == 0 && er == EXP_NONE) e[i] = 0;
+            const double* ph = A_hi + i * lda + k0;
+            const double* pl = A_lo + i * lda + k0;
+            if (VEC == 2 && k0 + 3 < K) {
+                double2 h0 = __ldg(reinterpret_cast<const double2*>(ph));
+                double2 h1 = __ldg(reinterpret_cast<const double2*>(ph + 2));
+                double2 l0 = __ldg(reinterpret_cast<const double2*>(pl));
+                double2 l1 = __ldg(reinterpret_cast<const double2*>(pl + 2));
+                hi[0] = h0.x; hi[1] = h0.y; hi[2] = h1.x; hi[3] = h1.y;
+                lo[0] = l0.x; lo[1] = l0.y; lo[2] = l1.x; lo[3] = l1.y;
+            } else {
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (k0 + r < K) { hi[r] = __ldg(ph + r); lo[r] = __ldg(pl + r); }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<uint4*>(planes + i16_offset(mt, KC, k0 + r, lane)) = split_digits_i16(hi[r], lo[r], ex);
+    }
+}
+
+__global__ void __launch_bounds__(256, 4) split_cols_i16_kernel(const double* __restrict__ B_hi,
+                                                              const double* __restrict__ B_lo,
+                                                              int64_t ldb, int64_t K, int64_t N,
+                                                              int64_t Kp, int32_t* f,
+                                                              int16_t* __restrict__ planes) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t k0 = (int64_t)blockIdx.x * 32 + 4 * w;
+    if (k0 >= Kp) return;
+    const int64_t KC = Kp / BK;
+    const int64_t tiles = (N + TN - 1) / TN;
+    for (int64_t nt = blockIdx.y; nt < tiles; nt += gridDim.y) {
+        const int64_t j = nt * TN + lane;
+        double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+        int ex = 0;
+        if (j < N) {
+            const int32_t fr = f[j];
+            ex = effective_exponent(fr);
+            if (blockIdx.x == 0 && w == 0 && fr == EXP_NONE) f[j] = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (k0 + r < K) {
+                    hi[r] = __ldg(B_hi + (k0 + r) * ldb + j);
+                    lo[r] = __ldg(B_lo + (k0 + r) * ldb + j);
+                }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<uint4*>(planes + i16_offset(nt, KC, k0 + r, lane)) = split_digits_i16(hi[r], lo[r], ex);
+    }
+}
+
 int num_sms() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 152;
@@ -303,6 +428,26 @@ int num_sms() {
 }
 
 }  // namespace
+
+cudaError_t launch_split_rows_i16(const double* A_hi, const double* A_lo, int64_t lda, int64_t M,
+                                  int64_t K, int64_t Kp, int32_t* e, int16_t* planes, cudaStream_t st) {
+    const int64_t Mp = round_up(M, TM);
+    if (Mp == 0 || Kp == 0) return cudaSuccess;
+    dim3 grid((unsigned)((Kp + 31) / 32), (unsigned)std::min<int64_t>(Mp / TM, 65535));
+    const bool vec = ((uintptr_t)A_hi % 16 == 0) && ((uintptr_t)A_lo % 16 == 0) && (lda % 2 == 0);
+    if (vec) split_rows_i16_kernel<2><<<grid, 256, 0, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
+    else split_rows_i16_kernel<1><<<grid, 256, 0, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_cols_i16(const double* B_hi, const double* B_lo, int64_t ldb, int64_t K,
+                                  int64_t N, int64_t Kp, int32_t* f, int16_t* planes, cudaStream_t st) {
+    const int64_t Np = round_up(N, TN);
+    if (Np == 0 || Kp == 0) return cudaSuccess;
+    dim3 grid((unsigned)((Kp + 31) / 32), (unsigned)std::min<int64_t>(Np / TN, 65535));
+    split_cols_i16_kernel<<<grid, 256, 0, st>>>(B_hi, B_lo, ldb, K, N, Kp, f, planes);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_init_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int64_t K,
                                   cudaStream_t st) {

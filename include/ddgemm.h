@@ -207,6 +207,56 @@ ddgemm_status dd_recombine(int64_t M, int64_t N, const double* P, int splits,
                            double* C_hi, double* C_lo, int64_t ldc, void* stream);
 
 /* ------------------------------------------------------------------ */
+/* Integer-pipe variant of the slice-pair GEMM                          */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The same product, with the slice-pair GEMM (step 2) on the integer pipe:
+ * the 13-bit parts are stored as int16 and every pair product is a
+ * 32 x 32 -> 64-bit integer multiply-add into an exact int64 sum.  The paper
+ * runs these products on FP64 tensor cores because they are exact there
+ * (eq. (5)); on GB300 the FP64 pipe, which also executes mma.sync f64, is the
+ * narrowest unit, while the exactness needs only integer arithmetic.  The
+ * part sums P_d are the same integers, so C is identical bit for bit to
+ * dd_gemm's.
+ *
+ * dd_gemm_i64: as dd_gemm_ws; `workspace` may be NULL, in which case it is
+ * taken from the stream-ordered allocator (DDGEMM_ERR_ALLOC on failure).
+ * dd_gemm_i64_workspace_size / dd_gemm_i64_layout: its workspace bytes and
+ * automatic k-split for this shape on the current device.
+ */
+ddgemm_status dd_gemm_i64_layout(int64_t M, int64_t N, int64_t K, int* splits);
+ddgemm_status dd_gemm_i64_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+ddgemm_status dd_gemm_i64(int64_t M, int64_t N, int64_t K,
+                          const double* A_hi, const double* A_lo, int64_t lda,
+                          const double* B_hi, const double* B_lo, int64_t ldb,
+                          double* C_hi, double* C_lo, int64_t ldc,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Step 1 for the integer pipe: exponents e (f) exactly as dd_split_rows
+ * (dd_split_cols), parts as int16 in the layout
+ *   planes[((((tile * KC + kc) * 8 + kk) * 32 + ti) * 8) + s]
+ * holding D_s of element (row or column tile * 32 + ti, k = kc * 8 + kk)
+ * (8 * Mp * Kp int16 for A, 8 * Np * Kp for B; 0 outside the matrix).
+ */
+ddgemm_status dd_split_rows_i16(int64_t M, int64_t K,
+                                const double* A_hi, const double* A_lo, int64_t lda,
+                                int16_t* planes, int32_t* e, void* stream);
+ddgemm_status dd_split_cols_i16(int64_t K, int64_t N,
+                                const double* B_hi, const double* B_lo, int64_t ldb,
+                                int16_t* planes, int32_t* f, void* stream);
+
+/*
+ * Step 2 on the integer pipe: P exactly as dd_slice_gemm (splits x 8 x Mp x
+ * Np doubles holding the int64 sums, which are below 2^53), from the int16
+ * part planes of dd_split_rows_i16 / dd_split_cols_i16.
+ */
+ddgemm_status dd_slice_gemm_i64(int64_t M, int64_t N, int64_t K,
+                                const int16_t* planesA, const int16_t* planesB,
+                                int splits, double* P, void* stream);
+
+/* ------------------------------------------------------------------ */
 /* Diagnostics                                                          */
 /* ------------------------------------------------------------------ */
 
@@ -219,8 +269,8 @@ ddgemm_status dd_recombine(int64_t M, int64_t N, const double* P, int splits,
 ddgemm_status dd_fp64_tensor_roof(double* tflops, void* stream);
 
 /*
- * Number of times a slice-GEMM thread block gave up waiting for its operand
- * copies on the current device (each wait is bounded in time; a block that
+ * Number of times a slice-GEMM thread block (either variant) gave up waiting
+ * for its operand copies on the current device (each wait is bounded in time; a block that
  * gives up stops early and its P tile is incomplete).  Synchronises the
  * device, reads the counter and resets it to 0.  Zero in normal operation.
  */
