@@ -27,6 +27,7 @@ __all__ = [
     "dd_gemm", "dd_gemm_ws", "dd_gemm_host", "dd_gemm_noalloc", "layout", "workspace_size",
     "split_rows", "split_cols", "slice_gemm", "recombine", "wait_timeouts", "fp64_tensor_roof",
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
+    "split", "split_i16",
 ]
 
 SLICES = 8
@@ -71,6 +72,8 @@ _SIGNATURES = {
     "dd_split_rows_i16": ([_i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr], _int),
     "dd_split_cols_i16": ([_i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr], _int),
     "dd_slice_gemm_i64": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
+    "dd_split": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
+    "dd_split_i16": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
 }
 
 
@@ -375,3 +378,35 @@ def slice_gemm_i64(M: int, N: int, K: int, planesA, planesB, splits: int, P=None
     _check("dd_slice_gemm_i64", load().dd_slice_gemm_i64(M, N, K, planesA.data_ptr(), planesB.data_ptr(), splits,
                                                          P.data_ptr(), _stream_handle(stream)))
     return P
+
+
+def _split_both(fn, A_hi, A_lo, B_hi, B_lo, pA, e, pB, f, dtype, stream):
+    torch = _torch()
+    for t, n in ((A_hi, "A_hi"), (A_lo, "A_lo"), (B_hi, "B_hi"), (B_lo, "B_lo")):
+        _mat(t, n)
+    M, K = A_hi.shape
+    K2, N = B_hi.shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    Mp, Np, Kp = -(-M // TILE_M) * TILE_M, -(-N // TILE_N) * TILE_N, -(-K // CHUNK_K) * CHUNK_K
+    dev = A_hi.device
+    pA = torch.empty(SLICES * Mp * Kp, dtype=dtype, device=dev) if pA is None else pA
+    pB = torch.empty(SLICES * Np * Kp, dtype=dtype, device=dev) if pB is None else pB
+    e = torch.empty(M, dtype=torch.int32, device=dev) if e is None else e
+    f = torch.empty(N, dtype=torch.int32, device=dev) if f is None else f
+    if pA.numel() < SLICES * Mp * Kp or pB.numel() < SLICES * Np * Kp or e.numel() < M or f.numel() < N:
+        raise ValueError("output buffers too small")
+    _check(fn, getattr(load(), fn)(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi), B_hi.data_ptr(),
+                                   B_lo.data_ptr(), _ld(B_hi), pA.data_ptr(), e.data_ptr(), pB.data_ptr(),
+                                   f.data_ptr(), _stream_handle(stream)))
+    return pA, e, pB, f
+
+
+def split(A_hi, A_lo, B_hi, B_lo, planesA=None, e=None, planesB=None, f=None, stream=None):
+    """Step 1 for both operands (three launches): (planesA, e, planesB, f)."""
+    return _split_both("dd_split", A_hi, A_lo, B_hi, B_lo, planesA, e, planesB, f, _torch().float64, stream)
+
+
+def split_i16(A_hi, A_lo, B_hi, B_lo, planesA=None, e=None, planesB=None, f=None, stream=None):
+    """Step 1 for both operands with int16 parts: (planesA, e, planesB, f)."""
+    return _split_both("dd_split_i16", A_hi, A_lo, B_hi, B_lo, planesA, e, planesB, f, _torch().int16, stream)

@@ -127,6 +127,22 @@ ddgemm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DDGEMM_OK : D
         if (err_ != cudaSuccess) return DDGEMM_ERR_CUDA; \
     } while (0)
 
+// Step 1 for any subset of the operands (null hi = operand absent): exponent
+// reset, exponents, split into FP64 or int16 part planes -- three launches.
+cudaError_t run_split(int64_t M, int64_t N, int64_t K, int64_t Kp, const double* A_hi, const double* A_lo,
+                      int64_t lda, int32_t* e, void* pA, const double* B_hi, const double* B_lo, int64_t ldb,
+                      int32_t* f, void* pB, bool i16, cudaStream_t st) {
+    SplitOperand a{A_hi, A_lo, lda, M, e}, b{B_hi, B_lo, ldb, N, f};
+    const SplitOperand* pa = (e != nullptr && M > 0) ? &a : nullptr;
+    const SplitOperand* pb = (f != nullptr && N > 0) ? &b : nullptr;
+    cudaError_t err = launch_init_exponents(pa ? e : nullptr, M, pb ? f : nullptr, N, K, st);
+    if (err == cudaSuccess) err = launch_exponents(pa, pb, K, st);
+    if (err == cudaSuccess)
+        err = i16 ? launch_split_i16(pa, pb, K, Kp, static_cast<int16_t*>(pA), static_cast<int16_t*>(pB), st)
+                  : launch_split_f64(pa, pb, K, Kp, static_cast<double*>(pA), static_cast<double*>(pB), st);
+    return err;
+}
+
 // The launch sequence on a workspace laid out by make_layout.
 ddgemm_status run_gemm(const Layout& L, int64_t M, int64_t N, int64_t K, const double* A_hi,
                        const double* A_lo, int64_t lda, const double* B_hi, const double* B_lo,
@@ -138,11 +154,7 @@ ddgemm_status run_gemm(const Layout& L, int64_t M, int64_t N, int64_t K, const d
     double* pA = reinterpret_cast<double*>(ws + L.off_A);
     double* pB = reinterpret_cast<double*>(ws + L.off_B);
     double* P = reinterpret_cast<double*>(ws + L.off_P);
-    DDG_TRY(launch_init_exponents(e, M, f, N, K, st));
-    DDG_TRY(launch_row_exponents(A_hi, lda, M, K, e, st));
-    DDG_TRY(launch_col_exponents(B_hi, ldb, K, N, f, st));
-    DDG_TRY(launch_split_rows(A_hi, A_lo, lda, M, K, L.Kp, e, pA, st));
-    DDG_TRY(launch_split_cols(B_hi, B_lo, ldb, K, N, L.Kp, f, pB, st));
+    DDG_TRY(run_split(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, false, st));
     DDG_TRY(launch_slice_gemm(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
     DDG_TRY(launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
     return DDGEMM_OK;
@@ -159,11 +171,7 @@ ddgemm_status run_gemm_i64(const Layout& L, int64_t M, int64_t N, int64_t K, con
     int16_t* pA = reinterpret_cast<int16_t*>(ws + L.off_A);
     int16_t* pB = reinterpret_cast<int16_t*>(ws + L.off_B);
     double* P = reinterpret_cast<double*>(ws + L.off_P);
-    DDG_TRY(launch_init_exponents(e, M, f, N, K, st));
-    DDG_TRY(launch_row_exponents(A_hi, lda, M, K, e, st));
-    DDG_TRY(launch_col_exponents(B_hi, ldb, K, N, f, st));
-    DDG_TRY(launch_split_rows_i16(A_hi, A_lo, lda, M, K, L.Kp, e, pA, st));
-    DDG_TRY(launch_split_cols_i16(B_hi, B_lo, ldb, K, N, L.Kp, f, pB, st));
+    DDG_TRY(run_split(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, true, st));
     DDG_TRY(launch_slice_gemm_i64(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
     DDG_TRY(launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
     return DDGEMM_OK;
@@ -305,9 +313,7 @@ ddgemm_status dd_split_rows(int64_t M, int64_t K, const double* A_hi, const doub
     if ((uintptr_t)planes % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t Kp = round_up(K, BK);
-    DDG_TRY(launch_init_exponents(e, M, nullptr, 0, K, st));
-    DDG_TRY(launch_row_exponents(A_hi, lda, M, K, e, st));
-    DDG_TRY(launch_split_rows(A_hi, A_lo, lda, M, K, Kp, e, planes, st));
+    DDG_TRY(run_split(M, 0, K, Kp, A_hi, A_lo, lda, e, planes, nullptr, nullptr, 1, nullptr, nullptr, false, st));
     return DDGEMM_OK;
 }
 
@@ -321,10 +327,36 @@ ddgemm_status dd_split_cols(int64_t K, int64_t N, const double* B_hi, const doub
     if ((uintptr_t)planes % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t Kp = round_up(K, BK);
-    DDG_TRY(launch_init_exponents(nullptr, 0, f, N, K, st));
-    DDG_TRY(launch_col_exponents(B_hi, ldb, K, N, f, st));
-    DDG_TRY(launch_split_cols(B_hi, B_lo, ldb, K, N, Kp, f, planes, st));
+    DDG_TRY(run_split(0, N, K, Kp, nullptr, nullptr, 1, nullptr, nullptr, B_hi, B_lo, ldb, f, planes, false, st));
     return DDGEMM_OK;
+}
+
+// Step 1 for both operands in three launches.
+static ddgemm_status split_both(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                                int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb, void* planesA,
+                                int32_t* e, void* planesB, int32_t* f, bool i16, void* stream) {
+    ddgemm_status s = check_shapes(M, N, K, lda, ldb, std::max<int64_t>(1, N));
+    if (s != DDGEMM_OK) return s;
+    if (M > 0 && (e == nullptr || (K > 0 && (A_hi == nullptr || A_lo == nullptr || planesA == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (N > 0 && (f == nullptr || (K > 0 && (B_hi == nullptr || B_lo == nullptr || planesB == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    const int64_t Kp = round_up(K, BK);
+    return from_cuda(run_split(M, N, K, Kp, A_hi, A_lo, lda, M > 0 ? e : nullptr, planesA, B_hi, B_lo, ldb,
+                               N > 0 ? f : nullptr, planesB, i16, static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status dd_split(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
+                       const double* B_hi, const double* B_lo, int64_t ldb, double* planesA, int32_t* e,
+                       double* planesB, int32_t* f, void* stream) {
+    return split_both(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, planesA, e, planesB, f, false, stream);
+}
+
+ddgemm_status dd_split_i16(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
+                           const double* B_hi, const double* B_lo, int64_t ldb, int16_t* planesA, int32_t* e,
+                           int16_t* planesB, int32_t* f, void* stream) {
+    return split_both(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, planesA, e, planesB, f, true, stream);
 }
 
 ddgemm_status dd_slice_gemm(int64_t M, int64_t N, int64_t K, const double* planesA,
@@ -422,9 +454,7 @@ ddgemm_status dd_split_rows_i16(int64_t M, int64_t K, const double* A_hi, const 
     if ((uintptr_t)planes % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t Kp = round_up(K, BK);
-    DDG_TRY(launch_init_exponents(e, M, nullptr, 0, K, st));
-    DDG_TRY(launch_row_exponents(A_hi, lda, M, K, e, st));
-    DDG_TRY(launch_split_rows_i16(A_hi, A_lo, lda, M, K, Kp, e, planes, st));
+    DDG_TRY(run_split(M, 0, K, Kp, A_hi, A_lo, lda, e, planes, nullptr, nullptr, 1, nullptr, nullptr, true, st));
     return DDGEMM_OK;
 }
 
@@ -438,9 +468,7 @@ ddgemm_status dd_split_cols_i16(int64_t K, int64_t N, const double* B_hi, const 
     if ((uintptr_t)planes % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t Kp = round_up(K, BK);
-    DDG_TRY(launch_init_exponents(nullptr, 0, f, N, K, st));
-    DDG_TRY(launch_col_exponents(B_hi, ldb, K, N, f, st));
-    DDG_TRY(launch_split_cols_i16(B_hi, B_lo, ldb, K, N, Kp, f, planes, st));
+    DDG_TRY(run_split(0, N, K, Kp, nullptr, nullptr, 1, nullptr, nullptr, B_hi, B_lo, ldb, f, planes, true, st));
     return DDGEMM_OK;
 }
 

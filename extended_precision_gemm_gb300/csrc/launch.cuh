@@ -6,25 +6,28 @@
 
 namespace ddg {
 
-// Step 1: exponents and part planes.  Exponent arrays are accumulated with
-// atomicMax and must be reset by launch_init_exponents first.
+// Step 1: exponents and part planes.  An operand is A (its rows) or B (its
+// columns); `rows` counts rows of A or columns of B; element (r, k) is
+// hi[r * ld + k] for A and hi[k * ld + r] for B.  Exponent arrays are
+// accumulated with atomicMax and must be reset by launch_init_exponents
+// first.  Either operand may be null.
+struct SplitOperand {
+    const double* hi;
+    const double* lo;
+    int64_t ld;
+    int64_t rows;
+    int32_t* exp;
+};
 cudaError_t launch_init_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int64_t K,
                                   cudaStream_t st);
-cudaError_t launch_row_exponents(const double* A_hi, int64_t lda, int64_t M, int64_t K,
-                                 int32_t* e, cudaStream_t st);
-cudaError_t launch_col_exponents(const double* B_hi, int64_t ldb, int64_t K, int64_t N,
-                                 int32_t* f, cudaStream_t st);
-cudaError_t launch_split_rows(const double* A_hi, const double* A_lo, int64_t lda, int64_t M,
-                              int64_t K, int64_t Kp, int32_t* e, double* planes, cudaStream_t st);
-cudaError_t launch_split_cols(const double* B_hi, const double* B_lo, int64_t ldb, int64_t K,
-                              int64_t N, int64_t Kp, int32_t* f, double* planes, cudaStream_t st);
-
-// Step 1, int16 parts for the integer-pipe slice GEMM (layout
+cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, cudaStream_t st);
+// FP64 parts in the tiled layout of the mma.sync slice GEMM.
+cudaError_t launch_split_f64(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
+                             double* planesA, double* planesB, cudaStream_t st);
+// int16 parts for the integer-pipe slice GEMM (layout
 // [tile][k-chunk][k in chunk][row in tile][part]).
-cudaError_t launch_split_rows_i16(const double* A_hi, const double* A_lo, int64_t lda, int64_t M,
-                                  int64_t K, int64_t Kp, int32_t* e, int16_t* planes, cudaStream_t st);
-cudaError_t launch_split_cols_i16(const double* B_hi, const double* B_lo, int64_t ldb, int64_t K,
-                                  int64_t N, int64_t Kp, int32_t* f, int16_t* planes, cudaStream_t st);
+cudaError_t launch_split_i16(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
+                             int16_t* planesA, int16_t* planesB, cudaStream_t st);
 
 // Step 2: slice-pair GEMM into `splits` partial sets of 8 planes Mp x Np.
 cudaError_t launch_slice_gemm(const double* planesA, const double* planesB, int64_t Mp,

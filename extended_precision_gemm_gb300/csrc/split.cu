@@ -4,7 +4,10 @@
 // double double into 8 parts of 13 bits: 4 quarters of hi, 4 of lo) with the
 // parts of a row of A / column of B placed on one exponent grid (the goal of
 // Section 3, Problems 3.2 and 3.4).  Bandwidth-bound: each input element is
-// read once as (hi, lo) and written as 8 doubles.
+// read as (hi, lo) and written as 8 parts.
+//
+// Three launches cover both operands: exponent reset, exponents (rows of A
+// and columns of B in one grid), split (A tiles and B tiles in one grid).
 #include <algorithm>
 #include <climits>
 
@@ -21,9 +24,10 @@ __device__ __forceinline__ uint64_t abs_bits(double x) {
 }
 
 // ---------------------------------------------------------------------------
-// Exponents: e[i] = max over the row of the smallest e with |A_hi| < 2^e.
-// The maximum of |x| is taken on the IEEE bit patterns (for non-negative
-// doubles the integer order of the bits is the order of the values).
+// Exponents: e[i] = max over the row of the smallest e with |A_hi| < 2^e
+// (f[j] likewise over the column of B).  The maximum of |x| is taken on the
+// IEEE bit patterns (for non-negative doubles the integer order of the bits
+// is the order of the values) and combined over k-chunks with atomicMax.
 // ---------------------------------------------------------------------------
 
 __global__ void init_exponents_kernel(int32_t* e, int64_t M, int32_t* f, int64_t N, int32_t value) {
@@ -32,74 +36,87 @@ __global__ void init_exponents_kernel(int32_t* e, int64_t M, int32_t* f, int64_t
     if (f != nullptr && i < N) f[i] = value;
 }
 
-// One warp per row and k-chunk; 128-bit loads when VEC == 2.
-template <int VEC>
-__global__ void __launch_bounds__(256) row_exponents_kernel(const double* __restrict__ A_hi,
-                                                            int64_t lda, int64_t M, int64_t K,
-                                                            int64_t kchunk, int32_t* e) {
-    const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (row >= M) return;
-    const int64_t k0 = (int64_t)blockIdx.y * kchunk;
-    const int64_t k1 = min(K, k0 + kchunk);
-    const double* p = A_hi + row * lda;
-    uint64_t m = 0;
-    if (VEC == 2) {
-        // four independent 128-bit loads in flight per lane
-        uint64_t m1 = 0, m2 = 0, m3 = 0;
-        int64_t k = k0 + 2 * lane;
-        for (; k + 193 < k1; k += 256) {
-            const double2 v0 = __ldg(reinterpret_cast<const double2*>(p + k));
-            const double2 v1 = __ldg(reinterpret_cast<const double2*>(p + k + 64));
-            const double2 v2 = __ldg(reinterpret_cast<const double2*>(p + k + 128));
-            const double2 v3 = __ldg(reinterpret_cast<const double2*>(p + k + 192));
-            m = max(m, max(abs_bits(v0.x), abs_bits(v0.y)));
-            m1 = max(m1, max(abs_bits(v1.x), abs_bits(v1.y)));
-            m2 = max(m2, max(abs_bits(v2.x), abs_bits(v2.y)));
-            m3 = max(m3, max(abs_bits(v3.x), abs_bits(v3.y)));
-        }
-        for (; k < k1; k += 64) {
-            if (k + 1 < k1) {
-                double2 v = __ldg(reinterpret_cast<const double2*>(p + k));
-                m = max(m, max(abs_bits(v.x), abs_bits(v.y)));
-            } else {
-                m = max(m, abs_bits(__ldg(p + k)));
-            }
-        }
-        m = max(max(m, m1), max(m2, m3));
-    } else {
-        for (int64_t k = k0 + lane; k < k1; k += 32) m = max(m, abs_bits(__ldg(p + k)));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = max(m, (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)m, off));
-    if (lane == 0 && m != 0) atomicMax(&e[row], exponent_from_abs_bits(m));
-}
+// Work split of the exponent grid.  A-items: 8 rows of A (one warp per row)
+// x one k-chunk; B-items: 256 columns of B (one thread per column) x one
+// k-chunk.  Chunks are sized so both operands have about the same number of
+// items of about the same size, and blocks alternate between the two
+// (even block: A-item, odd block: B-item), so neither operand forms a tail.
+struct ExpGrid {
+    const double* A_hi; int64_t lda, M, a_kchunk, a_ksplit, a_items;
+    const double* B_hi; int64_t ldb, N, b_kchunk, b_ksplit, b_items;
+    int64_t K;
+    int32_t* e; int32_t* f;
+};
 
-// One thread per column and k-chunk; a warp reads 32 consecutive columns of a
-// row (256 contiguous bytes) per load.
-__global__ void __launch_bounds__(128) col_exponents_kernel(const double* __restrict__ B_hi,
-                                                            int64_t ldb, int64_t K, int64_t N,
-                                                            int64_t kchunk, int32_t* f) {
-    const int64_t col = (int64_t)blockIdx.x * 128 + threadIdx.x;
-    if (col >= N) return;
-    const int64_t k0 = (int64_t)blockIdx.y * kchunk;
-    const int64_t k1 = min(K, k0 + kchunk);
-    const double* p = B_hi + col;
-    uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
-    int64_t k = k0;
-    for (; k + 7 < k1; k += 8) {  // eight loads in flight per thread
-        const double x0 = __ldg(p + (k + 0) * ldb), x1 = __ldg(p + (k + 1) * ldb);
-        const double x2 = __ldg(p + (k + 2) * ldb), x3 = __ldg(p + (k + 3) * ldb);
-        const double x4 = __ldg(p + (k + 4) * ldb), x5 = __ldg(p + (k + 5) * ldb);
-        const double x6 = __ldg(p + (k + 6) * ldb), x7 = __ldg(p + (k + 7) * ldb);
-        m0 = max(m0, max(abs_bits(x0), abs_bits(x4)));
-        m1 = max(m1, max(abs_bits(x1), abs_bits(x5)));
-        m2 = max(m2, max(abs_bits(x2), abs_bits(x6)));
-        m3 = max(m3, max(abs_bits(x3), abs_bits(x7)));
+template <int VEC>
+__global__ void __launch_bounds__(256) exponents_kernel(ExpGrid g) {
+    const bool both = g.a_items > 0 && g.b_items > 0;
+    const bool is_a = both ? (blockIdx.x & 1) == 0 : g.a_items > 0;
+    const int64_t bid = both ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+    if (is_a) {
+        if (bid >= g.a_items) return;
+        const int lane = threadIdx.x & 31;
+        const int64_t row = (bid / g.a_ksplit) * 8 + (threadIdx.x >> 5);
+        if (row >= g.M) return;
+        const int64_t k0 = (bid % g.a_ksplit) * g.a_kchunk;
+        const int64_t k1 = min(g.K, k0 + g.a_kchunk);
+        const double* p = g.A_hi + row * g.lda;
+        uint64_t m = 0;
+        if (VEC == 2) {
+            // four independent 128-bit loads in flight per lane
+            uint64_t m1 = 0, m2 = 0, m3 = 0;
+            int64_t k = k0 + 2 * lane;
+            for (; k + 193 < k1; k += 256) {
+                const double2 v0 = __ldg(reinterpret_cast<const double2*>(p + k));
+                const double2 v1 = __ldg(reinterpret_cast<const double2*>(p + k + 64));
+                const double2 v2 = __ldg(reinterpret_cast<const double2*>(p + k + 128));
+                const double2 v3 = __ldg(reinterpret_cast<const double2*>(p + k + 192));
+                m = max(m, max(abs_bits(v0.x), abs_bits(v0.y)));
+                m1 = max(m1, max(abs_bits(v1.x), abs_bits(v1.y)));
+                m2 = max(m2, max(abs_bits(v2.x), abs_bits(v2.y)));
+                m3 = max(m3, max(abs_bits(v3.x), abs_bits(v3.y)));
+            }
+            for (; k < k1; k += 64) {
+                if (k + 1 < k1) {
+                    double2 v = __ldg(reinterpret_cast<const double2*>(p + k));
+                    m = max(m, max(abs_bits(v.x), abs_bits(v.y)));
+                } else {
+                    m = max(m, abs_bits(__ldg(p + k)));
+                }
+            }
+            m = max(max(m, m1), max(m2, m3));
+        } else {
+            for (int64_t k = k0 + lane; k < k1; k += 32) m = max(m, abs_bits(__ldg(p + k)));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            m = max(m, (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)m, off));
+        if (lane == 0 && m != 0) atomicMax(&g.e[row], exponent_from_abs_bits(m));
+    } else {
+        if (bid >= g.b_items) return;
+        const int64_t b = bid;
+        const int64_t col = (b / g.b_ksplit) * 256 + threadIdx.x;
+        if (col >= g.N) return;
+        const int64_t k0 = (b % g.b_ksplit) * g.b_kchunk;
+        const int64_t k1 = min(g.K, k0 + g.b_kchunk);
+        const double* p = g.B_hi + col;
+        const int64_t ldb = g.ldb;
+        uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+        int64_t k = k0;
+        for (; k + 7 < k1; k += 8) {  // eight loads in flight per thread
+            const double x0 = __ldg(p + (k + 0) * ldb), x1 = __ldg(p + (k + 1) * ldb);
+            const double x2 = __ldg(p + (k + 2) * ldb), x3 = __ldg(p + (k + 3) * ldb);
+            const double x4 = __ldg(p + (k + 4) * ldb), x5 = __ldg(p + (k + 5) * ldb);
+            const double x6 = __ldg(p + (k + 6) * ldb), x7 = __ldg(p + (k + 7) * ldb);
+            m0 = max(m0, max(abs_bits(x0), abs_bits(x4)));
+            m1 = max(m1, max(abs_bits(x1), abs_bits(x5)));
+            m2 = max(m2, max(abs_bits(x2), abs_bits(x6)));
+            m3 = max(m3, max(abs_bits(x3), abs_bits(x7)));
+        }
+        for (; k < k1; ++k) m0 = max(m0, abs_bits(__ldg(p + k * ldb)));
+        const uint64_t m = max(max(m0, m1), max(m2, m3));
+        if (m != 0) atomicMax(&g.f[col], exponent_from_abs_bits(m));
     }
-    for (; k < k1; ++k) m0 = max(m0, abs_bits(__ldg(p + k * ldb)));
-    uint64_t m = max(max(m0, m1), max(m2, m3));
-    if (m != 0) atomicMax(&f[col], exponent_from_abs_bits(m));
 }
 
 // ---------------------------------------------------------------------------
@@ -203,219 +220,199 @@ __device__ __forceinline__ uint4 split_digits_i16(double hi, double lo, int e) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Each split block covers one 32-row (A) or 32-column (B) tile and 32
-// consecutive k (4 k-chunks).  Its parts form one contiguous 64 KB block of
-// the plane array ([chunk][part][k4 group][row in tile][k % 4]); the block is
-// assembled in shared memory and written with one bulk asynchronous copy
-// (TMA engine), so every DRAM line is written whole.
+// ---------------------------------------------------------------------------
+// Split.  A work item is one 32-row tile of A (32-column tile of B) and 32
+// consecutive k (4 k-chunks): 32 lanes = rows (columns) x 8 warps = groups
+// of 4 consecutive k.  Items [0, a_items) are A's, the rest B's.
+// FP64 parts: the item's parts form one contiguous 64 KB block of the plane
+// array ([chunk][part][k4 group][row in tile][k % 4]), assembled in shared
+// memory and written by one bulk asynchronous copy (TMA engine), so every
+// DRAM line is written whole.
+// int16 parts: layout [tile][k-chunk][k in chunk][row in tile][part]; each
+// lane writes the 16 bytes of one element, a warp 512 contiguous bytes.
+// ---------------------------------------------------------------------------
+
 constexpr int SPLIT_THREADS = 256;
-constexpr int SPLIT_CHUNKS = 32 / BK;                              // k-chunks per block
+constexpr int SPLIT_CHUNKS = 32 / BK;                                                // k-chunks per item
 constexpr size_t SPLIT_SMEM = (size_t)SPLIT_CHUNKS * CHUNK_DOUBLES * sizeof(double);  // 64 KB
-constexpr int PART_STRIDE = (BK / 4) * TM * 4;                     // doubles between parts s, s+1
+constexpr int PART_STRIDE = (BK / 4) * TM * 4;                                       // doubles between parts
+
+struct SplitGrid {
+    const double* A_hi; const double* A_lo; int64_t lda, M, a_tiles;
+    const double* B_hi; const double* B_lo; int64_t ldb, N, b_tiles;
+    int64_t K, Kp, KT;  // KT = k-items per tile
+    int32_t* e; int32_t* f;
+    void* planesA; void* planesB;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Parts of 4 consecutive elements (k0 .. k0+3) of one row or column into the
-// staging block, two elements per 16-byte shared-memory store.
-__device__ __forceinline__ void stage_parts(const double (&hi)[4], const double (&lo)[4], int ex,
-                                            double* dst) {
-#pragma unroll
-    for (int r = 0; r < 4; r += 2) {
-        double d0[S], d1[S];
-        split_digits(hi[r], lo[r], ex, d0);
-        split_digits(hi[r + 1], lo[r + 1], ex, d1);
-#pragma unroll
-        for (int s = 0; s < S; ++s)
-            *reinterpret_cast<double2*>(dst + s * PART_STRIDE + r) = make_double2(d0[s], d1[s]);
-    }
-}
-
-// Write the staged block (`chunks` k-chunks) to global memory and wait until
-// the copy has read shared memory, so the stage can be refilled.
-__device__ __forceinline__ void flush_stage(double* stage, double* gdst, int chunks) {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t bytes = (uint32_t)chunks * CHUNK_DOUBLES * sizeof(double);
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-                     "r"(smem_u32(stage)), "r"(bytes)
-                     : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-    }
-    __syncthreads();
-}
-
-// Rows of A.  Block = 32 rows (lanes) x 8 groups of 4 consecutive k (warps);
-// blockIdx.x walks k in steps of 32, blockIdx.y strides over the row tiles.
-// Each thread reads 4 hi and 4 lo values of its row (two 128-bit loads each
-// when VEC == 2) and stages its 32 parts.
+// Load the 4 consecutive elements (k0 .. k0+3) of row / column `r` handled by
+// this thread (zeros outside the matrix) and the exponent of that row or
+// column; also writes back the final exponent of an all-zero row/column.
 template <int VEC>
-__global__ void __launch_bounds__(SPLIT_THREADS, 3) split_rows_kernel(const double* __restrict__ A_hi,
-                                                                   const double* __restrict__ A_lo,
-                                                                   int64_t lda, int64_t M, int64_t K,
-                                                                   int64_t Kp, int32_t* e,
-                                                                   double* __restrict__ planes) {
-    extern __shared__ __align__(128) double stage[];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t KC = Kp / BK;
-    const int64_t kc0 = (int64_t)blockIdx.x * SPLIT_CHUNKS;
-    const int chunks = (int)min((int64_t)SPLIT_CHUNKS, KC - kc0);
-    const int64_t k0 = kc0 * BK + 4 * w;
-    const bool active = (w >> 1) < chunks;  // this warp's k-chunk exists
-    double* dst = stage + (((w >> 1) * S * (BK / 4) + (w & 1)) * TM + lane) * 4;
-    const int64_t tiles = (M + TM - 1) / TM;
-    for (int64_t mt = blockIdx.y; mt < tiles; mt += gridDim.y) {
-        if (active) {
-            const int64_t i = mt * TM + lane;
-            double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-            int ex = 0;
-            if (i < M) {
-                const int32_t er = e[i];
-                ex = effective_exponent(er);
-                if (blockIdx.x == 0 && w == 0 && er == EXP_NONE) e[i] = 0;
-                const double* ph = A_hi + i * lda + k0;
-                const double* pl = A_lo + i * lda + k0;
-                if (VEC == 2 && k0 + 3 < K) {
-                    double2 h0 = __ldg(reinterpret_cast<const double2*>(ph));
-                    double2 h1 = __ldg(reinterpret_cast<const double2*>(ph + 2));
-                    double2 l0 = __ldg(reinterpret_cast<const double2*>(pl));
-                    double2 l1 = __ldg(reinterpret_cast<const double2*>(pl + 2));
-                    hi[0] = h0.x; hi[1] = h0.y; hi[2] = h1.x; hi[3] = h1.y;
-                    lo[0] = l0.x; lo[1] = l0.y; lo[2] = l1.x; lo[3] = l1.y;
-                } else {
+__device__ __forceinline__ int load_item(const SplitGrid& g, bool is_a, int64_t tile, int64_t k0, int lane,
+                                         int w, int64_t kt, double (&hi)[4], double (&lo)[4]) {
 #pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        if (k0 + r < K) { hi[r] = __ldg(ph + r); lo[r] = __ldg(pl + r); }
-                }
-            }
-            stage_parts(hi, lo, ex, dst);
+    for (int r = 0; r < 4; ++r) hi[r] = lo[r] = 0.0;
+    const int64_t rr = tile * TM + lane;
+    if (is_a) {
+        if (rr >= g.M) return 0;
+        const int32_t er = g.e[rr];
+        if (kt == 0 && w == 0 && er == EXP_NONE) g.e[rr] = 0;
+        const double* ph = g.A_hi + rr * g.lda + k0;
+        const double* pl = g.A_lo + rr * g.lda + k0;
+        if (VEC == 2 && k0 + 3 < g.K) {
+            double2 h0 = __ldg(reinterpret_cast<const double2*>(ph));
+            double2 h1 = __ldg(reinterpret_cast<const double2*>(ph + 2));
+            double2 l0 = __ldg(reinterpret_cast<const double2*>(pl));
+            double2 l1 = __ldg(reinterpret_cast<const double2*>(pl + 2));
+            hi[0] = h0.x; hi[1] = h0.y; hi[2] = h1.x; hi[3] = h1.y;
+            lo[0] = l0.x; lo[1] = l0.y; lo[2] = l1.x; lo[3] = l1.y;
+        } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (k0 + r < g.K) { hi[r] = __ldg(ph + r); lo[r] = __ldg(pl + r); }
         }
-        flush_stage(stage, planes + (mt * KC + kc0) * CHUNK_DOUBLES, chunks);
+        return effective_exponent(er);
     }
+    if (rr >= g.N) return 0;
+    const int32_t fr = g.f[rr];
+    if (kt == 0 && w == 0 && fr == EXP_NONE) g.f[rr] = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+        if (k0 + r < g.K) {
+            hi[r] = __ldg(g.B_hi + (k0 + r) * g.ldb + rr);
+            lo[r] = __ldg(g.B_lo + (k0 + r) * g.ldb + rr);
+        }
+    return effective_exponent(fr);
 }
 
-// Columns of B (K x N row-major).  Block = 32 columns (lanes) x 8 groups of 4
-// consecutive k (warps), grid as split_rows_kernel; every load of a warp
-// reads 32 consecutive columns of one row.  Stages and writes as
-// split_rows_kernel, in B's plane layout.
-__global__ void __launch_bounds__(SPLIT_THREADS, 3) split_cols_kernel(const double* __restrict__ B_hi,
-                                                                   const double* __restrict__ B_lo,
-                                                                   int64_t ldb, int64_t K, int64_t N,
-                                                                   int64_t Kp, int32_t* f,
-                                                                   double* __restrict__ planes) {
-    extern __shared__ __align__(128) double stage[];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t KC = Kp / BK;
-    const int64_t kc0 = (int64_t)blockIdx.x * SPLIT_CHUNKS;
-    const int chunks = (int)min((int64_t)SPLIT_CHUNKS, KC - kc0);
-    const int64_t k0 = kc0 * BK + 4 * w;
-    const bool active = (w >> 1) < chunks;
-    double* dst = stage + (((w >> 1) * S * (BK / 4) + (w & 1)) * TN + lane) * 4;
-    const int64_t tiles = (N + TN - 1) / TN;
-    for (int64_t nt = blockIdx.y; nt < tiles; nt += gridDim.y) {
-        if (active) {
-            const int64_t j = nt * TN + lane;
-            double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-            int ex = 0;
-            if (j < N) {
-                const int32_t fr = f[j];
-                ex = effective_exponent(fr);
-                if (blockIdx.x == 0 && w == 0 && fr == EXP_NONE) f[j] = 0;
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    if (k0 + r < K) {
-                        hi[r] = __ldg(B_hi + (k0 + r) * ldb + j);
-                        lo[r] = __ldg(B_lo + (k0 + r) * ldb + j);
-                    }
-            }
-            stage_parts(hi, lo, ex, dst);
-        }
-        flush_stage(stage, planes + (nt * KC + kc0) * CHUNK_DOUBLES, chunks);
-    }
+// Decomposition of a work item index.
+struct Item {
+    bool is_a;
+    int64_t tile, kt;
+    int chunks;  // k-chunks present (the last k-item of a tile may be short)
+};
+
+__device__ __forceinline__ Item item_of(const SplitGrid& g, int64_t item, int64_t KC) {
+    Item it;
+    it.is_a = item < g.a_tiles * g.KT;
+    const int64_t local = it.is_a ? item : item - g.a_tiles * g.KT;
+    it.tile = local / g.KT;
+    it.kt = local % g.KT;
+    it.chunks = (int)min((int64_t)SPLIT_CHUNKS, KC - it.kt * SPLIT_CHUNKS);
+    return it;
 }
 
-// ---------------------------------------------------------------------------
-// Part planes as int16 for the integer-pipe slice GEMM.  Layout
-// [tile][k-chunk][k in chunk][row in tile][part]: the 8 parts of one element
-// are 16 contiguous bytes, so one 128-bit load brings all of them.  A warp
-// (32 rows or columns of a tile, one k) writes 512 contiguous bytes.
-// ---------------------------------------------------------------------------
+// Each block walks its items with a stride of the grid; the loads of the next
+// item are issued before the current one is split, so their latency overlaps
+// the digit arithmetic and the stores.  Each warp stages its own 8 parts x
+// (32 rows x 4 k) = 8 KB in shared memory and writes them with eight 1 KB
+// bulk stores (TMA engine); before refilling its stage it only waits until
+// its own previous stores have read it -- no block-wide barrier.
+template <int VEC>
+__global__ void __launch_bounds__(SPLIT_THREADS, 3) split_f64_kernel(SplitGrid g) {
+    extern __shared__ __align__(128) double stage[];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t items = (g.a_tiles + g.b_tiles) * g.KT;
+    const int64_t KC = g.Kp / BK;
+    constexpr int WARP_STAGE = S * TM * 4;  // 1024 doubles
+    double* ws = stage + w * WARP_STAGE;    // [part][row][k % 4]
+    double nhi[4] = {0, 0, 0, 0}, nlo[4] = {0, 0, 0, 0};
+    int nex = 0;
+    bool pending = false;
+    int64_t item = blockIdx.x;
+    Item nit;
+    if (item < items) {
+        nit = item_of(g, item, KC);
+        if ((w >> 1) < nit.chunks)
+            nex = load_item<VEC>(g, nit.is_a, nit.tile, nit.kt * 32 + 4 * w, lane, w, nit.kt, nhi, nlo);
+    }
+    for (; item < items; item += gridDim.x) {
+        const Item it = nit;
+        double hi[4], lo[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) { hi[r] = nhi[r]; lo[r] = nlo[r]; }
+        const int ex = nex;
+        const int64_t next = item + gridDim.x;
+        if (next < items) {
+            nit = item_of(g, next, KC);
+            if ((w >> 1) < nit.chunks)
+                nex = load_item<VEC>(g, nit.is_a, nit.tile, nit.kt * 32 + 4 * w, lane, w, nit.kt, nhi, nlo);
+        }
+        if ((w >> 1) >= it.chunks) continue;  // this warp's k-chunk does not exist
+        if (pending) {
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+        }
+#pragma unroll
+        for (int r = 0; r < 4; r += 2) {
+            double d0[S], d1[S];
+            split_digits(hi[r], lo[r], ex, d0);
+            split_digits(hi[r + 1], lo[r + 1], ex, d1);
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+                *reinterpret_cast<double2*>(ws + (s * TM + lane) * 4 + r) = make_double2(d0[s], d1[s]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            // part s of this warp's (k-chunk, k4 group) is 1 KB contiguous in the plane block
+            double* base = static_cast<double*>(it.is_a ? g.planesA : g.planesB) +
+                           (it.tile * KC + it.kt * SPLIT_CHUNKS + (w >> 1)) * CHUNK_DOUBLES + (w & 1) * TM * 4;
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(base + s * PART_STRIDE),
+                             "r"(smem_u32(ws + s * TM * 4)), "r"((uint32_t)(TM * 4 * sizeof(double)))
+                             : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        pending = true;
+    }
+    // the stage must stay valid until the last stores have read it
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+}
 
 __device__ __forceinline__ int64_t i16_offset(int64_t tile, int64_t KC, int64_t k, int ti) {
     return (((tile * KC + k / BK) * BK + k % BK) * TM + ti) * S;
 }
 
 template <int VEC>
-__global__ void __launch_bounds__(256, 4) split_rows_i16_kernel(const double* __restrict__ A_hi,
-                                                              const double* __restrict__ A_lo,
-                                                              int64_t lda, int64_t M, int64_t K,
-                                                              int64_t Kp, int32_t* e,
-                                                              int16_t* __restrict__ planes) {
+__global__ void __launch_bounds__(SPLIT_THREADS, 4) split_i16_kernel(SplitGrid g) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t k0 = (int64_t)blockIdx.x * 32 + 4 * w;
-    if (k0 >= Kp) return;
-    const int64_t KC = Kp / BK;
-    const int64_t tiles = (M + TM - 1) / TM;
-    for (int64_t mt = blockIdx.y; mt < tiles; mt += gridDim.y) {
-        const int64_t i = mt * TM + lane;
-        double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-        int ex = 0;
-        if (i < M) {
-            const int32_t er = e[i];
-            ex = effective_exponent(er);
-            if (blockIdx.x == 0 && w == 0 && er == EXP_NONE) e[i] = 0;
-            const double* ph = A_hi + i * lda + k0;
-            const double* pl = A_lo + i * lda + k0;
-            if (VEC == 2 && k0 + 3 < K) {
-                double2 h0 = __ldg(reinterpret_cast<const double2*>(ph));
-                double2 h1 = __ldg(reinterpret_cast<const double2*>(ph + 2));
-                double2 l0 = __ldg(reinterpret_cast<const double2*>(pl));
-                double2 l1 = __ldg(reinterpret_cast<const double2*>(pl + 2));
-                hi[0] = h0.x; hi[1] = h0.y; hi[2] = h1.x; hi[3] = h1.y;
-                lo[0] = l0.x; lo[1] = l0.y; lo[2] = l1.x; lo[3] = l1.y;
-            } else {
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    if (k0 + r < K) { hi[r] = __ldg(ph + r); lo[r] = __ldg(pl + r); }
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            *reinterpret_cast<uint4*>(planes + i16_offset(mt, KC, k0 + r, lane)) = split_digits_i16(hi[r], lo[r], ex);
+    const int64_t items = (g.a_tiles + g.b_tiles) * g.KT;
+    const int64_t KC = g.Kp / BK;
+    double nhi[4] = {0, 0, 0, 0}, nlo[4] = {0, 0, 0, 0};
+    int nex = 0;
+    int64_t item = blockIdx.x;
+    Item nit;
+    if (item < items) {
+        nit = item_of(g, item, KC);
+        if ((w >> 1) < nit.chunks)
+            nex = load_item<VEC>(g, nit.is_a, nit.tile, nit.kt * 32 + 4 * w, lane, w, nit.kt, nhi, nlo);
     }
-}
-
-__global__ void __launch_bounds__(256, 4) split_cols_i16_kernel(const double* __restrict__ B_hi,
-                                                              const double* __restrict__ B_lo,
-                                                              int64_t ldb, int64_t K, int64_t N,
-                                                              int64_t Kp, int32_t* f,
-                                                              int16_t* __restrict__ planes) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t k0 = (int64_t)blockIdx.x * 32 + 4 * w;
-    if (k0 >= Kp) return;
-    const int64_t KC = Kp / BK;
-    const int64_t tiles = (N + TN - 1) / TN;
-    for (int64_t nt = blockIdx.y; nt < tiles; nt += gridDim.y) {
-        const int64_t j = nt * TN + lane;
-        double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-        int ex = 0;
-        if (j < N) {
-            const int32_t fr = f[j];
-            ex = effective_exponent(fr);
-            if (blockIdx.x == 0 && w == 0 && fr == EXP_NONE) f[j] = 0;
+    for (; item < items; item += gridDim.x) {
+        const Item it = nit;
+        double hi[4], lo[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (k0 + r < K) {
-                    hi[r] = __ldg(B_hi + (k0 + r) * ldb + j);
-                    lo[r] = __ldg(B_lo + (k0 + r) * ldb + j);
-                }
+        for (int r = 0; r < 4; ++r) { hi[r] = nhi[r]; lo[r] = nlo[r]; }
+        const int ex = nex;
+        const int64_t next = item + gridDim.x;
+        if (next < items) {
+            nit = item_of(g, next, KC);
+            if ((w >> 1) < nit.chunks)
+                nex = load_item<VEC>(g, nit.is_a, nit.tile, nit.kt * 32 + 4 * w, lane, w, nit.kt, nhi, nlo);
         }
+        if ((w >> 1) >= it.chunks) continue;
+        const int64_t k0 = it.kt * 32 + 4 * w;
+        int16_t* planes = static_cast<int16_t*>(it.is_a ? g.planesA : g.planesB);
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            *reinterpret_cast<uint4*>(planes + i16_offset(nt, KC, k0 + r, lane)) = split_digits_i16(hi[r], lo[r], ex);
+            *reinterpret_cast<uint4*>(planes + i16_offset(it.tile, KC, k0 + r, lane)) = split_digits_i16(hi[r], lo[r], ex);
     }
 }
 
@@ -429,92 +426,97 @@ int num_sms() {
 
 }  // namespace
 
-cudaError_t launch_split_rows_i16(const double* A_hi, const double* A_lo, int64_t lda, int64_t M,
-                                  int64_t K, int64_t Kp, int32_t* e, int16_t* planes, cudaStream_t st) {
-    const int64_t Mp = round_up(M, TM);
-    if (Mp == 0 || Kp == 0) return cudaSuccess;
-    dim3 grid((unsigned)((Kp + 31) / 32), (unsigned)std::min<int64_t>(Mp / TM, 65535));
-    const bool vec = ((uintptr_t)A_hi % 16 == 0) && ((uintptr_t)A_lo % 16 == 0) && (lda % 2 == 0);
-    if (vec) split_rows_i16_kernel<2><<<grid, 256, 0, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
-    else split_rows_i16_kernel<1><<<grid, 256, 0, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_split_cols_i16(const double* B_hi, const double* B_lo, int64_t ldb, int64_t K,
-                                  int64_t N, int64_t Kp, int32_t* f, int16_t* planes, cudaStream_t st) {
-    const int64_t Np = round_up(N, TN);
-    if (Np == 0 || Kp == 0) return cudaSuccess;
-    dim3 grid((unsigned)((Kp + 31) / 32), (unsigned)std::min<int64_t>(Np / TN, 65535));
-    split_cols_i16_kernel<<<grid, 256, 0, st>>>(B_hi, B_lo, ldb, K, N, Kp, f, planes);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_init_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int64_t K,
                                   cudaStream_t st) {
-    int64_t n = M > N ? M : N;
+    int64_t n = std::max(e ? M : 0, f ? N : 0);
     if (n == 0) return cudaSuccess;
     // K = 0 has no elements to take a maximum over: every exponent is final 0.
     init_exponents_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(e, M, f, N, K == 0 ? 0 : EXP_NONE);
     return cudaGetLastError();
 }
 
-cudaError_t launch_row_exponents(const double* A_hi, int64_t lda, int64_t M, int64_t K,
-                                 int32_t* e, cudaStream_t st) {
-    if (M == 0 || K == 0) return cudaSuccess;
-    const int64_t row_blocks = (M + 7) / 8;
-    const int64_t want = 4LL * num_sms();
-    int64_t ksplit = (want + row_blocks - 1) / row_blocks;
-    ksplit = std::max<int64_t>(1, std::min<int64_t>(ksplit, (K + 511) / 512));
-    const int64_t kchunk = round_up((K + ksplit - 1) / ksplit, 64);
-    ksplit = (K + kchunk - 1) / kchunk;
-    dim3 grid((unsigned)row_blocks, (unsigned)ksplit);
-    const bool vec = ((uintptr_t)A_hi % 16 == 0) && (lda % 2 == 0);
-    if (vec) row_exponents_kernel<2><<<grid, 256, 0, st>>>(A_hi, lda, M, K, kchunk, e);
-    else row_exponents_kernel<1><<<grid, 256, 0, st>>>(A_hi, lda, M, K, kchunk, e);
+cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, cudaStream_t st) {
+    if (K == 0) return cudaSuccess;
+    ExpGrid g{};
+    g.K = K;
+    const int64_t a_rows = A ? (A->rows + 7) / 8 : 0;
+    const int64_t b_cols = B ? (B->rows + 255) / 256 : 0;
+    if (a_rows + b_cols == 0) return cudaSuccess;
+    // About 16 blocks per SM in total, at least 64 (A) / 16 (B) k per chunk.
+    const int64_t want = std::max<int64_t>(1, 16LL * num_sms() / ((A ? 1 : 0) + (B ? 1 : 0)));
+    if (A) {
+        int64_t ks = std::max<int64_t>(1, std::min<int64_t>((want + a_rows - 1) / a_rows, (K + 63) / 64));
+        g.a_kchunk = round_up((K + ks - 1) / ks, 64);
+        g.a_ksplit = (K + g.a_kchunk - 1) / g.a_kchunk;
+        g.A_hi = A->hi; g.lda = A->ld; g.M = A->rows; g.e = A->exp;
+        g.a_items = a_rows * g.a_ksplit;
+    }
+    if (B) {
+        int64_t ks = std::max<int64_t>(1, std::min<int64_t>((want + b_cols - 1) / b_cols, (K + 15) / 16));
+        g.b_kchunk = (K + ks - 1) / ks;
+        g.b_ksplit = (K + g.b_kchunk - 1) / g.b_kchunk;
+        g.B_hi = B->hi; g.ldb = B->ld; g.N = B->rows; g.f = B->exp;
+        g.b_items = b_cols * g.b_ksplit;
+    }
+    const int64_t blocks = (g.a_items > 0 && g.b_items > 0) ? 2 * std::max(g.a_items, g.b_items)
+                                                            : g.a_items + g.b_items;
+    const bool vec = !A || (((uintptr_t)A->hi % 16 == 0) && (A->ld % 2 == 0));
+    if (vec) exponents_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(g);
+    else exponents_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(g);
     return cudaGetLastError();
 }
 
-cudaError_t launch_col_exponents(const double* B_hi, int64_t ldb, int64_t K, int64_t N,
-                                 int32_t* f, cudaStream_t st) {
-    if (N == 0 || K == 0) return cudaSuccess;
-    const int64_t col_blocks = (N + 127) / 128;
-    const int64_t want = 4LL * num_sms();
-    int64_t ksplit = (want + col_blocks - 1) / col_blocks;
-    ksplit = std::max<int64_t>(1, std::min<int64_t>(ksplit, (K + 63) / 64));
-    const int64_t kchunk = (K + ksplit - 1) / ksplit;
-    ksplit = (K + kchunk - 1) / kchunk;
-    dim3 grid((unsigned)col_blocks, (unsigned)ksplit);
-    col_exponents_kernel<<<grid, 128, 0, st>>>(B_hi, ldb, K, N, kchunk, f);
-    return cudaGetLastError();
+static SplitGrid make_split_grid(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
+                                 void* planesA, void* planesB) {
+    SplitGrid g{};
+    g.K = K;
+    g.Kp = Kp;
+    g.KT = (Kp / BK + SPLIT_CHUNKS - 1) / SPLIT_CHUNKS;
+    if (A) { g.A_hi = A->hi; g.A_lo = A->lo; g.lda = A->ld; g.M = A->rows; g.a_tiles = (A->rows + TM - 1) / TM; g.e = A->exp; }
+    if (B) { g.B_hi = B->hi; g.B_lo = B->lo; g.ldb = B->ld; g.N = B->rows; g.b_tiles = (B->rows + TN - 1) / TN; g.f = B->exp; }
+    g.planesA = planesA;
+    g.planesB = planesB;
+    return g;
 }
 
-cudaError_t launch_split_rows(const double* A_hi, const double* A_lo, int64_t lda, int64_t M,
-                              int64_t K, int64_t Kp, int32_t* e, double* planes, cudaStream_t st) {
-    const int64_t Mp = round_up(M, TM);
-    if (Mp == 0 || Kp == 0) return cudaSuccess;
-    dim3 grid((unsigned)((Kp / BK + SPLIT_CHUNKS - 1) / SPLIT_CHUNKS), (unsigned)std::min<int64_t>(Mp / TM, 65535));
-    const bool vec = ((uintptr_t)A_hi % 16 == 0) && ((uintptr_t)A_lo % 16 == 0) && (lda % 2 == 0);
+static bool a_vec(const SplitOperand* A) {
+    return !A || (((uintptr_t)A->hi % 16 == 0) && ((uintptr_t)A->lo % 16 == 0) && (A->ld % 2 == 0));
+}
+
+// One resident wave of blocks: each block walks many items (prefetching).
+static unsigned split_blocks(int64_t items, int per_sm) {
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    return (unsigned)std::max<int64_t>(1, std::min(items, cap));
+}
+
+cudaError_t launch_split_f64(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
+                             double* planesA, double* planesB, cudaStream_t st) {
+    if (Kp == 0) return cudaSuccess;
+    SplitGrid g = make_split_grid(A, B, K, Kp, planesA, planesB);
+    const int64_t items = (g.a_tiles + g.b_tiles) * g.KT;
+    if (items == 0) return cudaSuccess;
     cudaError_t err;
-    if (vec) {
-        err = cudaFuncSetAttribute(split_rows_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
+    if (a_vec(A)) {
+        err = cudaFuncSetAttribute(split_f64_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
         if (err != cudaSuccess) return err;
-        split_rows_kernel<2><<<grid, SPLIT_THREADS, SPLIT_SMEM, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
+        split_f64_kernel<2><<<split_blocks(items, 3), SPLIT_THREADS, SPLIT_SMEM, st>>>(g);
     } else {
-        err = cudaFuncSetAttribute(split_rows_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
+        err = cudaFuncSetAttribute(split_f64_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
         if (err != cudaSuccess) return err;
-        split_rows_kernel<1><<<grid, SPLIT_THREADS, SPLIT_SMEM, st>>>(A_hi, A_lo, lda, M, K, Kp, e, planes);
+        split_f64_kernel<1><<<split_blocks(items, 3), SPLIT_THREADS, SPLIT_SMEM, st>>>(g);
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_split_cols(const double* B_hi, const double* B_lo, int64_t ldb, int64_t K,
-                              int64_t N, int64_t Kp, int32_t* f, double* planes, cudaStream_t st) {
-    const int64_t Np = round_up(N, TN);
-    if (Np == 0 || Kp == 0) return cudaSuccess;
-    dim3 grid((unsigned)((Kp / BK + SPLIT_CHUNKS - 1) / SPLIT_CHUNKS), (unsigned)std::min<int64_t>(Np / TN, 65535));
-    cudaError_t err = cudaFuncSetAttribute(split_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
-    if (err != cudaSuccess) return err;
-    split_cols_kernel<<<grid, SPLIT_THREADS, SPLIT_SMEM, st>>>(B_hi, B_lo, ldb, K, N, Kp, f, planes);
+cudaError_t launch_split_i16(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
+                             int16_t* planesA, int16_t* planesB, cudaStream_t st) {
+    if (Kp == 0) return cudaSuccess;
+    SplitGrid g = make_split_grid(A, B, K, Kp, planesA, planesB);
+    const int64_t items = (g.a_tiles + g.b_tiles) * g.KT;
+    if (items == 0) return cudaSuccess;
+    const unsigned blocks = split_blocks(items, 4 * 4);  // several resident waves: no shared memory to share
+    if (a_vec(A)) split_i16_kernel<2><<<blocks, SPLIT_THREADS, 0, st>>>(g);
+    else split_i16_kernel<1><<<blocks, SPLIT_THREADS, 0, st>>>(g);
     return cudaGetLastError();
 }
 

@@ -79,9 +79,9 @@ ddgemm_status dd_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* by
  * C = A * B (double double), caller-provided workspace.
  * The paper's five steps (Section 2): split into 8 parts, rewrite, multiply on
  * the tensor cores, extract, add the parts into a double double; here run as
- * seven kernels on `stream`: exponent init, row / column exponents, row /
- * column split into part planes, the slice-pair GEMM (FP64 mma.sync), and the
- * recombination.  `workspace` is a device buffer of at least
+ * five kernels on `stream`: exponent reset, row / column exponents, split of
+ * both operands into part planes, the slice-pair GEMM (FP64 mma.sync), and
+ * the recombination.  `workspace` is a device buffer of at least
  * dd_gemm_workspace_size() bytes, 256-byte aligned; its contents on entry do
  * not matter and it must not be used by anything else until the work on
  * `stream` completes.  C must not overlap A, B or the workspace.
@@ -181,6 +181,16 @@ ddgemm_status dd_split_cols(int64_t K, int64_t N,
                             double* planes, int32_t* f, void* stream);
 
 /*
+ * Step 1 for both operands at once (what dd_gemm runs): dd_split_rows on A
+ * and dd_split_cols on B, in three launches (exponent reset, exponents of
+ * both, split of both).  Same outputs and layouts as the two calls.
+ */
+ddgemm_status dd_split(int64_t M, int64_t N, int64_t K,
+                       const double* A_hi, const double* A_lo, int64_t lda,
+                       const double* B_hi, const double* B_lo, int64_t ldb,
+                       double* planesA, int32_t* e, double* planesB, int32_t* f, void* stream);
+
+/*
  * Step 2 (slice-pair GEMM, eqs. (3)-(4) of the paper grouped by index sum):
  *   P[z][d][i][j] = sum_{s+t=d} sum_{k in split z} A_s[i,k] * B_t[k,j],
  *   d = 0..7, for the 36 pairs s + t <= 7, on the FP64 tensor pipe
@@ -246,6 +256,12 @@ ddgemm_status dd_split_rows_i16(int64_t M, int64_t K,
 ddgemm_status dd_split_cols_i16(int64_t K, int64_t N,
                                 const double* B_hi, const double* B_lo, int64_t ldb,
                                 int16_t* planes, int32_t* f, void* stream);
+
+/* Both operands at once, as dd_split, with int16 parts. */
+ddgemm_status dd_split_i16(int64_t M, int64_t N, int64_t K,
+                           const double* A_hi, const double* A_lo, int64_t lda,
+                           const double* B_hi, const double* B_lo, int64_t ldb,
+                           int16_t* planesA, int32_t* e, int16_t* planesB, int32_t* f, void* stream);
 
 /*
  * Step 2 on the integer pipe: P exactly as dd_slice_gemm (splits x 8 x Mp x

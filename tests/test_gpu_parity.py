@@ -269,3 +269,22 @@ def test_many_row_tiles():
     M_hi, M_lo, *_ = slices.sliced_dd_gemm(A_hi[rows], A_lo[rows], B_hi, B_lo)
     assert np.array_equal(G_hi.view(np.int64), M_hi.view(np.int64))
     assert np.array_equal(G_lo.view(np.int64), M_lo.view(np.int64))
+
+
+@pytest.mark.parametrize("M,N,K,dist", SHAPES[:4])
+def test_combined_split_equals_separate(M, N, K, dist):
+    A_hi, A_lo, B_hi, B_lo = _inputs(M, N, K, dist)
+    t = [dev(x) for x in (A_hi, A_lo, B_hi, B_lo)]
+    pA, e, pB, f = ddg.split(*t)
+    qA, e2 = ddg.split_rows(t[0], t[1])
+    qB, f2 = ddg.split_cols(t[2], t[3])
+    assert torch_equal(pA, qA) and torch_equal(pB, qB) and torch_equal(e, e2) and torch_equal(f, f2)
+    iA, ie, iB, jf = ddg.split_i16(*t)
+    rA, re_ = ddg.split_rows_i16(t[0], t[1])
+    rB, rf = ddg.split_cols_i16(t[2], t[3])
+    assert torch_equal(iA, rA) and torch_equal(iB, rB) and torch_equal(ie, re_) and torch_equal(jf, rf)
+
+
+def torch_equal(a, b):
+    import torch
+    return bool(torch.equal(a, b))
