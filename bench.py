@@ -443,11 +443,12 @@ def run_ours(args, w):
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clock_info,
         "int_pipe_variant": {
-            "what": "same 13-bit parts and 36 pairs; products as IMAD.WIDE (32x32->64) into exact int64 "
-                    "sums; C identical bit for bit to the FP64 tensor-pipe path",
+            "what": "same 13-bit parts and 36 pairs; products as 32-bit integer multiply-adds into int32 "
+                    "partial sums flushed into exact int64 totals; C identical bit for bit to the FP64 "
+                    "tensor-pipe path",
             "value": units_i / t_i / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_i / args.steps,
             "identical_to_fp64_path": same_i, "k_splits": splits_i,
-            "roofline": {"bound": "alu", "kernel": "slice_gemm_i64_kernel (mad.wide.s32)",
+            "roofline": {"bound": "alu", "kernel": "slice_gemm_i64_kernel (32-bit IMAD)",
                          "achieved": PAIRS * M * N * K / ti_gemm / 1e12,
                          "peak": IMAD_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3, "unit": "Tops/s",
                          "frac": (PAIRS * M * N * K / ti_gemm / 1e12) / (IMAD_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3),

@@ -321,7 +321,7 @@ def workspace_size_i64(M: int, N: int, K: int) -> int:
 
 def dd_gemm_i64(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, workspace=None, stream=None):
     """The product with the slice-pair GEMM on the integer pipe (int16 parts,
-    exact int64 sums); identical results to dd_gemm.  `workspace` (uint8
+    32-bit multiply-adds, exact int64 totals); identical results to dd_gemm.  `workspace` (uint8
     tensor of workspace_size_i64 bytes) is optional."""
     M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
     wp = workspace.data_ptr() if workspace is not None else None

@@ -45,11 +45,12 @@ int choose_splits(int64_t Mp, int64_t Np, int64_t KC, Engine eng) {
     if (tiles == 0 || KC <= 1) return 1;
     const int per_sm = eng == Engine::kFp64Tensor ? slice_gemm_ctas_per_sm() : slice_gemm_i64_ctas_per_sm();
     const int64_t slots = (int64_t)device_sms() * per_sm;
+    const int64_t blocks_per_tile = eng == Engine::kFp64Tensor ? 1 : 2;  // the integer kernel takes half tiles
     int best = 1;
     double best_score = -1.0;
     const int64_t max_s = std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, KC / 4));
     for (int64_t s = 1; s <= max_s; ++s) {
-        const int64_t blocks = tiles * s;
+        const int64_t blocks = tiles * blocks_per_tile * s;
         const int64_t waves = (blocks + slots - 1) / slots;
         const double eff = (double)blocks / (double)(waves * slots);
         const double score = eff - 0.002 * (double)s;

@@ -222,8 +222,9 @@ ddgemm_status dd_recombine(int64_t M, int64_t N, const double* P, int splits,
 
 /*
  * The same product, with the slice-pair GEMM (step 2) on the integer pipe:
- * the 13-bit parts are stored as int16 and every pair product is a
- * 32 x 32 -> 64-bit integer multiply-add into an exact int64 sum.  The paper
+ * the 13-bit parts are stored as int16 and every pair product is a 32-bit
+ * integer multiply-add into an int32 partial sum, added into an exact int64
+ * total before it could overflow.  The paper
  * runs these products on FP64 tensor cores because they are exact there
  * (eq. (5)); on GB300 the FP64 pipe, which also executes mma.sync f64, is the
  * narrowest unit, while the exactness needs only integer arithmetic.  The
