@@ -53,6 +53,8 @@ BF16_NOMINAL_TF = 2250.0
 FALLBACK_BF16_TF = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 LAUNCHES_PER_STEP = 5  # exponent reset, exponents, split, slice GEMM, recombine
+SIMT_OPS = 17          # FP64 operations per k of the comparator's dd multiply-add
+FP64_PER_CLK_SM = 2    # FP64 (DFMA/DADD/DMUL) instructions per clock per SM (GB300)
 IMAD_PER_CLK_SM = 64   # 32-bit integer multiply-add (also 32x32->64 wide) per clock per SM
 SM_COUNT = 152
 SM_MAX_GHZ = 2.07
@@ -397,6 +399,22 @@ def run_ours(args, w):
     del ws_i, pA16, pB16, Pi
     assert ddg.wait_timeouts() == 0
 
+    # ---- the comparator: plain double-double arithmetic on the FP64 ALUs ----
+    S_hi = torch.empty_like(C_hi)
+    S_lo = torch.empty_like(C_lo)
+    ddg.dd_gemm_simt(dA_hi, dA_lo, dB_hi, dB_lo, S_hi, S_lo, stream=stream)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        ddg.dd_gemm_simt(dA_hi, dA_lo, dB_hi, dB_lo, S_hi, S_lo, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    units_s, t_s = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    Sr_hi = S_hi[:8].cpu().numpy()
+    Sr_lo = S_lo[:8].cpu().numpy()
+    del S_hi, S_lo
+
     if rank != 0:
         return None
 
@@ -415,6 +433,9 @@ def run_ours(args, w):
     normwise = float(np.linalg.norm(d) / (np.linalg.norm(A_hi[rows] + A_lo[rows])
                                           * np.linalg.norm(B_hi + B_lo)))
 
+    n8 = min(8, len(rows))
+    ds = (Sr_hi[:n8] - R_hi[:n8]) + (Sr_lo[:n8] - R_lo[:n8])
+    simt_norm = float(np.linalg.norm(ds) / (np.linalg.norm(A_hi[:n8] + A_lo[:n8]) * np.linalg.norm(B_hi + B_lo)))
     value = units / t_max / 1e9
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -456,6 +477,19 @@ def run_ours(args, w):
                                         f"{SM_MAX_GHZ} GHz", "ms_per_launch": 1e3 * ti_gemm,
                          "ops_per_launch": PAIRS * M * N * K},
             "ms_split_int16": 1e3 * ti_split, "ms_recombine": 1e3 * ti_recomb,
+        },
+        "simt_comparator": {
+            "what": "plain double-double arithmetic on the FP64 ALUs, one accumulator per output "
+                    "(17 FP64 operations per k), no splitting",
+            "value": units_s / t_s / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_s / args.steps,
+            "roofline": {"bound": "alu", "kernel": "simt_dd_gemm_kernel (FP64 pipe)",
+                         "achieved": SIMT_OPS * M * N * K / (t_s / args.steps) / 1e12,
+                         "peak": FP64_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3, "unit": "T FP64 ops/s",
+                         "frac": (SIMT_OPS * M * N * K / (t_s / args.steps) / 1e12)
+                                 / (FP64_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3),
+                         "peak_source": f"{FP64_PER_CLK_SM} FP64 instructions/clk/SM x {SM_COUNT} SMs x "
+                                        f"{SM_MAX_GHZ} GHz"},
+            "normwise_vs_exact_oracle_first_rows": simt_norm,
         },
     }
 

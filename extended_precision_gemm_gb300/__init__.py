@@ -27,7 +27,7 @@ __all__ = [
     "dd_gemm", "dd_gemm_ws", "dd_gemm_host", "dd_gemm_noalloc", "layout", "workspace_size",
     "split_rows", "split_cols", "slice_gemm", "recombine", "wait_timeouts", "fp64_tensor_roof",
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
-    "split", "split_i16",
+    "split", "split_i16", "dd_gemm_simt",
 ]
 
 SLICES = 8
@@ -74,6 +74,7 @@ _SIGNATURES = {
     "dd_slice_gemm_i64": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
     "dd_split": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
     "dd_split_i16": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
+    "dd_gemm_simt": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
 }
 
 
@@ -410,3 +411,13 @@ def split(A_hi, A_lo, B_hi, B_lo, planesA=None, e=None, planesB=None, f=None, st
 def split_i16(A_hi, A_lo, B_hi, B_lo, planesA=None, e=None, planesB=None, f=None, stream=None):
     """Step 1 for both operands with int16 parts: (planesA, e, planesB, f)."""
     return _split_both("dd_split_i16", A_hi, A_lo, B_hi, B_lo, planesA, e, planesB, f, _torch().int16, stream)
+
+
+def dd_gemm_simt(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, stream=None):
+    """The comparator: plain double-double arithmetic on the FP64 ALUs, one
+    accumulator per output (no splitting)."""
+    M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
+    _check("dd_gemm_simt", load().dd_gemm_simt(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                               B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                               C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi), _stream_handle(stream)))
+    return C_hi, C_lo

@@ -402,6 +402,19 @@ ddgemm_status dd_wait_timeouts(unsigned int* count) {
     return s;
 }
 
+// ---- the comparator ----
+
+ddgemm_status dd_gemm_simt(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                           int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb, double* C_hi,
+                           double* C_lo, int64_t ldc, void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    if ((M + 31) / 32 > 65535) return DDGEMM_ERR_UNSUPPORTED;
+    return from_cuda(launch_simt_dd_gemm(A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc, M, N, K,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 // ---- integer-pipe variant ----
 
 ddgemm_status dd_gemm_i64_layout(int64_t M, int64_t N, int64_t K, int* splits) {

@@ -49,6 +49,12 @@ cudaError_t launch_recombine(const double* P, int splits, int64_t Mp, int64_t Np
 // (TFLOP/s); synchronises `st`.
 cudaError_t measure_dmma_roof(double* tflops, cudaStream_t st);
 
+// The comparator: double-double GEMM on the FP64 ALUs, one accumulator per
+// output, k in order.
+cudaError_t launch_simt_dd_gemm(const double* A_hi, const double* A_lo, int64_t lda, const double* B_hi,
+                                const double* B_lo, int64_t ldb, double* C_hi, double* C_lo, int64_t ldc,
+                                int64_t M, int64_t N, int64_t K, cudaStream_t st);
+
 // Diagnostics of the bounded waits inside the slice GEMM.
 cudaError_t read_and_reset_wait_timeouts(unsigned int* count);
 

@@ -217,6 +217,26 @@ ddgemm_status dd_recombine(int64_t M, int64_t N, const double* P, int splits,
                            double* C_hi, double* C_lo, int64_t ldc, void* stream);
 
 /* ------------------------------------------------------------------ */
+/* Comparator                                                           */
+/* ------------------------------------------------------------------ */
+
+/*
+ * C = A * B with plain double-double arithmetic on the FP64 ALUs, no
+ * splitting: the second method of Section 4.2 of the paper (one thread per
+ * inner product, double-double multiply and add).  Per k, in order:
+ *   p = a_hi b_hi; e = fma(a_hi, b_hi, -p); e += a_hi b_lo + a_lo b_hi;
+ *   (s, t) = two_sum(c_hi, p); t = (t + c_lo) + e;
+ *   (c_hi, c_lo) = quick_two_sum(s, t).
+ * Not the method under evaluation: it is the reference point the paper
+ * compares against.  Same argument checks as dd_gemm (including K <=
+ * DDGEMM_MAX_K); M <= 2097120.
+ */
+ddgemm_status dd_gemm_simt(int64_t M, int64_t N, int64_t K,
+                           const double* A_hi, const double* A_lo, int64_t lda,
+                           const double* B_hi, const double* B_lo, int64_t ldb,
+                           double* C_hi, double* C_lo, int64_t ldc, void* stream);
+
+/* ------------------------------------------------------------------ */
 /* Integer-pipe variant of the slice-pair GEMM                          */
 /* ------------------------------------------------------------------ */
 
