@@ -65,6 +65,9 @@ def _load():
             f.argtypes = [i64, i64, i64, dp, dp, i64, dp, dp, i64,
                           i64, ip, i64, ip, dp, dp, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
+            g = lib.oracle_md_gemm_block
+            g.restype = ctypes.c_int
+            g.argtypes = [ctypes.c_int, i64, i64, i64, dp, i64, dp, i64, i64, ip, i64, ip, dp, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -103,3 +106,33 @@ def exact_dd_gemm(A_hi, A_lo, B_hi, B_lo, rows=None, cols=None, threads: int = 0
     if rc != 0:
         raise ValueError({1: "bad argument", 2: "non-finite input", 3: "out of host memory"}.get(rc, rc))
     return out_hi, out_lo
+
+
+def exact_md_gemm(A_parts, B_parts, rows=None, cols=None, threads: int = 0):
+    """Exact product of multiple-double matrices (A = sum of the planes in
+    A_parts, B likewise), rounded once into len(A_parts) non-overlapping
+    doubles: x_0 = RN(X), x_1 = RN(X - x_0), ...  Returns the list of part
+    planes for the chosen rows and columns."""
+    A_parts = [_f64(a) for a in A_parts]
+    B_parts = [_f64(b) for b in B_parts]
+    np_ = len(A_parts)
+    if len(B_parts) != np_:
+        raise ValueError("A and B need the same number of parts")
+    M, K = A_parts[0].shape
+    K2, N = B_parts[0].shape
+    if K2 != K or any(a.shape != (M, K) for a in A_parts) or any(b.shape != (K, N) for b in B_parts):
+        raise ValueError("shape mismatch")
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.arange(N, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    outs = [np.zeros((rows.size, cols.size)) for _ in range(np_)]
+    PtrArr = ctypes.c_void_p * np_
+    a_ptrs = PtrArr(*[a.ctypes.data for a in A_parts])
+    b_ptrs = PtrArr(*[b.ctypes.data for b in B_parts])
+    o_ptrs = PtrArr(*[o.ctypes.data for o in outs])
+    rc = _load().oracle_md_gemm_block(np_, M, N, K, ctypes.cast(a_ptrs, ctypes.c_void_p), K,
+                                      ctypes.cast(b_ptrs, ctypes.c_void_p), N,
+                                      rows.size, rows.ctypes.data, cols.size, cols.ctypes.data,
+                                      ctypes.cast(o_ptrs, ctypes.c_void_p), int(threads))
+    if rc != 0:
+        raise ValueError({1: "bad argument", 2: "non-finite input", 3: "out of host memory"}.get(rc, rc))
+    return outs

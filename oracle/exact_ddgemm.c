@@ -276,6 +276,98 @@ int oracle_dd_gemm_block(int64_t M, int64_t N, int64_t K,
     return 0;
 }
 
+/*
+ * Multiple doubles with `np` parts (2: double double, 4: quad double): the
+ * exact value X_ij = sum_k (sum_p A_p[i,k]) (sum_q B_q[k,j]) rounded once to
+ * np non-overlapping doubles, x_0 = RN(X), x_1 = RN(X - x_0), ...,
+ * x_{np-1} = RN(X - x_0 - ... - x_{np-2}) ("Multiple Double Arithmetic on
+ * NVIDIA Tensor Cores", Definition 1.1: a multiple double is an unevaluated
+ * sum of non-overlapping doubles).  Apart[p] / Bpart[p] are the part planes
+ * (row-major, leading dimensions lda / ldb); out[p] receives part p of the
+ * nrows x ncols block.  Return codes as oracle_dd_gemm_block.
+ */
+#define MAX_PARTS 8
+
+static void entry_md(const dec_t* arow, const dec_t* bcol, int64_t K, int np, acc_t* acc,
+                     double* const* out, int64_t t) {
+    acc_clear(acc);
+    for (int64_t k = 0; k < K; ++k) {
+        const dec_t* x = arow + np * k;
+        const dec_t* y = bcol + np * k;
+        for (int p = 0; p < np; ++p)
+            for (int q = 0; q < np; ++q) acc_add_product(acc, &x[p], &y[q]);
+    }
+    int neg;
+    acc_normalize(acc, &neg);
+    for (int p = 0; p < np; ++p) {
+        double v = acc_round(acc, neg);
+        out[p][t] = v + 0.0;
+        if (v == 0.0 || !isfinite(v)) {
+            for (int r = p + 1; r < np; ++r) out[r][t] = 0.0;
+            return;
+        }
+        /* subtract v exactly and continue with the remainder */
+        if (neg)
+            for (int i = acc->lo; i <= acc->hi; ++i) acc->limb[i] = -acc->limb[i];
+        dec_t h, one;
+        decompose(-v, &h);
+        one.m = 1; one.e = 0; one.neg = 0;
+        acc_add_product(acc, &h, &one);
+        acc_normalize(acc, &neg);
+    }
+}
+
+int oracle_md_gemm_block(int np, int64_t M, int64_t N, int64_t K,
+                         const double* const* Apart, int64_t lda,
+                         const double* const* Bpart, int64_t ldb,
+                         int64_t nrows, const int64_t* rows,
+                         int64_t ncols, const int64_t* cols,
+                         double* const* out, int nthreads) {
+    if (np < 1 || np > MAX_PARTS) return 1;
+    if (M < 0 || N < 0 || K < 0 || (int64_t)np * np * K > 4 * MAX_K || nrows < 0 || ncols < 0) return 1;
+    if (nrows == 0 || ncols == 0) return 0;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return 1;
+    for (int64_t c = 0; c < ncols; ++c)
+        if (cols[c] < 0 || cols[c] >= N) return 1;
+    if (K == 0) {
+        for (int p = 0; p < np; ++p)
+            for (int64_t t = 0; t < nrows * ncols; ++t) out[p][t] = 0.0;
+        return 0;
+    }
+    size_t kk = (size_t)np * (size_t)K;
+    dec_t* adec = (dec_t*)malloc(sizeof(dec_t) * kk * (size_t)nrows);
+    dec_t* bdec = (dec_t*)malloc(sizeof(dec_t) * kk * (size_t)ncols);
+    if (!adec || !bdec) { free(adec); free(bdec); return 3; }
+    int bad = 0;
+    for (int64_t r = 0; r < nrows; ++r)
+        for (int64_t k = 0; k < K; ++k)
+            for (int p = 0; p < np; ++p)
+                bad |= decompose(Apart[p][rows[r] * lda + k], &adec[r * kk + (size_t)np * k + p]);
+    for (int64_t c = 0; c < ncols; ++c)
+        for (int64_t k = 0; k < K; ++k)
+            for (int p = 0; p < np; ++p)
+                bad |= decompose(Bpart[p][k * ldb + cols[c]], &bdec[c * kk + (size_t)np * k + p]);
+    if (bad) { free(adec); free(bdec); return 2; }
+    int64_t total = nrows * ncols;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel
+    {
+        acc_t* acc = (acc_t*)malloc(sizeof(acc_t));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t t = 0; t < total; ++t) {
+            int64_t r = t / ncols, c = t % ncols;
+            entry_md(adec + r * kk, bdec + c * kk, K, np, acc, out, t);
+        }
+        free(acc);
+    }
+    free(adec);
+    free(bdec);
+    return 0;
+}
+
 /* Number of threads an OpenMP parallel region uses by default. */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

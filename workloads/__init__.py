@@ -28,7 +28,7 @@ import dataclasses
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "make_dd", "make_workload", "two_sum_np"]
+__all__ = ["Workload", "WORKLOADS", "make_dd", "make_workload", "two_sum_np", "make_md"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -102,3 +102,38 @@ def make_dd(M: int, N: int, K: int, dist: str, seed: int):
 def make_workload(index: int):
     w = WORKLOADS[index]
     return make_dd(w.M, w.N, w.K, w.dist, w.seed)
+
+
+def _draw_md(rng, rows, cols, dist, scale_axis, parts):
+    """A multiple double with `parts` planes: x_0 as the high word of the
+    distribution, then x_{p+1} = ulp(x_p)/2 * U[-1,1], which keeps every part
+    below half an ulp of the previous one (non-overlapping, normalised)."""
+    shape = (rows, cols)
+    if dist in ("uniform", "uniform_exp20"):
+        x0 = rng.uniform(-1.0, 1.0, shape)
+        if dist == "uniform_exp20":
+            x0 = np.ldexp(x0, rng.integers(-20, 21, shape))
+    elif dist in ("normal", "normal_rowcol30"):
+        x0 = rng.standard_normal(shape)
+        if dist == "normal_rowcol30":
+            if scale_axis == 0:
+                x0 = np.ldexp(x0, rng.integers(-30, 31, rows)[:, None])
+            else:
+                x0 = np.ldexp(x0, rng.integers(-30, 31, cols)[None, :])
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    out = [np.ascontiguousarray(x0)]
+    for _ in range(parts - 1):
+        half_ulp = np.spacing(np.abs(out[-1])) * 0.5
+        nxt = np.where(out[-1] == 0, 0.0, half_ulp * rng.uniform(-1.0, 1.0, shape))
+        out.append(np.ascontiguousarray(nxt))
+    return out
+
+
+def make_md(M: int, N: int, K: int, dist: str, seed: int, parts: int = 4):
+    """A (M x K) and B (K x N) multiple-double operands as lists of `parts`
+    planes each (same draw order as make_dd: A's draws, then B's)."""
+    rng = np.random.default_rng(seed)
+    A = _draw_md(rng, M, K, dist, 0, parts)
+    B = _draw_md(rng, K, N, dist, 1, parts)
+    return A, B
