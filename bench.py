@@ -219,6 +219,12 @@ def oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, rows):
     return time.perf_counter() - t0, C_hi, C_lo
 
 
+def oracle_md_rows(A_parts, B_parts, rows):
+    import numpy as np
+    import oracle
+    return oracle.exact_md_gemm(A_parts, B_parts, rows=np.asarray(rows))
+
+
 def cpu_baseline(w, A_hi, A_lo, B_hi, B_lo, target_s: float = 12.0):
     import oracle
     r0 = list(range(min(16, w.M)))   # one row per core or so: calibrates the parallel rate
@@ -415,6 +421,25 @@ def run_ours(args, w):
     Sr_lo = S_lo[:8].cpu().numpy()
     del S_hi, S_lo
 
+    # ---- quad doubles on the integer pipe (same shape and distribution) ----
+    QA, QB = workloads.make_md(M, N, K, w.dist, w.seed, 4)
+    tQA = [torch.from_numpy(x).to(dev) for x in QA]
+    tQB = [torch.from_numpy(x).to(dev) for x in QB]
+    QC = [torch.empty((M, N), dtype=torch.float64, device=dev) for _ in range(4)]
+    ws_q = torch.empty(ddg.qd_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    ddg.qd_gemm(tQA, tQB, QC, workspace=ws_q, stream=stream)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        ddg.qd_gemm(tQA, tQB, QC, workspace=ws_q, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    units_q, t_q = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    qd_rows = [QC[p][:2].cpu().numpy() for p in range(4)]
+    del tQA, tQB, QC, ws_q
+    assert ddg.wait_timeouts() == 0
+
     if rank != 0:
         return None
 
@@ -433,6 +458,9 @@ def run_ours(args, w):
     normwise = float(np.linalg.norm(d) / (np.linalg.norm(A_hi[rows] + A_lo[rows])
                                           * np.linalg.norm(B_hi + B_lo)))
 
+    QR = oracle_md_rows(QA, QB, [0, 1])
+    dq = sum(qd_rows[p] - QR[p] for p in range(4))
+    qd_norm = float(np.linalg.norm(dq) / (np.linalg.norm(sum(a[:2] for a in QA)) * np.linalg.norm(sum(QB))))
     n8 = min(8, len(rows))
     ds = (Sr_hi[:n8] - R_hi[:n8]) + (Sr_lo[:n8] - R_lo[:n8])
     simt_norm = float(np.linalg.norm(ds) / (np.linalg.norm(A_hi[:n8] + A_lo[:n8]) * np.linalg.norm(B_hi + B_lo)))
@@ -477,6 +505,15 @@ def run_ours(args, w):
                                         f"{SM_MAX_GHZ} GHz", "ms_per_launch": 1e3 * ti_gemm,
                          "ops_per_launch": PAIRS * M * N * K},
             "ms_split_int16": 1e3 * ti_split, "ms_recombine": 1e3 * ti_recomb,
+        },
+        "qd_int_pipe": {
+            "what": "quad-double GEMM (4 doubles per number): 16 parts of 13 bits, 136 pairs on the "
+                    "integer pipe, exact sums rounded once into 4 doubles",
+            "workload": w.name.replace("dd_gemm", "qd_gemm"),
+            "value": units_q / t_q / 1e9, "unit": "qd-GFLOP/s (2MNK/s)", "ms_per_step": 1e3 * t_q / args.steps,
+            "slice_pairs": 136,
+            "multiply_adds_per_s": 136 * M * N * K / (t_q / args.steps),
+            "normwise_vs_exact_oracle_2_rows": qd_norm,
         },
         "simt_comparator": {
             "what": "plain double-double arithmetic on the FP64 ALUs, one accumulator per output "

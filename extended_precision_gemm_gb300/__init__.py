@@ -28,6 +28,7 @@ __all__ = [
     "split_rows", "split_cols", "slice_gemm", "recombine", "wait_timeouts", "fp64_tensor_roof",
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
     "split", "split_i16", "dd_gemm_simt",
+    "QD_MAX_K", "qd_gemm", "qd_layout", "qd_workspace_size", "qd_split", "qd_slice_gemm", "qd_recombine",
 ]
 
 SLICES = 8
@@ -75,6 +76,12 @@ _SIGNATURES = {
     "dd_split": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
     "dd_split_i16": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
     "dd_gemm_simt": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
+    "qd_gemm_layout": ([_i64, _i64, _i64, _ptr], _int),
+    "qd_gemm_workspace_size": ([_i64, _i64, _i64, _ptr], _int),
+    "qd_gemm": ([_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, ctypes.c_size_t, _ptr], _int),
+    "qd_split": ([_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
+    "qd_slice_gemm": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
+    "qd_recombine": ([_i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _i64, _ptr], _int),
 }
 
 
@@ -421,3 +428,96 @@ def dd_gemm_simt(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, stream=None):
                                                B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
                                                C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi), _stream_handle(stream)))
     return C_hi, C_lo
+
+
+# ---- quad doubles (4 doubles per number) on the integer pipe ----
+
+QD_MAX_K = 1 << 23
+QD_PARTS = 16
+
+
+def _ptr_array(tensors):
+    arr = (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+    return arr
+
+
+def _qd_planes(X, name):
+    if len(X) != 4:
+        raise ValueError(f"{name} must be a list of 4 planes")
+    for t in X:
+        _mat(t, name)
+    if any(t.shape != X[0].shape or t.stride() != X[0].stride() for t in X):
+        raise ValueError(f"the planes of {name} must share shape and strides")
+    return X
+
+
+def qd_layout(M: int, N: int, K: int) -> int:
+    sp = _int()
+    _check("qd_gemm_layout", load().qd_gemm_layout(M, N, K, ctypes.byref(sp)))
+    return sp.value
+
+
+def qd_workspace_size(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check("qd_gemm_workspace_size", load().qd_gemm_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def qd_gemm(A, B, C=None, workspace=None, stream=None):
+    """Quad-double product: A, B lists of 4 float64 planes (x0 + x1 + x2 + x3);
+    returns the 4 planes of C."""
+    torch = _torch()
+    A, B = _qd_planes(A, "A"), _qd_planes(B, "B")
+    M, K = A[0].shape
+    K2, N = B[0].shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    if C is None:
+        C = [torch.empty((M, N), dtype=torch.float64, device=A[0].device) for _ in range(4)]
+    C = _qd_planes(C, "C")
+    pa, pb, pc = _ptr_array(A), _ptr_array(B), _ptr_array(C)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("qd_gemm", load().qd_gemm(M, N, K, ctypes.cast(pa, ctypes.c_void_p), _ld(A[0]),
+                                     ctypes.cast(pb, ctypes.c_void_p), _ld(B[0]),
+                                     ctypes.cast(pc, ctypes.c_void_p), _ld(C[0]), wp, wn, _stream_handle(stream)))
+    return C
+
+
+def qd_split(A, B, stream=None):
+    """(planesA int16, e, planesB int16, f) of the quad-double split."""
+    torch = _torch()
+    A, B = _qd_planes(A, "A"), _qd_planes(B, "B")
+    M, K = A[0].shape
+    N = B[0].shape[1]
+    Mp, Np, Kp = -(-M // TILE_M) * TILE_M, -(-N // TILE_N) * TILE_N, -(-K // CHUNK_K) * CHUNK_K
+    dev = A[0].device
+    pA = torch.empty(QD_PARTS * Mp * Kp, dtype=torch.int16, device=dev)
+    pB = torch.empty(QD_PARTS * Np * Kp, dtype=torch.int16, device=dev)
+    e = torch.empty(M, dtype=torch.int32, device=dev)
+    f = torch.empty(N, dtype=torch.int32, device=dev)
+    pa, pb = _ptr_array(A), _ptr_array(B)
+    _check("qd_split", load().qd_split(M, N, K, ctypes.cast(pa, ctypes.c_void_p), _ld(A[0]),
+                                       ctypes.cast(pb, ctypes.c_void_p), _ld(B[0]), pA.data_ptr(), e.data_ptr(),
+                                       pB.data_ptr(), f.data_ptr(), _stream_handle(stream)))
+    return pA, e, pB, f
+
+
+def qd_slice_gemm(M: int, N: int, K: int, planesA, planesB, splits: int, stream=None):
+    """P (splits x 16 x Mp x Np doubles) of the quad-double slice GEMM."""
+    torch = _torch()
+    Mp, Np = -(-M // TILE_M) * TILE_M, -(-N // TILE_N) * TILE_N
+    P = torch.empty((splits, QD_PARTS, Mp, Np), dtype=torch.float64, device=planesA.device)
+    _check("qd_slice_gemm", load().qd_slice_gemm(M, N, K, planesA.data_ptr(), planesB.data_ptr(), splits,
+                                                 P.data_ptr(), _stream_handle(stream)))
+    return P
+
+
+def qd_recombine(M: int, N: int, P, e, f, stream=None):
+    """The 4 planes of C from P and the exponents."""
+    torch = _torch()
+    C = [torch.empty((M, N), dtype=torch.float64, device=P.device) for _ in range(4)]
+    pc = _ptr_array(C)
+    _check("qd_recombine", load().qd_recombine(M, N, P.data_ptr(), P.shape[0], e.data_ptr(), f.data_ptr(),
+                                               ctypes.cast(pc, ctypes.c_void_p), max(N, 1), _stream_handle(stream)))
+    return C

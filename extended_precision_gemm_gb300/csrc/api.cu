@@ -35,7 +35,7 @@ int device_sms() {
 
 // Which slice GEMM a layout is for: FP64 parts for mma.sync f64, or int16
 // parts for the integer pipe.
-enum class Engine { kFp64Tensor, kInt64Pipe };
+enum class Engine { kFp64Tensor, kInt64Pipe, kQuadInt64 };
 
 // k-split of the slice GEMM: the smallest split count whose waves of blocks
 // fill the GPU best (tiles * splits over whole waves of resident blocks),
@@ -43,9 +43,12 @@ enum class Engine { kFp64Tensor, kInt64Pipe };
 int choose_splits(int64_t Mp, int64_t Np, int64_t KC, Engine eng) {
     const int64_t tiles = (Mp / TM) * (Np / TN);
     if (tiles == 0 || KC <= 1) return 1;
-    const int per_sm = eng == Engine::kFp64Tensor ? slice_gemm_ctas_per_sm() : slice_gemm_i64_ctas_per_sm();
+    const int per_sm = eng == Engine::kFp64Tensor ? slice_gemm_ctas_per_sm()
+                       : eng == Engine::kInt64Pipe ? slice_gemm_i64_ctas_per_sm()
+                                                   : slice_gemm_qd_ctas_per_sm();
     const int64_t slots = (int64_t)device_sms() * per_sm;
-    const int64_t blocks_per_tile = eng == Engine::kFp64Tensor ? 1 : 2;  // the integer kernel takes half tiles
+    // blocks per 32 x 32 tile: the integer kernels take half / quarter tiles
+    const int64_t blocks_per_tile = eng == Engine::kFp64Tensor ? 1 : eng == Engine::kInt64Pipe ? 2 : 4;
     int best = 1;
     double best_score = -1.0;
     const int64_t max_s = std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, KC / 4));
@@ -67,13 +70,14 @@ Layout make_layout(int64_t M, int64_t N, int64_t K, Engine eng = Engine::kFp64Te
     L.KC = L.Kp / BK;
     L.splits = choose_splits(L.Mp, L.Np, L.KC, eng);
     const int64_t part_bytes = eng == Engine::kFp64Tensor ? 8 : 2;
+    const int64_t parts = eng == Engine::kQuadInt64 ? 16 : S;
     int64_t off = 0;
     auto take = [&](int64_t bytes) { int64_t o = off; off = round_up(off + bytes, kAlign); return o; };
     L.off_e = take(L.Mp * 4);
     L.off_f = take(L.Np * 4);
-    L.off_A = take(S * L.Mp * L.Kp * part_bytes);
-    L.off_B = take(S * L.Np * L.Kp * part_bytes);
-    L.off_P = take((int64_t)L.splits * S * L.Mp * L.Np * 8);
+    L.off_A = take(parts * L.Mp * L.Kp * part_bytes);
+    L.off_B = take(parts * L.Np * L.Kp * part_bytes);
+    L.off_P = take((int64_t)L.splits * parts * L.Mp * L.Np * 8);
     L.total = off;
     return L;
 }
@@ -395,10 +399,11 @@ ddgemm_status dd_fp64_tensor_roof(double* tflops, void* stream) {
 
 ddgemm_status dd_wait_timeouts(unsigned int* count) {
     if (count == nullptr) return DDGEMM_ERR_INVALID_ARG;
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, c = 0;
     ddgemm_status s = from_cuda(read_and_reset_wait_timeouts(&a));
     if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_i64(&b));
-    *count = a + b;
+    if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_qd(&c));
+    *count = a + b + c;
     return s;
 }
 
@@ -500,6 +505,127 @@ ddgemm_status dd_slice_gemm_i64(int64_t M, int64_t N, int64_t K, const int16_t* 
         return DDGEMM_ERR_INVALID_ARG;
     return from_cuda(launch_slice_gemm_i64(planesA, planesB, Mp, Np, Kp, splits, P,
                                            static_cast<cudaStream_t>(stream)));
+}
+
+// ---- quad doubles on the integer pipe ----
+
+static ddgemm_status check_qd_args(int64_t M, int64_t N, int64_t K, const double* const* A, int64_t lda,
+                                   const double* const* B, int64_t ldb, double* const* C, int64_t ldc) {
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) || ldc < std::max<int64_t>(1, N))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if ((round_up(M, TM) / TM) * (round_up(N, TN) / TN) * 4 > kMaxTiles) return DDGEMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    if (A == nullptr || B == nullptr || C == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    const int64_t a = span_bytes(M, K, lda), b = span_bytes(K, N, ldb), c = span_bytes(M, N, ldc);
+    for (int p = 0; p < 4; ++p) {
+        if (C[p] == nullptr || (K > 0 && (A[p] == nullptr || B[p] == nullptr))) return DDGEMM_ERR_INVALID_ARG;
+        for (int q = 0; q < 4; ++q) {
+            if (ranges_overlap(C[p], c, A[q], a) || ranges_overlap(C[p], c, B[q], b)) return DDGEMM_ERR_INVALID_ARG;
+            if (q != p && ranges_overlap(C[p], c, C[q], c)) return DDGEMM_ERR_INVALID_ARG;
+        }
+    }
+    return DDGEMM_OK;
+}
+
+static ddgemm_status run_qd(const Layout& L, int64_t M, int64_t N, int64_t K, const double* const* A, int64_t lda,
+                            const double* const* B, int64_t ldb, double* const* C, int64_t ldc, char* ws,
+                            cudaStream_t st) {
+    int32_t* e = reinterpret_cast<int32_t*>(ws + L.off_e);
+    int32_t* f = reinterpret_cast<int32_t*>(ws + L.off_f);
+    int16_t* pA = reinterpret_cast<int16_t*>(ws + L.off_A);
+    int16_t* pB = reinterpret_cast<int16_t*>(ws + L.off_B);
+    double* P = reinterpret_cast<double*>(ws + L.off_P);
+    SplitOperand a{A[0], A[1], lda, M, e}, b{B[0], B[1], ldb, N, f};
+    DDG_TRY(launch_init_exponents(e, M, f, N, K, st));
+    DDG_TRY(launch_exponents(&a, &b, K, st));
+    DDG_TRY(launch_split_qd(A, lda, M, e, B, ldb, N, f, K, L.Kp, pA, pB, st));
+    DDG_TRY(launch_slice_gemm_qd(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_TRY(launch_recombine_qd(P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
+    return DDGEMM_OK;
+}
+
+ddgemm_status qd_gemm_layout(int64_t M, int64_t N, int64_t K, int* splits) {
+    if (M < 0 || N < 0 || K < 0 || splits == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    *splits = make_layout(M, N, K, Engine::kQuadInt64).splits;
+    return DDGEMM_OK;
+}
+
+ddgemm_status qd_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    if (bytes == nullptr || M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    *bytes = (size_t)make_layout(M, N, K, Engine::kQuadInt64).total;
+    return DDGEMM_OK;
+}
+
+ddgemm_status qd_gemm(int64_t M, int64_t N, int64_t K, const double* const* A, int64_t lda,
+                      const double* const* B, int64_t ldb, double* const* C, int64_t ldc, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    ddgemm_status s = check_qd_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (s != DDGEMM_OK || M == 0 || N == 0) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Layout L = make_layout(M, N, K, Engine::kQuadInt64);
+    if (workspace != nullptr) {
+        if ((uintptr_t)workspace % kAlign != 0 || workspace_bytes < (size_t)L.total) return DDGEMM_ERR_INVALID_ARG;
+        return run_qd(L, M, N, K, A, lda, B, ldb, C, ldc, static_cast<char*>(workspace), st);
+    }
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    s = run_qd(L, M, N, K, A, lda, B, ldb, C, ldc, static_cast<char*>(ws), st);
+    cudaError_t fe = cudaFreeAsync(ws, st);
+    if (s == DDGEMM_OK && fe != cudaSuccess) s = DDGEMM_ERR_CUDA;
+    return s;
+}
+
+ddgemm_status qd_split(int64_t M, int64_t N, int64_t K, const double* const* A, int64_t lda,
+                       const double* const* B, int64_t ldb, int16_t* planesA, int32_t* e, int16_t* planesB,
+                       int32_t* f, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if ((M > 0 && (e == nullptr || A == nullptr || (K > 0 && planesA == nullptr))) ||
+        (N > 0 && (f == nullptr || B == nullptr || (K > 0 && planesB == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t Kp = round_up(K, BK);
+    SplitOperand a{M > 0 ? A[0] : nullptr, nullptr, lda, M, e}, b{N > 0 ? B[0] : nullptr, nullptr, ldb, N, f};
+    DDG_TRY(launch_init_exponents(M > 0 ? e : nullptr, M, N > 0 ? f : nullptr, N, K, st));
+    DDG_TRY(launch_exponents(M > 0 ? &a : nullptr, N > 0 ? &b : nullptr, K, st));
+    DDG_TRY(launch_split_qd(M > 0 ? A : nullptr, lda, M, e, N > 0 ? B : nullptr, ldb, N, f, K, Kp, planesA,
+                            planesB, st));
+    return DDGEMM_OK;
+}
+
+ddgemm_status qd_slice_gemm(int64_t M, int64_t N, int64_t K, const int16_t* planesA, const int16_t* planesB,
+                            int splits, double* P, void* stream) {
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    const int64_t Mp = round_up(M, TM), Np = round_up(N, TN), Kp = round_up(K, BK), KC = Kp / BK;
+    if (splits < 1 || splits > kMaxSplits || (KC > 0 && splits > KC) || (KC == 0 && splits != 1))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (P == nullptr || (K > 0 && (planesA == nullptr || planesB == nullptr))) return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0 || (uintptr_t)P % 16 != 0)
+        return DDGEMM_ERR_INVALID_ARG;
+    return from_cuda(launch_slice_gemm_qd(planesA, planesB, Mp, Np, Kp, splits, P, static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, const int32_t* e, const int32_t* f,
+                           double* const* C, int64_t ldc, void* stream) {
+    if (M < 0 || N < 0 || ldc < std::max<int64_t>(1, N) || splits < 1 || splits > kMaxSplits)
+        return DDGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    if (P == nullptr || e == nullptr || f == nullptr || C == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    for (int p = 0; p < 4; ++p)
+        if (C[p] == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    const int64_t Mp = round_up(M, TM), Np = round_up(N, TN);
+    return from_cuda(launch_recombine_qd(P, splits, Mp, Np, e, f, M, N, C, ldc, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

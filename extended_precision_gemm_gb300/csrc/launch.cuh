@@ -55,6 +55,20 @@ cudaError_t launch_simt_dd_gemm(const double* A_hi, const double* A_lo, int64_t 
                                 const double* B_lo, int64_t ldb, double* C_hi, double* C_lo, int64_t ldc,
                                 int64_t M, int64_t N, int64_t K, cudaStream_t st);
 
+// Quad doubles on the integer pipe: 16 int16 parts per element, 136 pairs,
+// exact sums rounded once into 4 doubles.  A / B / C are arrays of 4 plane
+// pointers.
+cudaError_t launch_split_qd(const double* const* A, int64_t lda, int64_t M, const int32_t* e,
+                            const double* const* B, int64_t ldb, int64_t N, const int32_t* f, int64_t K,
+                            int64_t Kp, int16_t* planesA, int16_t* planesB, cudaStream_t st);
+cudaError_t launch_slice_gemm_qd(const int16_t* planesA, const int16_t* planesB, int64_t Mp, int64_t Np,
+                                 int64_t Kp, int splits, double* P, cudaStream_t st);
+int slice_gemm_qd_ctas_per_sm();
+cudaError_t launch_recombine_qd(const double* P, int splits, int64_t Mp, int64_t Np, const int32_t* e,
+                                const int32_t* f, int64_t M, int64_t N, double* const* C, int64_t ldc,
+                                cudaStream_t st);
+cudaError_t read_and_reset_wait_timeouts_qd(unsigned int* count);
+
 // Diagnostics of the bounded waits inside the slice GEMM.
 cudaError_t read_and_reset_wait_timeouts(unsigned int* count);
 

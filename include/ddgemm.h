@@ -294,6 +294,48 @@ ddgemm_status dd_slice_gemm_i64(int64_t M, int64_t N, int64_t K,
                                 int splits, double* P, void* stream);
 
 /* ------------------------------------------------------------------ */
+/* Quad doubles (4 doubles per number) on the integer pipe              */
+/* ------------------------------------------------------------------ */
+
+/*
+ * C = A * B for quad-double matrices: every number is x0 + x1 + x2 + x3, four
+ * non-overlapping doubles (|x_{p+1}| <= ulp(x_p)/2), passed as four row-major
+ * planes sharing one leading dimension (A, B, C: host arrays of 4 device
+ * pointers).  The method of Section 2 of the paper for more parts ("a
+ * quartered quad double matrix has 16 times the size", Table 2): 16 parts of
+ * 13 bits on a shared row / column exponent, the 136 index-sum pairs
+ * s + t <= 15 as exact integer sums on the integer pipe, and the 16 parts of
+ * the product summed exactly and rounded once into four doubles
+ * (c0 = RN(X), c1 = RN(X - c0), ...).  K <= QDGEMM_MAX_K (2^23) keeps every
+ * part sum below 2^53.  `workspace` (qd_gemm_workspace_size bytes, 256-byte
+ * aligned) may be NULL: then it comes from the stream-ordered allocator.
+ */
+#define QDGEMM_MAX_K (1 << 23)
+ddgemm_status qd_gemm_layout(int64_t M, int64_t N, int64_t K, int* splits);
+ddgemm_status qd_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+ddgemm_status qd_gemm(int64_t M, int64_t N, int64_t K,
+                      const double* const* A, int64_t lda,
+                      const double* const* B, int64_t ldb,
+                      double* const* C, int64_t ldc,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The steps of qd_gemm.  qd_split: exponents e (M) and f (N) as for double
+ * doubles (from the leading planes) and the 16 int16 parts of every element,
+ * layout planes[((((tile * KC + kc) * 8 + kk) * 32 + ti) * 16) + s]
+ * (16 * Mp * Kp int16 for A, 16 * Np * Kp for B).  qd_slice_gemm: P
+ * (splits x 16 x Mp x Np doubles holding exact integers).  qd_recombine: the
+ * four output planes from P and the exponents.
+ */
+ddgemm_status qd_split(int64_t M, int64_t N, int64_t K,
+                       const double* const* A, int64_t lda, const double* const* B, int64_t ldb,
+                       int16_t* planesA, int32_t* e, int16_t* planesB, int32_t* f, void* stream);
+ddgemm_status qd_slice_gemm(int64_t M, int64_t N, int64_t K, const int16_t* planesA,
+                            const int16_t* planesB, int splits, double* P, void* stream);
+ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, const int32_t* e,
+                           const int32_t* f, double* const* C, int64_t ldc, void* stream);
+
+/* ------------------------------------------------------------------ */
 /* Diagnostics                                                          */
 /* ------------------------------------------------------------------ */
 
