@@ -130,3 +130,42 @@ def test_i64_maximum_k_closed_form():
     P_sum = host(P.sum(dim=0))[:, 0, 0]
     for d in range(8):
         assert P_sum[d] == K * sum(D[s] * D[d - s] for s in range(d + 1))
+
+
+def test_i64_edge_shapes_and_strides():
+    import torch
+    # empty products and K = 0
+    z = torch.zeros((4, 0), dtype=torch.float64, device="cuda")
+    zb = torch.zeros((0, 3), dtype=torch.float64, device="cuda")
+    C_hi, C_lo = ddg.dd_gemm_i64(z, z, zb, zb)
+    assert C_hi.shape == (4, 3) and not host(C_hi).any() and not np.signbit(host(C_hi)).any()
+    e = torch.zeros((0, 5), dtype=torch.float64, device="cuda")
+    C_hi, _ = ddg.dd_gemm_i64(e, e, torch.ones((5, 2), dtype=torch.float64, device="cuda"),
+                              torch.zeros((5, 2), dtype=torch.float64, device="cuda"))
+    assert C_hi.shape == (0, 2)
+    # strided, unaligned operands equal the contiguous result
+    M, N, K = 19, 23, 37
+    A_hi, A_lo, B_hi, B_lo = workloads.make_dd(M, N, K, "normal", 30)
+    ref_hi, ref_lo = ddg.dd_gemm_i64(dev(A_hi), dev(A_lo), dev(B_hi), dev(B_lo))
+    big = torch.zeros((M, K + 5), dtype=torch.float64, device="cuda")
+    bigl = torch.zeros((M, K + 5), dtype=torch.float64, device="cuda")
+    big[:, 1:K + 1], bigl[:, 1:K + 1] = dev(A_hi), dev(A_lo)
+    bB = torch.zeros((K, N + 3), dtype=torch.float64, device="cuda")
+    bBl = torch.zeros((K, N + 3), dtype=torch.float64, device="cuda")
+    bB[:, 1:N + 1], bBl[:, 1:N + 1] = dev(B_hi), dev(B_lo)
+    C_hi, C_lo = ddg.dd_gemm_i64(big[:, 1:K + 1], bigl[:, 1:K + 1], bB[:, 1:N + 1], bBl[:, 1:N + 1])
+    assert torch.equal(C_hi, ref_hi) and torch.equal(C_lo, ref_lo)
+
+
+def test_i64_extreme_scales_match_fp64_path():
+    M, N, K = 12, 10, 33
+    A_hi, A_lo, B_hi, B_lo = workloads.make_dd(M, N, K, "normal", 77)
+    ra = np.array([-600, -520, -300, 0, 300, 500, 900, -1000, 1000, 10, -10, 0])
+    cb = np.array([-500, -560, 100, 0, -300, 20, 100, 40, -1040, 0])
+    A_hi, A_lo = np.ldexp(A_hi, ra[:, None]), np.ldexp(A_lo, ra[:, None])
+    B_hi, B_lo = np.ldexp(B_hi, cb[None, :]), np.ldexp(B_lo, cb[None, :])
+    t = [dev(x) for x in (A_hi, A_lo, B_hi, B_lo)]
+    I_hi, I_lo = ddg.dd_gemm_i64(*t)
+    F_hi, F_lo = ddg.dd_gemm(*t)
+    assert np.array_equal(host(I_hi).view(np.int64), host(F_hi).view(np.int64))
+    assert np.array_equal(host(I_lo).view(np.int64), host(F_lo).view(np.int64))

@@ -80,3 +80,32 @@ def test_qd_large_sampled():
         assert np.array_equal(G[p][:, cols].view(np.int64), C_ref[p].view(np.int64))
     R = oracle.exact_md_gemm(A, B, rows=rows[:2])
     assert _normwise([g[:2] for g in G], R, [a[rows[:2]] for a in A], B) <= QD_GATE
+
+
+def test_qd_edges_zero_rows_and_k0():
+    import torch
+    A, B = workloads.make_md(9, 7, 20, "normal_rowcol30", 24, 4)
+    for a in A:
+        a[2] = 0.0          # an all-zero row: exponent 0, parts 0, outputs +0
+    for b in B:
+        b[:, 4] = 0.0
+    C = [host(c) for c in ddg.qd_gemm([dev(a) for a in A], [dev(b) for b in B])]
+    C_ref, *_ = slices_md.sliced_md_gemm(A, B, 16)
+    for p in range(4):
+        assert np.array_equal(C[p].view(np.int64), C_ref[p].view(np.int64))
+    assert not any(c[2].any() for c in C) and not any(np.signbit(c[2]).any() for c in C)
+    z = [torch.zeros((3, 0), dtype=torch.float64, device="cuda") for _ in range(4)]
+    zb = [torch.zeros((0, 2), dtype=torch.float64, device="cuda") for _ in range(4)]
+    C = ddg.qd_gemm(z, zb)
+    assert all(c.shape == (3, 2) and not host(c).any() for c in C)
+
+
+def test_qd_rejects_k_beyond_bound():
+    lib = ddg.load()
+    import ctypes
+    arr = (ctypes.c_void_p * 4)(1 << 20, 1 << 21, 1 << 22, 1 << 23)
+    brr = (ctypes.c_void_p * 4)(1 << 30, 1 << 31, 1 << 32, 1 << 33)
+    crr = (ctypes.c_void_p * 4)(1 << 40, 1 << 41, 1 << 42, 1 << 43)
+    K = ddg.QD_MAX_K + 1
+    assert lib.qd_gemm(2, 2, K, ctypes.cast(arr, ctypes.c_void_p), K, ctypes.cast(brr, ctypes.c_void_p), 2,
+                       ctypes.cast(crr, ctypes.c_void_p), 2, None, 0, None) == 2
