@@ -29,6 +29,8 @@ __all__ = [
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
     "split", "split_i16", "dd_gemm_simt",
     "QD_MAX_K", "qd_gemm", "qd_layout", "qd_workspace_size", "qd_split", "qd_slice_gemm", "qd_recombine",
+    "TC_SLICES", "TC_TILE_M", "TC_TILE_N", "TC_CHUNK_K", "TC_MAX_K_SPLIT",
+    "dd_gemm_tc", "tc_layout", "tc_workspace_size", "split_bf16", "slice_gemm_tc", "recombine_tc",
 ]
 
 SLICES = 8
@@ -82,6 +84,13 @@ _SIGNATURES = {
     "qd_split": ([_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
     "qd_slice_gemm": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
     "qd_recombine": ([_i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _i64, _ptr], _int),
+    "dd_gemm_tc_layout": ([_i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr], _int),
+    "dd_gemm_tc_workspace_size": ([_i64, _i64, _i64, _ptr], _int),
+    "dd_gemm_tc": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64,
+                    _ptr, ctypes.c_size_t, _ptr], _int),
+    "dd_split_bf16": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
+    "dd_slice_gemm_tc": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
+    "dd_recombine_tc": ([_i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _ptr, _i64, _ptr], _int),
 }
 
 
@@ -521,3 +530,95 @@ def qd_recombine(M: int, N: int, P, e, f, stream=None):
     _check("qd_recombine", load().qd_recombine(M, N, P.data_ptr(), P.shape[0], e.data_ptr(), f.data_ptr(),
                                                ctypes.cast(pc, ctypes.c_void_p), max(N, 1), _stream_handle(stream)))
     return C
+
+
+# ---- double doubles with 8-bit parts on the bf16 tensor cores (tcgen05) ----
+
+TC_SLICES = 13
+TC_TILE_M = 128
+TC_TILE_N = 256
+TC_CHUNK_K = 64
+TC_MAX_K_SPLIT = 8192
+
+
+def tc_layout(M: int, N: int, K: int):
+    """(Mp, Np, Kp, splits) of the bf16 tensor-core variant for this shape."""
+    Mp, Np, Kp, sp = _i64(), _i64(), _i64(), _int()
+    _check("dd_gemm_tc_layout", load().dd_gemm_tc_layout(M, N, K, ctypes.byref(Mp), ctypes.byref(Np),
+                                                         ctypes.byref(Kp), ctypes.byref(sp)))
+    return Mp.value, Np.value, Kp.value, sp.value
+
+
+def tc_workspace_size(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check("dd_gemm_tc_workspace_size", load().dd_gemm_tc_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def dd_gemm_tc(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, workspace=None, stream=None):
+    """The product with 13 bf16 parts of 8 bits per element and the 91 part-pair
+    products on the tensor cores (tcgen05), exact sums rounded once.
+    `workspace` (uint8 tensor of tc_workspace_size bytes) is optional."""
+    M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("dd_gemm_tc", load().dd_gemm_tc(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                           B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                           C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi), wp, wn,
+                                           _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def split_bf16(A_hi, A_lo, B_hi, B_lo, planesA=None, e=None, planesB=None, f=None, stream=None):
+    """Step 1 of the bf16 variant: (planesA, e, planesB, f); parts as bf16 bit
+    patterns (int16 tensors) in the swizzled block layout of ddgemm.h."""
+    torch = _torch()
+    for t_, n in ((A_hi, "A_hi"), (A_lo, "A_lo"), (B_hi, "B_hi"), (B_lo, "B_lo")):
+        _mat(t_, n)
+    M, K = A_hi.shape
+    K2, N = B_hi.shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    Mp, Np, Kp = -(-M // TC_TILE_M) * TC_TILE_M, -(-N // TC_TILE_N) * TC_TILE_N, -(-K // TC_CHUNK_K) * TC_CHUNK_K
+    dev = A_hi.device
+    pA = torch.empty(TC_SLICES * Mp * Kp, dtype=torch.int16, device=dev) if planesA is None else planesA
+    pB = torch.empty(TC_SLICES * Np * Kp, dtype=torch.int16, device=dev) if planesB is None else planesB
+    e = torch.empty(M, dtype=torch.int32, device=dev) if e is None else e
+    f = torch.empty(N, dtype=torch.int32, device=dev) if f is None else f
+    if pA.numel() < TC_SLICES * Mp * Kp or pB.numel() < TC_SLICES * Np * Kp or e.numel() < M or f.numel() < N:
+        raise ValueError("output buffers too small")
+    _check("dd_split_bf16", load().dd_split_bf16(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                                 B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi), pA.data_ptr(),
+                                                 e.data_ptr(), pB.data_ptr(), f.data_ptr(), _stream_handle(stream)))
+    return pA, e, pB, f
+
+
+def slice_gemm_tc(M: int, N: int, K: int, planesA, planesB, splits: int, P=None, stream=None):
+    """Step 2 of the bf16 variant: P (splits x 13 x Mp x Np int32), the exact part
+    sums of each k-split."""
+    torch = _torch()
+    Mp, Np = -(-M // TC_TILE_M) * TC_TILE_M, -(-N // TC_TILE_N) * TC_TILE_N
+    if P is None:
+        P = torch.empty((splits, TC_SLICES, Mp, Np), dtype=torch.int32, device=planesA.device)
+    if P.numel() < splits * TC_SLICES * Mp * Np:
+        raise ValueError("output buffer too small")
+    _check("dd_slice_gemm_tc", load().dd_slice_gemm_tc(M, N, K, planesA.data_ptr(), planesB.data_ptr(), splits,
+                                                       P.data_ptr(), _stream_handle(stream)))
+    return P
+
+
+def recombine_tc(M: int, N: int, P, e, f, splits=None, C_hi=None, C_lo=None, stream=None):
+    """Step 3 of the bf16 variant: (C_hi, C_lo) from P and the exponents of split_bf16."""
+    torch = _torch()
+    splits = P.shape[0] if splits is None else splits
+    if C_hi is None:
+        C_hi = torch.empty((M, N), dtype=torch.float64, device=P.device)
+    if C_lo is None:
+        C_lo = torch.empty((M, N), dtype=torch.float64, device=P.device)
+    _mat(C_hi, "C_hi"), _mat(C_lo, "C_lo")
+    if C_hi.stride() != C_lo.stride():
+        raise ValueError("hi and lo planes must share strides")
+    _check("dd_recombine_tc", load().dd_recombine_tc(M, N, P.data_ptr(), splits, e.data_ptr(), f.data_ptr(),
+                                                     C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi),
+                                                     _stream_handle(stream)))
+    return C_hi, C_lo

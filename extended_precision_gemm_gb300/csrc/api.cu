@@ -399,11 +399,12 @@ ddgemm_status dd_fp64_tensor_roof(double* tflops, void* stream) {
 
 ddgemm_status dd_wait_timeouts(unsigned int* count) {
     if (count == nullptr) return DDGEMM_ERR_INVALID_ARG;
-    unsigned int a = 0, b = 0, c = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0;
     ddgemm_status s = from_cuda(read_and_reset_wait_timeouts(&a));
     if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_i64(&b));
     if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_qd(&c));
-    *count = a + b + c;
+    if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_tc(&d));
+    *count = a + b + c + d;
     return s;
 }
 
@@ -626,6 +627,197 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
         if (C[p] == nullptr) return DDGEMM_ERR_INVALID_ARG;
     const int64_t Mp = round_up(M, TM), Np = round_up(N, TN);
     return from_cuda(launch_recombine_qd(P, splits, Mp, Np, e, f, M, N, C, ldc, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Double doubles with 8-bit parts on the bf16 tensor cores.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr int64_t kTcM = DDGEMM_TC_TILE_M, kTcN = DDGEMM_TC_TILE_N, kTcK = DDGEMM_TC_CHUNK_K;
+constexpr int kTcParts = DDGEMM_TC_SLICES;
+constexpr int kTcMaxSplits = 65535;  // grid.y of the slice GEMM
+
+struct TcLayout {
+    int64_t Mp, Np, Kp;
+    int splits;
+    int64_t off_e, off_f, off_A, off_B, off_P, total;
+};
+
+// k-split of the bf16 slice GEMM: at least enough splits that each covers at
+// most DDGEMM_TC_MAX_K_SPLIT of k (exact int32 part sums); beyond that, the
+// count whose waves of blocks (one per SM) fill the GPU best, each split
+// keeping at least 512 of k, with a small cost per split (each writes its own
+// part sums).
+int choose_tc_splits(int64_t Mp, int64_t Np, int64_t Kp) {
+    const int64_t KB = Kp / kTcK;
+    const int64_t tiles = (Mp / kTcM) * (Np / kTcN);
+    const int64_t per_split = DDGEMM_TC_MAX_K_SPLIT / kTcK;
+    const int64_t smin = std::max<int64_t>(1, (KB + per_split - 1) / per_split);
+    if (tiles == 0 || KB == 0) return 1;
+    const int64_t smax = std::max<int64_t>(smin, std::min<int64_t>(KB / 8, 4 * smin + 8));
+    const int64_t slots = device_sms();
+    int64_t best = smin;
+    double best_score = -1.0;
+    for (int64_t s = smin; s <= smax; ++s) {
+        const int64_t kb_per = (KB + s - 1) / s;
+        if ((KB + kb_per - 1) / kb_per != s) continue;  // some split would be empty
+        const int64_t blocks = tiles * s;
+        const int64_t waves = (blocks + slots - 1) / slots;
+        const double eff = (double)blocks / (double)(waves * slots);
+        const double score = eff - 0.01 * (double)(s - smin) / (double)smin;
+        if (score > best_score + 1e-12) { best_score = score; best = s; }
+    }
+    return (int)best;
+}
+
+TcLayout make_tc_layout(int64_t M, int64_t N, int64_t K) {
+    TcLayout L;
+    L.Mp = round_up(M, kTcM);
+    L.Np = round_up(N, kTcN);
+    L.Kp = round_up(K, kTcK);
+    L.splits = choose_tc_splits(L.Mp, L.Np, L.Kp);
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) { int64_t o = off; off = round_up(off + bytes, kAlign); return o; };
+    L.off_e = take(L.Mp * 4);
+    L.off_f = take(L.Np * 4);
+    L.off_A = take((int64_t)kTcParts * L.Mp * L.Kp * 2);
+    L.off_B = take((int64_t)kTcParts * L.Np * L.Kp * 2);
+    L.off_P = take((int64_t)L.splits * kTcParts * L.Mp * L.Np * 4);
+    L.total = off;
+    return L;
+}
+
+ddgemm_status check_tc_shapes(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if ((round_up(M, kTcM) / kTcM) * (round_up(N, kTcN) / kTcN) > kMaxTiles) return DDGEMM_ERR_UNSUPPORTED;
+    return DDGEMM_OK;
+}
+
+cudaError_t run_split_tc(int64_t M, int64_t N, int64_t K, int64_t Kp, const double* A_hi, const double* A_lo,
+                         int64_t lda, int32_t* e, uint16_t* pA, const double* B_hi, const double* B_lo, int64_t ldb,
+                         int32_t* f, uint16_t* pB, cudaStream_t st) {
+    SplitOperand a{A_hi, A_lo, lda, M, e}, b{B_hi, B_lo, ldb, N, f};
+    const SplitOperand* pa = (e != nullptr && M > 0) ? &a : nullptr;
+    const SplitOperand* pb = (f != nullptr && N > 0) ? &b : nullptr;
+    cudaError_t err = launch_init_exponents(pa ? e : nullptr, M, pb ? f : nullptr, N, K, st);
+    if (err == cudaSuccess) err = launch_exponents(pa, pb, K, st);
+    if (err == cudaSuccess) err = launch_split_bf16(pa, pb, K, Kp, pa ? pA : nullptr, pb ? pB : nullptr, st);
+    return err;
+}
+
+ddgemm_status run_gemm_tc(const TcLayout& L, int64_t M, int64_t N, int64_t K, const double* A_hi,
+                          const double* A_lo, int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb,
+                          double* C_hi, double* C_lo, int64_t ldc, char* ws, cudaStream_t st) {
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    int32_t* e = reinterpret_cast<int32_t*>(ws + L.off_e);
+    int32_t* f = reinterpret_cast<int32_t*>(ws + L.off_f);
+    uint16_t* pA = reinterpret_cast<uint16_t*>(ws + L.off_A);
+    uint16_t* pB = reinterpret_cast<uint16_t*>(ws + L.off_B);
+    int32_t* P = reinterpret_cast<int32_t*>(ws + L.off_P);
+    DDG_TRY(run_split_tc(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, st));
+    DDG_TRY(launch_slice_gemm_tc(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_TRY(launch_recombine_tc(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
+    return DDGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ddgemm_status dd_gemm_tc_layout(int64_t M, int64_t N, int64_t K, int64_t* Mp, int64_t* Np, int64_t* Kp,
+                                int* splits) {
+    ddgemm_status s = check_tc_shapes(M, N, K);
+    if (s != DDGEMM_OK) return s;
+    TcLayout L = make_tc_layout(M, N, K);
+    if (Mp) *Mp = L.Mp;
+    if (Np) *Np = L.Np;
+    if (Kp) *Kp = L.Kp;
+    if (splits) *splits = L.splits;
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_gemm_tc_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    if (bytes == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    ddgemm_status s = check_tc_shapes(M, N, K);
+    if (s != DDGEMM_OK) return s;
+    *bytes = (size_t)make_tc_layout(M, N, K).total;
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
+                         const double* B_hi, const double* B_lo, int64_t ldb, double* C_hi, double* C_lo,
+                         int64_t ldc, void* workspace, size_t workspace_bytes, void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc);
+    if (s == DDGEMM_OK) s = check_tc_shapes(M, N, K);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    TcLayout L = make_tc_layout(M, N, K);
+    const int64_t c = span_bytes(M, N, ldc);
+    if (workspace != nullptr) {
+        if ((uintptr_t)workspace % kAlign != 0 || workspace_bytes < (size_t)L.total) return DDGEMM_ERR_INVALID_ARG;
+        if (ranges_overlap(workspace, L.total, C_hi, c) || ranges_overlap(workspace, L.total, C_lo, c))
+            return DDGEMM_ERR_INVALID_ARG;
+        return run_gemm_tc(L, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc,
+                           static_cast<char*>(workspace), st);
+    }
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    s = run_gemm_tc(L, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc, static_cast<char*>(ws), st);
+    cudaError_t fe = cudaFreeAsync(ws, st);
+    if (s == DDGEMM_OK && fe != cudaSuccess) s = DDGEMM_ERR_CUDA;
+    return s;
+}
+
+ddgemm_status dd_split_bf16(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
+                            const double* B_hi, const double* B_lo, int64_t ldb, uint16_t* planesA, int32_t* e,
+                            uint16_t* planesB, int32_t* f, void* stream) {
+    ddgemm_status s = check_shapes(M, N, K, lda, ldb, std::max<int64_t>(1, N));
+    if (s == DDGEMM_OK) s = check_tc_shapes(M, N, K);
+    if (s != DDGEMM_OK) return s;
+    if (M > 0 && (e == nullptr || (K > 0 && (A_hi == nullptr || A_lo == nullptr || planesA == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (N > 0 && (f == nullptr || (K > 0 && (B_hi == nullptr || B_lo == nullptr || planesB == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    const int64_t Kp = round_up(K, kTcK);
+    return from_cuda(run_split_tc(M, N, K, Kp, A_hi, A_lo, lda, M > 0 ? e : nullptr, planesA, B_hi, B_lo, ldb,
+                                  N > 0 ? f : nullptr, planesB, static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status dd_slice_gemm_tc(int64_t M, int64_t N, int64_t K, const uint16_t* planesA, const uint16_t* planesB,
+                               int splits, int32_t* P, void* stream) {
+    ddgemm_status s = check_tc_shapes(M, N, K);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    const int64_t Mp = round_up(M, kTcM), Np = round_up(N, kTcN), Kp = round_up(K, kTcK), KB = Kp / kTcK;
+    if (splits < 1 || splits > kTcMaxSplits || (KB > 0 && splits > KB) || (KB == 0 && splits != 1))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (KB > 0 && ((KB + splits - 1) / splits) * kTcK > DDGEMM_TC_MAX_K_SPLIT) return DDGEMM_ERR_INVALID_ARG;
+    if (P == nullptr || (K > 0 && (planesA == nullptr || planesB == nullptr))) return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0 || (uintptr_t)P % 16 != 0)
+        return DDGEMM_ERR_INVALID_ARG;
+    return from_cuda(launch_slice_gemm_tc(planesA, planesB, Mp, Np, Kp, splits, P, static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status dd_recombine_tc(int64_t M, int64_t N, const int32_t* P, int splits, const int32_t* e,
+                              const int32_t* f, double* C_hi, double* C_lo, int64_t ldc, void* stream) {
+    if (M < 0 || N < 0 || ldc < std::max<int64_t>(1, N)) return DDGEMM_ERR_INVALID_ARG;
+    if (splits < 1 || splits > kTcMaxSplits) return DDGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    if (P == nullptr || e == nullptr || f == nullptr || C_hi == nullptr || C_lo == nullptr)
+        return DDGEMM_ERR_INVALID_ARG;
+    const int64_t Mp = round_up(M, kTcM), Np = round_up(N, kTcN);
+    return from_cuda(launch_recombine_tc(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -69,6 +69,18 @@ cudaError_t launch_recombine_qd(const double* P, int splits, int64_t Mp, int64_t
                                 cudaStream_t st);
 cudaError_t read_and_reset_wait_timeouts_qd(unsigned int* count);
 
+// The variant with 8-bit parts on the bf16 tensor cores (tcgen05): 13 bf16
+// parts per element in swizzled blocks, 91 pairs accumulated in tensor
+// memory, int32 part sums per k-split, exact sum rounded once.
+cudaError_t launch_split_bf16(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
+                              uint16_t* planesA, uint16_t* planesB, cudaStream_t st);
+cudaError_t launch_slice_gemm_tc(const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
+                                 int64_t Kp, int splits, int32_t* P, cudaStream_t st);
+cudaError_t launch_recombine_tc(const int32_t* P, int splits, int64_t Mp, int64_t Np, const int32_t* e,
+                                const int32_t* f, int64_t M, int64_t N, double* C_hi, double* C_lo, int64_t ldc,
+                                cudaStream_t st);
+cudaError_t read_and_reset_wait_timeouts_tc(unsigned int* count);
+
 // Diagnostics of the bounded waits inside the slice GEMM.
 cudaError_t read_and_reset_wait_timeouts(unsigned int* count);
 

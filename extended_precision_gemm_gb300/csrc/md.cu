@@ -21,6 +21,7 @@
 
 #include "async_copy.cuh"
 #include "common.cuh"
+#include "wide_int.cuh"
 #include "launch.cuh"
 
 namespace ddg {
@@ -30,84 +31,7 @@ constexpr int SQ = 16;                      // parts per quad double
 constexpr int NPQ = 4;                      // doubles per quad double
 constexpr int FIXQ = SQ * DIGIT;            // 208 fraction bits
 constexpr uint64_t ABS_MASK = 0x7FFFFFFFFFFFFFFFULL;
-typedef unsigned __int128 u128;
-
-// 256-bit two's-complement integer.
-struct U256 {
-    u128 lo, hi;
-};
-
-__device__ __forceinline__ U256 u256_zero() { return U256{0, 0}; }
-
-__device__ __forceinline__ U256 u256_add(U256 a, U256 b) {
-    U256 r;
-    r.lo = a.lo + b.lo;
-    r.hi = a.hi + b.hi + (r.lo < a.lo ? 1 : 0);
-    return r;
-}
-
-__device__ __forceinline__ U256 u256_neg(U256 a) {
-    U256 r;
-    r.lo = ~a.lo + 1;
-    r.hi = ~a.hi + (r.lo == 0 ? 1 : 0);
-    return r;
-}
-
-__device__ __forceinline__ bool u256_is_neg(U256 a) { return (uint64_t)(a.hi >> 127) != 0; }
-__device__ __forceinline__ bool u256_is_zero(U256 a) { return a.lo == 0 && a.hi == 0; }
-
-// m * 2^sh for m < 2^64, 0 <= sh <= 190.
-__device__ __forceinline__ U256 u256_shl(uint64_t m, int sh) {
-    U256 r;
-    if (sh >= 128) {
-        r.lo = 0;
-        r.hi = (u128)m << (sh - 128);
-    } else if (sh == 0) {
-        r.lo = m;
-        r.hi = 0;
-    } else {
-        r.lo = (u128)m << sh;
-        r.hi = (u128)m >> (128 - sh);
-    }
-    return r;
-}
-
-// Bits [off, off + n) of a, n <= 32.
-__device__ __forceinline__ uint32_t u256_bits(U256 a, int off, int n) {
-    const uint32_t mask = (n == 32) ? 0xFFFFFFFFu : ((1u << n) - 1);
-    if (off >= 128) return (uint32_t)(a.hi >> (off - 128)) & mask;
-    if (off + n <= 128) return (uint32_t)(a.lo >> off) & mask;
-    return (uint32_t)((a.lo >> off) | (a.hi << (128 - off))) & mask;
-}
-
-__device__ __forceinline__ int u256_msb(U256 a) {  // a != 0, non-negative
-    if (a.hi != 0) {
-        const uint64_t h1 = (uint64_t)(a.hi >> 64);
-        return h1 ? 255 - __clzll((long long)h1) : 191 - __clzll((long long)(uint64_t)a.hi);
-    }
-    const uint64_t l1 = (uint64_t)(a.lo >> 64);
-    return l1 ? 127 - __clzll((long long)l1) : 63 - __clzll((long long)(uint64_t)a.lo);
-}
-
-// a >> sh (logical), 0 < sh < 256.
-__device__ __forceinline__ U256 u256_shr(U256 a, int sh) {
-    U256 r;
-    if (sh >= 128) {
-        r.lo = a.hi >> (sh - 128);
-        r.hi = 0;
-    } else {
-        r.lo = (a.lo >> sh) | (a.hi << (128 - sh));
-        r.hi = a.hi >> sh;
-    }
-    return r;
-}
-
-// Are any of the bits below position `sh` set (sh >= 1)?
-__device__ __forceinline__ bool u256_any_below(U256 a, int sh) {
-    if (sh >= 256) return !u256_is_zero(a);
-    if (sh >= 128) return a.lo != 0 || (sh > 128 && (a.hi << (256 - sh)) != 0);
-    return (a.lo << (128 - sh)) != 0;
-}
+using namespace wide;
 
 struct Unp {
     uint64_t m;
@@ -395,24 +319,6 @@ __device__ __forceinline__ long long exact_double_to_int(double v) {
     return (b >> 63) ? -(long long)mag : (long long)mag;
 }
 
-// keep * 2^lsb as a double (keep <= 2^53, exact when representable);
-// +-inf when it reaches 2^1024.
-__device__ __forceinline__ double make_double(uint64_t keep, int lsb, uint64_t sign) {
-    if (keep == 0) return __longlong_as_double((long long)(sign << 63));
-    const int t = 63 - __clzll((long long)keep);
-    const int E = lsb + t;  // exponent of the leading bit
-    uint64_t bits;
-    if (E > 1023) {
-        bits = 0x7FF0000000000000ULL;
-    } else if (E >= -1022) {
-        const uint64_t mant = (keep << (52 - t)) & ((1ULL << 52) - 1);
-        bits = ((uint64_t)(E + 1023) << 52) | mant;
-    } else {
-        bits = keep << (lsb + 1074);  // subnormal: lsb >= -1074 by construction
-    }
-    return __longlong_as_double((long long)((sign << 63) | bits));
-}
-
 __global__ void __launch_bounds__(256) recombine_qd_kernel(const double* __restrict__ P, int splits, int64_t Mp,
                                                            int64_t Np, const int32_t* __restrict__ e,
                                                            const int32_t* __restrict__ f, int64_t M, int64_t N,
@@ -434,44 +340,10 @@ __global__ void __launch_bounds__(256) recombine_qd_kernel(const double* __restr
             X = u256_add(X, v < 0 ? u256_neg(t) : t);
         }
         const int q = effective_exponent(e[i]) + fj - DIGIT * (SQ + 1);
-        bool stop = false;
+        double out[NPQ];
+        round_into_doubles<NPQ>(X, q, out);
 #pragma unroll
-        for (int p = 0; p < NPQ; ++p) {
-            double out = 0.0;
-            if (!stop && !u256_is_zero(X)) {
-                const uint64_t sign = u256_is_neg(X) ? 1ULL : 0ULL;
-                const U256 mag = sign ? u256_neg(X) : X;
-                const int t = u256_msb(mag);
-                const int top = q + t;
-                const int lsb = max(top - 52, -1074);
-                const int shift = lsb - q;
-                uint64_t keep;
-                int klsb;
-                U256 used;  // the rounded magnitude in units of 2^q
-                if (shift <= 0) {
-                    keep = (uint64_t)mag.lo;
-                    klsb = q;
-                    used = mag;
-                } else {
-                    keep = (uint64_t)u256_shr(mag, shift).lo;
-                    const bool rbit = u256_bits(mag, shift - 1, 1) != 0;
-                    const bool sticky = shift >= 2 && u256_any_below(mag, shift - 1);
-                    if (rbit && (sticky || (keep & 1))) keep += 1;
-                    klsb = lsb;
-                    used = u256_shl(keep, shift);
-                    if (keep >> 53) { keep >>= 1; klsb += 1; }  // rounded up to 2^53
-                }
-                out = make_double(keep, klsb, sign);
-                if (isinf(out)) {
-                    stop = true;
-                } else {
-                    X = u256_add(X, sign ? used : u256_neg(used));
-                }
-            } else {
-                stop = true;
-            }
-            Cs[p][i * ldc + j] = __dadd_rn(out, 0.0);
-        }
+        for (int p = 0; p < NPQ; ++p) Cs[p][i * ldc + j] = out[p];
     }
 }
 

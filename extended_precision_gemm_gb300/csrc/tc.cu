@@ -1,0 +1,506 @@
+// tc.cu -- the double-double GEMM with 8-bit parts on GB300's bf16 tensor
+// cores (tcgen05 MMA, accumulators in tensor memory).
+//
+// "Multiple Double Arithmetic on NVIDIA Tensor Cores", Section 1, relates the
+// rewriting to the Ozaki scheme, where accurate products are computed by
+// lower precision arithmetic, and Section 2 eqs. (1)-(5) rest on one fact:
+// parts on a shared grid have few nonzero bits, so their products and sums of
+// products are exact in the accumulator.  "Ozaki 2.5: Engineering the
+// Deconstruction Path of fp64-Emulated Dense Matrix Multiplication on FP8
+// Tensor Cores" (summary) applies the same idea to 8-bit tensor pipes.  Here
+// the parts are 8 bits wide, so that each is exact in bf16:
+//
+//  1. split: e' = e + 1 (e the shared exponent of the 13-bit method), X =
+//     trunc((hi + lo) 2^(104 - e')) (|X| < 2^103), and the 13 balanced
+//     base-256 digits of X, least significant first: D_s = ((X + 128) mod 256)
+//     - 128, X <- (X - D_s) / 256, D_0 the rest; every |D_s| <= 128.  Parts
+//     are stored as bf16 in blocks of 128 (A) or 256 (B) rows x 64 k, each
+//     block in the 128-byte swizzled K-major layout the tensor core reads;
+//  2. P_d = sum_{s+t=d} A_s B_t^T, d = 0..12 (91 pairs), on the tensor cores:
+//     each product is at most 2^14, so 256 of them sum to at most 2^22 and the
+//     f32 accumulator is exact; every 256 products per output ("a chunk") the
+//     accumulator is read from tensor memory and added into an exact int32
+//     total (|P_d| <= 13 K 2^14 < 2^31 for K <= 8192 per k-split);
+//  3. Z = sum_d P_d 2^(8 (12 - d)) exactly (256-bit), rounded once to the
+//     nearest double double of Z 2^(e'_i + f'_j - 112).
+#include <algorithm>
+
+#include "async_copy.cuh"
+#include "common.cuh"
+#include "fixed_point.cuh"
+#include "launch.cuh"
+#include "tcgen05.cuh"
+#include "wide_int.cuh"
+
+namespace ddg {
+namespace {
+
+constexpr int TS = DDGEMM_TC_SLICES;        // 13 parts
+constexpr int TD = DDGEMM_TC_DIGIT_BITS;    // 8 bits per part
+constexpr int TBM = DDGEMM_TC_TILE_M;       // 128 rows of A per block
+constexpr int TBN = DDGEMM_TC_TILE_N;       // 256 columns of B per block
+constexpr int TBK = DDGEMM_TC_CHUNK_K;      // 64 k per block (128-byte rows)
+constexpr int KSPLIT_MAX = DDGEMM_TC_MAX_K_SPLIT;  // 8192 k per slice-GEMM CTA
+static_assert(TS * TD == fxp::FIX_BITS, "13 parts of 8 bits cover the 104-bit fixed-point value");
+static_assert(TBK * 2 == 128, "one block row is one 128-byte swizzle row");
+
+constexpr int A_BLOCK_BYTES = TBM * TBK * 2;  // 16 KB
+constexpr int B_BLOCK_BYTES = TBN * TBK * 2;  // 32 KB
+constexpr int STAGES = 4;
+constexpr int STAGE_BYTES = A_BLOCK_BYTES + B_BLOCK_BYTES;
+constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+constexpr int CHUNK_BLOCKS = 4;   // blocks of 64 k summed in f32 before a flush (256 products)
+constexpr int UMMA_K = 16;        // k of one tcgen05.mma (kind::f16)
+constexpr int EPI_WARPS = 8;
+constexpr int GEMM_THREADS = 64 + EPI_WARPS * 32;  // producer warp, MMA warp, epilogue
+constexpr uint32_t TMEM_COLS = 512;  // two f32 accumulators of 128 x 256
+constexpr uint32_t IDESC = tc5::idesc_bf16_f32(TBM, TBN);
+constexpr unsigned long long WAIT_NS = 2000000000ULL;  // bounded waits: 2 s
+constexpr int TILE_GROUP = 8;     // row blocks per group in the tile order (L2 reuse)
+
+static_assert(CHUNK_BLOCKS * TBK * 128 * 128 <= (1 << 22), "a chunk's f32 sums stay within 2^22");
+static_assert((long long)TS * KSPLIT_MAX * 128 * 128 < (1LL << 31), "int32 totals per k-split");
+
+__device__ unsigned int g_wait_timeouts_tc = 0;
+
+// ---------------------------------------------------------------------------
+// Step 1: bf16 parts.
+// ---------------------------------------------------------------------------
+
+// Byte offset of element (row r, 16-byte chunk kc of k) in a block: rows of
+// 128 bytes, chunk kc of row r stored at position kc ^ (r % 8).
+__device__ __forceinline__ uint32_t swizzled(int r, int kc) { return (uint32_t)(r * 128 + ((kc ^ (r & 7)) << 4)); }
+
+// bf16 bit pattern of a small integer (|d| <= 256: exact in float and in bf16).
+__device__ __forceinline__ uint32_t bf16_bits(int d) { return __float_as_uint(__int2float_rn(d)) >> 16; }
+
+// The 13 balanced base-256 digits of the element (hi, lo) against exponent
+// e' (most significant first), packed: out[s] holds the bf16 of digit s.
+__device__ __forceinline__ void balanced_parts(double hi, double lo, int ep, uint32_t (&out)[TS]) {
+    uint64_t sign;
+    const unsigned __int128 mag = fxp::fixed_point(hi, lo, ep, sign);
+    __int128 X = sign ? -(__int128)mag : (__int128)mag;
+#pragma unroll
+    for (int s = TS - 1; s >= 1; --s) {
+        const int d = (int)(((uint32_t)(uint64_t)X + 128u) & 255u) - 128;
+        out[s] = bf16_bits(d);
+        X = (X - d) >> TD;  // exact: X - d is a multiple of 256
+    }
+    out[0] = bf16_bits((int)(long long)X);
+}
+
+struct TcSplitGrid {
+    const double* A_hi; const double* A_lo; int64_t lda, M; int32_t* e; int64_t a_tasks;
+    const double* B_hi; const double* B_lo; int64_t ldb, N; int32_t* f; int64_t b_tasks;
+    int64_t K, KB;  // KB = k-blocks of 64
+    uint16_t* planesA; uint16_t* planesB;
+};
+
+// One warp per task.  A task: 4 rows of A x one k-block (lane = row (lane/8),
+// 8 consecutive k (lane%8)): 512 contiguous bytes of hi per row read, 512
+// contiguous bytes per part written.  B task: 32 columns of B x one k-block
+// (lane = column, looping over the 8 chunks of 8 k): each load instruction
+// reads 256 contiguous bytes of a row of B, and each thread writes whole
+// 128-byte rows of every part.  Rows / k beyond the matrix are written as 0.
+__global__ void __launch_bounds__(256) split_bf16_kernel(TcSplitGrid g) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gridDim.x * 8;
+    const int64_t tasks = g.a_tasks + g.b_tasks;
+    for (int64_t task = gw; task < tasks; task += nw) {
+        if (task < g.a_tasks) {
+            const int64_t rg = task / g.KB, kb = task % g.KB;
+            const int64_t r = rg * 4 + (lane >> 3);
+            const int kc = lane & 7;
+            const int64_t k0 = kb * TBK + kc * 8;
+            double hi[8], lo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) hi[j] = lo[j] = 0.0;
+            int ep = 1;
+            if (r < g.M) {
+                const int32_t er = g.e[r];
+                if (kb == 0 && kc == 0 && er == EXP_NONE) g.e[r] = 0;
+                ep = effective_exponent(er) + 1;
+                const double* ph = g.A_hi + r * g.lda;
+                const double* pl = g.A_lo + r * g.lda;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (k0 + j < g.K) { hi[j] = __ldg(ph + k0 + j); lo[j] = __ldg(pl + k0 + j); }
+            }
+            uint32_t w[TS][4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                uint32_t p0[TS], p1[TS];
+                balanced_parts(hi[j], lo[j], ep, p0);
+                balanced_parts(hi[j + 1], lo[j + 1], ep, p1);
+#pragma unroll
+                for (int s = 0; s < TS; ++s) w[s][j >> 1] = p0[s] | (p1[s] << 16);
+            }
+            const int64_t mt = r / TBM;
+            const int rin = (int)(r % TBM);
+#pragma unroll
+            for (int s = 0; s < TS; ++s) {
+                uint8_t* blk = reinterpret_cast<uint8_t*>(g.planesA + ((mt * TS + s) * g.KB + kb) * (TBM * TBK));
+                *reinterpret_cast<uint4*>(blk + swizzled(rin, kc)) = make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
+            }
+        } else {
+            const int64_t local = task - g.a_tasks;
+            const int64_t cg = local / g.KB, kb = local % g.KB;
+            const int64_t n = cg * 32 + lane;
+            int ep = 1;
+            if (n < g.N) {
+                const int32_t fr = g.f[n];
+                if (kb == 0 && fr == EXP_NONE) g.f[n] = 0;
+                ep = effective_exponent(fr) + 1;
+            }
+            const int64_t nt = n / TBN;
+            const int nin = (int)(n % TBN);
+#pragma unroll 1
+            for (int kc = 0; kc < 8; ++kc) {
+                const int64_t k0 = kb * TBK + kc * 8;
+                double hi[8], lo[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const bool in = n < g.N && k0 + j < g.K;
+                    hi[j] = in ? __ldg(g.B_hi + (k0 + j) * g.ldb + n) : 0.0;
+                    lo[j] = in ? __ldg(g.B_lo + (k0 + j) * g.ldb + n) : 0.0;
+                }
+                uint32_t w[TS][4];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    uint32_t p0[TS], p1[TS];
+                    balanced_parts(hi[j], lo[j], ep, p0);
+                    balanced_parts(hi[j + 1], lo[j + 1], ep, p1);
+#pragma unroll
+                    for (int s = 0; s < TS; ++s) w[s][j >> 1] = p0[s] | (p1[s] << 16);
+                }
+#pragma unroll
+                for (int s = 0; s < TS; ++s) {
+                    uint8_t* blk = reinterpret_cast<uint8_t*>(g.planesB + ((nt * TS + s) * g.KB + kb) * (TBN * TBK));
+                    *reinterpret_cast<uint4*>(blk + swizzled(nin, kc)) = make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Step 2: P_d on the tensor cores.  One CTA per (128 x 256 output block,
+// k-split); 10 warps:
+//   warp 0 (one thread): bulk copies of the part blocks into a 4-stage ring;
+//   warp 1: allocates 512 TMEM columns (two f32 accumulators of 128 x 256);
+//           one thread issues the MMAs (4 per 64-k block);
+//   warps 2-9: read each finished chunk from TMEM (warp w reads lanes
+//           32 (w % 4) .. +31, i.e. rows, and one half of the columns), add it
+//           into int32 totals in registers, and store the totals of P_d.
+// The order of work is d = 0..12, then s = 0..d (t = d - s), then k-blocks;
+// a chunk is 4 consecutive k-blocks of one d (the last chunk of a d may be
+// shorter).  Chunks alternate between the two accumulators, so the MMAs of
+// one chunk overlap the read-out of the previous one.
+// ---------------------------------------------------------------------------
+
+struct TcGemmArgs {
+    const uint16_t* planesA;
+    const uint16_t* planesB;
+    int32_t* P;       // [split][d][Mp][Np]
+    int64_t Mp, Np;
+    int64_t KB;       // k-blocks in the planes
+    int64_t kb_per_split;
+    int MT, NT;       // output blocks along M and N
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile(
+        "{\n"
+        " .reg .b64 st;\n"
+        " mbarrier.arrive.shared::cta.b64 st, [%0];\n"
+        "}\n" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void note_timeout(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicAdd(&g_wait_timeouts_tc, 1u);
+}
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1) slice_gemm_tc_kernel(TcGemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[2 * STAGES + 4 + 1];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // output block of this CTA (grouped order: TILE_GROUP row blocks share
+    // their column blocks while they are in L2)
+    const int64_t tile = blockIdx.x;
+    const int64_t per_group = (int64_t)TILE_GROUP * g.NT;
+    const int64_t group = tile / per_group;
+    const int64_t first_m = group * TILE_GROUP;
+    const int64_t gsize = min((int64_t)TILE_GROUP, (int64_t)g.MT - first_m);
+    const int64_t mt = first_m + (tile % per_group) % gsize;
+    const int64_t nt = (tile % per_group) / gsize;
+    const int64_t z = blockIdx.y;
+    const int64_t kb0 = z * g.kb_per_split;
+    const int64_t nkb = max((int64_t)0, min(g.KB, kb0 + g.kb_per_split) - kb0);
+
+    const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[STAGES]);
+    const uint32_t accf0 = smem_addr(&bars[2 * STAGES]), acce0 = smem_addr(&bars[2 * STAGES + 2]);
+    const uint32_t done_bar = smem_addr(&bars[2 * STAGES + 4]);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, EPI_WARPS);
+        }
+        mbar_init(done_bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc5::tmem_alloc(smem_addr(&tmem_slot), TMEM_COLS);
+        tc5::tmem_relinquish();
+    }
+    tc5::fence_before_sync();
+    __syncthreads();
+    tc5::fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- producer ----
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            for (int d = 0; d < TS && !abort_flag; ++d) {
+                for (int s = 0; s <= d && !abort_flag; ++s) {
+                    const int t = d - s;
+                    const uint16_t* a_src = g.planesA + ((mt * TS + s) * g.KB + kb0) * (TBM * TBK);
+                    const uint16_t* b_src = g.planesB + ((nt * TS + t) * g.KB + kb0) * (TBN * TBK);
+                    for (int64_t kb = 0; kb < nkb; ++kb) {
+                        if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1, WAIT_NS)) {
+                            note_timeout(&abort_flag);
+                            break;
+                        }
+                        uint8_t* dst = smem + stage * STAGE_BYTES;
+                        mbar_expect_tx(full0 + 8 * stage, STAGE_BYTES);
+                        bulk_load(dst, a_src + kb * (TBM * TBK), A_BLOCK_BYTES, full0 + 8 * stage);
+                        bulk_load(dst + A_BLOCK_BYTES, b_src + kb * (TBN * TBK), B_BLOCK_BYTES, full0 + 8 * stage);
+                        ++issued;
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                }
+            }
+            // copies still in flight must land before the CTA exits
+            const int64_t first = issued > STAGES ? issued - STAGES : 0;
+            for (int64_t j = first; j < issued; ++j)
+                if (!mbar_wait_bounded(full0 + 8 * (uint32_t)(j % STAGES), (uint32_t)((j / STAGES) & 1), WAIT_NS))
+                    note_timeout(&abort_flag);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer ----
+            uint32_t stage = 0, phase = 0;
+            int64_t chunk = 0;
+            uint32_t buf = 0;
+            bool ok = true;
+            for (int d = 0; d < TS && ok; ++d) {
+                const int64_t nblk = (int64_t)(d + 1) * nkb;
+                int64_t b = 0;
+                for (int s = 0; s <= d && ok; ++s) {
+                    for (int64_t kb = 0; kb < nkb; ++kb, ++b) {
+                        if (b % CHUNK_BLOCKS == 0) {
+                            buf = (uint32_t)(chunk & 1);
+                            const uint32_t use = (uint32_t)(chunk >> 1);
+                            if (abort_flag || !mbar_wait_bounded(acce0 + 8 * buf, (use & 1) ^ 1, WAIT_NS)) {
+                                if (!abort_flag) note_timeout(&abort_flag);
+                                ok = false;
+                                break;
+                            }
+                            tc5::fence_after_sync();
+                        }
+                        if (abort_flag || !mbar_wait_bounded(full0 + 8 * stage, phase, WAIT_NS)) {
+                            if (!abort_flag) note_timeout(&abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc5::fence_after_sync();
+                        const uint32_t a_addr = smem_addr(smem + stage * STAGE_BYTES);
+                        const uint32_t b_addr = a_addr + A_BLOCK_BYTES;
+                        const uint32_t d_tmem = tmem + buf * TBN;
+#pragma unroll
+                        for (int kk = 0; kk < TBK / UMMA_K; ++kk)
+                            tc5::mma_bf16(d_tmem, tc5::desc_kmajor_sw128(a_addr + kk * UMMA_K * 2),
+                                          tc5::desc_kmajor_sw128(b_addr + kk * UMMA_K * 2), IDESC,
+                                          (b % CHUNK_BLOCKS != 0 || kk != 0) ? 1u : 0u);
+                        tc5::commit(empty0 + 8 * stage);  // the stage is free once these MMAs are done
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                        if ((b + 1) % CHUNK_BLOCKS == 0 || b + 1 == nblk) {
+                            tc5::commit(accf0 + 8 * buf);  // the chunk is complete
+                            ++chunk;
+                        }
+                    }
+                }
+            }
+            // every MMA issued has finished before tensor memory is released
+            tc5::commit(done_bar);
+            if (!mbar_wait_bounded(done_bar, 0, WAIT_NS)) note_timeout(&abort_flag);
+        }
+    } else {
+        // ---- epilogue: warps 2..9 ----
+        const int q = warp & 3;                  // TMEM lanes 32q .. 32q + 31
+        const int half = (warp - 2) >> 2;        // columns 128 half .. + 127
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
+        int64_t chunk = 0;
+        bool ok = true;
+        for (int d = 0; d < TS; ++d) {
+            int32_t acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0;
+            const int64_t nch = ok ? ((int64_t)(d + 1) * nkb + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS : 0;
+            for (int64_t c = 0; c < nch; ++c, ++chunk) {
+                const uint32_t buf = (uint32_t)(chunk & 1), use = (uint32_t)(chunk >> 1);
+                if (abort_flag || !mbar_wait_bounded(accf0 + 8 * buf, use & 1, WAIT_NS)) {
+                    if (!abort_flag) note_timeout(&abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc5::fence_after_sync();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t v[32];
+                    tc5::ld32(lane_base + buf * TBN + j * 32, v);
+                    // an integer-valued f32 x with |x| <= 2^22: x + 1.5 2^23 lies
+                    // in [2^23, 2^24], where the bit pattern is linear in x
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc[j * 32 + i] += __float_as_int(__fadd_rn(__uint_as_float(v[i]), 12582912.0f)) - 0x4B400000;
+                }
+                tc5::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+            }
+            int32_t* dst = g.P + (((z * TS + d) * g.Mp + mt * TBM + row) * g.Np + nt * TBN + half * 128);
+#pragma unroll
+            for (int i = 0; i < 128; i += 4)
+                *reinterpret_cast<int4*>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+        }
+    }
+
+    tc5::fence_before_sync();
+    __syncthreads();
+    tc5::fence_after_sync();
+    if (warp == 1) {
+        __syncwarp();  // the whole warp, converged, releases tensor memory
+        tc5::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Step 3: exact sum of the parts and one rounding into a double double.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
+                                                           int64_t Np, const int32_t* __restrict__ e,
+                                                           const int32_t* __restrict__ f, int64_t M, int64_t N,
+                                                           double* __restrict__ C_hi, double* __restrict__ C_lo,
+                                                           int64_t ldc) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= N) return;
+    const int64_t plane = Mp * Np;
+    const int fj = effective_exponent(f[j]) + 1;
+    for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
+        wide::U256 Z = wide::u256_zero();
+#pragma unroll
+        for (int d = 0; d < TS; ++d) {
+            long long v = 0;
+            for (int zz = 0; zz < splits; ++zz) v += __ldg(P + ((int64_t)zz * TS + d) * plane + i * Np + j);
+            Z = wide::u256_add(Z, wide::u256_from_signed(v, TD * (TS - 1 - d)));
+        }
+        const int q = effective_exponent(e[i]) + 1 + fj - TD * (TS + 1);
+        double out[2];
+        wide::round_into_doubles<2>(Z, q, out);
+        C_hi[i * ldc + j] = out[0];
+        C_lo[i * ldc + j] = out[1];
+    }
+}
+
+int num_sms_tc() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 152;
+    return sms;
+}
+
+}  // namespace
+
+cudaError_t launch_split_bf16(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
+                              uint16_t* planesA, uint16_t* planesB, cudaStream_t st) {
+    if (Kp == 0) return cudaSuccess;
+    TcSplitGrid g{};
+    g.K = K;
+    g.KB = Kp / TBK;
+    if (A) {
+        g.A_hi = A->hi; g.A_lo = A->lo; g.lda = A->ld; g.M = A->rows; g.e = A->exp;
+        g.a_tasks = (round_up(A->rows, TBM) / 4) * g.KB;
+    }
+    if (B) {
+        g.B_hi = B->hi; g.B_lo = B->lo; g.ldb = B->ld; g.N = B->rows; g.f = B->exp;
+        g.b_tasks = (round_up(B->rows, TBN) / 32) * g.KB;
+    }
+    g.planesA = planesA;
+    g.planesB = planesB;
+    const int64_t tasks = g.a_tasks + g.b_tasks;
+    if (tasks == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms_tc() * 8));
+    split_bf16_kernel<<<blocks, 256, 0, st>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_slice_gemm_tc(const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
+                                 int64_t Kp, int splits, int32_t* P, cudaStream_t st) {
+    if (Mp == 0 || Np == 0) return cudaSuccess;
+    if (splits < 1 || Mp % TBM != 0 || Np % TBN != 0 || Kp % TBK != 0) return cudaErrorInvalidValue;
+    if (((Kp / TBK + splits - 1) / splits) * TBK > KSPLIT_MAX) return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(slice_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    if (err != cudaSuccess) return err;
+    TcGemmArgs g;
+    g.planesA = planesA;
+    g.planesB = planesB;
+    g.P = P;
+    g.Mp = Mp;
+    g.Np = Np;
+    g.KB = Kp / TBK;
+    g.kb_per_split = (g.KB + splits - 1) / splits;
+    g.MT = (int)(Mp / TBM);
+    g.NT = (int)(Np / TBN);
+    dim3 grid((unsigned)((int64_t)g.MT * g.NT), (unsigned)splits);
+    slice_gemm_tc_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_recombine_tc(const int32_t* P, int splits, int64_t Mp, int64_t Np, const int32_t* e,
+                                const int32_t* f, int64_t M, int64_t N, double* C_hi, double* C_lo, int64_t ldc,
+                                cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    const unsigned gx = (unsigned)((N + 255) / 256);
+    const unsigned gy = (unsigned)(M < 65535 ? M : 65535);
+    recombine_tc_kernel<<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_reset_wait_timeouts_tc(unsigned int* count) {
+    cudaError_t err = cudaDeviceSynchronize();
+    if (err != cudaSuccess) return err;
+    err = cudaMemcpyFromSymbol(count, g_wait_timeouts_tc, sizeof(unsigned int));
+    if (err != cudaSuccess) return err;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_wait_timeouts_tc, &zero, sizeof(unsigned int));
+}
+
+}  // namespace ddg

@@ -1,0 +1,102 @@
+// tcgen05.cuh -- the fifth-generation tensor core instructions of sm_100-class
+// GPUs (tcgen05.*, PTX ISA) used by the bf16 slice GEMM: tensor memory
+// (TMEM) allocation, the MMA from shared-memory operands into a TMEM
+// accumulator, completion tracking through an mbarrier, and TMEM loads.
+#pragma once
+
+#include <cstdint>
+
+namespace ddg {
+namespace tc5 {
+
+// Allocate `ncols` TMEM columns (a power of two, 32..512) for this CTA; the
+// TMEM address is written to shared memory at `dst`.  Executed by one whole
+// warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Order tcgen05 operations around a thread synchronisation (barrier or
+// mbarrier): `before` ahead of the signalling side, `after` behind the
+// waiting side.
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D (TMEM, f32) = A * B^T (+ D if `accumulate`), A and B bf16 in shared
+// memory described by matrix descriptors, shape and types in `idesc`
+// (kind::f16).  Issued by one thread; asynchronous.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier when every tcgen05 operation issued so far by
+// this thread has completed.
+__device__ __forceinline__ void commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of one lane per thread (the warp reads
+// its 32 lanes), waiting for the load to complete before returning.
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+          "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+          "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte
+// swizzled layout: rows of 128 bytes (64 bf16 of k), the 16-byte chunks of
+// row r XOR-permuted by r % 8, groups of 8 rows 1024 bytes apart (the stride
+// byte offset); the leading byte offset is unused for this layout.  The
+// block must start on a 1024-byte boundary; the start address may then be
+// advanced by the byte offset of a k sub-step within the 128-byte row.
+__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4)  // start address >> 4
+           | ((uint64_t)1 << 16)                // leading byte offset (unused)
+           | ((uint64_t)(1024 >> 4) << 32)      // stride byte offset >> 4
+           | ((uint64_t)1 << 46)                // descriptor version
+           | ((uint64_t)2 << 61);               // 128-byte swizzle
+}
+
+// Instruction descriptor of kind::f16 for bf16 A and B, f32 accumulator,
+// both operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                       // accumulator format: f32
+           | (1u << 7)                     // A format: bf16
+           | (1u << 10)                    // B format: bf16
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+}  // namespace tc5
+}  // namespace ddg

@@ -336,6 +336,82 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
                            const int32_t* f, double* const* C, int64_t ldc, void* stream);
 
 /* ------------------------------------------------------------------ */
+/* Double doubles with 8-bit parts on the bf16 tensor cores (tcgen05)   */
+/* ------------------------------------------------------------------ */
+
+/*
+ * C = A * B (double double) with the slice-pair products on GB300's bf16
+ * tensor cores.  The paper relates its rewriting to the Ozaki scheme, which
+ * computes accurate products with lower precision arithmetic (Section 1), and
+ * its exactness argument (Section 2, eqs. (1)-(5)) only needs parts with few
+ * nonzero bits on a shared grid; "Ozaki 2.5: Engineering the Deconstruction
+ * Path of fp64-Emulated Dense Matrix Multiplication on FP8 Tensor Cores"
+ * (summary) applies the idea to 8-bit tensor pipes.  The paper has no bf16
+ * variant; this one keeps its steps and changes the width of a part:
+ *   - shared exponent e' = e + 1 (e as for dd_gemm, one bit of headroom);
+ *     X = trunc((hi + lo) 2^(104 - e')); 13 balanced base-256 digits of X
+ *     (least significant first, D = ((X + 128) mod 256) - 128, the top digit
+ *     the rest): every part is an integer in [-128, 128], exact in bf16;
+ *   - P_d = sum_{s+t=d} A_s B_t for d = 0..12 (91 pairs) with tcgen05.mma
+ *     (bf16 in, f32 accumulators in tensor memory), exact: 256 products of at
+ *     most 2^14 are summed in f32 and then added into exact int32 totals;
+ *   - Z = sum_d P_d 2^(8 (12 - d)) (exact) rounded once to the nearest double
+ *     double of Z 2^(e'_i + f'_j - 112) (ties to even; zeros are +0).
+ * Its result is not bit-identical to dd_gemm's (other parts, one rounding);
+ * both are within the same normwise bound of the exact product.
+ * Same arguments and conventions as dd_gemm; K <= DDGEMM_MAX_K.  `workspace`
+ * (dd_gemm_tc_workspace_size bytes, 256-byte aligned) may be NULL: then it
+ * comes from the stream-ordered allocator (DDGEMM_ERR_ALLOC on failure).
+ */
+#define DDGEMM_TC_SLICES 13         /* parts per double double */
+#define DDGEMM_TC_DIGIT_BITS 8      /* bits per part */
+#define DDGEMM_TC_TILE_M 128        /* rows of A per part block / output block */
+#define DDGEMM_TC_TILE_N 256        /* columns of B per part block / output block */
+#define DDGEMM_TC_CHUNK_K 64        /* k per part block (one 128-byte row) */
+#define DDGEMM_TC_MAX_K_SPLIT 8192  /* k per slice-GEMM block: int32 part sums stay exact */
+
+/*
+ * Padded extents (Mp = M rounded up to 128, Np = N rounded up to 256, Kp = K
+ * rounded up to 64) and the k-split of the slice GEMM (every split covers at
+ * most DDGEMM_TC_MAX_K_SPLIT of k).  Any output pointer may be NULL.
+ */
+ddgemm_status dd_gemm_tc_layout(int64_t M, int64_t N, int64_t K,
+                                int64_t* Mp, int64_t* Np, int64_t* Kp, int* splits);
+ddgemm_status dd_gemm_tc_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K,
+                         const double* A_hi, const double* A_lo, int64_t lda,
+                         const double* B_hi, const double* B_lo, int64_t ldb,
+                         double* C_hi, double* C_lo, int64_t ldc,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The steps of dd_gemm_tc (all device pointers; used by the parity tests).
+ *
+ * dd_split_bf16: e (M int32) and f (N int32) receive the exponents e, f of
+ * dd_split (the parts use e + 1, f + 1), and the parts as bf16 bit patterns:
+ *   planesA: 13 * Mp * Kp uint16, block (mt, s, kb) of 128 x 64 at element
+ *            ((mt * 13 + s) * (Kp / 64) + kb) * 8192;
+ *   planesB: 13 * Np * Kp uint16, block (nt, t, kb) of 256 x 64 at element
+ *            ((nt * 13 + t) * (Kp / 64) + kb) * 16384;
+ *   inside a block, element (row r, k) is at byte
+ *            r * 128 + (((k / 8) ^ (r % 8)) * 16) + (k % 8) * 2
+ *   (rows of B's blocks are columns of B; padding rows / k hold 0).
+ * dd_slice_gemm_tc: P, splits x 13 x Mp x Np int32 (row-major Mp x Np per
+ *   split and part): the exact part sums of each k-split; splits as given by
+ *   dd_gemm_tc_layout (1 <= splits, and ceil(Kp/64 / splits) * 64 <= 8192).
+ * dd_recombine_tc: C from P and the exponents of dd_split_bf16.
+ * Errors as for the dd_gemm steps.
+ */
+ddgemm_status dd_split_bf16(int64_t M, int64_t N, int64_t K,
+                            const double* A_hi, const double* A_lo, int64_t lda,
+                            const double* B_hi, const double* B_lo, int64_t ldb,
+                            uint16_t* planesA, int32_t* e, uint16_t* planesB, int32_t* f, void* stream);
+ddgemm_status dd_slice_gemm_tc(int64_t M, int64_t N, int64_t K, const uint16_t* planesA,
+                               const uint16_t* planesB, int splits, int32_t* P, void* stream);
+ddgemm_status dd_recombine_tc(int64_t M, int64_t N, const int32_t* P, int splits, const int32_t* e,
+                              const int32_t* f, double* C_hi, double* C_lo, int64_t ldc, void* stream);
+
+/* ------------------------------------------------------------------ */
 /* Diagnostics                                                          */
 /* ------------------------------------------------------------------ */
 
@@ -348,7 +424,7 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
 ddgemm_status dd_fp64_tensor_roof(double* tflops, void* stream);
 
 /*
- * Number of times a slice-GEMM thread block (either variant) gave up waiting
+ * Number of times a slice-GEMM thread block (any variant) gave up waiting
  * for its operand copies on the current device (each wait is bounded in time; a block that
  * gives up stops early and its P tile is incomplete).  Synchronises the
  * device, reads the counter and resets it to 0.  Zero in normal operation.
