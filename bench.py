@@ -46,6 +46,7 @@ METRIC = "double-double GEMM dd-GFLOPS (2MNK/s) at 4096^3; % of FP64 tensor-pipe
 UNIT = "dd-GFLOP/s"
 DEFAULT_WORKLOAD = 2
 PAIRS = 36          # slice pairs with index sum <= 7 (8 parts per double double)
+TC_PAIRS = 91       # part pairs with index sum <= 12 (13 parts of 8 bits, bf16 tensor-core variant)
 SPLIT_BYTES = 80    # per input element: 16 B read (hi, lo) + 8 parts * 8 B written
 RECOMB_BYTES = 80   # per output element: 8 part sums * 8 B read + 16 B written
 FP64_NOMINAL_TF = 1.25
@@ -405,6 +406,45 @@ def run_ours(args, w):
     del ws_i, pA16, pB16, Pi
     assert ddg.wait_timeouts() == 0
 
+    # ---- 8-bit parts on the bf16 tensor cores (tcgen05), exact sums rounded once ----
+    ws_t = torch.empty(ddg.tc_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    T_hi = torch.empty_like(C_hi)
+    T_lo = torch.empty_like(C_lo)
+
+    def step_tc():
+        ddg.dd_gemm_tc(dA_hi, dA_lo, dB_hi, dB_lo, T_hi, T_lo, workspace=ws_t, stream=stream)
+
+    for _ in range(args.warmup):
+        step_tc()
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step_tc()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    units_t, t_t = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    del ws_t
+    _, _, _, splits_t = ddg.tc_layout(M, N, K)
+    pA8, e8, pB8, f8 = ddg.split_bf16(dA_hi, dA_lo, dB_hi, dB_lo, stream=stream)
+    Pt = ddg.slice_gemm_tc(M, N, K, pA8, pB8, splits_t, stream=stream)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        ddg.split_bf16(dA_hi, dA_lo, dB_hi, dB_lo, pA8, e8, pB8, f8, stream=stream)
+        evs[i][1].record(stream)
+        ddg.slice_gemm_tc(M, N, K, pA8, pB8, splits_t, Pt, stream=stream)
+        evs[i][2].record(stream)
+        ddg.recombine_tc(M, N, Pt, e8, f8, splits_t, T_hi, T_lo, stream=stream)
+        evs[i][3].record(stream)
+    torch.cuda.synchronize(dev)
+    tt_split = allreduce_max(dist, sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1e3, dev)
+    tt_gemm = allreduce_max(dist, sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1e3, dev)
+    tt_recomb = allreduce_max(dist, sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1e3, dev)
+    del pA8, pB8, Pt
+    assert ddg.wait_timeouts() == 0
+
     # ---- the comparator: plain double-double arithmetic on the FP64 ALUs ----
     S_hi = torch.empty_like(C_hi)
     S_lo = torch.empty_like(C_lo)
@@ -458,6 +498,13 @@ def run_ours(args, w):
     normwise = float(np.linalg.norm(d) / (np.linalg.norm(A_hi[rows] + A_lo[rows])
                                           * np.linalg.norm(B_hi + B_lo)))
 
+    Tg_hi = T_hi[rows].cpu().numpy()
+    Tg_lo = T_lo[rows].cpu().numpy()
+    dt = (Tg_hi - R_hi) + (Tg_lo - R_lo)
+    tc_norm = float(np.linalg.norm(dt) / (np.linalg.norm(A_hi[rows] + A_lo[rows]) * np.linalg.norm(B_hi + B_lo)))
+    tc_flops = TC_PAIRS * 2.0 * M * N * K
+    tc_tf = tc_flops / tt_gemm / 1e12
+
     QR = oracle_md_rows(QA, QB, [0, 1])
     dq = sum(qd_rows[p] - QR[p] for p in range(4))
     qd_norm = float(np.linalg.norm(dq) / (np.linalg.norm(sum(a[:2] for a in QA)) * np.linalg.norm(sum(QB))))
@@ -505,6 +552,20 @@ def run_ours(args, w):
                                         f"{SM_MAX_GHZ} GHz", "ms_per_launch": 1e3 * ti_gemm,
                          "ops_per_launch": PAIRS * M * N * K},
             "ms_split_int16": 1e3 * ti_split, "ms_recombine": 1e3 * ti_recomb,
+        },
+        "bf16_tensor_variant": {
+            "what": "13 balanced 8-bit parts per element (exact in bf16), the 91 part pairs with index sum "
+                    "<= 12 as tcgen05.mma (bf16 in, f32 accumulators in tensor memory, flushed every 256 "
+                    "products into exact int32 totals), the exact part sums rounded once to a double double",
+            "value": units_t / t_t / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_t / args.steps,
+            "k_splits": splits_t,
+            "normwise_vs_exact_oracle": tc_norm, "rows_checked": len(rows),
+            "roofline": {"bound": "tensor", "kernel": "slice_gemm_tc_kernel (tcgen05.mma kind::f16, bf16)",
+                         "achieved": tc_tf, "peak": bf16_tf, "unit": "TFLOP/s", "frac": tc_tf / bf16_tf,
+                         "peak_source": f"{peak_src} cuBLAS bf16 burst", "flops_per_launch": tc_flops,
+                         "ms_per_launch": 1e3 * tt_gemm},
+            "ms_split_bf16": 1e3 * tt_split, "ms_recombine": 1e3 * tt_recomb,
+            "launches_per_step": 5,
         },
         "qd_int_pipe": {
             "what": "quad-double GEMM (4 doubles per number): 16 parts of 13 bits, 136 pairs on the "

@@ -74,19 +74,30 @@ __device__ __forceinline__ uint32_t swizzled(int r, int kc) { return (uint32_t)(
 // bf16 bit pattern of a small integer (|d| <= 256: exact in float and in bf16).
 __device__ __forceinline__ uint32_t bf16_bits(int d) { return __float_as_uint(__int2float_rn(d)) >> 16; }
 
+// bf16 bit pattern of E - 128 for an integer 0 <= E <= 255: the f32 with bits
+// 0x4B000000 | E is 2^23 + E, and subtracting 2^23 + 128 is exact.
+__device__ __forceinline__ uint32_t bf16_of_biased(uint32_t E) {
+    return __float_as_uint(__fsub_rn(__uint_as_float(0x4B000000u | E), 8388736.0f)) >> 16;
+}
+
 // The 13 balanced base-256 digits of the element (hi, lo) against exponent
-// e' (most significant first), packed: out[s] holds the bf16 of digit s.
+// e' (most significant first), as bf16 bit patterns.  With C = 128 (256^11 +
+// ... + 256 + 1), the base-256 digits of X + C below 256^12 are D_s + 128
+// (s = 12 .. 1, least significant first), and (X + C) / 256^12 rounded down
+// is D_0: the balanced digits are read off one addition.
 __device__ __forceinline__ void balanced_parts(double hi, double lo, int ep, uint32_t (&out)[TS]) {
     uint64_t sign;
     const unsigned __int128 mag = fxp::fixed_point(hi, lo, ep, sign);
-    __int128 X = sign ? -(__int128)mag : (__int128)mag;
+    const unsigned __int128 C = ((unsigned __int128)0x80808080u << 64) | 0x8080808080808080ULL;
+    const unsigned __int128 Y = (sign ? (unsigned __int128)0 - mag : mag) + C;
+    const uint64_t y0 = (uint64_t)Y, y1 = (uint64_t)(Y >> 64);
 #pragma unroll
-    for (int s = TS - 1; s >= 1; --s) {
-        const int d = (int)(((uint32_t)(uint64_t)X + 128u) & 255u) - 128;
-        out[s] = bf16_bits(d);
-        X = (X - d) >> TD;  // exact: X - d is a multiple of 256
+    for (int s = 1; s < TS; ++s) {
+        const int b = TS - 1 - s;  // byte of Y, least significant = 0
+        const uint32_t E = (uint32_t)((b < 8 ? (y0 >> (8 * b)) : (y1 >> (8 * (b - 8)))) & 0xFFu);
+        out[s] = bf16_of_biased(E);
     }
-    out[0] = bf16_bits((int)(long long)X);
+    out[0] = bf16_bits((int)((int64_t)y1 >> 32));
 }
 
 struct TcSplitGrid {
@@ -94,6 +105,7 @@ struct TcSplitGrid {
     const double* B_hi; const double* B_lo; int64_t ldb, N; int32_t* f; int64_t b_tasks;
     int64_t K, KB;  // KB = k-blocks of 64
     uint16_t* planesA; uint16_t* planesB;
+    bool a_vec;     // A_hi, A_lo 16-byte aligned and lda even: 128-bit loads
 };
 
 // One warp per task.  A task: 4 rows of A x one k-block (lane = row (lane/8),
@@ -102,7 +114,7 @@ struct TcSplitGrid {
 // (lane = column, looping over the 8 chunks of 8 k): each load instruction
 // reads 256 contiguous bytes of a row of B, and each thread writes whole
 // 128-byte rows of every part.  Rows / k beyond the matrix are written as 0.
-__global__ void __launch_bounds__(256) split_bf16_kernel(TcSplitGrid g) {
+__global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * 8;
@@ -121,11 +133,20 @@ __global__ void __launch_bounds__(256) split_bf16_kernel(TcSplitGrid g) {
                 const int32_t er = g.e[r];
                 if (kb == 0 && kc == 0 && er == EXP_NONE) g.e[r] = 0;
                 ep = effective_exponent(er) + 1;
-                const double* ph = g.A_hi + r * g.lda;
-                const double* pl = g.A_lo + r * g.lda;
+                const double* ph = g.A_hi + r * g.lda + k0;
+                const double* pl = g.A_lo + r * g.lda + k0;
+                if (g.a_vec && k0 + 8 <= g.K) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (k0 + j < g.K) { hi[j] = __ldg(ph + k0 + j); lo[j] = __ldg(pl + k0 + j); }
+                    for (int j = 0; j < 8; j += 2) {
+                        const double2 h2 = __ldg(reinterpret_cast<const double2*>(ph + j));
+                        const double2 l2 = __ldg(reinterpret_cast<const double2*>(pl + j));
+                        hi[j] = h2.x; hi[j + 1] = h2.y; lo[j] = l2.x; lo[j + 1] = l2.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (k0 + j < g.K) { hi[j] = __ldg(ph + j); lo[j] = __ldg(pl + j); }
+                }
             }
             uint32_t w[TS][4];
 #pragma unroll
@@ -405,6 +426,104 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) slice_gemm_tc_kernel(TcGemmAr
 // Step 3: exact sum of the parts and one rounding into a double double.
 // ---------------------------------------------------------------------------
 
+typedef unsigned __int128 u128;
+
+__device__ __forceinline__ int msb128(u128 x) {  // x != 0
+    const uint64_t h = (uint64_t)(x >> 64);
+    return h ? 127 - __clzll((long long)h) : 63 - __clzll((long long)(uint64_t)x);
+}
+
+// Round a nonzero magnitude M = mh 2^64 + ml (M < 2^192, mh = M >> 64) to 53
+// bits, ties to even: M = keep 2^r + rem exactly, keep <= 2^53 (2^53 only as
+// 2^52 2^(r+1) after renormalising), |rem| <= 2^(r-1), rem signed.
+__device__ __forceinline__ void round53(u128 mh, uint64_t ml, uint64_t& keep, int& r, __int128& rem) {
+    const int t = mh ? 64 + msb128(mh) : 63 - __clzll((long long)ml);
+    r = t - 52;
+    if (r <= 0) {  // M < 2^53: exact
+        keep = ml;
+        r = 0;
+        rem = 0;
+        return;
+    }
+    // keep = M >> r (53 bits), low = M mod 2^r (r <= 139 - 52 = 87 bits)
+    u128 low;
+    if (r >= 64) {
+        keep = (uint64_t)(mh >> (r - 64));
+        low = ((mh & ((((u128)1) << (r - 64)) - 1)) << 64) | ml;
+    } else {
+        keep = (uint64_t)((mh << (64 - r)) | (u128)(ml >> r));
+        low = ml & ((1ULL << r) - 1);
+    }
+    const u128 half = ((u128)1) << (r - 1);
+    if (low > half || (low == half && (keep & 1))) {
+        keep += 1;
+        rem = (__int128)low - (__int128)(((u128)1) << r);
+    } else {
+        rem = (__int128)low;
+    }
+    if (keep >> 53) { keep >>= 1; r += 1; }  // 2^53 = 2^52 * 2: exact
+}
+
+// Step 3 for one output: Z = sum_d v_d 256^(12 - d) exactly, then the nearest
+// double double of Z 2^q.  Z is formed from two Horner sums that fit 128 bits
+// (|Z_l| < 2^91 for d = 6..12, |Z_h| < 2^83 for d = 0..5) as Z = Z_h 2^56 + Z_l
+// in three 64-bit words.  When q >= -1022 and the result stays below 2^1023
+// (every nonzero part is then a normal double) the rounding uses 128-bit
+// integer steps; otherwise the general 256-bit routine.
+__device__ __forceinline__ void recombine_one(const long long (&v)[TS], int q, double& c_hi, double& c_lo) {
+    u128 zl = 0, zh = 0;
+#pragma unroll
+    for (int d = 6; d < TS; ++d) zl = (zl << TD) + (u128)(__int128)v[d];
+#pragma unroll
+    for (int d = 0; d < 6; ++d) zh = (zh << TD) + (u128)(__int128)v[d];
+    // 192-bit two's complement Z = (w2, w1, w0)
+    const uint64_t l0 = (uint64_t)zl, l1 = (uint64_t)(zl >> 64);
+    const int64_t l2 = (int64_t)l1 >> 63;
+    const uint64_t h0 = (uint64_t)zh << 56, h1 = (uint64_t)(zh >> 8);
+    const int64_t h2 = (int64_t)((__int128)zh >> 72);
+    const uint64_t w0 = l0 + h0;
+    const uint64_t c0 = w0 < l0;
+    const uint64_t t1 = l1 + h1;
+    const uint64_t c1 = (t1 < l1) + ((t1 + c0) < t1);
+    const uint64_t w1 = t1 + c0;
+    const int64_t w2 = l2 + h2 + (int64_t)c1;
+    if (w0 == 0 && w1 == 0 && w2 == 0) { c_hi = 0.0; c_lo = 0.0; return; }
+    const uint64_t sign = w2 < 0 ? 1ULL : 0ULL;
+    uint64_t m0 = w0, m1 = w1, m2 = (uint64_t)w2;
+    if (sign) {  // magnitude of the 192-bit value
+        m0 = ~m0 + 1;
+        const uint64_t k0 = (m0 == 0);
+        m1 = ~m1 + k0;
+        const uint64_t k1 = k0 && (m1 == 0);
+        m2 = ~m2 + k1;
+    }
+    const u128 mh = ((u128)m2 << 64) | m1;
+    const int t = mh ? 64 + msb128(mh) : 63 - __clzll((long long)m0);
+    if (q >= -1022 && t + q <= 1022) {
+        uint64_t keep;
+        int r;
+        __int128 rem;
+        round53(mh, m0, keep, r, rem);
+        c_hi = wide::make_double(keep, r + q, sign);
+        if (rem == 0) { c_lo = 0.0; return; }
+        const uint64_t sl = sign ^ (rem < 0 ? 1ULL : 0ULL);
+        const u128 rm = rem < 0 ? (u128)(-rem) : (u128)rem;
+        uint64_t keep2;
+        int r2;
+        __int128 rem2;
+        round53(rm >> 64, (uint64_t)rm, keep2, r2, rem2);
+        c_lo = wide::make_double(keep2, r2 + q, sl);
+        return;
+    }
+    wide::U256 Z;
+    Z.lo = ((u128)w1 << 64) | w0;
+    Z.hi = (u128)(__int128)w2;
+    double out[2];
+    wide::round_into_doubles<2>(Z, q, out);
+    c_hi = out[0];
+    c_lo = out[1];
+}
+
 __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
                                                            int64_t Np, const int32_t* __restrict__ e,
                                                            const int32_t* __restrict__ f, int64_t M, int64_t N,
@@ -415,18 +534,19 @@ __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __rest
     const int64_t plane = Mp * Np;
     const int fj = effective_exponent(f[j]) + 1;
     for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
-        wide::U256 Z = wide::u256_zero();
+        long long v[TS];
+        const int32_t* p = P + i * Np + j;
 #pragma unroll
-        for (int d = 0; d < TS; ++d) {
-            long long v = 0;
-            for (int zz = 0; zz < splits; ++zz) v += __ldg(P + ((int64_t)zz * TS + d) * plane + i * Np + j);
-            Z = wide::u256_add(Z, wide::u256_from_signed(v, TD * (TS - 1 - d)));
+        for (int d = 0; d < TS; ++d) v[d] = __ldg(p + (int64_t)d * plane);
+        for (int zz = 1; zz < splits; ++zz) {
+#pragma unroll
+            for (int d = 0; d < TS; ++d) v[d] += __ldg(p + ((int64_t)zz * TS + d) * plane);
         }
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (TS + 1);
-        double out[2];
-        wide::round_into_doubles<2>(Z, q, out);
-        C_hi[i * ldc + j] = out[0];
-        C_lo[i * ldc + j] = out[1];
+        double hi, lo;
+        recombine_one(v, q, hi, lo);
+        C_hi[i * ldc + j] = hi;
+        C_lo[i * ldc + j] = lo;
     }
 }
 
@@ -448,6 +568,7 @@ cudaError_t launch_split_bf16(const SplitOperand* A, const SplitOperand* B, int6
     if (A) {
         g.A_hi = A->hi; g.A_lo = A->lo; g.lda = A->ld; g.M = A->rows; g.e = A->exp;
         g.a_tasks = (round_up(A->rows, TBM) / 4) * g.KB;
+        g.a_vec = (uintptr_t)A->hi % 16 == 0 && (uintptr_t)A->lo % 16 == 0 && A->ld % 2 == 0;
     }
     if (B) {
         g.B_hi = B->hi; g.B_lo = B->lo; g.ldb = B->ld; g.N = B->rows; g.f = B->exp;
