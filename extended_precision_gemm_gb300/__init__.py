@@ -29,7 +29,7 @@ __all__ = [
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
     "split", "split_i16", "dd_gemm_simt",
     "QD_MAX_K", "qd_gemm", "qd_layout", "qd_workspace_size", "qd_split", "qd_slice_gemm", "qd_recombine",
-    "TC_SLICES", "TC_TILE_M", "TC_TILE_N", "TC_CHUNK_K", "TC_MAX_K_SPLIT",
+    "TC_SLICES", "TC_TILE_M", "TC_BLOCK_M", "TC_TILE_N", "TC_CHUNK_K", "TC_MAX_K_SPLIT",
     "dd_gemm_tc", "tc_layout", "tc_workspace_size", "split_bf16", "slice_gemm_tc", "recombine_tc",
 ]
 
@@ -535,7 +535,8 @@ def qd_recombine(M: int, N: int, P, e, f, stream=None):
 # ---- double doubles with 8-bit parts on the bf16 tensor cores (tcgen05) ----
 
 TC_SLICES = 13
-TC_TILE_M = 128
+TC_TILE_M = 256
+TC_BLOCK_M = 128
 TC_TILE_N = 256
 TC_CHUNK_K = 64
 TC_MAX_K_SPLIT = 8192

@@ -651,7 +651,7 @@ struct TcLayout {
 // most DDGEMM_TC_MAX_K_SPLIT of k (exact int32 part sums); beyond that, the
 // count whose waves of blocks (one per SM) fill the GPU best, each split
 // keeping at least 512 of k, with a small cost per split (each writes its own
-// part sums).
+// part sums).  One output block occupies a pair of SMs.
 int choose_tc_splits(int64_t Mp, int64_t Np, int64_t Kp) {
     const int64_t KB = Kp / kTcK;
     const int64_t tiles = (Mp / kTcM) * (Np / kTcN);
@@ -659,7 +659,7 @@ int choose_tc_splits(int64_t Mp, int64_t Np, int64_t Kp) {
     const int64_t smin = std::max<int64_t>(1, (KB + per_split - 1) / per_split);
     if (tiles == 0 || KB == 0) return 1;
     const int64_t smax = std::max<int64_t>(smin, std::min<int64_t>(KB / 8, 4 * smin + 8));
-    const int64_t slots = device_sms();
+    const int64_t slots = device_sms() / 2;  // one output block per CTA pair (two SMs)
     int64_t best = smin;
     double best_score = -1.0;
     for (int64_t s = smin; s <= smax; ++s) {

@@ -52,6 +52,43 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Plain arrive on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile(
+        "{\n"
+        " .reg .b64 st;\n"
+        " mbarrier.arrive.shared::cta.b64 st, [%0];\n"
+        "}\n" ::"r"(bar)
+        : "memory");
+}
+
+// Arrive on the barrier at shared-memory offset `bar` of CTA `rank` of this
+// cluster.  (The arrivals of the slice GEMM announce data the tensor core
+// reads or tensor memory it may overwrite; no generic-proxy data is published
+// through them, so the default semantics suffice and no cluster-scope fence
+// is paid per arrival.)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+    asm volatile(
+        "{\n"
+        " .reg .b32 ra;\n"
+        " mapa.shared::cluster.u32 ra, %0, %1;\n"
+        " mbarrier.arrive.shared::cluster.b64 _, [ra];\n"
+        "}\n" ::"r"(bar),
+        "r"(rank)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Arrive on the barrier, announcing `bytes` of copies that will complete it.
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile(

@@ -74,6 +74,51 @@ __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&v)[32]) {
         : "memory");
 }
 
+// ---- CTA pairs (cta_group::2): one MMA spans the tensor cores of two SMs ----
+//
+// The two CTAs of a cluster of 2 are peers.  Tensor memory is allocated
+// collectively (one warp of each CTA) at the same address in both.  An MMA
+// issued by one thread of the even CTA with M = 256 reads rows 0-127 of A from
+// the even CTA's shared memory and rows 128-255 from the odd CTA's (same
+// offset), the first N/2 rows of B from the even CTA and the rest from the
+// odd CTA, and writes rows 0-127 of D to the even CTA's tensor memory and rows
+// 128-255 to the odd CTA's.
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask`
+// when the pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void commit_pair(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
 // swizzled layout: rows of 128 bytes (64 bf16 of k), the 16-byte chunks of
 // row r XOR-permuted by r % 8, groups of 8 rows 1024 bytes apart (the stride

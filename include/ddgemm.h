@@ -353,7 +353,7 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
  *     (least significant first, D = ((X + 128) mod 256) - 128, the top digit
  *     the rest): every part is an integer in [-128, 128], exact in bf16;
  *   - P_d = sum_{s+t=d} A_s B_t for d = 0..12 (91 pairs) with tcgen05.mma
- *     (bf16 in, f32 accumulators in tensor memory), exact: 256 products of at
+ *     (bf16 in, f32 accumulators in tensor memory), exact: 512 products of at
  *     most 2^14 are summed in f32 and then added into exact int32 totals;
  *   - Z = sum_d P_d 2^(8 (12 - d)) (exact) rounded once to the nearest double
  *     double of Z 2^(e'_i + f'_j - 112) (ties to even; zeros are +0).
@@ -365,13 +365,14 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
  */
 #define DDGEMM_TC_SLICES 13         /* parts per double double */
 #define DDGEMM_TC_DIGIT_BITS 8      /* bits per part */
-#define DDGEMM_TC_TILE_M 128        /* rows of A per part block / output block */
-#define DDGEMM_TC_TILE_N 256        /* columns of B per part block / output block */
+#define DDGEMM_TC_TILE_M 256        /* rows of C per output block (a CTA pair); Mp is a multiple */
+#define DDGEMM_TC_BLOCK_M 128       /* rows of A per part block */
+#define DDGEMM_TC_TILE_N 256        /* columns of B per part block / of C per output block */
 #define DDGEMM_TC_CHUNK_K 64        /* k per part block (one 128-byte row) */
 #define DDGEMM_TC_MAX_K_SPLIT 8192  /* k per slice-GEMM block: int32 part sums stay exact */
 
 /*
- * Padded extents (Mp = M rounded up to 128, Np = N rounded up to 256, Kp = K
+ * Padded extents (Mp = M rounded up to 256, Np = N rounded up to 256, Kp = K
  * rounded up to 64) and the k-split of the slice GEMM (every split covers at
  * most DDGEMM_TC_MAX_K_SPLIT of k).  Any output pointer may be NULL.
  */
@@ -389,8 +390,8 @@ ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K,
  *
  * dd_split_bf16: e (M int32) and f (N int32) receive the exponents e, f of
  * dd_split (the parts use e + 1, f + 1), and the parts as bf16 bit patterns:
- *   planesA: 13 * Mp * Kp uint16, block (mt, s, kb) of 128 x 64 at element
- *            ((mt * 13 + s) * (Kp / 64) + kb) * 8192;
+ *   planesA: 13 * Mp * Kp uint16, block (mb, s, kb) of 128 x 64 (rows
+ *            128 mb .. 128 mb + 127) at element ((mb * 13 + s) * (Kp / 64) + kb) * 8192;
  *   planesB: 13 * Np * Kp uint16, block (nt, t, kb) of 256 x 64 at element
  *            ((nt * 13 + t) * (Kp / 64) + kb) * 16384;
  *   inside a block, element (row r, k) is at byte

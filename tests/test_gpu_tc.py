@@ -32,10 +32,9 @@ def bf16_values(bits):
     return v.astype(np.int64)
 
 
-def unswizzle(planes, rows, K, block_rows):
+def unswizzle(planes, Rp, K, block_rows):
     """Part blocks (block, s, kb) of block_rows x 64 in the 128-byte swizzled
-    layout of include/ddgemm.h -> D[s, row, k] for the padded extents."""
-    Rp = -(-rows // block_rows) * block_rows
+    layout of include/ddgemm.h -> D[s, row, k] for Rp padded rows."""
     Kp = -(-K // 64) * 64
     KB = Kp // 64
     a = bf16_values(planes).reshape(Rp // block_rows, sb.S, KB, block_rows, 8, 8)  # [blk][s][kb][r][pchunk][e]
@@ -44,6 +43,10 @@ def unswizzle(planes, rows, K, block_rows):
     for kc in range(8):
         out[:, :, :, r, kc, :] = a[:, :, :, r, kc ^ (r % 8), :]
     return out.transpose(1, 0, 3, 2, 4, 5).reshape(sb.S, Rp, Kp)
+
+
+def pad(n, m):
+    return -(-n // m) * m
 
 
 def model(A_hi, A_lo, B_hi, B_lo):
@@ -60,8 +63,8 @@ def test_split_bf16_bit_exact(M, N, K, dist):
     e_ref, f_ref, DA_ref, DB_ref = model(A_hi, A_lo, B_hi, B_lo)
     # the exponent arrays hold the 13-bit method's exponents; the parts use + 1
     assert np.array_equal(host(e) + 1, e_ref) and np.array_equal(host(f) + 1, f_ref)
-    DA = unswizzle(host(pA), M, K, ddg.TC_TILE_M)
-    DB = unswizzle(host(pB), N, K, ddg.TC_TILE_N)
+    DA = unswizzle(host(pA), pad(M, ddg.TC_TILE_M), K, ddg.TC_BLOCK_M)
+    DB = unswizzle(host(pB), pad(N, ddg.TC_TILE_N), K, ddg.TC_TILE_N)
     assert np.array_equal(DA[:, :M, :K], DA_ref)
     assert np.array_equal(DB[:, :N, :K], DB_ref.transpose(0, 2, 1))
     assert not DA[:, M:, :].any() and not DA[:, :, K:].any()
@@ -165,8 +168,8 @@ def test_k_beyond_one_split_is_split_and_exact():
 
 def _extreme_element():
     """A double double whose parts (exponent e' = 0) are -127 then twelve times
-    -128: every product of two lower parts is 2^14, so a chunk of 256 of them
-    sums to exactly 2^22, the bound of the f32 accumulation."""
+    -128: every product of two lower parts is 2^14, so a chunk of 512 of them
+    sums to exactly 2^23, the bound of the f32 accumulation."""
     from fractions import Fraction
     X = -(127 * 256**12 + 128 * (256**12 - 1) // 255)
     v = Fraction(X, 2**104)
@@ -184,14 +187,14 @@ def test_largest_parts_accumulate_exactly():
     assert sb.digits_of(hi, lo, 0) == [-127] + [-128] * 12
     pA, e, pB, f = ddg.split_bf16(dev(A_hi), dev(A_lo), dev(B_hi), dev(B_lo))
     assert (host(e) == -1).all() and (host(f) == -1).all()
-    DA = unswizzle(host(pA), M, K, ddg.TC_TILE_M)
-    assert (DA[0] == -127).all() and (DA[1:] == -128).all()
+    DA = unswizzle(host(pA), pad(M, ddg.TC_TILE_M), K, ddg.TC_BLOCK_M)
+    assert (DA[0, :M] == -127).all() and (DA[1:, :M] == -128).all()
     P = host(ddg.slice_gemm_tc(M, N, K, pA, pB, 1)).astype(np.int64)[0]
     _, _, DAr, DBr = model(A_hi[:2], A_lo[:2], B_hi[:, :2], B_lo[:, :2])
     P_ref = sb.slice_products(DAr, DBr)
     assert P_ref[12, 0, 0] == K * (2 * 127 * 128 + 11 * 128 * 128)
     assert np.array_equal(P[:, :2, :2], P_ref)
-    assert np.all(P == P[:, :1, :1])          # every output identical
+    assert np.all(P[:, :M, :N] == P[:, :1, :1])   # every output identical
     C_hi, C_lo = ddg.dd_gemm_tc(dev(A_hi), dev(A_lo), dev(B_hi), dev(B_lo))
     X = oracle.exact_dd_gemm(A_hi[:2], A_lo[:2], B_hi[:, :2], B_lo[:, :2])
     assert normwise(host(C_hi)[:2, :2], host(C_lo)[:2, :2], *X, A_hi[:2], A_lo[:2], B_hi[:, :2], B_lo[:, :2]) <= GATE
