@@ -74,33 +74,33 @@ __device__ unsigned int g_wait_timeouts_tc = 0;
 // 128 bytes, chunk kc of row r stored at position kc ^ (r % 8).
 __device__ __forceinline__ uint32_t swizzled(int r, int kc) { return (uint32_t)(r * 128 + ((kc ^ (r & 7)) << 4)); }
 
-// bf16 bit pattern of a small integer (|d| <= 256: exact in float and in bf16).
-__device__ __forceinline__ uint32_t bf16_bits(int d) { return __float_as_uint(__int2float_rn(d)) >> 16; }
-
-// bf16 bit pattern of E - 128 for an integer 0 <= E <= 255: the f32 with bits
-// 0x4B000000 | E is 2^23 + E, and subtracting 2^23 + 128 is exact.
-__device__ __forceinline__ uint32_t bf16_of_biased(uint32_t E) {
-    return __float_as_uint(__fsub_rn(__uint_as_float(0x4B000000u | E), 8388736.0f)) >> 16;
-}
-
 // The 13 balanced base-256 digits of the element (hi, lo) against exponent
-// e' (most significant first), as bf16 bit patterns.  With C = 128 (256^11 +
-// ... + 256 + 1), the base-256 digits of X + C below 256^12 are D_s + 128
-// (s = 12 .. 1, least significant first), and (X + C) / 256^12 rounded down
-// is D_0: the balanced digits are read off one addition.
-__device__ __forceinline__ void balanced_parts(double hi, double lo, int ep, uint32_t (&out)[TS]) {
+// e' (most significant first), each as the bit pattern of an f32 whose upper
+// half is the digit's bf16 (every digit has at most 8 significant bits).
+// With C = 128 (256^11 + ... + 256 + 1), the base-256 digits of X + C below
+// 256^12 are D_s + 128 (s = 12 .. 1, least significant first), and
+// (X + C) / 256^12 rounded down is D_0: the balanced digits are read off one
+// addition.  A byte E placed under the exponent field of 2^23 (bits
+// 0x4B0000EE) is the f32 2^23 + E, and subtracting 2^23 + 128 leaves E - 128
+// exactly.
+__device__ __forceinline__ void balanced_parts(double hi, double lo, int ep, uint32_t (&f32)[TS]) {
     uint64_t sign;
     const unsigned __int128 mag = fxp::fixed_point(hi, lo, ep, sign);
     const unsigned __int128 C = ((unsigned __int128)0x80808080u << 64) | 0x8080808080808080ULL;
     const unsigned __int128 Y = (sign ? (unsigned __int128)0 - mag : mag) + C;
-    const uint64_t y0 = (uint64_t)Y, y1 = (uint64_t)(Y >> 64);
+    const uint32_t w[4] = {(uint32_t)Y, (uint32_t)(Y >> 32), (uint32_t)(Y >> 64), (uint32_t)(Y >> 96)};
 #pragma unroll
     for (int s = 1; s < TS; ++s) {
         const int b = TS - 1 - s;  // byte of Y, least significant = 0
-        const uint32_t E = (uint32_t)((b < 8 ? (y0 >> (8 * b)) : (y1 >> (8 * (b - 8)))) & 0xFFu);
-        out[s] = bf16_of_biased(E);
+        const uint32_t bits = __byte_perm(w[b >> 2], 0x4B000000u, 0x7440u | (uint32_t)(b & 3));
+        f32[s] = __float_as_uint(__fsub_rn(__uint_as_float(bits), 8388736.0f));
     }
-    out[0] = bf16_bits((int)((int64_t)y1 >> 32));
+    f32[0] = __float_as_uint(__int2float_rn((int)w[3]));
+}
+
+// Two parts' bf16 patterns in one word (first element in the low half).
+__device__ __forceinline__ uint32_t pack_bf16(uint32_t f_first, uint32_t f_second) {
+    return __byte_perm(f_first, f_second, 0x7632u);
 }
 
 struct TcSplitGrid {
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
                 balanced_parts(hi[j], lo[j], ep, p0);
                 balanced_parts(hi[j + 1], lo[j + 1], ep, p1);
 #pragma unroll
-                for (int s = 0; s < TS; ++s) w[s][j >> 1] = p0[s] | (p1[s] << 16);
+                for (int s = 0; s < TS; ++s) w[s][j >> 1] = pack_bf16(p0[s], p1[s]);
             }
             const int64_t mt = r / TBM;
             const int rin = (int)(r % TBM);
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
                 balanced_parts(hi[j], lo[j], ep, p0);
                 balanced_parts(hi[j + 1], lo[j + 1], ep, p1);
 #pragma unroll
-                for (int s = 0; s < TS; ++s) w[s][j >> 1] = p0[s] | (p1[s] << 16);
+                for (int s = 0; s < TS; ++s) w[s][j >> 1] = pack_bf16(p0[s], p1[s]);
             }
             const int64_t nt = n / TBN;
             const int nin = (int)(n % TBN);
@@ -215,8 +215,8 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
 // N = 256, K = 16 (tcgen05 cta_group::2): each CTA holds its 128 rows of A and
 // its 128 rows of B (columns of C) for a k-block, and its 128 rows of the
 // accumulators.  10 warps per CTA:
-//   warp 0 (one thread): bulk copies of this CTA's part halves into a 6-stage
-//           ring (32 KB per stage);
+//   warp 0 (one thread): bulk copies of this CTA's part halves into a 3-stage
+//           ring (64 KB per stage: two 64-k blocks of one pair (s, t));
 //   warp 1: allocates 512 TMEM columns in both CTAs (two f32 accumulators of
 //           128 x 256 per CTA); in the even CTA one thread issues the MMAs (4
 //           per 64-k block) once both CTAs' stage is full; in the odd CTA one
@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
 //           32 (w % 4) .. +31, i.e. rows, and one half of the columns), add it
 //           into int32 totals in registers, and store the totals of P_d.
 // The order of work is d = 0..12, then s = 0..d (t = d - s), then k-blocks;
-// a chunk is 4 consecutive k-blocks of one d (the last chunk of a d may be
-// shorter).  Chunks alternate between the two accumulators, so the MMAs of
+// a chunk is 8 consecutive k-blocks of one d (512 products per output; the
+// last chunk of a d may be shorter).  Chunks alternate between the two accumulators, so the MMAs of
 // one chunk overlap the read-out of the previous one.  Completion of MMAs
 // reaches both CTAs through multicast commits; the release of an
 // accumulator needs all 16 epilogue warps of the pair.
