@@ -555,7 +555,7 @@ def run_ours(args, w):
         },
         "bf16_tensor_variant": {
             "what": "13 balanced 8-bit parts per element (exact in bf16), the 91 part pairs with index sum "
-                    "<= 12 as tcgen05.mma (bf16 in, f32 accumulators in tensor memory, flushed every 256 "
+                    "<= 12 as tcgen05.mma (bf16 in, f32 accumulators in tensor memory, flushed every 512 "
                     "products into exact int32 totals), the exact part sums rounded once to a double double",
             "value": units_t / t_t / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_t / args.steps,
             "k_splits": splits_t,
