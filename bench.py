@@ -477,7 +477,21 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     units_q, t_q = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
     qd_rows = [QC[p][:2].cpu().numpy() for p in range(4)]
-    del tQA, tQB, QC, ws_q
+    del ws_q
+    # the same quad-double product with 27 bf16 parts on the tensor cores
+    ws_qt = torch.empty(ddg.qd_tc_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    ddg.qd_gemm_tc(tQA, tQB, QC, workspace=ws_qt, stream=stream)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        ddg.qd_gemm_tc(tQA, tQB, QC, workspace=ws_qt, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    units_qt, t_qt = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    qdt_rows = [QC[p][:2].cpu().numpy() for p in range(4)]
+    splits_qt = ddg.qd_tc_layout(M, N, K)[3]
+    del tQA, tQB, QC, ws_qt
     assert ddg.wait_timeouts() == 0
 
     if rank != 0:
@@ -508,6 +522,8 @@ def run_ours(args, w):
     QR = oracle_md_rows(QA, QB, [0, 1])
     dq = sum(qd_rows[p] - QR[p] for p in range(4))
     qd_norm = float(np.linalg.norm(dq) / (np.linalg.norm(sum(a[:2] for a in QA)) * np.linalg.norm(sum(QB))))
+    dqt = sum(qdt_rows[p] - QR[p] for p in range(4))
+    qdt_norm = float(np.linalg.norm(dqt) / (np.linalg.norm(sum(a[:2] for a in QA)) * np.linalg.norm(sum(QB))))
     n8 = min(8, len(rows))
     ds = (Sr_hi[:n8] - R_hi[:n8]) + (Sr_lo[:n8] - R_lo[:n8])
     simt_norm = float(np.linalg.norm(ds) / (np.linalg.norm(A_hi[:n8] + A_lo[:n8]) * np.linalg.norm(B_hi + B_lo)))
@@ -566,6 +582,15 @@ def run_ours(args, w):
                          "ms_per_launch": 1e3 * tt_gemm},
             "ms_split_bf16": 1e3 * tt_split, "ms_recombine": 1e3 * tt_recomb,
             "launches_per_step": 5,
+        },
+        "qd_bf16_tensor_variant": {
+            "what": "quad-double GEMM with 27 balanced 8-bit parts (exact in bf16), the 378 part pairs with "
+                    "index sum <= 26 as tcgen05.mma on CTA pairs, exact sums rounded once into 4 doubles",
+            "workload": w.name.replace("dd_gemm", "qd_gemm"),
+            "value": units_qt / t_qt / 1e9, "unit": "qd-GFLOP/s (2MNK/s)",
+            "ms_per_step": 1e3 * t_qt / args.steps, "k_splits": splits_qt, "slice_pairs": 378,
+            "bf16_tflops_whole_product": 378 * 2.0 * M * N * K / (t_qt / args.steps) / 1e12,
+            "normwise_vs_exact_oracle_2_rows": qdt_norm,
         },
         "qd_int_pipe": {
             "what": "quad-double GEMM (4 doubles per number): 16 parts of 13 bits, 136 pairs on the "

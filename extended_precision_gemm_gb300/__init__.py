@@ -31,6 +31,8 @@ __all__ = [
     "QD_MAX_K", "qd_gemm", "qd_layout", "qd_workspace_size", "qd_split", "qd_slice_gemm", "qd_recombine",
     "TC_SLICES", "TC_TILE_M", "TC_BLOCK_M", "TC_TILE_N", "TC_CHUNK_K", "TC_MAX_K_SPLIT",
     "dd_gemm_tc", "tc_layout", "tc_workspace_size", "split_bf16", "slice_gemm_tc", "recombine_tc",
+    "TC_QD_SLICES", "TC_QD_MAX_K_SPLIT", "qd_gemm_tc", "qd_tc_layout", "qd_tc_workspace_size", "qd_split_bf16",
+    "qd_slice_gemm_tc", "qd_recombine_tc",
 ]
 
 SLICES = 8
@@ -91,6 +93,12 @@ _SIGNATURES = {
     "dd_split_bf16": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
     "dd_slice_gemm_tc": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
     "dd_recombine_tc": ([_i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _ptr, _i64, _ptr], _int),
+    "qd_gemm_tc_layout": ([_i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr], _int),
+    "qd_gemm_tc_workspace_size": ([_i64, _i64, _i64, _ptr], _int),
+    "qd_gemm_tc": ([_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, ctypes.c_size_t, _ptr], _int),
+    "qd_split_bf16": ([_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
+    "qd_slice_gemm_tc": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
+    "qd_recombine_tc": ([_i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _i64, _ptr], _int),
 }
 
 
@@ -623,3 +631,95 @@ def recombine_tc(M: int, N: int, P, e, f, splits=None, C_hi=None, C_lo=None, str
                                                      C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi),
                                                      _stream_handle(stream)))
     return C_hi, C_lo
+
+
+# ---- quad doubles with 27 bf16 parts on the tensor cores ----
+
+TC_QD_SLICES = 27
+
+
+def _vp(arr):
+    return ctypes.cast(arr, ctypes.c_void_p)
+
+TC_QD_MAX_K_SPLIT = 4096
+
+
+def qd_tc_layout(M: int, N: int, K: int):
+    """(Mp, Np, Kp, splits) of the bf16 quad-double variant for this shape."""
+    Mp, Np, Kp, sp = _i64(), _i64(), _i64(), _int()
+    _check("qd_gemm_tc_layout", load().qd_gemm_tc_layout(M, N, K, ctypes.byref(Mp), ctypes.byref(Np),
+                                                         ctypes.byref(Kp), ctypes.byref(sp)))
+    return Mp.value, Np.value, Kp.value, sp.value
+
+
+def qd_tc_workspace_size(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check("qd_gemm_tc_workspace_size", load().qd_gemm_tc_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def qd_gemm_tc(A, B, C=None, workspace=None, stream=None):
+    """C = A @ B for quad doubles (lists of four planes each) with 27 bf16 parts
+    and the 378 part pairs on the tensor cores; exact sums rounded once."""
+    torch = _torch()
+    A = [_qd_planes(A, "A")[p] for p in range(4)]
+    B = [_qd_planes(B, "B")[p] for p in range(4)]
+    M, K = A[0].shape
+    K2, N = B[0].shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    if C is None:
+        C = [torch.empty((M, N), dtype=torch.float64, device=A[0].device) for _ in range(4)]
+    C = _qd_planes(C, "C")
+    pa, pb, pc = _ptr_array(A), _ptr_array(B), _ptr_array(C)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("qd_gemm_tc", load().qd_gemm_tc(M, N, K, _vp(pa), _ld(A[0]), _vp(pb), _ld(B[0]), _vp(pc), _ld(C[0]), wp, wn,
+                                           _stream_handle(stream)))
+    return C
+
+
+def qd_split_bf16(A, B, stream=None):
+    """Step 1 of the bf16 quad-double variant: (planesA, e, planesB, f)."""
+    torch = _torch()
+    A = _qd_planes(A, "A")
+    B = _qd_planes(B, "B")
+    M, K = A[0].shape
+    N = B[0].shape[1]
+    Mp, Np, Kp = -(-M // TC_TILE_M) * TC_TILE_M, -(-N // TC_TILE_N) * TC_TILE_N, -(-K // TC_CHUNK_K) * TC_CHUNK_K
+    dev = A[0].device
+    pA = torch.empty(TC_QD_SLICES * Mp * Kp, dtype=torch.int16, device=dev)
+    pB = torch.empty(TC_QD_SLICES * Np * Kp, dtype=torch.int16, device=dev)
+    e = torch.empty(M, dtype=torch.int32, device=dev)
+    f = torch.empty(N, dtype=torch.int32, device=dev)
+    pa, pb = _ptr_array(A), _ptr_array(B)
+    _check("qd_split_bf16", load().qd_split_bf16(M, N, K, _vp(pa), _ld(A[0]), _vp(pb), _ld(B[0]),
+                                                 pA.data_ptr(), e.data_ptr(), pB.data_ptr(), f.data_ptr(),
+                                                 _stream_handle(stream)))
+    return pA, e, pB, f
+
+
+def qd_slice_gemm_tc(M: int, N: int, K: int, planesA, planesB, splits: int, P=None, stream=None):
+    """Step 2: P (splits x 27 x Mp x Np int32)."""
+    torch = _torch()
+    Mp, Np = -(-M // TC_TILE_M) * TC_TILE_M, -(-N // TC_TILE_N) * TC_TILE_N
+    if P is None:
+        P = torch.empty((splits, TC_QD_SLICES, Mp, Np), dtype=torch.int32, device=planesA.device)
+    if P.numel() < splits * TC_QD_SLICES * Mp * Np:
+        raise ValueError("output buffer too small")
+    _check("qd_slice_gemm_tc", load().qd_slice_gemm_tc(M, N, K, planesA.data_ptr(), planesB.data_ptr(), splits,
+                                                       P.data_ptr(), _stream_handle(stream)))
+    return P
+
+
+def qd_recombine_tc(M: int, N: int, P, e, f, splits=None, C=None, stream=None):
+    """Step 3: the four planes of C from P and the exponents."""
+    torch = _torch()
+    splits = P.shape[0] if splits is None else splits
+    if C is None:
+        C = [torch.empty((M, N), dtype=torch.float64, device=P.device) for _ in range(4)]
+    C = _qd_planes(C, "C")
+    pc = _ptr_array(C)
+    _check("qd_recombine_tc", load().qd_recombine_tc(M, N, P.data_ptr(), splits, e.data_ptr(), f.data_ptr(),
+                                                     _vp(pc), _ld(C[0]), _stream_handle(stream)))
+    return C

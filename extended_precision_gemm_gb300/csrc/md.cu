@@ -22,6 +22,7 @@
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "wide_int.cuh"
+#include "fixed_point_md.cuh"
 #include "launch.cuh"
 
 namespace ddg {
@@ -32,75 +33,6 @@ constexpr int NPQ = 4;                      // doubles per quad double
 constexpr int FIXQ = SQ * DIGIT;            // 208 fraction bits
 constexpr uint64_t ABS_MASK = 0x7FFFFFFFFFFFFFFFULL;
 using namespace wide;
-
-struct Unp {
-    uint64_t m;
-    int E;  // |x| = m 2^E
-};
-
-__device__ __forceinline__ Unp unpack_abs(uint64_t bits) {
-    const uint64_t a = bits & ABS_MASK;
-    const int biased = (int)(a >> 52);
-    Unp u;
-    if (biased == 0) { u.m = a & ((1ULL << 52) - 1); u.E = -1074; }
-    else { u.m = (a & ((1ULL << 52) - 1)) | (1ULL << 52); u.E = biased - 1075; }
-    return u;
-}
-
-// X = floor(|x0 + x1 + x2 + x3| 2^(208 - e)) for a normalised quad double
-// (|x_{p+1}| <= ulp(x_p) / 2) and the sign of the element.  With every part
-// signed relative to the leading one, the parts that are integers at this
-// scale add exactly; at the first part j with a fraction, floor(a_j + rest)
-// = floor(a_j) when a_j has a nonzero fraction (the rest is below half its
-// last bit), else floor(a_j) - 1 when the first nonzero later part is
-// negative (the borrow of Problem 3.3, eq. (7)).
-__device__ __forceinline__ U256 fixed_point_qd(const double (&x)[NPQ], int e, uint64_t& sign_out) {
-    int lead = -1;
-#pragma unroll
-    for (int p = NPQ - 1; p >= 0; --p)
-        if (((uint64_t)__double_as_longlong(x[p]) & ABS_MASK) != 0) lead = p;
-    sign_out = 0;
-    if (lead < 0) return u256_zero();
-    const uint64_t sign = (uint64_t)__double_as_longlong(x[lead]) >> 63;
-    sign_out = sign;
-    U256 X = u256_zero();
-    bool done = false;
-#pragma unroll
-    for (int p = 0; p < NPQ; ++p) {
-        const uint64_t b = (uint64_t)__double_as_longlong(x[p]);
-        if (done || (b & ABS_MASK) == 0) continue;
-        const bool negp = ((b >> 63) != sign);  // part sign relative to the element
-        const Unp u = unpack_abs(b);
-        const int sh = u.E + FIXQ - e;
-        if (sh >= 0) {
-            U256 t = u256_shl(u.m, sh > 190 ? 190 : sh);
-            X = u256_add(X, negp ? u256_neg(t) : t);
-            continue;
-        }
-        // first part with a fraction: its floor, and the borrow
-        const int rs = -sh;
-        const uint64_t ip = rs >= 64 ? 0 : (u.m >> rs);
-        const bool frac = rs >= 64 ? (u.m != 0) : ((u.m & ((1ULL << rs) - 1)) != 0);
-        int64_t F;
-        if (!negp) F = (int64_t)ip;
-        else F = -(int64_t)(ip + (frac ? 1 : 0));
-        if (!frac) {
-#pragma unroll
-            for (int r = 0; r < NPQ; ++r) {
-                if (r <= p) continue;
-                const uint64_t c = (uint64_t)__double_as_longlong(x[r]);
-                if ((c & ABS_MASK) != 0) {
-                    if ((c >> 63) != sign) F -= 1;
-                    break;
-                }
-            }
-        }
-        U256 t = u256_shl((uint64_t)(F < 0 ? -F : F), 0);
-        X = u256_add(X, F < 0 ? u256_neg(t) : t);
-        done = true;
-    }
-    return X;
-}
 
 // ---------------------------------------------------------------------------
 // Step 1: exponents come from the double-double exponent kernel on the
@@ -144,7 +76,7 @@ __global__ void __launch_bounds__(256) split_qd_kernel(QdOperand A, QdOperand B,
                 for (int p = 0; p < NPQ; ++p) x[p] = __ldg(op.p[p] + off);
             }
             uint64_t sign;
-            const U256 X = fixed_point_qd(x, ex, sign);
+            const U256 X = fxp::fixed_point_qd<FIXQ>(x, ex, sign);
             uint32_t wd[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {

@@ -28,6 +28,7 @@
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "fixed_point.cuh"
+#include "fixed_point_md.cuh"
 #include "launch.cuh"
 #include "tcgen05.cuh"
 #include "wide_int.cuh"
@@ -40,8 +41,13 @@ constexpr int TD = DDGEMM_TC_DIGIT_BITS;    // 8 bits per part
 constexpr int TBM = DDGEMM_TC_BLOCK_M;      // 128 rows of A per block
 constexpr int TBN = DDGEMM_TC_TILE_N;       // 256 columns of B per block
 constexpr int TBK = DDGEMM_TC_CHUNK_K;      // 64 k per block (128-byte rows)
-constexpr int KSPLIT_MAX = DDGEMM_TC_MAX_K_SPLIT;  // 8192 k per slice-GEMM CTA
+constexpr int QS = DDGEMM_TC_QD_SLICES;     // 27 parts of a quad double
+constexpr int QFIX = QS * TD;               // 216 fraction bits
 static_assert(TS * TD == fxp::FIX_BITS, "13 parts of 8 bits cover the 104-bit fixed-point value");
+
+// Largest k per slice-GEMM CTA (a k-split) for NP parts: NP 2^14 per k-step
+// keeps the int32 totals of a split below 2^31.
+__host__ __device__ constexpr int ksplit_max(int np) { return np <= TS ? DDGEMM_TC_MAX_K_SPLIT : DDGEMM_TC_QD_MAX_K_SPLIT; }
 static_assert(TBK * 2 == 128, "one block row is one 128-byte swizzle row");
 
 constexpr int PAIR_M = DDGEMM_TC_TILE_M;    // 256 output rows per CTA pair
@@ -62,7 +68,8 @@ constexpr unsigned long long WAIT_NS = 2000000000ULL;  // bounded waits: 2 s
 constexpr int TILE_GROUP = 8;     // row blocks per group in the tile order (L2 reuse)
 
 static_assert(CHUNK_BLOCKS * TBK * 128 * 128 <= (1 << 23), "a chunk's f32 sums stay within 2^23");
-static_assert((long long)TS * KSPLIT_MAX * 128 * 128 < (1LL << 31), "int32 totals per k-split");
+static_assert((long long)TS * ksplit_max(TS) * 128 * 128 < (1LL << 31), "int32 totals per k-split");
+static_assert((long long)QS * ksplit_max(QS) * 128 * 128 < (1LL << 31), "int32 totals per k-split");
 
 __device__ unsigned int g_wait_timeouts_tc = 0;
 
@@ -248,6 +255,7 @@ __device__ __forceinline__ void note_timeout(volatile int* abort_flag) {
     atomicAdd(&g_wait_timeouts_tc, 1u);
 }
 
+template <int NP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     slice_gemm_tc_kernel(TcGemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
@@ -307,12 +315,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             // ---- producer (both CTAs): a stage holds up to two k-blocks of one pair ----
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
-            for (int d = 0; d < TS && !abort_flag; ++d) {
+            for (int d = 0; d < NP && !abort_flag; ++d) {
                 for (int s = 0; s <= d && !abort_flag; ++s) {
                     const int t = d - s;
-                    const uint16_t* a_src = g.planesA + ((a_block * TS + s) * g.KB + kb0) * (TBM * TBK);
+                    const uint16_t* a_src = g.planesA + ((a_block * NP + s) * g.KB + kb0) * (TBM * TBK);
                     const uint16_t* b_src =
-                        g.planesB + ((nt * TS + t) * g.KB + kb0) * (TBN * TBK) + rank * (TBN / 2) * TBK;
+                        g.planesB + ((nt * NP + t) * g.KB + kb0) * (TBN * TBK) + rank * (TBN / 2) * TBK;
                     for (int64_t kb = 0; kb < nkb; kb += STAGE_BLOCKS) {
                         const int nb = (int)min((int64_t)STAGE_BLOCKS, nkb - kb);
                         if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1, WAIT_NS)) {
@@ -351,7 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             const int nkb32 = (int)nkb;
             uint32_t stage = 0, phase = 0, chunk = 0, buf = 0;
             bool ok = true;
-            for (int d = 0; d < TS && ok; ++d) {
+            for (int d = 0; d < NP && ok; ++d) {
                 int left = (d + 1) * nkb32;  // k-blocks of this d still to issue
                 int in_chunk = 0;            // k-blocks issued into the current chunk
                 for (int s = 0; s <= d && ok; ++s) {
@@ -404,7 +412,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         } else if (lane == 0) {
             // ---- forwarder (odd CTA): its stage s is full -> tell the even CTA ----
             uint32_t stage = 0, phase = 0;
-            const int64_t total = (int64_t)(TS * (TS + 1) / 2) * ((nkb + STAGE_BLOCKS - 1) / STAGE_BLOCKS);
+            const int64_t total = (int64_t)(NP * (NP + 1) / 2) * ((nkb + STAGE_BLOCKS - 1) / STAGE_BLOCKS);
             for (int64_t j = 0; j < total; ++j) {
                 if (abort_flag || !mbar_wait_bounded(full0 + 8 * stage, phase, WAIT_NS)) {
                     if (!abort_flag) note_timeout(&abort_flag);
@@ -425,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
         int64_t chunk = 0;
         bool ok = true;
-        for (int d = 0; d < TS; ++d) {
+        for (int d = 0; d < NP; ++d) {
             int32_t acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
@@ -455,7 +463,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
             int32_t* dst =
-                g.P + (((z * TS + d) * g.Mp + mt * PAIR_M + rank * TBM + row) * g.Np + nt * TBN + half * 128);
+                g.P + (((z * NP + d) * g.Mp + mt * PAIR_M + rank * TBM + row) * g.Np + nt * TBN + half * 128);
 #pragma unroll
             for (int i = 0; i < 128; i += 4)
                 *reinterpret_cast<int4*>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
@@ -600,6 +608,131 @@ __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __rest
     }
 }
 
+// ---------------------------------------------------------------------------
+// Quad doubles: 27 parts of 8 bits.  X = trunc(x 2^(216 - e')) for x the sum
+// of the four doubles (|X| < 2^215, in 256-bit arithmetic), and its 27
+// balanced base-256 digits read off Y = X + 128 (256^25 + ... + 1) as for
+// double doubles; the same block layout with 27 parts; the exact sum of the
+// 27 part sums rounded once into four doubles.
+// ---------------------------------------------------------------------------
+
+struct TcQdSplitGrid {
+    const double* A[4]; int64_t lda, M; int32_t* e; int64_t a_tasks;
+    const double* B[4]; int64_t ldb, N; int32_t* f; int64_t b_tasks;
+    int64_t K, KB;
+    uint16_t* planesA; uint16_t* planesB;
+};
+
+// Y = X + C for the element (x0..x3) against e', as eight 32-bit words.
+__device__ __forceinline__ void qd_biased(const double (&x)[4], int ep, uint32_t (&y)[8]) {
+    uint64_t sign;
+    wide::U256 X = fxp::fixed_point_qd<QFIX>(x, ep, sign);
+    if (sign) X = wide::u256_neg(X);
+    wide::U256 C;  // 128 in each of the 26 low bytes
+    C.lo = ((wide::u128)0x8080808080808080ULL << 64) | 0x8080808080808080ULL;
+    C.hi = ((wide::u128)0x8080ULL << 64) | 0x8080808080808080ULL;
+    const wide::U256 Y = wide::u256_add(X, C);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        y[w] = (uint32_t)(Y.lo >> (32 * w));
+        y[4 + w] = (uint32_t)(Y.hi >> (32 * w));
+    }
+}
+
+// f32 bit pattern (upper half = bf16) of part s of a biased value.
+__device__ __forceinline__ uint32_t qd_part(const uint32_t (&y)[8], int s) {
+    if (s == 0) return __float_as_uint(__int2float_rn((int)(y[6] >> 16) | ((int)y[7] << 16)));  // Y >> 208, signed
+    const int b = QS - 1 - s;
+    const uint32_t bits = __byte_perm(y[b >> 2], 0x4B000000u, 0x7440u | (uint32_t)(b & 3));
+    return __float_as_uint(__fsub_rn(__uint_as_float(bits), 8388736.0f));
+}
+
+// One warp per task of 256 elements, as for double doubles: an A task is 4 rows
+// x 64 k (lane = row (lane/8), 8 consecutive k (lane%8)), a B task 32 columns
+// x 8 k (lane = column).  Each lane forms Y for its 8 elements, then writes one
+// 16-byte chunk of each of the 27 part rows.
+__global__ void __launch_bounds__(256) split_bf16_qd_kernel(TcQdSplitGrid g) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gridDim.x * 8;
+    const int64_t tasks = g.a_tasks + g.b_tasks;
+    for (int64_t task = gw; task < tasks; task += nw) {
+        const bool is_a = task < g.a_tasks;
+        int64_t r, kb;
+        int kc;
+        if (is_a) {
+            kb = task % g.KB;
+            r = (task / g.KB) * 4 + (lane >> 3);
+            kc = lane & 7;
+        } else {
+            const int64_t local = task - g.a_tasks;
+            const int64_t kq = local % (g.KB * 8);
+            kb = kq >> 3;
+            kc = (int)(kq & 7);
+            r = (local / (g.KB * 8)) * 32 + lane;
+        }
+        const int64_t rows = is_a ? g.M : g.N;
+        int ep = 1;
+        if (r < rows) {
+            int32_t* ex = is_a ? g.e : g.f;
+            const int32_t er = ex[r];
+            if (kb == 0 && kc == 0 && er == EXP_NONE) ex[r] = 0;
+            ep = effective_exponent(er) + 1;
+        }
+        const int64_t k0 = kb * TBK + kc * 8;
+        uint32_t y[8][8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            double x[4] = {0.0, 0.0, 0.0, 0.0};
+            if (r < rows && k0 + j < g.K) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    x[q] = is_a ? __ldg(g.A[q] + r * g.lda + k0 + j) : __ldg(g.B[q] + (k0 + j) * g.ldb + r);
+            }
+            qd_biased(x, ep, y[j]);
+        }
+        uint16_t* planes = is_a ? g.planesA : g.planesB;
+        const int brows = is_a ? TBM : TBN;
+        const int64_t blk = r / brows;
+        const int rin = (int)(r % brows);
+#pragma unroll
+        for (int s = 0; s < QS; ++s) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) w[j >> 1] = pack_bf16(qd_part(y[j], s), qd_part(y[j + 1], s));
+            uint8_t* base = reinterpret_cast<uint8_t*>(planes + ((blk * QS + s) * g.KB + kb) * ((int64_t)brows * TBK));
+            *reinterpret_cast<uint4*>(base + swizzled(rin, kc)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) recombine_tc_qd_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
+                                                              int64_t Np, const int32_t* __restrict__ e,
+                                                              const int32_t* __restrict__ f, int64_t M, int64_t N,
+                                                              double* C0, double* C1, double* C2, double* C3,
+                                                              int64_t ldc) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= N) return;
+    const int64_t plane = Mp * Np;
+    const int fj = effective_exponent(f[j]) + 1;
+    double* Cs[4] = {C0, C1, C2, C3};
+    for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
+        const int32_t* p = P + i * Np + j;
+        wide::U256 Z = wide::u256_zero();
+#pragma unroll
+        for (int d = 0; d < QS; ++d) {
+            long long v = 0;
+            for (int zz = 0; zz < splits; ++zz) v += __ldg(p + ((int64_t)zz * QS + d) * plane);
+            Z = wide::u256_add(Z, wide::u256_from_signed(v, TD * (QS - 1 - d)));
+        }
+        const int q = effective_exponent(e[i]) + 1 + fj - TD * (QS + 1);
+        double out[4];
+        wide::round_into_doubles<4>(Z, q, out);
+#pragma unroll
+        for (int pq = 0; pq < 4; ++pq) Cs[pq][i * ldc + j] = out[pq];
+    }
+}
+
 int num_sms_tc() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 152;
@@ -633,12 +766,14 @@ cudaError_t launch_split_bf16(const SplitOperand* A, const SplitOperand* B, int6
     return cudaGetLastError();
 }
 
-cudaError_t launch_slice_gemm_tc(const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
-                                 int64_t Kp, int splits, int32_t* P, cudaStream_t st) {
+template <int NP>
+static cudaError_t launch_slice_gemm_parts(const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
+                                           int64_t Kp, int splits, int32_t* P, cudaStream_t st) {
     if (Mp == 0 || Np == 0) return cudaSuccess;
     if (splits < 1 || Mp % PAIR_M != 0 || Np % TBN != 0 || Kp % TBK != 0) return cudaErrorInvalidValue;
-    if (((Kp / TBK + splits - 1) / splits) * TBK > KSPLIT_MAX) return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(slice_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    if (((Kp / TBK + splits - 1) / splits) * TBK > ksplit_max(NP)) return cudaErrorInvalidValue;
+    cudaError_t err =
+        cudaFuncSetAttribute(slice_gemm_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
     if (err != cudaSuccess) return err;
     TcGemmArgs g;
     g.planesA = planesA;
@@ -651,8 +786,18 @@ cudaError_t launch_slice_gemm_tc(const uint16_t* planesA, const uint16_t* planes
     g.MT = (int)(Mp / PAIR_M);
     g.NT = (int)(Np / TBN);
     dim3 grid((unsigned)(2 * (int64_t)g.MT * g.NT), (unsigned)splits);  // clusters of 2 along x
-    slice_gemm_tc_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(g);
+    slice_gemm_tc_kernel<NP><<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(g);
     return cudaGetLastError();
+}
+
+cudaError_t launch_slice_gemm_tc(const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
+                                 int64_t Kp, int splits, int32_t* P, cudaStream_t st) {
+    return launch_slice_gemm_parts<TS>(planesA, planesB, Mp, Np, Kp, splits, P, st);
+}
+
+cudaError_t launch_slice_gemm_tc_qd(const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
+                                    int64_t Kp, int splits, int32_t* P, cudaStream_t st) {
+    return launch_slice_gemm_parts<QS>(planesA, planesB, Mp, Np, Kp, splits, P, st);
 }
 
 cudaError_t launch_recombine_tc(const int32_t* P, int splits, int64_t Mp, int64_t Np, const int32_t* e,
@@ -662,6 +807,42 @@ cudaError_t launch_recombine_tc(const int32_t* P, int splits, int64_t Mp, int64_
     const unsigned gx = (unsigned)((N + 255) / 256);
     const unsigned gy = (unsigned)(M < 65535 ? M : 65535);
     recombine_tc_kernel<<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_bf16_qd(const double* const* A, int64_t lda, int64_t M, int32_t* e, const double* const* B,
+                                 int64_t ldb, int64_t N, int32_t* f, int64_t K, int64_t Kp, uint16_t* planesA,
+                                 uint16_t* planesB, cudaStream_t st) {
+    if (Kp == 0) return cudaSuccess;
+    TcQdSplitGrid g{};
+    g.K = K;
+    g.KB = Kp / TBK;
+    if (A && M > 0) {
+        for (int q = 0; q < 4; ++q) g.A[q] = A[q];
+        g.lda = lda; g.M = M; g.e = e;
+        g.a_tasks = (round_up(M, PAIR_M) / 4) * g.KB;
+    }
+    if (B && N > 0) {
+        for (int q = 0; q < 4; ++q) g.B[q] = B[q];
+        g.ldb = ldb; g.N = N; g.f = f;
+        g.b_tasks = (round_up(N, TBN) / 32) * g.KB * 8;
+    }
+    g.planesA = planesA;
+    g.planesB = planesB;
+    const int64_t tasks = g.a_tasks + g.b_tasks;
+    if (tasks == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms_tc() * 8));
+    split_bf16_qd_kernel<<<blocks, 256, 0, st>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_recombine_tc_qd(const int32_t* P, int splits, int64_t Mp, int64_t Np, const int32_t* e,
+                                   const int32_t* f, int64_t M, int64_t N, double* const* C, int64_t ldc,
+                                   cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    const unsigned gx = (unsigned)((N + 255) / 256);
+    const unsigned gy = (unsigned)(M < 65535 ? M : 65535);
+    recombine_tc_qd_kernel<<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C[0], C[1], C[2], C[3], ldc);
     return cudaGetLastError();
 }
 

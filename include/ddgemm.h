@@ -370,6 +370,8 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
 #define DDGEMM_TC_TILE_N 256        /* columns of B per part block / of C per output block */
 #define DDGEMM_TC_CHUNK_K 64        /* k per part block (one 128-byte row) */
 #define DDGEMM_TC_MAX_K_SPLIT 8192  /* k per slice-GEMM block: int32 part sums stay exact */
+#define DDGEMM_TC_QD_SLICES 27      /* parts per quad double (216 bits) */
+#define DDGEMM_TC_QD_MAX_K_SPLIT 4096 /* k per slice-GEMM block for quad doubles */
 
 /*
  * Padded extents (Mp = M rounded up to 256, Np = N rounded up to 256, Kp = K
@@ -411,6 +413,35 @@ ddgemm_status dd_slice_gemm_tc(int64_t M, int64_t N, int64_t K, const uint16_t* 
                                const uint16_t* planesB, int splits, int32_t* P, void* stream);
 ddgemm_status dd_recombine_tc(int64_t M, int64_t N, const int32_t* P, int splits, const int32_t* e,
                               const int32_t* f, double* C_hi, double* C_lo, int64_t ldc, void* stream);
+
+/*
+ * Quad doubles (four doubles per number, as for qd_gemm) with the parts on the
+ * bf16 tensor cores: the scheme of dd_gemm_tc with 27 balanced 8-bit parts
+ * (X = trunc(x 2^(216 - e')) for x the sum of the four doubles, e' = e + 1 with
+ * e from the leading doubles), the 378 pairs s + t <= 26 with tcgen05.mma on
+ * CTA pairs, and the exact sum of the 27 part sums rounded once into four
+ * non-overlapping doubles (c0 = RN(X), c1 = RN(X - c0), ...).  The paper
+ * applies its rewriting to general multiple doubles (Section 2, Tables 1-2);
+ * this is that rewriting with 8-bit parts.  Arguments as qd_gemm;
+ * K <= QDGEMM_MAX_K; a k-split covers at most DDGEMM_TC_QD_MAX_K_SPLIT of k.
+ * Steps: qd_split_bf16 (parts in the block layout of dd_split_bf16 with 27
+ * parts), qd_slice_gemm_tc (P: splits x 27 x Mp x Np int32), qd_recombine_tc.
+ */
+ddgemm_status qd_gemm_tc_layout(int64_t M, int64_t N, int64_t K,
+                                int64_t* Mp, int64_t* Np, int64_t* Kp, int* splits);
+ddgemm_status qd_gemm_tc_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+ddgemm_status qd_gemm_tc(int64_t M, int64_t N, int64_t K,
+                         const double* const* A, int64_t lda,
+                         const double* const* B, int64_t ldb,
+                         double* const* C, int64_t ldc,
+                         void* workspace, size_t workspace_bytes, void* stream);
+ddgemm_status qd_split_bf16(int64_t M, int64_t N, int64_t K,
+                            const double* const* A, int64_t lda, const double* const* B, int64_t ldb,
+                            uint16_t* planesA, int32_t* e, uint16_t* planesB, int32_t* f, void* stream);
+ddgemm_status qd_slice_gemm_tc(int64_t M, int64_t N, int64_t K, const uint16_t* planesA,
+                               const uint16_t* planesB, int splits, int32_t* P, void* stream);
+ddgemm_status qd_recombine_tc(int64_t M, int64_t N, const int32_t* P, int splits, const int32_t* e,
+                              const int32_t* f, double* const* C, int64_t ldc, void* stream);
 
 /* ------------------------------------------------------------------ */
 /* Diagnostics                                                          */

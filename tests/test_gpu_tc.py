@@ -32,17 +32,17 @@ def bf16_values(bits):
     return v.astype(np.int64)
 
 
-def unswizzle(planes, Rp, K, block_rows):
+def unswizzle(planes, Rp, K, block_rows, parts=sb.S):
     """Part blocks (block, s, kb) of block_rows x 64 in the 128-byte swizzled
     layout of include/ddgemm.h -> D[s, row, k] for Rp padded rows."""
     Kp = -(-K // 64) * 64
     KB = Kp // 64
-    a = bf16_values(planes).reshape(Rp // block_rows, sb.S, KB, block_rows, 8, 8)  # [blk][s][kb][r][pchunk][e]
+    a = bf16_values(planes).reshape(Rp // block_rows, parts, KB, block_rows, 8, 8)  # [blk][s][kb][r][pchunk][e]
     r = np.arange(block_rows)
     out = np.empty_like(a)
     for kc in range(8):
         out[:, :, :, r, kc, :] = a[:, :, :, r, kc ^ (r % 8), :]
-    return out.transpose(1, 0, 3, 2, 4, 5).reshape(sb.S, Rp, Kp)
+    return out.transpose(1, 0, 3, 2, 4, 5).reshape(parts, Rp, Kp)
 
 
 def pad(n, m):
