@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(256) split_bf16_qd_kernel(TcQdSplitGrid g) {
     }
 }
 
-__global__ void __launch_bounds__(256) recombine_tc_qd_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
+__global__ void __launch_bounds__(256, 2) recombine_tc_qd_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
                                                               int64_t Np, const int32_t* __restrict__ e,
                                                               const int32_t* __restrict__ f, int64_t M, int64_t N,
                                                               double* C0, double* C1, double* C2, double* C3,
@@ -718,13 +718,17 @@ __global__ void __launch_bounds__(256) recombine_tc_qd_kernel(const int32_t* __r
     double* Cs[4] = {C0, C1, C2, C3};
     for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
         const int32_t* p = P + i * Np + j;
+        // all loads of a split are issued before any is used
+        long long v[QS];
+#pragma unroll
+        for (int d = 0; d < QS; ++d) v[d] = __ldg(p + (int64_t)d * plane);
+        for (int zz = 1; zz < splits; ++zz) {
+#pragma unroll
+            for (int d = 0; d < QS; ++d) v[d] += __ldg(p + ((int64_t)zz * QS + d) * plane);
+        }
         wide::U256 Z = wide::u256_zero();
 #pragma unroll
-        for (int d = 0; d < QS; ++d) {
-            long long v = 0;
-            for (int zz = 0; zz < splits; ++zz) v += __ldg(p + ((int64_t)zz * QS + d) * plane);
-            Z = wide::u256_add(Z, wide::u256_from_signed(v, TD * (QS - 1 - d)));
-        }
+        for (int d = 0; d < QS; ++d) Z = wide::u256_add(Z, wide::u256_from_signed(v[d], TD * (QS - 1 - d)));
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (QS + 1);
         double out[4];
         wide::round_into_doubles<4>(Z, q, out);
