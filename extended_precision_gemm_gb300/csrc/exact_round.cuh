@@ -1,0 +1,200 @@
+// exact_round.cuh -- the exact sum of part sums on a base-256 grid and its
+// rounding into non-overlapping doubles, with 64-bit limbs (the fast path of
+// the bf16 variants' recombination).
+//
+//   Z = sum_{d=0}^{NP-1} v_d 256^(NP-1-d),   |v_d| < 2^46,
+//
+// is formed exactly in W 64-bit limbs (two's complement, least significant
+// first) by Horner's rule over groups of three parts (a group
+// v_a 2^16 + v_b 2^8 + v_c stays below 2^63), and Z 2^q is rounded into NOUT
+// doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0), ... (ties to even).  The
+// fast path needs every part to be a normal double: q >= -1022 (a nonzero
+// remainder is at least 2^q) and the result below 2^1023; the caller checks
+// fast_path_ok() and otherwise uses the general 256-bit routine.
+#pragma once
+
+#include <cstdint>
+
+#include "wide_int.cuh"
+
+namespace ddg {
+namespace xr {
+
+// Z = Z 2^SH + h for 0 < SH < 64 and a signed h (|h| < 2^63).
+template <int W, int SH>
+__device__ __forceinline__ void horner(uint64_t (&z)[W], long long h) {
+#pragma unroll
+    for (int i = W - 1; i > 0; --i) z[i] = (z[i] << SH) | (z[i - 1] >> (64 - SH));
+    z[0] <<= SH;
+    const uint64_t s = (uint64_t)(h >> 63);  // sign extension of h
+    const uint64_t t0 = z[0] + (uint64_t)h;
+    uint64_t c = t0 < z[0];
+    z[0] = t0;
+#pragma unroll
+    for (int i = 1; i < W; ++i) {
+        const uint64_t u = z[i] + s;
+        const uint64_t c1 = u < z[i];
+        const uint64_t u2 = u + c;
+        c = c1 | (u2 < u);
+        z[i] = u2;
+    }
+}
+
+// v_a 256^(n-1) + ... + v_(a+n-1) for a group of n <= 3 parts.
+template <int N>
+__device__ __forceinline__ long long group(const long long* v) {
+    long long g = v[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i) g = g * 256 + v[i];
+    return g;
+}
+
+// Z as W limbs from the NP part sums.
+template <int NP, int W>
+__device__ __forceinline__ void exact_sum(const long long (&v)[NP], uint64_t (&z)[W]) {
+    constexpr int G = NP / 3, R = NP % 3;
+    const long long h0 = group<3>(&v[0]);
+    z[0] = (uint64_t)h0;
+#pragma unroll
+    for (int i = 1; i < W; ++i) z[i] = (uint64_t)(h0 >> 63);
+#pragma unroll
+    for (int g = 1; g < G; ++g) horner<W, 24>(z, group<3>(&v[3 * g]));
+    if (R == 1) horner<W, 8>(z, v[NP - 1]);
+    if (R == 2) horner<W, 16>(z, group<2>(&v[NP - 2]));
+}
+
+template <int W>
+__device__ __forceinline__ bool is_zero(const uint64_t (&m)[W]) {
+    uint64_t o = 0;
+#pragma unroll
+    for (int i = 0; i < W; ++i) o |= m[i];
+    return o == 0;
+}
+
+// Index of the leading 1 of a nonzero magnitude.
+template <int W>
+__device__ __forceinline__ int msb(const uint64_t (&m)[W]) {
+    int t = -1;
+#pragma unroll
+    for (int i = 0; i < W; ++i)
+        if (m[i] != 0) t = 64 * i + 63 - __clzll((long long)m[i]);
+    return t;
+}
+
+template <int W>
+__device__ __forceinline__ void negate(uint64_t (&m)[W]) {
+    uint64_t c = 1;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        const uint64_t u = ~m[i] + c;
+        c = c && (u == 0);
+        m[i] = u;
+    }
+}
+
+// Bits [b, b + 64) of m (b >= 0).
+template <int W>
+__device__ __forceinline__ uint64_t window(const uint64_t (&m)[W], int b) {
+    const int i = b >> 6, o = b & 63;
+    uint64_t lo = 0, hi = 0;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        if (j == i) lo = m[j];
+        if (j == i + 1) hi = m[j];
+    }
+    return o == 0 ? lo : (lo >> o) | (hi << (64 - o));
+}
+
+// Are any bits of m below position b set (b >= 0)?
+template <int W>
+__device__ __forceinline__ bool any_below(const uint64_t (&m)[W], int b) {
+    uint64_t o = 0;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        const int lo = 64 * j;
+        if (lo + 64 <= b) o |= m[j];
+        else if (lo < b) o |= m[j] & ((1ULL << (b - lo)) - 1);
+    }
+    return o != 0;
+}
+
+// Keep only the bits of m below position p (p >= 0).
+template <int W>
+__device__ __forceinline__ void keep_below(uint64_t (&m)[W], int p) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        const int lo = 64 * j;
+        if (lo >= p) m[j] = 0;
+        else if (lo + 64 > p) m[j] &= (1ULL << (p - lo)) - 1;
+    }
+}
+
+// m = 2^p - m for 0 <= m < 2^p (p < 64 W).
+template <int W>
+__device__ __forceinline__ void complement_to(uint64_t (&m)[W], int p) {
+    negate(m);
+    uint64_t c = 0;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        const uint64_t add = (j == (p >> 6)) ? (1ULL << (p & 63)) : 0;
+        const uint64_t u = m[j] + add;
+        const uint64_t c1 = u < m[j];
+        const uint64_t u2 = u + c;
+        c = c1 | (u2 < u);
+        m[j] = u2;
+    }
+}
+
+// The fast path applies: every part of Z 2^q is a normal double or zero.
+template <int W>
+__device__ __forceinline__ bool fast_path_ok(const uint64_t (&z)[W], int q) {
+    if (q < -1022) return false;
+    uint64_t m[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) m[i] = z[i];
+    if ((int64_t)m[W - 1] < 0) negate(m);
+    return is_zero(m) || msb(m) + q <= 1022;
+}
+
+// Z 2^q rounded into NOUT doubles (fast path only; +0 for zeros).
+template <int W, int NOUT>
+__device__ __forceinline__ void round_parts(const uint64_t (&z)[W], int q, double (&out)[NOUT]) {
+    uint64_t m[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) m[i] = z[i];
+    uint64_t sign = (uint64_t)m[W - 1] >> 63;
+    if (sign) negate(m);
+#pragma unroll
+    for (int p = 0; p < NOUT; ++p) {
+        if (is_zero(m)) {
+            out[p] = 0.0;
+            continue;
+        }
+        const int t = msb(m);
+        int pos = t - 52;  // exponent (relative to q) of the last kept bit
+        uint64_t keep;
+        bool up = false;
+        if (pos <= 0) {
+            keep = m[0];  // the whole value (< 2^53)
+            pos = 0;
+#pragma unroll
+            for (int i = 0; i < W; ++i) m[i] = 0;
+        } else {
+            const uint64_t x = window(m, pos - 1);  // round bit, then the 53 kept bits
+            keep = x >> 1;
+            const bool rbit = x & 1;
+            up = rbit && ((keep & 1) || any_below(m, pos - 1));
+            keep_below(m, pos);  // the tail below the kept bits
+            if (up) {
+                complement_to(m, pos);  // |tail - 2^pos|
+                keep += 1;
+                if (keep >> 53) { keep >>= 1; pos += 1; }
+            }
+        }
+        out[p] = wide::make_double(keep, pos + q, sign);
+        if (up) sign ^= 1;  // the remainder has the opposite sign
+    }
+}
+
+}  // namespace xr
+}  // namespace ddg

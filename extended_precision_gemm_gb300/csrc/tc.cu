@@ -32,6 +32,7 @@
 #include "launch.cuh"
 #include "tcgen05.cuh"
 #include "wide_int.cuh"
+#include "exact_round.cuh"
 
 namespace ddg {
 namespace {
@@ -484,104 +485,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 // Step 3: exact sum of the parts and one rounding into a double double.
 // ---------------------------------------------------------------------------
 
-typedef unsigned __int128 u128;
-
-__device__ __forceinline__ int msb128(u128 x) {  // x != 0
-    const uint64_t h = (uint64_t)(x >> 64);
-    return h ? 127 - __clzll((long long)h) : 63 - __clzll((long long)(uint64_t)x);
-}
-
-// Round a nonzero magnitude M = mh 2^64 + ml (M < 2^192, mh = M >> 64) to 53
-// bits, ties to even: M = keep 2^r + rem exactly, keep <= 2^53 (2^53 only as
-// 2^52 2^(r+1) after renormalising), |rem| <= 2^(r-1), rem signed.
-__device__ __forceinline__ void round53(u128 mh, uint64_t ml, uint64_t& keep, int& r, __int128& rem) {
-    const int t = mh ? 64 + msb128(mh) : 63 - __clzll((long long)ml);
-    r = t - 52;
-    if (r <= 0) {  // M < 2^53: exact
-        keep = ml;
-        r = 0;
-        rem = 0;
-        return;
-    }
-    // keep = M >> r (53 bits), low = M mod 2^r (r <= 139 - 52 = 87 bits)
-    u128 low;
-    if (r >= 64) {
-        keep = (uint64_t)(mh >> (r - 64));
-        low = ((mh & ((((u128)1) << (r - 64)) - 1)) << 64) | ml;
-    } else {
-        keep = (uint64_t)((mh << (64 - r)) | (u128)(ml >> r));
-        low = ml & ((1ULL << r) - 1);
-    }
-    const u128 half = ((u128)1) << (r - 1);
-    if (low > half || (low == half && (keep & 1))) {
-        keep += 1;
-        rem = (__int128)low - (__int128)(((u128)1) << r);
-    } else {
-        rem = (__int128)low;
-    }
-    if (keep >> 53) { keep >>= 1; r += 1; }  // 2^53 = 2^52 * 2: exact
-}
-
-// Step 3 for one output: Z = sum_d v_d 256^(12 - d) exactly, then the nearest
-// double double of Z 2^q.  Z is formed from two Horner sums that fit 128 bits
-// (|Z_l| < 2^91 for d = 6..12, |Z_h| < 2^83 for d = 0..5) as Z = Z_h 2^56 + Z_l
-// in three 64-bit words.  When q >= -1022 and the result stays below 2^1023
-// (every nonzero part is then a normal double) the rounding uses 128-bit
-// integer steps; otherwise the general 256-bit routine.
-__device__ __forceinline__ void recombine_one(const long long (&v)[TS], int q, double& c_hi, double& c_lo) {
-    u128 zl = 0, zh = 0;
-#pragma unroll
-    for (int d = 6; d < TS; ++d) zl = (zl << TD) + (u128)(__int128)v[d];
-#pragma unroll
-    for (int d = 0; d < 6; ++d) zh = (zh << TD) + (u128)(__int128)v[d];
-    // 192-bit two's complement Z = (w2, w1, w0)
-    const uint64_t l0 = (uint64_t)zl, l1 = (uint64_t)(zl >> 64);
-    const int64_t l2 = (int64_t)l1 >> 63;
-    const uint64_t h0 = (uint64_t)zh << 56, h1 = (uint64_t)(zh >> 8);
-    const int64_t h2 = (int64_t)((__int128)zh >> 72);
-    const uint64_t w0 = l0 + h0;
-    const uint64_t c0 = w0 < l0;
-    const uint64_t t1 = l1 + h1;
-    const uint64_t c1 = (t1 < l1) + ((t1 + c0) < t1);
-    const uint64_t w1 = t1 + c0;
-    const int64_t w2 = l2 + h2 + (int64_t)c1;
-    if (w0 == 0 && w1 == 0 && w2 == 0) { c_hi = 0.0; c_lo = 0.0; return; }
-    const uint64_t sign = w2 < 0 ? 1ULL : 0ULL;
-    uint64_t m0 = w0, m1 = w1, m2 = (uint64_t)w2;
-    if (sign) {  // magnitude of the 192-bit value
-        m0 = ~m0 + 1;
-        const uint64_t k0 = (m0 == 0);
-        m1 = ~m1 + k0;
-        const uint64_t k1 = k0 && (m1 == 0);
-        m2 = ~m2 + k1;
-    }
-    const u128 mh = ((u128)m2 << 64) | m1;
-    const int t = mh ? 64 + msb128(mh) : 63 - __clzll((long long)m0);
-    if (q >= -1022 && t + q <= 1022) {
-        uint64_t keep;
-        int r;
-        __int128 rem;
-        round53(mh, m0, keep, r, rem);
-        c_hi = wide::make_double(keep, r + q, sign);
-        if (rem == 0) { c_lo = 0.0; return; }
-        const uint64_t sl = sign ^ (rem < 0 ? 1ULL : 0ULL);
-        const u128 rm = rem < 0 ? (u128)(-rem) : (u128)rem;
-        uint64_t keep2;
-        int r2;
-        __int128 rem2;
-        round53(rm >> 64, (uint64_t)rm, keep2, r2, rem2);
-        c_lo = wide::make_double(keep2, r2 + q, sl);
-        return;
-    }
-    wide::U256 Z;
-    Z.lo = ((u128)w1 << 64) | w0;
-    Z.hi = (u128)(__int128)w2;
-    double out[2];
-    wide::round_into_doubles<2>(Z, q, out);
-    c_hi = out[0];
-    c_lo = out[1];
-}
-
 __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
                                                            int64_t Np, const int32_t* __restrict__ e,
                                                            const int32_t* __restrict__ f, int64_t M, int64_t N,
@@ -601,10 +504,19 @@ __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __rest
             for (int d = 0; d < TS; ++d) v[d] += __ldg(p + ((int64_t)zz * TS + d) * plane);
         }
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (TS + 1);
-        double hi, lo;
-        recombine_one(v, q, hi, lo);
-        C_hi[i * ldc + j] = hi;
-        C_lo[i * ldc + j] = lo;
+        uint64_t z[3];
+        xr::exact_sum<TS, 3>(v, z);
+        double out[2];
+        if (xr::fast_path_ok(z, q)) {
+            xr::round_parts<3, 2>(z, q, out);
+        } else {
+            wide::U256 Z;
+            Z.lo = ((wide::u128)z[1] << 64) | z[0];
+            Z.hi = (wide::u128)(__int128)(int64_t)z[2];
+            wide::round_into_doubles<2>(Z, q, out);
+        }
+        C_hi[i * ldc + j] = out[0];
+        C_lo[i * ldc + j] = out[1];
     }
 }
 
@@ -726,12 +638,18 @@ __global__ void __launch_bounds__(256, 2) recombine_tc_qd_kernel(const int32_t* 
 #pragma unroll
             for (int d = 0; d < QS; ++d) v[d] += __ldg(p + ((int64_t)zz * QS + d) * plane);
         }
-        wide::U256 Z = wide::u256_zero();
-#pragma unroll
-        for (int d = 0; d < QS; ++d) Z = wide::u256_add(Z, wide::u256_from_signed(v[d], TD * (QS - 1 - d)));
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (QS + 1);
+        uint64_t z[4];
+        xr::exact_sum<QS, 4>(v, z);
         double out[4];
-        wide::round_into_doubles<4>(Z, q, out);
+        if (xr::fast_path_ok(z, q)) {
+            xr::round_parts<4, 4>(z, q, out);
+        } else {
+            wide::U256 Z;
+            Z.lo = ((wide::u128)z[1] << 64) | z[0];
+            Z.hi = ((wide::u128)z[3] << 64) | z[2];
+            wide::round_into_doubles<4>(Z, q, out);
+        }
 #pragma unroll
         for (int pq = 0; pq < 4; ++pq) Cs[pq][i * ldc + j] = out[pq];
     }
