@@ -88,3 +88,43 @@ def test_k_split_exchange_is_exact():
         assert np.array_equal(got["P"], P)
         assert np.array_equal(got["C_hi"].view(np.int64), C_hi.view(np.int64))
         assert np.array_equal(got["C_lo"].view(np.int64), C_lo.view(np.int64))
+
+
+def _ksplit_bf16_worker(rank, world, port, out):
+    import workloads
+    from oracle import slices_bf16 as sb
+    _init(rank, world, port)
+    try:
+        A_hi, A_lo, B_hi, B_lo = workloads.make_dd(8, 10, 90, "uniform_exp20", 22)
+        K = A_hi.shape[1]
+        k0, k1 = rank * K // world, (rank + 1) * K // world
+        a_hi, a_lo, b_hi, b_lo = A_hi[:, k0:k1], A_lo[:, k0:k1], B_hi[k0:k1], B_lo[k0:k1]
+        e = torch.from_numpy(sb.row_exponents(a_hi))
+        f = torch.from_numpy(sb.col_exponents(b_hi))
+        dist.all_reduce(e, op=dist.ReduceOp.MAX)
+        dist.all_reduce(f, op=dist.ReduceOp.MAX)
+        P = torch.from_numpy(sb.slice_products(sb.split_rows(a_hi, a_lo, e.numpy()),
+                                               sb.split_cols(b_hi, b_lo, f.numpy())))
+        dist.all_reduce(P, op=dist.ReduceOp.SUM)  # int64 part sums: exact in any order
+        C_hi, C_lo = sb.recombine(P.numpy(), e.numpy(), f.numpy())
+        if rank == 0:
+            np.savez(out, P=P.numpy(), C_hi=C_hi, C_lo=C_lo)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_k_split_exchange_is_exact_for_bf16_parts():
+    """The same exchange for the 8-bit-part variant: integer part sums of the
+    k-slabs add up to the unsplit ones, so C is the single-rank model's."""
+    import workloads
+    from oracle import slices_bf16 as sb
+    port = _free_port()
+    with tempfile.TemporaryDirectory() as d:
+        out = os.path.join(d, "ks8.npz")
+        mp.spawn(_ksplit_bf16_worker, args=(2, port, out), nprocs=2, join=True)
+        got = np.load(out)
+        A_hi, A_lo, B_hi, B_lo = workloads.make_dd(8, 10, 90, "uniform_exp20", 22)
+        C_hi, C_lo, e, f, DA, DB, P = sb.sliced_dd_gemm(A_hi, A_lo, B_hi, B_lo)
+        assert np.array_equal(got["P"], P)
+        assert np.array_equal(got["C_hi"].view(np.int64), C_hi.view(np.int64))
+        assert np.array_equal(got["C_lo"].view(np.int64), C_lo.view(np.int64))
