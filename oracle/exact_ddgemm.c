@@ -277,7 +277,8 @@ int oracle_dd_gemm_block(int64_t M, int64_t N, int64_t K,
 }
 
 /*
- * Multiple doubles with `np` parts (2: double double, 4: quad double): the
+ * Multiple doubles with `np` parts (2: double double, 4: quad double, 8: octo
+ * double, 16: hexa double -- the sizes of the paper's Table 2): the
  * exact value X_ij = sum_k (sum_p A_p[i,k]) (sum_q B_q[k,j]) rounded once to
  * np non-overlapping doubles, x_0 = RN(X), x_1 = RN(X - x_0), ...,
  * x_{np-1} = RN(X - x_0 - ... - x_{np-2}) ("Multiple Double Arithmetic on
@@ -286,7 +287,7 @@ int oracle_dd_gemm_block(int64_t M, int64_t N, int64_t K,
  * (row-major, leading dimensions lda / ldb); out[p] receives part p of the
  * nrows x ncols block.  Return codes as oracle_dd_gemm_block.
  */
-#define MAX_PARTS 8
+#define MAX_PARTS 16  /* every product of two parts stays inside the accumulator's range */
 
 static void entry_md(const dec_t* arow, const dec_t* bcol, int64_t K, int np, acc_t* acc,
                      double* const* out, int64_t t) {

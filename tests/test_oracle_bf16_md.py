@@ -146,3 +146,68 @@ def _recombine_three_parts(P, e, f, nout):
 def test_planted_mistakes_are_caught(check, bad):
     with pytest.raises(AssertionError):
         check(bad)
+
+
+# ---- octo doubles (8 doubles, 54 parts) and hexa doubles (16 doubles, 107 parts) ----
+
+OD_HD = [(8, 54, -404), (16, 107, -828)]  # doubles, parts, log2 of the normwise gate
+
+
+def log2_normwise(C, R, A, B):
+    """log2 of the normwise error, formed from exact rational differences (the
+    errors of hexa doubles are far below the double range of their squares)."""
+    import math
+    tot = Fraction(0)
+    for i in range(C[0].shape[0]):
+        for j in range(C[0].shape[1]):
+            d = sum(Fraction(float(C[p][i, j])) - Fraction(float(R[p][i, j])) for p in range(len(C)))
+            tot += d * d
+    if tot == 0:
+        return -math.inf
+    den = np.linalg.norm(sum(A)) * np.linalg.norm(sum(B))
+    return (math.log2(tot.numerator) - math.log2(tot.denominator)) / 2 - math.log2(den)
+
+
+@pytest.mark.parametrize("n,S_,gate", OD_HD)
+def test_od_hd_parts_reconstruct(n, S_, gate):
+    A, _ = workloads.make_md(2, 1, 12, "uniform_exp20", 8 + n, n)
+    e = bm.row_exponents(A[0])
+    for i in range(2):
+        for k in range(12):
+            parts = [float(a[i, k]) for a in A]
+            D = bm.digits_of(parts, int(e[i]), S_)
+            v = sum(Fraction(x) for x in parts) * pow2(-int(e[i]))
+            r = v - sum(Fraction(d) * pow2(-8 * (s + 1)) for s, d in enumerate(D))
+            assert abs(r) < pow2(-8 * S_) and (r == 0 or (r > 0) == (v > 0))
+            assert -128 <= D[0] <= 128 and all(-128 <= d <= 127 for d in D[1:])
+
+
+@pytest.mark.parametrize("n,S_,gate", OD_HD)
+@pytest.mark.parametrize("dist", workloads.DISTS)
+def test_od_hd_chain_vs_exact(n, S_, gate, dist):
+    A, B = workloads.make_md(4, 3, 15, dist, 17, n)
+    C, *_ = bm.sliced_gemm(A, B, S_)
+    R = oracle.exact_md_gemm(A, B)
+    assert log2_normwise(C, R, A, B) <= gate
+
+
+@pytest.mark.parametrize("n,S_,gate", OD_HD)
+def test_od_hd_chain_exact_on_short_integers(n, S_, gate):
+    rng = np.random.default_rng(15)
+    A0 = rng.integers(-2**20, 2**20, (3, 5)).astype(np.float64)
+    B0 = rng.integers(-2**20, 2**20, (5, 2)).astype(np.float64)
+    C, *_ = bm.sliced_gemm([A0] + [np.zeros_like(A0)] * (n - 1), [B0] + [np.zeros_like(B0)] * (n - 1), S_)
+    assert np.array_equal(C[0], A0 @ B0) and not any(c.any() for c in C[1:])
+
+
+@pytest.mark.parametrize("n", [8, 16])
+def test_md_oracle_bruteforce_many_parts(n):
+    A, B = workloads.make_md(2, 2, 3, ["uniform", "normal"][n // 16], 40 + n, n)
+    C = oracle.exact_md_gemm(A, B)
+    for i in range(2):
+        for j in range(2):
+            X = sum(sum(Fraction(float(a[i, k])) for a in A) * sum(Fraction(float(b[k, j])) for b in B)
+                    for k in range(3))
+            ref = _exact_parts(X, n)
+            for p in range(n):
+                assert bits(C[p][i, j]) == bits(ref[p]), (i, j, p)
