@@ -33,6 +33,8 @@ __all__ = [
     "dd_gemm_tc", "tc_layout", "tc_workspace_size", "split_bf16", "slice_gemm_tc", "recombine_tc",
     "TC_QD_SLICES", "TC_QD_MAX_K_SPLIT", "qd_gemm_tc", "qd_tc_layout", "qd_tc_workspace_size", "qd_split_bf16",
     "qd_slice_gemm_tc", "qd_recombine_tc",
+    "MD_TC_PARTS", "md_gemm_tc", "md_tc_layout", "md_tc_workspace_size", "md_split_bf16", "md_slice_gemm_tc",
+    "md_recombine_tc",
 ]
 
 SLICES = 8
@@ -99,6 +101,12 @@ _SIGNATURES = {
     "qd_split_bf16": ([_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
     "qd_slice_gemm_tc": ([_i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
     "qd_recombine_tc": ([_i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _i64, _ptr], _int),
+    "md_gemm_tc_layout": ([_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr], _int),
+    "md_gemm_tc_workspace_size": ([_int, _i64, _i64, _i64, _ptr], _int),
+    "md_gemm_tc": ([_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, ctypes.c_size_t, _ptr], _int),
+    "md_split_bf16": ([_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
+    "md_slice_gemm_tc": ([_int, _i64, _i64, _i64, _ptr, _ptr, _int, _ptr, _ptr], _int),
+    "md_recombine_tc": ([_int, _i64, _i64, _ptr, _int, _ptr, _ptr, _ptr, _i64, _ptr], _int),
 }
 
 
@@ -721,5 +729,97 @@ def qd_recombine_tc(M: int, N: int, P, e, f, splits=None, C=None, stream=None):
     C = _qd_planes(C, "C")
     pc = _ptr_array(C)
     _check("qd_recombine_tc", load().qd_recombine_tc(M, N, P.data_ptr(), splits, e.data_ptr(), f.data_ptr(),
+                                                     _vp(pc), _ld(C[0]), _stream_handle(stream)))
+    return C
+
+
+# ---- octo (8) and hexa (16) doubles with bf16 parts on the tensor cores ----
+
+MD_TC_PARTS = {8: 54, 16: 107}
+
+
+def _md_planes(X, name, n):
+    if len(X) != n:
+        raise ValueError(f"{name} must be a list of {n} planes")
+    for t_ in X:
+        _mat(t_, name)
+    if any(t_.shape != X[0].shape or t_.stride() != X[0].stride() for t_ in X):
+        raise ValueError(f"the planes of {name} must share shape and strides")
+    return X
+
+
+def md_tc_layout(nparts: int, M: int, N: int, K: int):
+    Mp, Np, Kp, sp = _i64(), _i64(), _i64(), _int()
+    _check("md_gemm_tc_layout", load().md_gemm_tc_layout(nparts, M, N, K, ctypes.byref(Mp), ctypes.byref(Np),
+                                                         ctypes.byref(Kp), ctypes.byref(sp)))
+    return Mp.value, Np.value, Kp.value, sp.value
+
+
+def md_tc_workspace_size(nparts: int, M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check("md_gemm_tc_workspace_size", load().md_gemm_tc_workspace_size(nparts, M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def md_gemm_tc(A, B, C=None, workspace=None, stream=None):
+    """C = A @ B for octo or hexa doubles (lists of 8 or 16 planes) with 54 / 107
+    bf16 parts on the tensor cores; exact sums rounded once."""
+    torch = _torch()
+    n = len(A)
+    A, B = _md_planes(A, "A", n), _md_planes(B, "B", n)
+    M, K = A[0].shape
+    K2, N = B[0].shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    if C is None:
+        C = [torch.empty((M, N), dtype=torch.float64, device=A[0].device) for _ in range(n)]
+    C = _md_planes(C, "C", n)
+    pa, pb, pc = _ptr_array(A), _ptr_array(B), _ptr_array(C)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("md_gemm_tc", load().md_gemm_tc(n, M, N, K, _vp(pa), _ld(A[0]), _vp(pb), _ld(B[0]), _vp(pc), _ld(C[0]),
+                                           wp, wn, _stream_handle(stream)))
+    return C
+
+
+def md_split_bf16(A, B, stream=None):
+    """Step 1 for octo / hexa doubles: (planesA, e, planesB, f)."""
+    torch = _torch()
+    n = len(A)
+    A, B = _md_planes(A, "A", n), _md_planes(B, "B", n)
+    parts = MD_TC_PARTS.get(n, 0)
+    M, K = A[0].shape
+    N = B[0].shape[1]
+    Mp, Np, Kp = -(-M // TC_TILE_M) * TC_TILE_M, -(-N // TC_TILE_N) * TC_TILE_N, -(-K // TC_CHUNK_K) * TC_CHUNK_K
+    dev = A[0].device
+    pA = torch.empty(max(parts, 1) * Mp * Kp, dtype=torch.int16, device=dev)
+    pB = torch.empty(max(parts, 1) * Np * Kp, dtype=torch.int16, device=dev)
+    e = torch.empty(M, dtype=torch.int32, device=dev)
+    f = torch.empty(N, dtype=torch.int32, device=dev)
+    pa, pb = _ptr_array(A), _ptr_array(B)
+    _check("md_split_bf16", load().md_split_bf16(n, M, N, K, _vp(pa), _ld(A[0]), _vp(pb), _ld(B[0]), pA.data_ptr(),
+                                                 e.data_ptr(), pB.data_ptr(), f.data_ptr(), _stream_handle(stream)))
+    return pA, e, pB, f
+
+
+def md_slice_gemm_tc(nparts: int, M: int, N: int, K: int, planesA, planesB, splits: int, P=None, stream=None):
+    torch = _torch()
+    parts = MD_TC_PARTS[nparts]
+    Mp, Np = -(-M // TC_TILE_M) * TC_TILE_M, -(-N // TC_TILE_N) * TC_TILE_N
+    if P is None:
+        P = torch.empty((splits, parts, Mp, Np), dtype=torch.int32, device=planesA.device)
+    _check("md_slice_gemm_tc", load().md_slice_gemm_tc(nparts, M, N, K, planesA.data_ptr(), planesB.data_ptr(),
+                                                       splits, P.data_ptr(), _stream_handle(stream)))
+    return P
+
+
+def md_recombine_tc(nparts: int, M: int, N: int, P, e, f, splits=None, C=None, stream=None):
+    torch = _torch()
+    splits = P.shape[0] if splits is None else splits
+    if C is None:
+        C = [torch.empty((M, N), dtype=torch.float64, device=P.device) for _ in range(nparts)]
+    C = _md_planes(C, "C", nparts)
+    pc = _ptr_array(C)
+    _check("md_recombine_tc", load().md_recombine_tc(nparts, M, N, P.data_ptr(), splits, e.data_ptr(), f.data_ptr(),
                                                      _vp(pc), _ld(C[0]), _stream_handle(stream)))
     return C

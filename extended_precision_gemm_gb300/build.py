@@ -20,7 +20,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = BUILD / "libddgemm.so"
-SOURCES = ["split.cu", "slice_gemm.cu", "slice_gemm_i64.cu", "recombine.cu", "simt.cu", "md.cu", "tc.cu", "api.cu"]
+SOURCES = ["split.cu", "slice_gemm.cu", "slice_gemm_i64.cu", "recombine.cu", "simt.cu", "md.cu", "tc.cu", "tc_md.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",

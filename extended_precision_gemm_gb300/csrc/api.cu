@@ -403,8 +403,10 @@ ddgemm_status dd_wait_timeouts(unsigned int* count) {
     ddgemm_status s = from_cuda(read_and_reset_wait_timeouts(&a));
     if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_i64(&b));
     if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_qd(&c));
+    unsigned int m = 0;
     if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_tc(&d));
-    *count = a + b + c + d;
+    if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_tc_md(&m));
+    *count = a + b + c + d + m;
     return s;
 }
 
@@ -674,14 +676,21 @@ int choose_tc_splits(int64_t Mp, int64_t Np, int64_t Kp, int64_t max_k_split) {
     return (int)best;
 }
 
-// parts = 13 (double doubles) or 27 (quad doubles).
+// Largest k of one k-split for `parts` parts: the largest power of two with
+// parts K 2^14 < 2^31 (int32 part sums stay exact).
+int64_t tc_max_k_split(int parts) {
+    int64_t k = 1 << 20;
+    while ((int64_t)parts * k * 128 * 128 >= (1LL << 31)) k >>= 1;
+    return k;
+}
+
+// parts = 13 (double doubles), 27 (quad), 54 (octo) or 107 (hexa doubles).
 TcLayout make_tc_layout(int64_t M, int64_t N, int64_t K, int parts = kTcParts) {
     TcLayout L;
     L.Mp = round_up(M, kTcM);
     L.Np = round_up(N, kTcN);
     L.Kp = round_up(K, kTcK);
-    L.splits = choose_tc_splits(L.Mp, L.Np, L.Kp,
-                                parts == kTcParts ? DDGEMM_TC_MAX_K_SPLIT : DDGEMM_TC_QD_MAX_K_SPLIT);
+    L.splits = choose_tc_splits(L.Mp, L.Np, L.Kp, tc_max_k_split(parts));
     int64_t off = 0;
     auto take = [&](int64_t bytes) { int64_t o = off; off = round_up(off + bytes, kAlign); return o; };
     L.off_e = take(L.Mp * 4);
@@ -962,6 +971,158 @@ ddgemm_status qd_recombine_tc(int64_t M, int64_t N, const int32_t* P, int splits
         if (C[p] == nullptr) return DDGEMM_ERR_INVALID_ARG;
     const int64_t Mp = round_up(M, kTcM), Np = round_up(N, kTcN);
     return from_cuda(launch_recombine_tc_qd(P, splits, Mp, Np, e, f, M, N, C, ldc, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+// ---- octo and hexa doubles with bf16 parts ----
+
+namespace {
+
+int md_parts(int nparts) {
+    return nparts == 8 ? DDGEMM_TC_OD_SLICES : nparts == 16 ? DDGEMM_TC_HD_SLICES : 0;
+}
+
+ddgemm_status check_tc_md_args(int nparts, int64_t M, int64_t N, int64_t K, const double* const* A, int64_t lda,
+                               const double* const* B, int64_t ldb, double* const* C, int64_t ldc) {
+    if (md_parts(nparts) == 0) return DDGEMM_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) || ldc < std::max<int64_t>(1, N))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if ((round_up(M, kTcM) / kTcM) * (round_up(N, kTcN) / kTcN) > kMaxTiles) return DDGEMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    if (A == nullptr || B == nullptr || C == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    const int64_t a = span_bytes(M, K, lda), b = span_bytes(K, N, ldb), c = span_bytes(M, N, ldc);
+    for (int p = 0; p < nparts; ++p) {
+        if (C[p] == nullptr || (K > 0 && (A[p] == nullptr || B[p] == nullptr))) return DDGEMM_ERR_INVALID_ARG;
+        for (int q = 0; q < nparts; ++q) {
+            if (ranges_overlap(C[p], c, A[q], a) || ranges_overlap(C[p], c, B[q], b)) return DDGEMM_ERR_INVALID_ARG;
+            if (q != p && ranges_overlap(C[p], c, C[q], c)) return DDGEMM_ERR_INVALID_ARG;
+        }
+    }
+    return DDGEMM_OK;
+}
+
+cudaError_t run_split_tc_md(int nparts, int64_t M, int64_t N, int64_t K, int64_t Kp, const double* const* A,
+                            int64_t lda, int32_t* e, uint16_t* pA, const double* const* B, int64_t ldb, int32_t* f,
+                            uint16_t* pB, cudaStream_t st) {
+    const bool has_a = A != nullptr && e != nullptr && M > 0, has_b = B != nullptr && f != nullptr && N > 0;
+    SplitOperand a{has_a ? A[0] : nullptr, nullptr, lda, M, e}, b{has_b ? B[0] : nullptr, nullptr, ldb, N, f};
+    cudaError_t err = launch_init_exponents(has_a ? e : nullptr, M, has_b ? f : nullptr, N, K, st);
+    if (err == cudaSuccess) err = launch_exponents(has_a ? &a : nullptr, has_b ? &b : nullptr, K, st);
+    if (err == cudaSuccess)
+        err = launch_split_bf16_md(nparts, has_a ? A : nullptr, lda, M, e, has_b ? B : nullptr, ldb, N, f, K, Kp, pA,
+                                   pB, st);
+    return err;
+}
+
+ddgemm_status run_md_tc(int nparts, const TcLayout& L, int64_t M, int64_t N, int64_t K, const double* const* A,
+                        int64_t lda, const double* const* B, int64_t ldb, double* const* C, int64_t ldc, char* ws,
+                        cudaStream_t st) {
+    int32_t* e = reinterpret_cast<int32_t*>(ws + L.off_e);
+    int32_t* f = reinterpret_cast<int32_t*>(ws + L.off_f);
+    uint16_t* pA = reinterpret_cast<uint16_t*>(ws + L.off_A);
+    uint16_t* pB = reinterpret_cast<uint16_t*>(ws + L.off_B);
+    int32_t* P = reinterpret_cast<int32_t*>(ws + L.off_P);
+    DDG_TRY(run_split_tc_md(nparts, M, N, K, L.Kp, A, lda, e, pA, B, ldb, f, pB, st));
+    DDG_TRY(launch_slice_gemm_tc_md(nparts, pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_TRY(launch_recombine_tc_md(nparts, P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
+    return DDGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ddgemm_status md_gemm_tc_layout(int nparts, int64_t M, int64_t N, int64_t K, int64_t* Mp, int64_t* Np, int64_t* Kp,
+                                int* splits) {
+    if (md_parts(nparts) == 0) return DDGEMM_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    TcLayout L = make_tc_layout(M, N, K, md_parts(nparts));
+    if (Mp) *Mp = L.Mp;
+    if (Np) *Np = L.Np;
+    if (Kp) *Kp = L.Kp;
+    if (splits) *splits = L.splits;
+    return DDGEMM_OK;
+}
+
+ddgemm_status md_gemm_tc_workspace_size(int nparts, int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    if (md_parts(nparts) == 0) return DDGEMM_ERR_UNSUPPORTED;
+    if (bytes == nullptr || M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    *bytes = (size_t)make_tc_layout(M, N, K, md_parts(nparts)).total;
+    return DDGEMM_OK;
+}
+
+ddgemm_status md_gemm_tc(int nparts, int64_t M, int64_t N, int64_t K, const double* const* A, int64_t lda,
+                         const double* const* B, int64_t ldb, double* const* C, int64_t ldc, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    ddgemm_status s = check_tc_md_args(nparts, M, N, K, A, lda, B, ldb, C, ldc);
+    if (s != DDGEMM_OK || M == 0 || N == 0) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    TcLayout L = make_tc_layout(M, N, K, md_parts(nparts));
+    if (workspace != nullptr) {
+        if ((uintptr_t)workspace % kAlign != 0 || workspace_bytes < (size_t)L.total) return DDGEMM_ERR_INVALID_ARG;
+        return run_md_tc(nparts, L, M, N, K, A, lda, B, ldb, C, ldc, static_cast<char*>(workspace), st);
+    }
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    s = run_md_tc(nparts, L, M, N, K, A, lda, B, ldb, C, ldc, static_cast<char*>(ws), st);
+    cudaError_t fe = cudaFreeAsync(ws, st);
+    if (s == DDGEMM_OK && fe != cudaSuccess) s = DDGEMM_ERR_CUDA;
+    return s;
+}
+
+ddgemm_status md_split_bf16(int nparts, int64_t M, int64_t N, int64_t K, const double* const* A, int64_t lda,
+                            const double* const* B, int64_t ldb, uint16_t* planesA, int32_t* e, uint16_t* planesB,
+                            int32_t* f, void* stream) {
+    if (md_parts(nparts) == 0) return DDGEMM_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || K < 0 || lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if ((M > 0 && (e == nullptr || A == nullptr || (K > 0 && planesA == nullptr))) ||
+        (N > 0 && (f == nullptr || B == nullptr || (K > 0 && planesB == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    const int64_t Kp = round_up(K, kTcK);
+    return from_cuda(run_split_tc_md(nparts, M, N, K, Kp, M > 0 ? A : nullptr, lda, e, planesA, N > 0 ? B : nullptr,
+                                     ldb, f, planesB, static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status md_slice_gemm_tc(int nparts, int64_t M, int64_t N, int64_t K, const uint16_t* planesA,
+                               const uint16_t* planesB, int splits, int32_t* P, void* stream) {
+    if (md_parts(nparts) == 0) return DDGEMM_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    const int64_t Mp = round_up(M, kTcM), Np = round_up(N, kTcN), Kp = round_up(K, kTcK), KB = Kp / kTcK;
+    if (splits < 1 || splits > kTcMaxSplits || (KB > 0 && splits > KB) || (KB == 0 && splits != 1))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (KB > 0 && ((KB + splits - 1) / splits) * kTcK > tc_max_k_split(md_parts(nparts))) return DDGEMM_ERR_INVALID_ARG;
+    if (P == nullptr || (K > 0 && (planesA == nullptr || planesB == nullptr))) return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0 || (uintptr_t)P % 16 != 0)
+        return DDGEMM_ERR_INVALID_ARG;
+    return from_cuda(launch_slice_gemm_tc_md(nparts, planesA, planesB, Mp, Np, Kp, splits, P,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status md_recombine_tc(int nparts, int64_t M, int64_t N, const int32_t* P, int splits, const int32_t* e,
+                              const int32_t* f, double* const* C, int64_t ldc, void* stream) {
+    if (md_parts(nparts) == 0) return DDGEMM_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || ldc < std::max<int64_t>(1, N) || splits < 1 || splits > kTcMaxSplits)
+        return DDGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    if (P == nullptr || e == nullptr || f == nullptr || C == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    for (int p = 0; p < nparts; ++p)
+        if (C[p] == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    const int64_t Mp = round_up(M, kTcM), Np = round_up(N, kTcN);
+    return from_cuda(launch_recombine_tc_md(nparts, P, splits, Mp, Np, e, f, M, N, C, ldc,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

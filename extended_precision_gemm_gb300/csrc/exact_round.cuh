@@ -196,5 +196,52 @@ __device__ __forceinline__ void round_parts(const uint64_t (&z)[W], int q, doubl
     }
 }
 
+
+// Z 2^q rounded into nout doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0), ...
+// for any q: gradual underflow (a part below half the smallest subnormal is
+// 0) and overflow (an infinite part) end the expansion, and the remaining
+// parts are +0, as in the definition of the exact multiple-double product.
+template <int W>
+__device__ __forceinline__ void round_parts_general(const uint64_t (&z)[W], int q, double* out, int nout) {
+    uint64_t m[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) m[i] = z[i];
+    uint64_t sign = (uint64_t)m[W - 1] >> 63;
+    if (sign) negate(m);
+    bool stop = false;
+#pragma unroll 1
+    for (int p = 0; p < nout; ++p) {
+        if (stop || is_zero(m)) {
+            out[p] = 0.0;
+            stop = true;
+            continue;
+        }
+        const int t = msb(m);
+        int pos = max(t - 52, -1074 - q);  // last kept bit, relative to q
+        uint64_t keep = 0;
+        bool up = false;
+        if (pos <= 0) {
+            keep = m[0];  // exact (t <= 52)
+            pos = 0;
+#pragma unroll
+            for (int i = 0; i < W; ++i) m[i] = 0;
+        } else if (pos - 1 <= t) {
+            const uint64_t x = window(m, pos - 1);
+            keep = x >> 1;
+            up = (x & 1) && ((keep & 1) || any_below(m, pos - 1));
+            keep_below(m, pos);
+            if (up) {
+                complement_to(m, pos);
+                keep += 1;
+                if (keep >> 53) { keep >>= 1; pos += 1; }
+            }
+        }  // else: below half the smallest subnormal, rounds to 0
+        const double v = wide::make_double(keep, pos + q, sign);
+        if (keep == 0 || isinf(v)) stop = true;
+        out[p] = keep == 0 ? 0.0 : v;
+        if (up) sign ^= 1;
+    }
+}
+
 }  // namespace xr
 }  // namespace ddg

@@ -90,6 +90,17 @@ cudaError_t launch_recombine_tc_qd(const int32_t* P, int splits, int64_t Mp, int
                                    const int32_t* f, int64_t M, int64_t N, double* const* C, int64_t ldc,
                                    cudaStream_t st);
 
+// Octo (nin = 8) and hexa (nin = 16) doubles with 54 / 107 bf16 parts.
+cudaError_t launch_split_bf16_md(int nin, const double* const* A, int64_t lda, int64_t M, int32_t* e,
+                                 const double* const* B, int64_t ldb, int64_t N, int32_t* f, int64_t K, int64_t Kp,
+                                 uint16_t* planesA, uint16_t* planesB, cudaStream_t st);
+cudaError_t launch_slice_gemm_tc_md(int nin, const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
+                                    int64_t Kp, int splits, int32_t* P, cudaStream_t st);
+cudaError_t launch_recombine_tc_md(int nin, const int32_t* P, int splits, int64_t Mp, int64_t Np, const int32_t* e,
+                                   const int32_t* f, int64_t M, int64_t N, double* const* C, int64_t ldc,
+                                   cudaStream_t st);
+cudaError_t read_and_reset_wait_timeouts_tc_md(unsigned int* count);
+
 // Diagnostics of the bounded waits inside the slice GEMM.
 cudaError_t read_and_reset_wait_timeouts(unsigned int* count);
 

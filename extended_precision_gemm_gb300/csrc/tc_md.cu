@@ -1,0 +1,371 @@
+// tc_md.cu -- octo and hexa doubles (8 and 16 doubles per number) with 8-bit
+// parts on the bf16 tensor cores.
+//
+// "Multiple Double Arithmetic on NVIDIA Tensor Cores", Section 2: the
+// rewriting works for general multiple doubles; Table 2 gives the dimensions
+// of quartered quad, octo and hexa doubles.  The scheme of the double-double
+// and quad-double bf16 variants, for NIN doubles per number:
+//  1. e' = e + 1 (e from the leading doubles), X = trunc(x 2^(8 NP - e')) for
+//     x the sum of the NIN doubles (|X| < 2^(8 NP - 1), in WX 64-bit limbs),
+//     and its NP balanced base-256 digits read off Y = X + 128 (256^(NP-2) +
+//     ... + 1): the low bytes of Y are the digits + 128, its top the first
+//     digit.  NP = 54 for octo doubles (432 bits), 107 for hexa doubles (856);
+//  2. P_d = sum_{s+t=d} A_s B_t^T on the tensor cores (the pair kernel of
+//     tc_gemm.cuh with NP parts; a k-split covers at most 2048 / 1024 of k);
+//  3. Z = sum_d P_d 256^(NP-1-d) exactly (WZ limbs), rounded once into NIN
+//     doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0), ...
+#include "tc_gemm.cuh"
+#include "exact_round.cuh"
+
+namespace ddg {
+namespace {
+
+template <int NIN>
+struct MdShape;
+template <>
+struct MdShape<8> {
+    static constexpr int NP = DDGEMM_TC_OD_SLICES;  // 54 parts
+    static constexpr int WX = 7;                    // limbs of X and Y (|X| < 2^431)
+    static constexpr int WZ = 8;                    // limbs of Z (|Z| < 2^467)
+};
+template <>
+struct MdShape<16> {
+    static constexpr int NP = DDGEMM_TC_HD_SLICES;  // 107 parts
+    static constexpr int WX = 14;                   // |X| < 2^855
+    static constexpr int WZ = 14;                   // |Z| < 2^891
+};
+
+constexpr uint64_t ABS = 0x7FFFFFFFFFFFFFFFULL;
+
+struct UnpM {
+    uint64_t m;  // integer significand
+    int E;       // |x| = m 2^E
+};
+
+__device__ __forceinline__ UnpM unpack_m(uint64_t bits) {
+    const uint64_t a = bits & ABS;
+    const int biased = (int)(a >> 52);
+    UnpM u;
+    if (biased == 0) { u.m = a & ((1ULL << 52) - 1); u.E = -1074; }
+    else { u.m = (a & ((1ULL << 52) - 1)) | (1ULL << 52); u.E = biased - 1075; }
+    return u;
+}
+
+// X += (neg ? -1 : 1) m 2^sh for m < 2^53, 0 <= sh <= 64 W - 53.
+template <int W>
+__device__ __forceinline__ void add_shifted(uint64_t (&X)[W], uint64_t m, int sh, bool neg) {
+    const int i = sh >> 6, o = sh & 63;
+    const uint64_t lo = m << o, hi = o ? (m >> (64 - o)) : 0;
+    uint64_t t[W];
+#pragma unroll
+    for (int j = 0; j < W; ++j) t[j] = (j == i) ? lo : (j == i + 1) ? hi : 0;
+    if (neg) xr::negate(t);
+    uint64_t c = 0;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        const uint64_t u = X[j] + t[j];
+        const uint64_t c1 = u < X[j];
+        const uint64_t u2 = u + c;
+        c = c1 | (u2 < u);
+        X[j] = u2;
+    }
+}
+
+// X += F for a small signed F.
+template <int W>
+__device__ __forceinline__ void add_small(uint64_t (&X)[W], long long F) {
+    const uint64_t s = (uint64_t)(F >> 63);
+    uint64_t c = 0;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        const uint64_t add = j == 0 ? (uint64_t)F : s;
+        const uint64_t u = X[j] + add;
+        const uint64_t c1 = u < X[j];
+        const uint64_t u2 = u + c;
+        c = c1 | (u2 < u);
+        X[j] = u2;
+    }
+}
+
+// X = floor(|x_0 + ... + x_(NIN-1)| 2^(FIXB - e)) for a normalised multiple
+// double (|x_(p+1)| <= ulp(x_p) / 2) and the sign of the element.  With every
+// double signed relative to the leading one, the doubles that are integers at
+// this scale add exactly; at the first double with a fraction, floor(a + rest)
+// = floor(a) when a has a nonzero fraction (the rest is below half its last
+// bit), else floor(a) - 1 when the first nonzero later double is negative
+// (the borrow of Problem 3.3, eq. (7)).
+template <int NIN, int W>
+__device__ __forceinline__ void fixed_point_n(const double (&x)[NIN], int e, int FIXB, uint64_t (&X)[W],
+                                              uint64_t& sign_out) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) X[j] = 0;
+    int lead = -1;
+#pragma unroll
+    for (int p = NIN - 1; p >= 0; --p)
+        if (((uint64_t)__double_as_longlong(x[p]) & ABS) != 0) lead = p;
+    sign_out = 0;
+    if (lead < 0) return;
+    uint64_t sign = 0;
+#pragma unroll
+    for (int p = 0; p < NIN; ++p)
+        if (p == lead) sign = (uint64_t)__double_as_longlong(x[p]) >> 63;
+    sign_out = sign;
+    bool done = false;
+#pragma unroll
+    for (int p = 0; p < NIN; ++p) {
+        const uint64_t b = (uint64_t)__double_as_longlong(x[p]);
+        if (done || (b & ABS) == 0) continue;
+        const bool negp = (b >> 63) != sign;
+        const UnpM u = unpack_m(b);
+        const int sh = u.E + FIXB - e;
+        if (sh >= 0) {
+            add_shifted(X, u.m, min(sh, 64 * W - 53), negp);  // clamped only out of contract
+            continue;
+        }
+        const int rs = -sh;
+        const uint64_t ip = rs >= 64 ? 0 : (u.m >> rs);
+        const bool frac = rs >= 64 ? (u.m != 0) : ((u.m & ((1ULL << rs) - 1)) != 0);
+        long long F = negp ? -(long long)(ip + (frac ? 1 : 0)) : (long long)ip;
+        if (!frac) {
+            bool seen = false;
+#pragma unroll
+            for (int r = 0; r < NIN; ++r) {
+                if (r <= p || seen) continue;
+                const uint64_t c = (uint64_t)__double_as_longlong(x[r]);
+                if ((c & ABS) != 0) {
+                    if ((c >> 63) != sign) F -= 1;
+                    seen = true;
+                }
+            }
+        }
+        add_small(X, F);
+        done = true;
+    }
+}
+
+struct TcMdSplitGrid {
+    const double* A[16]; int64_t lda, M; int32_t* e; int64_t a_tasks;
+    const double* B[16]; int64_t ldb, N; int32_t* f; int64_t b_tasks;
+    int64_t K, KB;
+    uint16_t* planesA; uint16_t* planesB;
+};
+
+// Part s of a biased value Y as an f32 bit pattern (upper half = bf16).
+template <int NP, int W>
+__device__ __forceinline__ uint32_t md_part(const uint64_t (&y)[W], int s) {
+    if (s == 0) {  // the first digit: 16 bits from position 8 (NP - 1), signed
+        constexpr int pos = 8 * (NP - 1);
+        const int i = pos >> 6, o = pos & 63;
+        uint64_t v = 0, nx = 0;
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            if (j == i) v = y[j];
+            if (j == i + 1) nx = y[j];
+        }
+        const uint64_t bits = (v >> o) | (o > 48 ? nx << (64 - o) : 0);
+        return __float_as_uint(__int2float_rn((int)(int16_t)(uint16_t)bits));
+    }
+    const int b = NP - 1 - s;  // byte of Y
+    uint64_t limb = 0;
+#pragma unroll
+    for (int j = 0; j < W; ++j)
+        if (j == (b >> 3)) limb = y[j];
+    const uint32_t E = (uint32_t)(limb >> (8 * (b & 7))) & 0xFFu;
+    return __float_as_uint(__fsub_rn(__uint_as_float(0x4B000000u | E), 8388736.0f));
+}
+
+// One warp per task of 256 elements (A: 4 rows x 64 k, lane = row (lane/8),
+// 8 consecutive k (lane%8); B: 32 columns x 8 k, lane = column), as for the
+// other bf16 variants; each lane forms Y for its 8 elements, then writes one
+// 16-byte chunk of each of the NP part rows.
+template <int NIN>
+__global__ void __launch_bounds__(256) split_bf16_md_kernel(TcMdSplitGrid g) {
+    constexpr int NP = MdShape<NIN>::NP, W = MdShape<NIN>::WX;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gridDim.x * 8;
+    const int64_t tasks = g.a_tasks + g.b_tasks;
+    for (int64_t task = gw; task < tasks; task += nw) {
+        const bool is_a = task < g.a_tasks;
+        int64_t r, kb;
+        int kc;
+        if (is_a) {
+            kb = task % g.KB;
+            r = (task / g.KB) * 4 + (lane >> 3);
+            kc = lane & 7;
+        } else {
+            const int64_t local = task - g.a_tasks;
+            const int64_t kq = local % (g.KB * 8);
+            kb = kq >> 3;
+            kc = (int)(kq & 7);
+            r = (local / (g.KB * 8)) * 32 + lane;
+        }
+        const int64_t rows = is_a ? g.M : g.N;
+        int ep = 1;
+        if (r < rows) {
+            int32_t* ex = is_a ? g.e : g.f;
+            const int32_t er = ex[r];
+            if (kb == 0 && kc == 0 && er == EXP_NONE) ex[r] = 0;
+            ep = effective_exponent(er) + 1;
+        }
+        const int64_t k0 = kb * TBK + kc * 8;
+        uint64_t y[8][W];
+#pragma unroll 1
+        for (int j = 0; j < 8; ++j) {
+            double x[NIN];
+#pragma unroll
+            for (int q = 0; q < NIN; ++q) x[q] = 0.0;
+            if (r < rows && k0 + j < g.K) {
+#pragma unroll
+                for (int q = 0; q < NIN; ++q)
+                    x[q] = is_a ? __ldg(g.A[q] + r * g.lda + k0 + j) : __ldg(g.B[q] + (k0 + j) * g.ldb + r);
+            }
+            uint64_t X[W];
+            uint64_t sign;
+            fixed_point_n<NIN, W>(x, ep, 8 * NP, X, sign);
+            if (sign) xr::negate(X);
+            // + 128 in each of the NP - 1 low bytes
+            uint64_t c = 0;
+#pragma unroll
+            for (int i = 0; i < W; ++i) {
+                const int lo_byte = 8 * i, n = NP - 1 - lo_byte;  // bytes of C in this limb
+                const uint64_t Ci = n >= 8 ? 0x8080808080808080ULL : n > 0 ? (0x8080808080808080ULL >> (64 - 8 * n)) : 0;
+                const uint64_t u = X[i] + Ci;
+                const uint64_t c1 = u < X[i];
+                const uint64_t u2 = u + c;
+                c = c1 | (u2 < u);
+                y[j][i] = u2;
+            }
+        }
+        uint16_t* planes = is_a ? g.planesA : g.planesB;
+        const int brows = is_a ? TBM : TBN;
+        const int64_t blk = r / brows;
+        const int rin = (int)(r % brows);
+#pragma unroll 1
+        for (int s = 0; s < NP; ++s) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) w[j >> 1] = pack_bf16(md_part<NP, W>(y[j], s), md_part<NP, W>(y[j + 1], s));
+            uint8_t* base = reinterpret_cast<uint8_t*>(planes + ((blk * NP + s) * g.KB + kb) * ((int64_t)brows * TBK));
+            *reinterpret_cast<uint4*>(base + swizzled(rin, kc)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// Sum over the k-splits of part sum d of one output.
+__device__ __forceinline__ long long part_sum(const int32_t* p, int64_t plane, int NP, int splits, int d) {
+    long long v = 0;
+    for (int zz = 0; zz < splits; ++zz) v += __ldg(p + ((int64_t)zz * NP + d) * plane);
+    return v;
+}
+
+struct PlanePtrs {
+    double* c[16];  // the output planes (device pointers), passed by value
+};
+
+template <int NIN>
+__global__ void __launch_bounds__(256) recombine_tc_md_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
+                                                              int64_t Np, const int32_t* __restrict__ e,
+                                                              const int32_t* __restrict__ f, int64_t M, int64_t N,
+                                                              PlanePtrs C, int64_t ldc) {
+    constexpr int NP = MdShape<NIN>::NP, W = MdShape<NIN>::WZ;
+    constexpr int G = NP / 3, R = NP % 3;
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= N) return;
+    const int64_t plane = Mp * Np;
+    const int fj = effective_exponent(f[j]) + 1;
+    for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
+        const int32_t* p = P + i * Np + j;
+        // Horner over groups of three parts, the parts read group by group
+        uint64_t z[W];
+        {
+            const long long h0 = (part_sum(p, plane, NP, splits, 0) * 256 + part_sum(p, plane, NP, splits, 1)) * 256 +
+                                 part_sum(p, plane, NP, splits, 2);
+            z[0] = (uint64_t)h0;
+#pragma unroll
+            for (int w = 1; w < W; ++w) z[w] = (uint64_t)(h0 >> 63);
+        }
+#pragma unroll 1
+        for (int gi = 1; gi < G; ++gi) {
+            const long long h = (part_sum(p, plane, NP, splits, 3 * gi) * 256 + part_sum(p, plane, NP, splits, 3 * gi + 1)) *
+                                    256 + part_sum(p, plane, NP, splits, 3 * gi + 2);
+            xr::horner<W, 24>(z, h);
+        }
+        if (R == 1) xr::horner<W, 8>(z, part_sum(p, plane, NP, splits, NP - 1));
+        if (R == 2)
+            xr::horner<W, 16>(z, part_sum(p, plane, NP, splits, NP - 2) * 256 + part_sum(p, plane, NP, splits, NP - 1));
+        const int q = effective_exponent(e[i]) + 1 + fj - TD * (NP + 1);
+        double out[NIN];
+        xr::round_parts_general<W>(z, q, out, NIN);
+#pragma unroll
+        for (int pq = 0; pq < NIN; ++pq) C.c[pq][i * ldc + j] = out[pq];
+    }
+}
+
+template <int NIN>
+cudaError_t split_md(const double* const* A, int64_t lda, int64_t M, int32_t* e, const double* const* B, int64_t ldb,
+                     int64_t N, int32_t* f, int64_t K, int64_t Kp, uint16_t* planesA, uint16_t* planesB,
+                     cudaStream_t st) {
+    if (Kp == 0) return cudaSuccess;
+    TcMdSplitGrid g{};
+    g.K = K;
+    g.KB = Kp / TBK;
+    if (A && M > 0) {
+        for (int q = 0; q < NIN; ++q) g.A[q] = A[q];
+        g.lda = lda; g.M = M; g.e = e;
+        g.a_tasks = (round_up(M, PAIR_M) / 4) * g.KB;
+    }
+    if (B && N > 0) {
+        for (int q = 0; q < NIN; ++q) g.B[q] = B[q];
+        g.ldb = ldb; g.N = N; g.f = f;
+        g.b_tasks = (round_up(N, TBN) / 32) * g.KB * 8;
+    }
+    g.planesA = planesA;
+    g.planesB = planesB;
+    const int64_t tasks = g.a_tasks + g.b_tasks;
+    if (tasks == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms_tc() * 8));
+    split_bf16_md_kernel<NIN><<<blocks, 256, 0, st>>>(g);
+    return cudaGetLastError();
+}
+
+template <int NIN>
+cudaError_t recombine_md(const int32_t* P, int splits, int64_t Mp, int64_t Np, const int32_t* e, const int32_t* f,
+                         int64_t M, int64_t N, double* const* C, int64_t ldc, cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    PlanePtrs pc{};
+    for (int q = 0; q < NIN; ++q) pc.c[q] = C[q];
+    const unsigned gx = (unsigned)((N + 255) / 256);
+    const unsigned gy = (unsigned)(M < 65535 ? M : 65535);
+    recombine_tc_md_kernel<NIN><<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, pc, ldc);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_split_bf16_md(int nin, const double* const* A, int64_t lda, int64_t M, int32_t* e,
+                                 const double* const* B, int64_t ldb, int64_t N, int32_t* f, int64_t K, int64_t Kp,
+                                 uint16_t* planesA, uint16_t* planesB, cudaStream_t st) {
+    if (nin == 8) return split_md<8>(A, lda, M, e, B, ldb, N, f, K, Kp, planesA, planesB, st);
+    if (nin == 16) return split_md<16>(A, lda, M, e, B, ldb, N, f, K, Kp, planesA, planesB, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_slice_gemm_tc_md(int nin, const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
+                                    int64_t Kp, int splits, int32_t* P, cudaStream_t st) {
+    if (nin == 8) return launch_slice_gemm_parts<MdShape<8>::NP>(planesA, planesB, Mp, Np, Kp, splits, P, st);
+    if (nin == 16) return launch_slice_gemm_parts<MdShape<16>::NP>(planesA, planesB, Mp, Np, Kp, splits, P, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_recombine_tc_md(int nin, const int32_t* P, int splits, int64_t Mp, int64_t Np, const int32_t* e,
+                                   const int32_t* f, int64_t M, int64_t N, double* const* C, int64_t ldc,
+                                   cudaStream_t st) {
+    if (nin == 8) return recombine_md<8>(P, splits, Mp, Np, e, f, M, N, C, ldc, st);
+    if (nin == 16) return recombine_md<16>(P, splits, Mp, Np, e, f, M, N, C, ldc, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_reset_wait_timeouts_tc_md(unsigned int* count) { return reset_tc_timeouts(count); }
+
+}  // namespace ddg

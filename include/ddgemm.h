@@ -372,6 +372,8 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
 #define DDGEMM_TC_MAX_K_SPLIT 8192  /* k per slice-GEMM block: int32 part sums stay exact */
 #define DDGEMM_TC_QD_SLICES 27      /* parts per quad double (216 bits) */
 #define DDGEMM_TC_QD_MAX_K_SPLIT 4096 /* k per slice-GEMM block for quad doubles */
+#define DDGEMM_TC_OD_SLICES 54      /* parts per octo double (432 bits) */
+#define DDGEMM_TC_HD_SLICES 107     /* parts per hexa double (856 bits) */
 
 /*
  * Padded extents (Mp = M rounded up to 256, Np = N rounded up to 256, Kp = K
@@ -441,6 +443,36 @@ ddgemm_status qd_split_bf16(int64_t M, int64_t N, int64_t K,
 ddgemm_status qd_slice_gemm_tc(int64_t M, int64_t N, int64_t K, const uint16_t* planesA,
                                const uint16_t* planesB, int splits, int32_t* P, void* stream);
 ddgemm_status qd_recombine_tc(int64_t M, int64_t N, const int32_t* P, int splits, const int32_t* e,
+                              const int32_t* f, double* const* C, int64_t ldc, void* stream);
+
+/*
+ * Octo doubles (nparts = 8) and hexa doubles (nparts = 16) with the parts on
+ * the bf16 tensor cores: the scheme of qd_gemm_tc with DDGEMM_TC_OD_SLICES =
+ * 54 / DDGEMM_TC_HD_SLICES = 107 balanced 8-bit parts (X = trunc(x 2^(8 NP -
+ * e'))), the NP (NP + 1) / 2 pairs (1485 / 5778) on the tensor cores, and the
+ * exact sum of the part sums rounded once into nparts non-overlapping doubles
+ * (with gradual underflow; a zero or infinite part ends the expansion and the
+ * rest are +0).  The paper's Table 2 gives the dimensions of quartered octo
+ * and hexa doubles.  A, B, C are host arrays of nparts device pointers to
+ * row-major planes sharing one leading dimension.  K <= QDGEMM_MAX_K; a
+ * k-split covers at most 2048 (octo) / 1024 (hexa) of k.  Other nparts values
+ * return DDGEMM_ERR_UNSUPPORTED (quad doubles: qd_gemm_tc; double doubles:
+ * dd_gemm_tc).  Steps as for quad doubles, with NP parts.
+ */
+ddgemm_status md_gemm_tc_layout(int nparts, int64_t M, int64_t N, int64_t K,
+                                int64_t* Mp, int64_t* Np, int64_t* Kp, int* splits);
+ddgemm_status md_gemm_tc_workspace_size(int nparts, int64_t M, int64_t N, int64_t K, size_t* bytes);
+ddgemm_status md_gemm_tc(int nparts, int64_t M, int64_t N, int64_t K,
+                         const double* const* A, int64_t lda,
+                         const double* const* B, int64_t ldb,
+                         double* const* C, int64_t ldc,
+                         void* workspace, size_t workspace_bytes, void* stream);
+ddgemm_status md_split_bf16(int nparts, int64_t M, int64_t N, int64_t K,
+                            const double* const* A, int64_t lda, const double* const* B, int64_t ldb,
+                            uint16_t* planesA, int32_t* e, uint16_t* planesB, int32_t* f, void* stream);
+ddgemm_status md_slice_gemm_tc(int nparts, int64_t M, int64_t N, int64_t K, const uint16_t* planesA,
+                               const uint16_t* planesB, int splits, int32_t* P, void* stream);
+ddgemm_status md_recombine_tc(int nparts, int64_t M, int64_t N, const int32_t* P, int splits, const int32_t* e,
                               const int32_t* f, double* const* C, int64_t ldc, void* stream);
 
 /* ------------------------------------------------------------------ */

@@ -15,7 +15,7 @@ HEADER = pathlib.Path(__file__).resolve().parent.parent / "include" / "ddgemm.h"
 def declared_functions():
     text = HEADER.read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:dd|qd)_[a-z0-9_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:dd|qd|md)_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
