@@ -494,6 +494,37 @@ def run_ours(args, w):
     del tQA, tQB, QC, ws_qt
     assert ddg.wait_timeouts() == 0
 
+    # ---- octo and hexa doubles on the bf16 tensor cores (2048^3, same distribution) ----
+    md_results = {}
+    for n_md in (8, 16):
+        Mm = Nm = Km = 2048
+        MA, MB = workloads.make_md(Mm, Nm, Km, w.dist, w.seed, n_md)
+        tMA = [torch.from_numpy(x).to(dev) for x in MA]
+        tMB = [torch.from_numpy(x).to(dev) for x in MB]
+        del MA, MB
+        MC = [torch.empty((Mm, Nm), dtype=torch.float64, device=dev) for _ in range(n_md)]
+        ws_m = torch.empty(ddg.md_tc_workspace_size(n_md, Mm, Nm, Km), dtype=torch.uint8, device=dev)
+        ddg.md_gemm_tc(tMA, tMB, MC, workspace=ws_m, stream=stream)
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            ddg.md_gemm_tc(tMA, tMB, MC, workspace=ws_m, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        units_m, t_m = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * 2.0 * Mm * Nm * Km, dev)
+        parts_m = ddg.MD_TC_PARTS[n_md]
+        md_results[{8: "octo_double", 16: "hexa_double"}[n_md]] = {
+            "workload": f"{'od' if n_md == 8 else 'hd'}_gemm_2048x2048x2048_{w.dist}",
+            "value": units_m / t_m / 1e9, "unit": "GFLOP/s (2MNK/s)", "ms_per_step": 1e3 * t_m / args.steps,
+            "parts": parts_m, "slice_pairs": parts_m * (parts_m + 1) // 2,
+            "k_splits": ddg.md_tc_layout(n_md, Mm, Nm, Km)[3],
+            "bf16_tflops_whole_product": parts_m * (parts_m + 1) // 2 * 2.0 * Mm * Nm * Km / (t_m / args.steps) / 1e12,
+        }
+        del tMA, tMB, MC, ws_m
+        torch.cuda.empty_cache()
+    assert ddg.wait_timeouts() == 0
+
     if rank != 0:
         return None
 
@@ -592,6 +623,7 @@ def run_ours(args, w):
             "bf16_tflops_whole_product": 378 * 2.0 * M * N * K / (t_qt / args.steps) / 1e12,
             "normwise_vs_exact_oracle_2_rows": qdt_norm,
         },
+        "md_bf16_tensor_variants": md_results,
         "qd_int_pipe": {
             "what": "quad-double GEMM (4 doubles per number): 16 parts of 13 bits, 136 pairs on the "
                     "integer pipe, exact sums rounded once into 4 doubles",
