@@ -139,3 +139,32 @@ def test_bf16_variant_long_k_closed_form():
     # and the dropped pairs (index sums 13..24, < 13 2^14 2^-120 each, times 16)
     assert abs(got - exact) <= K * 16 * Fraction(2 + 13 * 13, 2**104)
     assert ddg.wait_timeouts() == 0
+
+
+def test_full_size_quad_double_bf16_variant():
+    """qd_gemm_tc on the 4096^3 wide-range shape (the quad-double leg bench.py
+    times): a sampled block bit for bit against the oracle's model, two whole
+    rows within the quad-double gate of the exact product."""
+    import torch
+    from oracle import slices_bf16_md as bm
+    w = workloads.WORKLOADS[2]
+    A, B = workloads.make_md(w.M, w.N, w.K, w.dist, w.seed, 4)
+    tA, tB = [dev(a) for a in A], [dev(b) for b in B]
+    ws = torch.empty(ddg.qd_tc_workspace_size(w.M, w.N, w.K), dtype=torch.uint8, device="cuda")
+    C = ddg.qd_gemm_tc(tA, tB, workspace=ws)
+    torch.cuda.synchronize()
+    del ws, tA, tB
+    assert ddg.wait_timeouts() == 0
+    rng = np.random.default_rng(300)
+    rows = np.unique(np.concatenate([[0, w.M - 1], rng.integers(0, w.M, 1)]))
+    cols = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, 4)]))
+    ridx = torch.from_numpy(rows).cuda()
+    G = [host(c[ridx]) for c in C]
+    M_ref, *_ = bm.sliced_gemm([a[rows] for a in A], [b[:, cols] for b in B])
+    for p in range(4):
+        assert np.array_equal(G[p][:, cols].view(np.int64), M_ref[p].view(np.int64)), p
+    r2 = rows[:2]
+    R = oracle.exact_md_gemm(A, B, rows=r2)
+    d = sum(G[p][:2] - R[p] for p in range(4))
+    err = float(np.linalg.norm(d) / (np.linalg.norm(sum(a[r2] for a in A)) * np.linalg.norm(sum(B))))
+    assert err <= 1e-57, err
