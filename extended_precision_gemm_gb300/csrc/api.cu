@@ -654,28 +654,6 @@ struct TcLayout {
 // count whose waves of blocks (one per SM) fill the GPU best, each split
 // keeping at least 512 of k, with a small cost per split (each writes its own
 // part sums).  One output block occupies a pair of SMs.
-int choose_tc_splits(int64_t Mp, int64_t Np, int64_t Kp, int64_t max_k_split) {
-    const int64_t KB = Kp / kTcK;
-    const int64_t tiles = (Mp / kTcM) * (Np / kTcN);
-    const int64_t per_split = max_k_split / kTcK;
-    const int64_t smin = std::max<int64_t>(1, (KB + per_split - 1) / per_split);
-    if (tiles == 0 || KB == 0) return 1;
-    const int64_t smax = std::max<int64_t>(smin, std::min<int64_t>(KB / 8, 4 * smin + 8));
-    const int64_t slots = device_sms() / 2;  // one output block per CTA pair (two SMs)
-    int64_t best = smin;
-    double best_score = -1.0;
-    for (int64_t s = smin; s <= smax; ++s) {
-        const int64_t kb_per = (KB + s - 1) / s;
-        if ((KB + kb_per - 1) / kb_per != s) continue;  // some split would be empty
-        const int64_t blocks = tiles * s;
-        const int64_t waves = (blocks + slots - 1) / slots;
-        const double eff = (double)blocks / (double)(waves * slots);
-        const double score = eff - 0.01 * (double)(s - smin) / (double)smin;
-        if (score > best_score + 1e-12) { best_score = score; best = s; }
-    }
-    return (int)best;
-}
-
 // Largest k of one k-split for `parts` parts: the largest power of two with
 // parts K 2^14 < 2^31 (int32 part sums stay exact).
 int64_t tc_max_k_split(int parts) {
@@ -684,13 +662,84 @@ int64_t tc_max_k_split(int parts) {
     return k;
 }
 
+// Pair passes over one k-block of the busiest CTA pair of the tensor-core GEMM
+// with s k-splits, dealing its units out as the kernel does: units numbered
+// from the heaviest diagonal down (then k-split, then output block), one unit
+// per pair and round, the order of the pairs reversed every other round.
+int64_t busiest_pair(int64_t tiles, int64_t s, int np, int64_t KB, int64_t pairs) {
+    const int64_t units = tiles * s * np, kb_per = (KB + s - 1) / s;
+    pairs = std::max<int64_t>(1, std::min(pairs, units));
+    int64_t worst = 0;
+    for (int64_t p = 0; p < pairs; ++p) {
+        int64_t w = 0;
+        for (int64_t r = 0;; ++r) {
+            const int64_t u = r * pairs + ((r & 1) ? pairs - 1 - p : p);
+            if (u >= units) break;
+            const int64_t d = np - 1 - u / (tiles * s), z = (u / tiles) % s;
+            w += (d + 1) * std::max<int64_t>(0, std::min(KB, (z + 1) * kb_per) - z * kb_per);
+        }
+        worst = std::max(worst, w);
+    }
+    return worst;
+}
+
+// k-splits of the tensor-core GEMM: at least enough for exact int32 sums;
+// more only where the finer units balance the persistent pairs by more than
+// the extra part sums cost.  Model (microseconds): a pair passes one k-block
+// of a 256 x 256 block (2 x 256 x 256 x 64 flops) in about 0.37 us, and each
+// k-split's int32 part sums are written and read back once at about 6 TB/s.
+int choose_tc_splits_uncached(int64_t Mp, int64_t Np, int64_t Kp, int parts) {
+    const int64_t KB = Kp / kTcK;
+    const int64_t tiles = (Mp / kTcM) * (Np / kTcN);
+    if (tiles == 0 || KB == 0) return 1;
+    const int64_t per_split = tc_max_k_split(parts) / kTcK;
+    const int64_t smin = std::max<int64_t>(1, (KB + per_split - 1) / per_split);
+    const int64_t smax = std::min<int64_t>(KB, std::max<int64_t>(4 * smin, 64));
+    const int64_t pairs = tc_resident_pairs();
+    const double t_pass = 0.37;
+    const double t_split = 2.0 * parts * (double)Mp * (double)Np * 4.0 / 6.0e6;
+    int64_t best = smin, evaluated = 0;
+    double best_t = -1.0;
+    for (int64_t s = smin; s <= smax; ++s) {
+        const int64_t kb_per = (KB + s - 1) / s;
+        if ((KB + kb_per - 1) / kb_per != s) continue;  // some split would be empty
+        // many units balance well anyway: bound the host work of the search
+        if (s > smin && (tiles * s * parts > (1 << 18) || evaluated > (1 << 21))) break;
+        evaluated += tiles * s * parts;
+        const double t = (double)busiest_pair(tiles, s, parts, KB, pairs) * t_pass + s * t_split;
+        if (best_t < 0.0 || t < best_t * 0.98) { best_t = t; best = s; }
+    }
+    return (int)best;
+}
+
+// The choice above, remembered for the last few shapes (layouts are asked for
+// on every call).
+int choose_tc_splits(int64_t Mp, int64_t Np, int64_t Kp, int parts) {
+    struct Entry { int64_t Mp, Np, Kp; int parts, splits; };
+    static std::mutex mu;
+    static Entry cache[16];
+    static int next = 0, used = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].Mp == Mp && cache[i].Np == Np && cache[i].Kp == Kp && cache[i].parts == parts)
+                return cache[i].splits;
+    }
+    const int s = choose_tc_splits_uncached(Mp, Np, Kp, parts);
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next] = Entry{Mp, Np, Kp, parts, s};
+    next = (next + 1) % 16;
+    used = std::min(used + 1, 16);
+    return s;
+}
+
 // parts = 13 (double doubles), 27 (quad), 54 (octo) or 107 (hexa doubles).
 TcLayout make_tc_layout(int64_t M, int64_t N, int64_t K, int parts = kTcParts) {
     TcLayout L;
     L.Mp = round_up(M, kTcM);
     L.Np = round_up(N, kTcN);
     L.Kp = round_up(K, kTcK);
-    L.splits = choose_tc_splits(L.Mp, L.Np, L.Kp, tc_max_k_split(parts));
+    L.splits = choose_tc_splits(L.Mp, L.Np, L.Kp, parts);
     int64_t off = 0;
     auto take = [&](int64_t bytes) { int64_t o = off; off = round_up(off + bytes, kAlign); return o; };
     L.off_e = take(L.Mp * 4);

@@ -80,6 +80,9 @@ cudaError_t launch_recombine_tc(const int32_t* P, int splits, int64_t Mp, int64_
                                 const int32_t* f, int64_t M, int64_t N, double* C_hi, double* C_lo, int64_t ldc,
                                 cudaStream_t st);
 cudaError_t read_and_reset_wait_timeouts_tc(unsigned int* count);
+// CTA pairs of the tensor-core GEMM resident at once (its persistent grid;
+// the same for every part count).
+int tc_resident_pairs();
 // Quad doubles with 27 bf16 parts (same block layout, 378 pairs).
 cudaError_t launch_split_bf16_qd(const double* const* A, int64_t lda, int64_t M, int32_t* e, const double* const* B,
                                  int64_t ldb, int64_t N, int32_t* f, int64_t K, int64_t Kp, uint16_t* planesA,

@@ -435,4 +435,6 @@ cudaError_t launch_recombine_tc_qd(const int32_t* P, int splits, int64_t Mp, int
 
 cudaError_t read_and_reset_wait_timeouts_tc(unsigned int* count) { return reset_tc_timeouts(count); }
 
+int tc_resident_pairs() { return resident_pairs<TS>(); }
+
 }  // namespace ddg

@@ -64,8 +64,10 @@ __device__ __forceinline__ uint32_t pack_bf16(uint32_t f_first, uint32_t f_secon
 }
 
 // ---------------------------------------------------------------------------
-// Step 2: P_d on the tensor cores.  One cluster of two CTAs (a CTA pair on two
-// SMs) per (256 x 256 output block, k-split); the pair's MMAs are M = 256,
+// Step 2: P_d on the tensor cores.  Persistent clusters of two CTAs (a CTA
+// pair on two SMs, as many pairs as can be resident) share out the units of
+// work (a diagonal d of a 256 x 256 output block and k-split: d + 1 pairs);
+// the pair's MMAs are M = 256,
 // N = 256, K = 16 (tcgen05 cta_group::2): each CTA holds its 128 rows of A and
 // its 128 rows of B (columns of C) for a k-block, and its 128 rows of the
 // accumulators.  10 warps per CTA:
@@ -79,10 +81,11 @@ __device__ __forceinline__ uint32_t pack_bf16(uint32_t f_first, uint32_t f_secon
 //   warps 2-9: read each finished chunk from TMEM (warp w reads lanes
 //           32 (w % 4) .. +31, i.e. rows, and one half of the columns), add it
 //           into int32 totals in registers, and store the totals of P_d.
-// The order of work is d = 0..12, then s = 0..d (t = d - s), then k-blocks;
-// a chunk is 8 consecutive k-blocks of one d (512 products per output; the
-// last chunk of a d may be shorter).  Chunks alternate between the two accumulators, so the MMAs of
-// one chunk overlap the read-out of the previous one.  Completion of MMAs
+// Within a unit the order of work is s = 0..d (t = d - s), then k-blocks; a
+// chunk is 8 consecutive k-blocks of one unit (512 products per output; the
+// last chunk of a unit may be shorter).  Chunks alternate between the two
+// accumulators, also across units, so the MMAs of one chunk overlap the
+// read-out of the previous one and the store of a finished unit.  Completion of MMAs
 // reaches both CTAs through multicast commits; the release of an
 // accumulator needs all 16 epilogue warps of the pair.
 // ---------------------------------------------------------------------------
@@ -95,7 +98,48 @@ struct TcGemmArgs {
     int64_t KB;       // k-blocks in the planes
     int64_t kb_per_split;
     int MT, NT;       // output blocks of 256 x 256 along M and N
+    int splits;       // k-splits
+    int pairs;        // CTA pairs in the grid
+    int64_t units;    // output blocks x k-splits x NP diagonals
 };
+
+// A unit of work: diagonal d of one output block and k-split, i.e. the d + 1
+// pairs (s, d - s) over the split's k-blocks.  Units are numbered from the
+// heaviest diagonal (d = NP - 1) down to d = 0; within a diagonal by k-split,
+// then by output block in grouped order (TILE_GROUP row blocks share their
+// column blocks while they are in L2).
+struct Unit {
+    int64_t mt, nt, z, kb0, nkb;
+    int d;
+};
+
+__device__ __forceinline__ Unit unit_of(const TcGemmArgs& g, int64_t u, int np) {
+    Unit w;
+    const int64_t tiles = (int64_t)g.MT * g.NT;
+    const int64_t per_d = tiles * g.splits;
+    w.d = np - 1 - (int)(u / per_d);
+    const int64_t rem = u % per_d;
+    w.z = rem / tiles;
+    const int64_t tile = rem % tiles;
+    const int64_t per_group = (int64_t)TILE_GROUP * g.NT;
+    const int64_t group = tile / per_group;
+    const int64_t first_m = group * TILE_GROUP;
+    const int64_t gsize = min((int64_t)TILE_GROUP, (int64_t)g.MT - first_m);
+    w.mt = first_m + (tile % per_group) % gsize;
+    w.nt = (tile % per_group) / gsize;
+    w.kb0 = w.z * g.kb_per_split;
+    w.nkb = max((int64_t)0, min(g.KB, w.kb0 + g.kb_per_split) - w.kb0);
+    return w;
+}
+
+// The r-th unit of CTA pair p: units are dealt out in rounds of one unit per
+// pair, the order of the pairs reversed every other round.  Unit weights only
+// fall along the numbering, so the pairs' totals stay within about one light
+// unit of each other, and in every round the pairs work on neighbouring
+// output blocks at the same diagonal (their copies share L2).
+__device__ __forceinline__ int64_t unit_index(const TcGemmArgs& g, int64_t p, int64_t r) {
+    return r * g.pairs + ((r & 1) ? g.pairs - 1 - p : p);
+}
 
 __device__ __forceinline__ void note_timeout(volatile int* abort_flag) {
     *abort_flag = 1;
@@ -115,19 +159,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
     const bool leader = rank == 0;
 
-    // output block of this pair (grouped order: TILE_GROUP row blocks share
-    // their column blocks while they are in L2)
-    const int64_t tile = blockIdx.x >> 1;
-    const int64_t per_group = (int64_t)TILE_GROUP * g.NT;
-    const int64_t group = tile / per_group;
-    const int64_t first_m = group * TILE_GROUP;
-    const int64_t gsize = min((int64_t)TILE_GROUP, (int64_t)g.MT - first_m);
-    const int64_t mt = first_m + (tile % per_group) % gsize;
-    const int64_t nt = (tile % per_group) / gsize;
-    const int64_t z = blockIdx.y;
-    const int64_t kb0 = z * g.kb_per_split;
-    const int64_t nkb = max((int64_t)0, min(g.KB, kb0 + g.kb_per_split) - kb0);
-    const int64_t a_block = mt * 2 + rank;  // this CTA's 128 rows of A
+    // both CTAs of a pair walk the same units
+    const int64_t pair = blockIdx.x >> 1;
 
     const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[STAGES]);
     const uint32_t pfull0 = smem_addr(&bars[2 * STAGES]);
@@ -162,12 +195,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             // ---- producer (both CTAs): a stage holds up to two k-blocks of one pair ----
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
-            for (int d = 0; d < NP && !abort_flag; ++d) {
+            for (int64_t r = 0, u; (u = unit_index(g, pair, r)) < g.units && !abort_flag; ++r) {
+                const Unit w = unit_of(g, u, NP);
+                const int d = w.d;
+                const int64_t a_block = w.mt * 2 + rank;  // this CTA's 128 rows of A
+                const int64_t nkb = w.nkb;
                 for (int s = 0; s <= d && !abort_flag; ++s) {
                     const int t = d - s;
-                    const uint16_t* a_src = g.planesA + ((a_block * NP + s) * g.KB + kb0) * (TBM * TBK);
+                    const uint16_t* a_src = g.planesA + ((a_block * NP + s) * g.KB + w.kb0) * (TBM * TBK);
                     const uint16_t* b_src =
-                        g.planesB + ((nt * NP + t) * g.KB + kb0) * (TBN * TBK) + rank * (TBN / 2) * TBK;
+                        g.planesB + ((w.nt * NP + t) * g.KB + w.kb0) * (TBN * TBK) + rank * (TBN / 2) * TBK;
                     for (int64_t kb = 0; kb < nkb; kb += STAGE_BLOCKS) {
                         const int nb = (int)min((int64_t)STAGE_BLOCKS, nkb - kb);
                         if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1, WAIT_NS)) {
@@ -203,10 +240,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t ring = smem_addr(smem);
             const uint64_t adesc0 = tc5::desc_kmajor_sw128(ring);
             const uint64_t bdesc0 = tc5::desc_kmajor_sw128(ring + STAGE_BLOCKS * A_BLOCK_BYTES);
-            const int nkb32 = (int)nkb;
             uint32_t stage = 0, phase = 0, chunk = 0, buf = 0;
-            bool ok = true;
-            for (int d = 0; d < NP && ok; ++d) {
+            bool ok = true, issued_any = false;
+            for (int64_t r = 0, u; (u = unit_index(g, pair, r)) < g.units && ok; ++r) {
+                const Unit w = unit_of(g, u, NP);
+                const int d = w.d;
+                const int nkb32 = (int)w.nkb;
                 int left = (d + 1) * nkb32;  // k-blocks of this d still to issue
                 int in_chunk = 0;            // k-blocks issued into the current chunk
                 for (int s = 0; s <= d && ok; ++s) {
@@ -236,6 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                             const uint64_t ad = adesc0 + off + (uint64_t)(j * (A_BLOCK_BYTES >> 4));
                             const uint64_t bd = bdesc0 + off + (uint64_t)(j * (B_HALF_BYTES >> 4));
                             tc5::mma_bf16_pair(d_tmem, ad, bd, IDESC, in_chunk != 0 ? 1u : 0u);
+                            issued_any = true;
 #pragma unroll
                             for (int kk = 1; kk < TBK / UMMA_K; ++kk)
                                 tc5::mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, IDESC, 1u);
@@ -254,12 +294,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             }
             // every MMA issued has finished (in both CTAs) before either
             // releases its tensor memory or shared memory
-            tc5::commit_pair(done_bar, 0x3);
-            if (!mbar_wait_bounded(done_bar, 0, WAIT_NS)) note_timeout(&abort_flag);
+            if (issued_any) {
+                tc5::commit_pair(done_bar, 0x3);
+                if (!mbar_wait_bounded(done_bar, 0, WAIT_NS)) note_timeout(&abort_flag);
+            }
         } else if (lane == 0) {
             // ---- forwarder (odd CTA): its stage s is full -> tell the even CTA ----
             uint32_t stage = 0, phase = 0;
-            const int64_t total = (int64_t)(NP * (NP + 1) / 2) * ((nkb + STAGE_BLOCKS - 1) / STAGE_BLOCKS);
+            int64_t total = 0;  // stages the producer fills for this pair's units
+            for (int64_t r = 0, u; (u = unit_index(g, pair, r)) < g.units; ++r) {
+                const Unit w = unit_of(g, u, NP);
+                total += (int64_t)(w.d + 1) * ((w.nkb + STAGE_BLOCKS - 1) / STAGE_BLOCKS);
+            }
             for (int64_t j = 0; j < total; ++j) {
                 if (abort_flag || !mbar_wait_bounded(full0 + 8 * stage, phase, WAIT_NS)) {
                     if (!abort_flag) note_timeout(&abort_flag);
@@ -269,8 +315,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
             // the even CTA's MMAs read this CTA's shared memory and write its
-            // tensor memory: wait until they have all finished
-            if (!mbar_wait_bounded(done_bar, 0, WAIT_NS)) note_timeout(&abort_flag);
+            // tensor memory: wait until they have all finished (a pair whose
+            // share is empty issues none)
+            if (total > 0 && !mbar_wait_bounded(done_bar, 0, WAIT_NS)) note_timeout(&abort_flag);
         }
     } else {
         // ---- epilogue: warps 2..9 (both CTAs) ----
@@ -280,11 +327,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
         int64_t chunk = 0;
         bool ok = true;
-        for (int d = 0; d < NP; ++d) {
+        for (int64_t r = 0, u; (u = unit_index(g, pair, r)) < g.units; ++r) {
+            const Unit w = unit_of(g, u, NP);
+            const int d = w.d;
             int32_t acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
-            const int64_t nch = ok ? ((int64_t)(d + 1) * nkb + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS : 0;
+            const int64_t nch = ok ? ((int64_t)(d + 1) * w.nkb + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS : 0;
             for (int64_t c = 0; c < nch; ++c, ++chunk) {
                 const uint32_t buf = (uint32_t)(chunk & 1), use = (uint32_t)(chunk >> 1);
                 if (abort_flag || !mbar_wait_bounded(accf0 + 8 * buf, use & 1, WAIT_NS)) {
@@ -309,8 +358,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     else mbar_arrive_remote(acce0 + 8 * buf, 0);
                 }
             }
-            int32_t* dst =
-                g.P + (((z * NP + d) * g.Mp + mt * PAIR_M + rank * TBM + row) * g.Np + nt * TBN + half * 128);
+            int32_t* dst = g.P + (((w.z * NP + d) * g.Mp + w.mt * PAIR_M + rank * TBM + row) * g.Np + w.nt * TBN +
+                                  half * 128);
 #pragma unroll
             for (int i = 0; i < 128; i += 4)
                 *reinterpret_cast<int4*>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
@@ -325,6 +374,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         __syncwarp();  // the whole warp, converged, releases tensor memory
         tc5::tmem_dealloc_pair(tmem, TMEM_COLS);
     }
+}
+
+int num_sms_tc() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 152;
+    return sms;
+}
+
+// CTA pairs of the GEMM that can be resident at once: a cluster of two needs
+// both SMs in one GPC, so this can be below half the SM count.
+template <int NP>
+int resident_pairs() {
+    static int cached = 0;
+    if (cached > 0) return cached;
+    int n = 0;
+    if (cudaFuncSetAttribute(slice_gemm_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) ==
+        cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * std::max(1, num_sms_tc() / 2)), 1, 1);
+        cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = GEMM_SMEM;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, slice_gemm_tc_kernel<NP>, &cfg) != cudaSuccess) n = 0;
+    }
+    if (n <= 0) (void)cudaGetLastError();  // no device: fall back to half the SMs
+    cached = n > 0 ? n : std::max(1, num_sms_tc() / 2);
+    return cached;
 }
 
 template <int NP>
@@ -346,7 +429,11 @@ cudaError_t launch_slice_gemm_parts(const uint16_t* planesA, const uint16_t* pla
     g.kb_per_split = (g.KB + splits - 1) / splits;
     g.MT = (int)(Mp / PAIR_M);
     g.NT = (int)(Np / TBN);
-    dim3 grid((unsigned)(2 * (int64_t)g.MT * g.NT), (unsigned)splits);  // clusters of 2 along x
+    g.splits = splits;
+    g.units = (int64_t)g.MT * g.NT * splits * NP;
+    // as many persistent CTA pairs as can be resident (never more than units)
+    g.pairs = (int)std::max<int64_t>(1, std::min<int64_t>(resident_pairs<NP>(), g.units));
+    dim3 grid((unsigned)(2 * g.pairs), 1);  // clusters of 2 along x
     slice_gemm_tc_kernel<NP><<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(g);
     return cudaGetLastError();
 }
@@ -361,12 +448,6 @@ cudaError_t reset_tc_timeouts(unsigned int* count) {
     return cudaMemcpyToSymbol(g_wait_timeouts_tc, &zero, sizeof(unsigned int));
 }
 
-int num_sms_tc() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 152;
-    return sms;
-}
 
 }  // namespace
 }  // namespace ddg
