@@ -79,13 +79,13 @@ struct TcSplitGrid {
     bool a_vec;     // A_hi, A_lo 16-byte aligned and lda even: 128-bit loads
 };
 
-// One warp per task, 256 elements each.  A task: 4 rows of A x one k-block
-// (lane = row (lane/8), 8 consecutive k (lane%8)): 512 contiguous bytes of hi
-// per row read, 512 contiguous bytes per part written.  B task: 32 columns of
-// B x 8 consecutive k (lane = column): each load instruction reads 256
-// contiguous bytes of a row of B; each lane writes one 16-byte chunk of its
-// part rows (the 8 tasks of a k-block complete the 128-byte rows in L2).
-// Rows / k beyond the matrix are written as 0.
+// One warp per task, 256 elements each: 4 rows of A, or 4 columns of B, x
+// one k-block (lane = row or column (lane/8), 8 consecutive k (lane%8)).  An
+// A lane reads 64 contiguous bytes of hi and of lo; for B each load
+// instruction reads eight whole 32-byte sectors (4 columns of 8 rows of B).
+// Each lane writes one 16-byte chunk of each part, so a warp writes whole
+// 128-byte part rows: 512 contiguous bytes per part.  Rows / k beyond the
+// matrix are written as 0.
 __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -137,16 +137,17 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
                 *reinterpret_cast<uint4*>(blk + swizzled(rin, kc)) = make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
             }
         } else {
-            // B task: 32 columns x 8 k (one 16-byte chunk of every part row)
+            // B task: 4 columns x one k-block (lane = column (lane/8), 8
+            // consecutive k (lane%8)), consecutive tasks on neighbouring columns
             const int64_t local = task - g.a_tasks;
-            const int64_t cg = local / (g.KB * 8), kq = local % (g.KB * 8);
-            const int64_t kb = kq >> 3;
-            const int kc = (int)(kq & 7);
-            const int64_t n = cg * 32 + lane;
+            const int64_t groups = g.b_tasks / g.KB;
+            const int64_t kb = local / groups, cg = local % groups;
+            const int64_t n = cg * 4 + (lane >> 3);
+            const int kc = lane & 7;
             int ep = 1;
             if (n < g.N) {
                 const int32_t fr = g.f[n];
-                if (kq == 0 && fr == EXP_NONE) g.f[n] = 0;
+                if (kb == 0 && kc == 0 && fr == EXP_NONE) g.f[n] = 0;
                 ep = effective_exponent(fr) + 1;
             }
             const int64_t k0 = kb * TBK + kc * 8;
@@ -181,6 +182,61 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
 // Step 3: exact sum of the parts and one rounding into a double double.
 // ---------------------------------------------------------------------------
 
+// Bits [75, 128) of a 128-bit magnitude normalised to bit 127, rounded to
+// nearest (ties to even) into a double with leading-bit exponent E; the
+// tail below the kept bits, or 2^75 minus it after rounding up, goes to rem.
+__device__ __forceinline__ uint64_t round_top53(wide::u128 nrm, int E, uint64_t sign, wide::u128& rem, bool& up) {
+    const uint64_t H = (uint64_t)(nrm >> 64), L = (uint64_t)nrm;
+    const uint64_t keep = H >> 11;
+    const bool rbit = (H >> 10) & 1;
+    up = rbit && ((keep & 1) || (H & 0x3FF) != 0 || L != 0);
+    const wide::u128 tail = nrm & ((((wide::u128)1) << 75) - 1);
+    rem = up ? (((wide::u128)1) << 75) - tail : tail;
+    // keep + up lies in [2^52, 2^53]: adding it to the biased exponent field
+    // minus one carries into the exponent when it reaches 2^53
+    return (sign << 63) | (((uint64_t)(E + 1022) << 52) + keep + (up ? 1 : 0));
+}
+
+__device__ __forceinline__ int msb128(wide::u128 m) {
+    const uint64_t hi = (uint64_t)(m >> 64), lo = (uint64_t)m;
+    return hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)lo);
+}
+
+// One k-split: |v_d| <= (d + 1) K 2^14 with 13 K 2^14 < 2^31, so the exact sum
+// Z = sum_d v_d 256^(12 - d) is below 2^124 in magnitude (below 2^127 for any
+// int32 v_d with |v_0| <= 2^30) and is formed in 128 bits from four groups (v_0; v_1..v_4; v_5..v_8; v_9..v_12: each group below
+// 2^56).  Z 2^q rounded into (hi, lo) when both are normal doubles or zero
+// (q >= -1022 and the leading bit of Z 2^q at most 2^1022); otherwise false.
+__device__ __forceinline__ bool round_dd_one_split(const long long (&v)[TS], int q, double& hi, double& lo) {
+    const long long g1 = ((v[1] * 256 + v[2]) * 256 + v[3]) * 256 + v[4];
+    const long long g2 = ((v[5] * 256 + v[6]) * 256 + v[7]) * 256 + v[8];
+    const long long g3 = ((v[9] * 256 + v[10]) * 256 + v[11]) * 256 + v[12];
+    const wide::u128 Z = ((wide::u128)(__int128)v[0] << 96) + ((wide::u128)(__int128)g1 << 64) +
+                         ((wide::u128)(__int128)g2 << 32) + (wide::u128)(__int128)g3;
+    const uint64_t sign = (uint64_t)(Z >> 127);
+    const wide::u128 M = sign ? (wide::u128)0 - Z : Z;
+    if (M == 0) {
+        hi = lo = 0.0;
+        return true;
+    }
+    const int t = msb128(M);
+    if (q < -1022 || t + q > 1022) return false;
+    const int n = 127 - t;
+    wide::u128 R;
+    bool up;
+    hi = __longlong_as_double((long long)round_top53(M << n, t + q, sign, R, up));
+    if (R == 0) {
+        lo = 0.0;
+        return true;
+    }
+    // R is a multiple of 2^n below 2^75: its leading bit is at t1 >= n
+    const int t1 = msb128(R);
+    wide::u128 R2;
+    bool up2;
+    lo = __longlong_as_double((long long)round_top53(R << (127 - t1), t1 - n + q, sign ^ (up ? 1 : 0), R2, up2));
+    return true;
+}
+
 __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
                                                            int64_t Np, const int32_t* __restrict__ e,
                                                            const int32_t* __restrict__ f, int64_t M, int64_t N,
@@ -200,6 +256,14 @@ __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __rest
             for (int d = 0; d < TS; ++d) v[d] += __ldg(p + ((int64_t)zz * TS + d) * plane);
         }
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (TS + 1);
+        if (splits == 1 && v[0] >= -(1LL << 30) && v[0] < (1LL << 30)) {  // always, for sums of the GEMM
+            double h, l;
+            if (round_dd_one_split(v, q, h, l)) {
+                C_hi[i * ldc + j] = h;
+                C_lo[i * ldc + j] = l;
+                continue;
+            }
+        }
         uint64_t z[3];
         xr::exact_sum<TS, 3>(v, z);
         double out[2];
@@ -366,7 +430,7 @@ cudaError_t launch_split_bf16(const SplitOperand* A, const SplitOperand* B, int6
     }
     if (B) {
         g.B_hi = B->hi; g.B_lo = B->lo; g.ldb = B->ld; g.N = B->rows; g.f = B->exp;
-        g.b_tasks = (round_up(B->rows, TBN) / 32) * g.KB * 8;
+        g.b_tasks = (round_up(B->rows, TBN) / 4) * g.KB;
     }
     g.planesA = planesA;
     g.planesB = planesB;

@@ -98,6 +98,56 @@ def test_recombine_tc_bit_exact(M, N, K, dist):
     assert np.array_equal(host(C_lo).view(np.int64), R_lo.view(np.int64))
 
 
+
+def _digits_of_sum(Z):
+    """13 part sums whose exact sum sum_d v_d 256^(12-d) is Z (v_0 = the bits
+    above 96, base-256 digits below; all negated for a negative Z)."""
+    s, a = (-1, -Z) if Z < 0 else (1, Z)
+    v = [(a >> (8 * (12 - d))) & 0xFF for d in range(1, 13)]
+    return [s * (a >> 96)] + [s * x for x in v]
+
+
+def test_recombine_tc_rounding_cases():
+    """Crafted part sums of one k-split against the oracle's rounding: ties of
+    the leading and the trailing double (to even, either way), carries to the
+    next power of two, exact small values, zero, both signs, the size limit of
+    the 128-bit path (|v_0| = 2^30) and scales at the ends of the normal range;
+    then random int32 part sums with one and two k-splits."""
+    crafted = [
+        (2**53 + 1) * 2**60 + 2**59,        # tie, odd: up
+        2**53 * 2**60 + 2**59,              # tie, even: down
+        (2**53 + 1) * 2**60 + 2**59 + 1,    # just above the tie
+        2**120 + (2**53 + 1) * 8 + 4,       # exact leading double, tie in the trailing one
+        2**120 + 2**53 * 8 + 4,
+        2**124 - 1,                         # rounds up to 2^124, trailing -1
+        12345, 1, 0,
+        (2**30 - 1) * 2**96 + 2**95 + 12345,
+        2**30 * 2**96 + 2**77 + 3,          # v_0 = 2^30: outside the 128-bit path
+        -(2**30) * 2**96 - 2**70 - 1,       # v_0 = -2^30 (inside) ...
+        -(2**30 + 1) * 2**96 + 5,           # ... and -2^30 - 1 (outside)
+    ]
+    crafted += [-z for z in crafted if z]
+    rng = np.random.default_rng(21)
+    E = [0, -912, -913, 700, 1000, 1010, -1000]  # q = e + f - 110: -1022 and -1023 at f = 0
+    M, Nc, Nr = len(E), len(crafted), 200
+    N = Nc + Nr
+    Mp, Np = pad(M, ddg.TC_TILE_M), pad(N, ddg.TC_TILE_N)
+    e = np.array(E, dtype=np.int32)
+    f = np.concatenate([np.zeros(Nc), rng.integers(-6, 7, Nr)]).astype(np.int32)
+    for splits in (1, 2):
+        P = np.zeros((splits, sb.S, Mp, Np), dtype=np.int32)
+        for c, Z in enumerate(crafted):
+            P[0, :, :M, c] = np.array(_digits_of_sum(Z), dtype=np.int64)[:, None]
+        lim = np.iinfo(np.int32)
+        P[:, :, :M, Nc:N] = rng.integers(lim.min, lim.max, (splits, sb.S, M, Nr), endpoint=True)
+        half = Nc + Nr // 2                 # half of the random columns inside the 128-bit path
+        P[:, 0, :M, Nc:half] = rng.integers(-2**30 // splits, 2**30 // splits, (splits, M, half - Nc))
+        C_hi, C_lo = ddg.recombine_tc(M, N, dev(P), dev(e), dev(f))
+        R_hi, R_lo = sb.recombine(P.astype(np.int64).sum(axis=0)[:, :M, :N], e + 1, f + 1)
+        assert np.array_equal(host(C_hi).view(np.int64), R_hi.view(np.int64)), splits
+        assert np.array_equal(host(C_lo).view(np.int64), R_lo.view(np.int64)), splits
+    assert ddg.wait_timeouts() == 0
+
 @pytest.mark.parametrize("M,N,K,dist", SHAPES)
 def test_dd_gemm_tc_matches_model_and_bound(M, N, K, dist):
     A_hi, A_lo, B_hi, B_lo = workloads.make_dd(M, N, K, dist, 11)
