@@ -237,46 +237,90 @@ __device__ __forceinline__ bool round_dd_one_split(const long long (&v)[TS], int
     return true;
 }
 
+// (hi, lo) of one output from its part sums (summed over the k-splits).
+__device__ __forceinline__ void recombine_one(const long long (&v)[TS], bool one_split, int q, double& hi,
+                                              double& lo) {
+    // the 128-bit path: always taken for the sums of one k-split of the GEMM
+    if (one_split && v[0] >= -(1LL << 30) && v[0] < (1LL << 30) && round_dd_one_split(v, q, hi, lo)) return;
+    uint64_t z[3];
+    xr::exact_sum<TS, 3>(v, z);
+    double out[2];
+    if (xr::fast_path_ok(z, q)) {
+        xr::round_parts<3, 2>(z, q, out);
+    } else {
+        wide::U256 Z;
+        Z.lo = ((wide::u128)z[1] << 64) | z[0];
+        Z.hi = (wide::u128)(__int128)(int64_t)z[2];
+        wide::round_into_doubles<2>(Z, q, out);
+    }
+    hi = out[0];
+    lo = out[1];
+}
+
+// V consecutive outputs of a row per thread (V = 4: 16-byte loads of every
+// part plane; vec_store: 16-byte stores of C when aligned).
+template <int V>
 __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
                                                            int64_t Np, const int32_t* __restrict__ e,
                                                            const int32_t* __restrict__ f, int64_t M, int64_t N,
                                                            double* __restrict__ C_hi, double* __restrict__ C_lo,
-                                                           int64_t ldc) {
-    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= N) return;
+                                                           int64_t ldc, bool vec_store) {
+    const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * V;
+    if (j0 >= N) return;
     const int64_t plane = Mp * Np;
-    const int fj = effective_exponent(f[j]) + 1;
+    int fj[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) fj[c] = j0 + c < N ? effective_exponent(f[j0 + c]) + 1 : 0;
     for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
-        long long v[TS];
-        const int32_t* p = P + i * Np + j;
+        const int32_t* p = P + i * Np + j0;
+        const int qi = effective_exponent(e[i]) + 1 - TD * (TS + 1);
+        double h[V], l[V];
+        if (splits == 1) {
+            int32_t w[TS][V];
 #pragma unroll
-        for (int d = 0; d < TS; ++d) v[d] = __ldg(p + (int64_t)d * plane);
-        for (int zz = 1; zz < splits; ++zz) {
+            for (int d = 0; d < TS; ++d) {
+                if constexpr (V == 4) {
+                    const int4 x = __ldg(reinterpret_cast<const int4*>(p + (int64_t)d * plane));
+                    w[d][0] = x.x; w[d][1] = x.y; w[d][2] = x.z; w[d][3] = x.w;
+                } else {
+                    w[d][0] = __ldg(p + (int64_t)d * plane);
+                }
+            }
 #pragma unroll
-            for (int d = 0; d < TS; ++d) v[d] += __ldg(p + ((int64_t)zz * TS + d) * plane);
-        }
-        const int q = effective_exponent(e[i]) + 1 + fj - TD * (TS + 1);
-        if (splits == 1 && v[0] >= -(1LL << 30) && v[0] < (1LL << 30)) {  // always, for sums of the GEMM
-            double h, l;
-            if (round_dd_one_split(v, q, h, l)) {
-                C_hi[i * ldc + j] = h;
-                C_lo[i * ldc + j] = l;
-                continue;
+            for (int c = 0; c < V; ++c) {
+                long long v[TS];
+#pragma unroll
+                for (int d = 0; d < TS; ++d) v[d] = w[d][c];
+                recombine_one(v, true, qi + fj[c], h[c], l[c]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < V; ++c) {
+                long long v[TS];
+#pragma unroll
+                for (int d = 0; d < TS; ++d) v[d] = 0;
+                for (int zz = 0; zz < splits; ++zz) {
+#pragma unroll
+                    for (int d = 0; d < TS; ++d) v[d] += __ldg(p + c + ((int64_t)zz * TS + d) * plane);
+                }
+                recombine_one(v, false, qi + fj[c], h[c], l[c]);
             }
         }
-        uint64_t z[3];
-        xr::exact_sum<TS, 3>(v, z);
-        double out[2];
-        if (xr::fast_path_ok(z, q)) {
-            xr::round_parts<3, 2>(z, q, out);
+        double* ch = C_hi + i * ldc + j0;
+        double* cl = C_lo + i * ldc + j0;
+        if (V == 4 && vec_store && j0 + 3 < N) {
+            reinterpret_cast<double2*>(ch)[0] = make_double2(h[0], h[1]);
+            reinterpret_cast<double2*>(ch)[1] = make_double2(h[2], h[3]);
+            reinterpret_cast<double2*>(cl)[0] = make_double2(l[0], l[1]);
+            reinterpret_cast<double2*>(cl)[1] = make_double2(l[2], l[3]);
         } else {
-            wide::U256 Z;
-            Z.lo = ((wide::u128)z[1] << 64) | z[0];
-            Z.hi = (wide::u128)(__int128)(int64_t)z[2];
-            wide::round_into_doubles<2>(Z, q, out);
+#pragma unroll
+            for (int c = 0; c < V; ++c)
+                if (j0 + c < N) {
+                    ch[c] = h[c];
+                    cl[c] = l[c];
+                }
         }
-        C_hi[i * ldc + j] = out[0];
-        C_lo[i * ldc + j] = out[1];
     }
 }
 
@@ -319,10 +363,10 @@ __device__ __forceinline__ uint32_t qd_part(const uint32_t (&y)[8], int s) {
     return __float_as_uint(__fsub_rn(__uint_as_float(bits), 8388736.0f));
 }
 
-// One warp per task of 256 elements, as for double doubles: an A task is 4 rows
-// x 64 k (lane = row (lane/8), 8 consecutive k (lane%8)), a B task 32 columns
-// x 8 k (lane = column).  Each lane forms Y for its 8 elements, then writes one
-// 16-byte chunk of each of the 27 part rows.
+// One warp per task of 256 elements, as for double doubles: 4 rows of A, or 4
+// columns of B, x 64 k (lane = row or column (lane/8), 8 consecutive k
+// (lane%8)).  Each lane forms Y for its 8 elements, then writes one 16-byte
+// chunk of each of the 27 part rows (a warp writes whole 128-byte rows).
 __global__ void __launch_bounds__(256) split_bf16_qd_kernel(TcQdSplitGrid g) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -337,11 +381,12 @@ __global__ void __launch_bounds__(256) split_bf16_qd_kernel(TcQdSplitGrid g) {
             r = (task / g.KB) * 4 + (lane >> 3);
             kc = lane & 7;
         } else {
+            // 4 columns x one k-block, consecutive tasks on neighbouring columns
             const int64_t local = task - g.a_tasks;
-            const int64_t kq = local % (g.KB * 8);
-            kb = kq >> 3;
-            kc = (int)(kq & 7);
-            r = (local / (g.KB * 8)) * 32 + lane;
+            const int64_t groups = g.b_tasks / g.KB;
+            kb = local / groups;
+            r = (local % groups) * 4 + (lane >> 3);
+            kc = lane & 7;
         }
         const int64_t rows = is_a ? g.M : g.N;
         int ep = 1;
@@ -457,7 +502,17 @@ cudaError_t launch_recombine_tc(const int32_t* P, int splits, int64_t Mp, int64_
     if (M == 0 || N == 0) return cudaSuccess;
     const unsigned gx = (unsigned)((N + 255) / 256);
     const unsigned gy = (unsigned)(M < 65535 ? M : 65535);
-    recombine_tc_kernel<<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc);
+    const bool vec_store = (uintptr_t)C_hi % 16 == 0 && (uintptr_t)C_lo % 16 == 0 && ldc % 2 == 0;
+    // one k-split with aligned part sums: 4 columns per thread (the rows of the
+    // planes are multiples of 256 columns, so every 4-column group is aligned)
+    if (splits == 1 && (uintptr_t)P % 16 == 0) {
+        const unsigned gx4 = (unsigned)((N + 1023) / 1024);
+        recombine_tc_kernel<4><<<dim3(gx4, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc,
+                                                                vec_store);
+    } else {
+        recombine_tc_kernel<1><<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc,
+                                                               false);
+    }
     return cudaGetLastError();
 }
 
@@ -476,7 +531,7 @@ cudaError_t launch_split_bf16_qd(const double* const* A, int64_t lda, int64_t M,
     if (B && N > 0) {
         for (int q = 0; q < 4; ++q) g.B[q] = B[q];
         g.ldb = ldb; g.N = N; g.f = f;
-        g.b_tasks = (round_up(N, TBN) / 32) * g.KB * 8;
+        g.b_tasks = (round_up(N, TBN) / 4) * g.KB;
     }
     g.planesA = planesA;
     g.planesB = planesB;

@@ -174,10 +174,10 @@ __device__ __forceinline__ uint32_t md_part(const uint64_t (&y)[W], int s) {
     return __float_as_uint(__fsub_rn(__uint_as_float(0x4B000000u | E), 8388736.0f));
 }
 
-// One warp per task of 256 elements (A: 4 rows x 64 k, lane = row (lane/8),
-// 8 consecutive k (lane%8); B: 32 columns x 8 k, lane = column), as for the
-// other bf16 variants; each lane forms Y for its 8 elements, then writes one
-// 16-byte chunk of each of the NP part rows.
+// One warp per task of 256 elements (4 rows of A, or 4 columns of B, x 64 k;
+// lane = row or column (lane/8), 8 consecutive k (lane%8)), as for the other
+// bf16 variants; each lane forms Y for its 8 elements, then writes one 16-byte
+// chunk of each of the NP part rows (a warp writes whole 128-byte rows).
 template <int NIN>
 __global__ void __launch_bounds__(256) split_bf16_md_kernel(TcMdSplitGrid g) {
     constexpr int NP = MdShape<NIN>::NP, W = MdShape<NIN>::WX;
@@ -194,11 +194,12 @@ __global__ void __launch_bounds__(256) split_bf16_md_kernel(TcMdSplitGrid g) {
             r = (task / g.KB) * 4 + (lane >> 3);
             kc = lane & 7;
         } else {
+            // 4 columns x one k-block, consecutive tasks on neighbouring columns
             const int64_t local = task - g.a_tasks;
-            const int64_t kq = local % (g.KB * 8);
-            kb = kq >> 3;
-            kc = (int)(kq & 7);
-            r = (local / (g.KB * 8)) * 32 + lane;
+            const int64_t groups = g.b_tasks / g.KB;
+            kb = local / groups;
+            r = (local % groups) * 4 + (lane >> 3);
+            kc = lane & 7;
         }
         const int64_t rows = is_a ? g.M : g.N;
         int ep = 1;
@@ -318,7 +319,7 @@ cudaError_t split_md(const double* const* A, int64_t lda, int64_t M, int32_t* e,
     if (B && N > 0) {
         for (int q = 0; q < NIN; ++q) g.B[q] = B[q];
         g.ldb = ldb; g.N = N; g.f = f;
-        g.b_tasks = (round_up(N, TBN) / 32) * g.KB * 8;
+        g.b_tasks = (round_up(N, TBN) / 4) * g.KB;
     }
     g.planesA = planesA;
     g.planesB = planesB;

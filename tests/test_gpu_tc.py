@@ -142,10 +142,17 @@ def test_recombine_tc_rounding_cases():
         P[:, :, :M, Nc:N] = rng.integers(lim.min, lim.max, (splits, sb.S, M, Nr), endpoint=True)
         half = Nc + Nr // 2                 # half of the random columns inside the 128-bit path
         P[:, 0, :M, Nc:half] = rng.integers(-2**30 // splits, 2**30 // splits, (splits, M, half - Nc))
-        C_hi, C_lo = ddg.recombine_tc(M, N, dev(P), dev(e), dev(f))
         R_hi, R_lo = sb.recombine(P.astype(np.int64).sum(axis=0)[:, :M, :N], e + 1, f + 1)
+        C_hi, C_lo = ddg.recombine_tc(M, N, dev(P), dev(e), dev(f))
         assert np.array_equal(host(C_hi).view(np.int64), R_hi.view(np.int64)), splits
         assert np.array_equal(host(C_lo).view(np.int64), R_lo.view(np.int64)), splits
+        # part sums 4 bytes off a 16-byte boundary, C with an odd leading dimension
+        flat = dev(np.concatenate([np.zeros(1, np.int32), P.ravel()]))
+        Pm = flat[1:].view(P.shape)
+        Wh, Wl = dev(np.zeros((M, N + 1))), dev(np.zeros((M, N + 1)))
+        ddg.recombine_tc(M, N, Pm, dev(e), dev(f), None, Wh[:, :N], Wl[:, :N])
+        assert np.array_equal(host(Wh)[:, :N].view(np.int64), R_hi.view(np.int64)), splits
+        assert np.array_equal(host(Wl)[:, :N].view(np.int64), R_lo.view(np.int64)), splits
     assert ddg.wait_timeouts() == 0
 
 @pytest.mark.parametrize("M,N,K,dist", SHAPES)
