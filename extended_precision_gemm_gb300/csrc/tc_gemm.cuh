@@ -6,7 +6,10 @@
 // own count of bounded waits that gave up).
 #pragma once
 
+#include <cuda.h>
+
 #include <algorithm>
+#include <cstring>
 
 #include "async_copy.cuh"
 #include "common.cuh"
@@ -67,17 +70,16 @@ __device__ __forceinline__ uint32_t pack_bf16(uint32_t f_first, uint32_t f_secon
 // Step 2: P_d on the tensor cores.  Persistent clusters of two CTAs (a CTA
 // pair on two SMs, as many pairs as can be resident) share out the units of
 // work (a diagonal d of a 256 x 256 output block and k-split: d + 1 pairs);
-// the pair's MMAs are M = 256,
-// N = 256, K = 16 (tcgen05 cta_group::2): each CTA holds its 128 rows of A and
-// its 128 rows of B (columns of C) for a k-block, and its 128 rows of the
-// accumulators.  10 warps per CTA:
-//   warp 0 (one thread): bulk copies of this CTA's part halves into a 3-stage
-//           ring (64 KB per stage: two 64-k blocks of one pair (s, t));
+// the pair's MMAs are M = 256, N = 256, K = 16 (tcgen05 cta_group::2): each
+// CTA holds its 128 rows of A and its 128 rows of B (columns of C) for a
+// k-block, and its 128 rows of the accumulators.  10 warps per CTA:
+//   warp 0 (one thread): tensor copies of this CTA's part halves into a
+//           3-stage ring (64 KB per stage: two 64-k blocks of one pair
+//           (s, t)); the copies of both CTAs complete on the even CTA's
+//           barrier of the stage (cta_group::2 copies);
 //   warp 1: allocates 512 TMEM columns in both CTAs (two f32 accumulators of
 //           128 x 256 per CTA); in the even CTA one thread issues the MMAs (4
-//           per 64-k block) once both CTAs' stage is full; in the odd CTA one
-//           thread forwards the completion of each of its stages to the even
-//           CTA;
+//           per 64-k block) once the stage is full in both CTAs;
 //   warps 2-9: read each finished chunk from TMEM (warp w reads lanes
 //           32 (w % 4) .. +31, i.e. rows, and one half of the columns), add it
 //           into int32 totals in registers, and store the totals of P_d.
@@ -85,14 +87,12 @@ __device__ __forceinline__ uint32_t pack_bf16(uint32_t f_first, uint32_t f_secon
 // chunk is 8 consecutive k-blocks of one unit (512 products per output; the
 // last chunk of a unit may be shorter).  Chunks alternate between the two
 // accumulators, also across units, so the MMAs of one chunk overlap the
-// read-out of the previous one and the store of a finished unit.  Completion of MMAs
-// reaches both CTAs through multicast commits; the release of an
+// read-out of the previous one and the store of a finished unit.  Completion
+// of MMAs reaches both CTAs through multicast commits; the release of an
 // accumulator needs all 16 epilogue warps of the pair.
 // ---------------------------------------------------------------------------
 
 struct TcGemmArgs {
-    const uint16_t* planesA;
-    const uint16_t* planesB;
     int32_t* P;       // [split][d][Mp][Np]
     int64_t Mp, Np;
     int64_t KB;       // k-blocks in the planes
@@ -148,9 +148,10 @@ __device__ __forceinline__ void note_timeout(volatile int* abort_flag) {
 
 template <int NP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
-    slice_gemm_tc_kernel(TcGemmArgs g) {
+    slice_gemm_tc_kernel(const __grid_constant__ TcGemmArgs g, const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[3 * STAGES + 4 + 1];
+    __shared__ __align__(8) uint64_t bars[2 * STAGES + 4 + 1];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -163,15 +164,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const int64_t pair = blockIdx.x >> 1;
 
     const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[STAGES]);
-    const uint32_t pfull0 = smem_addr(&bars[2 * STAGES]);
-    const uint32_t accf0 = smem_addr(&bars[3 * STAGES]), acce0 = smem_addr(&bars[3 * STAGES + 2]);
-    const uint32_t done_bar = smem_addr(&bars[3 * STAGES + 4]);
+    const uint32_t accf0 = smem_addr(&bars[2 * STAGES]), acce0 = smem_addr(&bars[2 * STAGES + 2]);
+    const uint32_t done_bar = smem_addr(&bars[2 * STAGES + 4]);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
-            mbar_init(pfull0 + 8 * i, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
@@ -193,6 +192,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---- producer (both CTAs): a stage holds up to two k-blocks of one pair ----
+            // The copies of both CTAs complete on the even CTA's full barrier
+            // (tensor copies with cta_group::2), which expects the bytes of both.
+            const uint32_t full_lead0 = cluster_addr(full0, 0);
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             for (int64_t r = 0, u; (u = unit_index(g, pair, r)) < g.units && !abort_flag; ++r) {
@@ -202,9 +204,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 const int64_t nkb = w.nkb;
                 for (int s = 0; s <= d && !abort_flag; ++s) {
                     const int t = d - s;
-                    const uint16_t* a_src = g.planesA + ((a_block * NP + s) * g.KB + w.kb0) * (TBM * TBK);
-                    const uint16_t* b_src =
-                        g.planesB + ((w.nt * NP + t) * g.KB + w.kb0) * (TBN * TBK) + rank * (TBN / 2) * TBK;
+                    // first 128-byte row of the k-blocks in the tensors of part rows
+                    const int a_row = (int)(((a_block * NP + s) * g.KB + w.kb0) * TBM);
+                    const int b_row = (int)(((w.nt * NP + t) * g.KB + w.kb0) * TBN + rank * (TBN / 2));
                     for (int64_t kb = 0; kb < nkb; kb += STAGE_BLOCKS) {
                         const int nb = (int)min((int64_t)STAGE_BLOCKS, nkb - kb);
                         if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1, WAIT_NS)) {
@@ -212,20 +214,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                             break;
                         }
                         uint8_t* dst = smem + stage * STAGE_BYTES;
-                        mbar_expect_tx(full0 + 8 * stage, (uint32_t)nb * (A_BLOCK_BYTES + B_HALF_BYTES));
-                        // consecutive k-blocks of A are contiguous; B's halves are not
-                        bulk_load(dst, a_src + kb * (TBM * TBK), (uint32_t)nb * A_BLOCK_BYTES, full0 + 8 * stage);
-                        for (int j = 0; j < nb; ++j)
-                            bulk_load(dst + STAGE_BLOCKS * A_BLOCK_BYTES + j * B_HALF_BYTES,
-                                      b_src + (kb + j) * (TBN * TBK), B_HALF_BYTES, full0 + 8 * stage);
+                        if (leader)
+                            mbar_expect_tx(full0 + 8 * stage, 2u * (uint32_t)nb * (A_BLOCK_BYTES + B_HALF_BYTES));
+                        const uint32_t bar = full_lead0 + 8 * stage;
+                        for (int j = 0; j < nb; ++j) {
+                            tma_load_2d_pair(dst + j * A_BLOCK_BYTES, &tmA, 0, a_row + (int)(kb + j) * TBM, bar);
+                            tma_load_2d_pair(dst + STAGE_BLOCKS * A_BLOCK_BYTES + j * B_HALF_BYTES, &tmB, 0,
+                                             b_row + (int)(kb + j) * TBN, bar);
+                        }
                         ++issued;
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
                 }
             }
-            // copies still in flight must land before the CTA exits
+            // copies still in flight (of both CTAs) must land before either
+            // CTA exits: the even CTA waits for its last stages to fill
             const int64_t first = issued > STAGES ? issued - STAGES : 0;
-            for (int64_t j = first; j < issued; ++j)
+            for (int64_t j = first; leader && j < issued; ++j)
                 if (!mbar_wait_bounded(full0 + 8 * (uint32_t)(j % STAGES), (uint32_t)((j / STAGES) & 1), WAIT_NS))
                     note_timeout(&abort_flag);
         }
@@ -251,8 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 for (int s = 0; s <= d && ok; ++s) {
                     for (int kb = 0; kb < nkb32; kb += STAGE_BLOCKS) {
                         const int nb = min(STAGE_BLOCKS, nkb32 - kb);
-                        if (!mbar_wait_bounded(full0 + 8 * stage, phase, WAIT_NS) ||
-                            !mbar_wait_bounded(pfull0 + 8 * stage, phase, WAIT_NS)) {
+                        if (!mbar_wait_bounded(full0 + 8 * stage, phase, WAIT_NS)) {  // both CTAs' copies
                             if (!abort_flag) note_timeout(&abort_flag);
                             ok = false;
                             break;
@@ -299,20 +303,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 if (!mbar_wait_bounded(done_bar, 0, WAIT_NS)) note_timeout(&abort_flag);
             }
         } else if (lane == 0) {
-            // ---- forwarder (odd CTA): its stage s is full -> tell the even CTA ----
-            uint32_t stage = 0, phase = 0;
-            int64_t total = 0;  // stages the producer fills for this pair's units
+            // ---- odd CTA: nothing to issue ----
+            int64_t total = 0;  // stages the producers fill for this pair's units
             for (int64_t r = 0, u; (u = unit_index(g, pair, r)) < g.units; ++r) {
                 const Unit w = unit_of(g, u, NP);
                 total += (int64_t)(w.d + 1) * ((w.nkb + STAGE_BLOCKS - 1) / STAGE_BLOCKS);
-            }
-            for (int64_t j = 0; j < total; ++j) {
-                if (abort_flag || !mbar_wait_bounded(full0 + 8 * stage, phase, WAIT_NS)) {
-                    if (!abort_flag) note_timeout(&abort_flag);
-                    break;
-                }
-                mbar_arrive_remote(pfull0 + 8 * stage, 0);
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
             // the even CTA's MMAs read this CTA's shared memory and write its
             // tensor memory: wait until they have all finished (a pair whose
@@ -410,6 +405,42 @@ int resident_pairs() {
     return cached;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        else
+            (void)cudaGetLastError();
+    }
+    return fn;
+}
+
+// The part blocks of one operand as a 2-D tensor of `rows` rows of 64 bf16
+// (128 bytes), copied in boxes of 128 rows.  The blocks are already swizzled
+// in memory, so the copies move bytes unchanged (no swizzle in the map).
+cudaError_t make_part_map(CUtensorMap* m, const uint16_t* planes, int64_t rows) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return cudaErrorNotSupported;
+    if (rows <= 0 || rows >= (1LL << 31) || (uintptr_t)planes % 16 != 0) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {(cuuint64_t)TBK, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)TBK * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)TBK, (cuuint32_t)TBM};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(planes), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int NP>
 cudaError_t launch_slice_gemm_parts(const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
                                            int64_t Kp, int splits, int32_t* P, cudaStream_t st) {
@@ -420,8 +451,6 @@ cudaError_t launch_slice_gemm_parts(const uint16_t* planesA, const uint16_t* pla
         cudaFuncSetAttribute(slice_gemm_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
     if (err != cudaSuccess) return err;
     TcGemmArgs g;
-    g.planesA = planesA;
-    g.planesB = planesB;
     g.P = P;
     g.Mp = Mp;
     g.Np = Np;
@@ -433,8 +462,16 @@ cudaError_t launch_slice_gemm_parts(const uint16_t* planesA, const uint16_t* pla
     g.units = (int64_t)g.MT * g.NT * splits * NP;
     // as many persistent CTA pairs as can be resident (never more than units)
     g.pairs = (int)std::max<int64_t>(1, std::min<int64_t>(resident_pairs<NP>(), g.units));
+    CUtensorMap tmA, tmB;  // with K = 0 no copy is issued: the maps stay unused
+    memset(&tmA, 0, sizeof(tmA));
+    memset(&tmB, 0, sizeof(tmB));
+    if (g.KB > 0) {
+        err = make_part_map(&tmA, planesA, (Mp / TBM) * NP * g.KB * TBM);
+        if (err == cudaSuccess) err = make_part_map(&tmB, planesB, (Np / TBN) * NP * g.KB * TBN);
+        if (err != cudaSuccess) return err;
+    }
     dim3 grid((unsigned)(2 * g.pairs), 1);  // clusters of 2 along x
-    slice_gemm_tc_kernel<NP><<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(g);
+    slice_gemm_tc_kernel<NP><<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(g, tmA, tmB);
     return cudaGetLastError();
 }
 
