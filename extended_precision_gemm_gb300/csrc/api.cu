@@ -751,10 +751,21 @@ TcLayout make_tc_layout(int64_t M, int64_t N, int64_t K, int parts = kTcParts) {
     return L;
 }
 
+// The tensor copies of the slice GEMM address the part blocks of an operand as
+// rows of 128 bytes with 32-bit coordinates: Mp (or Np) x parts x Kp/64 rows
+// must stay below 2^31 (2^31 rows are 256 GiB of parts, more than the device
+// holds, so this never binds in practice).
+bool tc_part_rows_ok(int64_t M, int64_t N, int64_t K, int parts) {
+    const int64_t kb = round_up(K, kTcK) / kTcK;
+    const int64_t lim = (1LL << 31) / std::max<int64_t>(1, (int64_t)parts * std::max<int64_t>(1, kb));
+    return round_up(M, kTcM) < lim && round_up(N, kTcN) < lim;
+}
+
 ddgemm_status check_tc_shapes(int64_t M, int64_t N, int64_t K) {
     if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
     if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
     if ((round_up(M, kTcM) / kTcM) * (round_up(N, kTcN) / kTcN) > kMaxTiles) return DDGEMM_ERR_UNSUPPORTED;
+    if (!tc_part_rows_ok(M, N, K, kTcParts)) return DDGEMM_ERR_UNSUPPORTED;
     return DDGEMM_OK;
 }
 
@@ -895,6 +906,7 @@ ddgemm_status check_tc_qd_args(int64_t M, int64_t N, int64_t K, const double* co
         return DDGEMM_ERR_INVALID_ARG;
     if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
     if ((round_up(M, kTcM) / kTcM) * (round_up(N, kTcN) / kTcN) > kMaxTiles) return DDGEMM_ERR_UNSUPPORTED;
+    if (!tc_part_rows_ok(M, N, K, kTcQdParts)) return DDGEMM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return DDGEMM_OK;
     if (A == nullptr || B == nullptr || C == nullptr) return DDGEMM_ERR_INVALID_ARG;
     const int64_t a = span_bytes(M, K, lda), b = span_bytes(K, N, ldb), c = span_bytes(M, N, ldc);
@@ -941,7 +953,7 @@ extern "C" {
 ddgemm_status qd_gemm_tc_layout(int64_t M, int64_t N, int64_t K, int64_t* Mp, int64_t* Np, int64_t* Kp,
                                 int* splits) {
     if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
-    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (K > QDGEMM_MAX_K || !tc_part_rows_ok(M, N, K, kTcQdParts)) return DDGEMM_ERR_UNSUPPORTED;
     TcLayout L = make_tc_layout(M, N, K, kTcQdParts);
     if (Mp) *Mp = L.Mp;
     if (Np) *Np = L.Np;
@@ -952,7 +964,7 @@ ddgemm_status qd_gemm_tc_layout(int64_t M, int64_t N, int64_t K, int64_t* Mp, in
 
 ddgemm_status qd_gemm_tc_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
     if (bytes == nullptr || M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
-    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (K > QDGEMM_MAX_K || !tc_part_rows_ok(M, N, K, kTcQdParts)) return DDGEMM_ERR_UNSUPPORTED;
     *bytes = (size_t)make_tc_layout(M, N, K, kTcQdParts).total;
     return DDGEMM_OK;
 }
@@ -1040,6 +1052,7 @@ ddgemm_status check_tc_md_args(int nparts, int64_t M, int64_t N, int64_t K, cons
         return DDGEMM_ERR_INVALID_ARG;
     if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
     if ((round_up(M, kTcM) / kTcM) * (round_up(N, kTcN) / kTcN) > kMaxTiles) return DDGEMM_ERR_UNSUPPORTED;
+    if (!tc_part_rows_ok(M, N, K, md_parts(nparts))) return DDGEMM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return DDGEMM_OK;
     if (A == nullptr || B == nullptr || C == nullptr) return DDGEMM_ERR_INVALID_ARG;
     const int64_t a = span_bytes(M, K, lda), b = span_bytes(K, N, ldb), c = span_bytes(M, N, ldc);
@@ -1088,7 +1101,7 @@ ddgemm_status md_gemm_tc_layout(int nparts, int64_t M, int64_t N, int64_t K, int
                                 int* splits) {
     if (md_parts(nparts) == 0) return DDGEMM_ERR_UNSUPPORTED;
     if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
-    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (K > QDGEMM_MAX_K || !tc_part_rows_ok(M, N, K, md_parts(nparts))) return DDGEMM_ERR_UNSUPPORTED;
     TcLayout L = make_tc_layout(M, N, K, md_parts(nparts));
     if (Mp) *Mp = L.Mp;
     if (Np) *Np = L.Np;
@@ -1100,7 +1113,7 @@ ddgemm_status md_gemm_tc_layout(int nparts, int64_t M, int64_t N, int64_t K, int
 ddgemm_status md_gemm_tc_workspace_size(int nparts, int64_t M, int64_t N, int64_t K, size_t* bytes) {
     if (md_parts(nparts) == 0) return DDGEMM_ERR_UNSUPPORTED;
     if (bytes == nullptr || M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
-    if (K > QDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if (K > QDGEMM_MAX_K || !tc_part_rows_ok(M, N, K, md_parts(nparts))) return DDGEMM_ERR_UNSUPPORTED;
     *bytes = (size_t)make_tc_layout(M, N, K, md_parts(nparts)).total;
     return DDGEMM_OK;
 }

@@ -378,7 +378,13 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
 /*
  * Padded extents (Mp = M rounded up to 256, Np = N rounded up to 256, Kp = K
  * rounded up to 64) and the k-split of the slice GEMM (every split covers at
- * most DDGEMM_TC_MAX_K_SPLIT of k).  Any output pointer may be NULL.
+ * most DDGEMM_TC_MAX_K_SPLIT of k; more splits only where they balance the
+ * persistent CTA pairs of the GEMM, e.g. for long K over few output blocks).
+ * Any output pointer may be NULL.  DDGEMM_ERR_UNSUPPORTED for K >
+ * DDGEMM_MAX_K, or when Mp (or Np) x parts x Kp / 64 reaches 2^31: the
+ * tensor copies address the part blocks as 128-byte rows with 32-bit
+ * coordinates (2^31 rows are 256 GiB of parts).  The same limits apply to the
+ * quad- and multiple-double variants below with their part counts.
  */
 ddgemm_status dd_gemm_tc_layout(int64_t M, int64_t N, int64_t K,
                                 int64_t* Mp, int64_t* Np, int64_t* Kp, int* splits);

@@ -93,3 +93,27 @@ def test_layout_padding(lib):
     # exponents + both plane sets + split P planes, each 256-byte aligned
     need = 256 + 256 + 8 * 64 * 16 * 8 + 8 * 32 * 16 * 8 + sp.value * 8 * 64 * 32 * 8
     assert n.value == need
+
+
+def test_tc_layouts_splits_and_limits(lib):
+    """k-splits of the tensor-core variants: enough for exact int32 part sums,
+    none empty; shapes whose part rows exceed 32-bit tensor coordinates are
+    refused before any launch."""
+    Mp, Np, Kp, sp = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int()
+    refs = [ctypes.byref(x) for x in (Mp, Np, Kp, sp)]
+    for M, N, K in [(4096, 4096, 4096), (256, 256, 65536), (1, 1, 1 << 20), (300, 5, 9000), (7, 7, 0)]:
+        assert lib.dd_gemm_tc_layout(M, N, K, *refs) == 0
+        KB = Kp.value // 64
+        need = -(-KB // (ddg.TC_MAX_K_SPLIT // 64)) if KB else 1
+        assert sp.value >= max(1, need)
+        if KB:
+            per = -(-KB // sp.value)
+            assert -(-KB // per) == sp.value                 # no empty split
+            assert per * 64 <= ddg.TC_MAX_K_SPLIT
+    assert lib.dd_gemm_tc_layout(4096, 4096, 4096, *refs) == 0 and sp.value == 1
+    # part rows: Mp x 13 x Kp/64 >= 2^31
+    assert lib.dd_gemm_tc_layout(1 << 20, 256, 1 << 24, *refs) == 2
+    assert lib.dd_gemm_tc_layout(256, 1 << 20, 1 << 24, *refs) == 2
+    assert lib.qd_gemm_tc_layout(1 << 20, 256, 1 << 23, *refs) == 2
+    assert lib.md_gemm_tc_layout(16, 1 << 16, 256, 1 << 20, *refs) == 2
+    assert lib.md_gemm_tc_layout(8, 4096, 4096, 4096, *refs) == 0
