@@ -17,9 +17,10 @@
 //     are stored as bf16 in blocks of 128 (A) or 256 (B) rows x 64 k, each
 //     block in the 128-byte swizzled K-major layout the tensor core reads;
 //  2. P_d = sum_{s+t=d} A_s B_t^T, d = 0..12 (91 pairs), on the tensor cores:
-//     each product is at most 2^14, so 512 of them sum to at most 2^23 and the
-//     f32 accumulator is exact; every 512 products per output ("a chunk") the
-//     accumulator is read from tensor memory and added into an exact int32
+//     each product is at most 2^14, so 1024 of them sum to at most 2^24, and
+//     every partial sum is an integer that f32 holds exactly; every 1024
+//     products per output ("a chunk") the accumulator is read from tensor
+//     memory and added into an exact int32
 //     total (|P_d| <= 13 K 2^14 < 2^31 for K <= 8192 per k-split);
 //  3. Z = sum_d P_d 2^(8 (12 - d)) exactly (256-bit), rounded once to the
 //     nearest double double of Z 2^(e'_i + f'_j - 112).

@@ -44,7 +44,7 @@ constexpr int STAGES = 3;
 constexpr int STAGE_BYTES = STAGE_BLOCKS * (A_BLOCK_BYTES + B_HALF_BYTES);  // 64 KB
 static_assert(PAIR_M == 2 * TBM, "a CTA pair covers two row blocks of A");
 constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024;  // + alignment slack
-constexpr int CHUNK_BLOCKS = 8;   // blocks of 64 k summed in f32 before a flush (512 products)
+constexpr int CHUNK_BLOCKS = 16;  // blocks of 64 k summed in f32 before a flush (1024 products)
 constexpr int UMMA_K = 16;        // k of one tcgen05.mma (kind::f16)
 constexpr int EPI_WARPS = 8;
 constexpr int GEMM_THREADS = 64 + EPI_WARPS * 32;  // producer warp, MMA warp, epilogue
@@ -53,7 +53,7 @@ constexpr uint32_t IDESC = tc5::idesc_bf16_f32(PAIR_M, TBN);  // pair MMA: M = 2
 constexpr unsigned long long WAIT_NS = 2000000000ULL;  // bounded waits: 2 s
 constexpr int TILE_GROUP = 8;     // row blocks per group in the tile order (L2 reuse)
 
-static_assert(CHUNK_BLOCKS * TBK * 128 * 128 <= (1 << 23), "a chunk's f32 sums stay within 2^23");
+static_assert(CHUNK_BLOCKS * TBK * 128 * 128 <= (1 << 24), "a chunk's f32 sums stay within 2^24");
 
 __device__ unsigned int g_wait_timeouts_tc = 0;
 
@@ -84,7 +84,7 @@ __device__ __forceinline__ uint32_t pack_bf16(uint32_t f_first, uint32_t f_secon
 //           32 (w % 4) .. +31, i.e. rows, and one half of the columns), add it
 //           into int32 totals in registers, and store the totals of P_d.
 // Within a unit the order of work is s = 0..d (t = d - s), then k-blocks; a
-// chunk is 8 consecutive k-blocks of one unit (512 products per output; the
+// chunk is 16 consecutive k-blocks of one unit (1024 products per output; the
 // last chunk of a unit may be shorter).  Chunks alternate between the two
 // accumulators, also across units, so the MMAs of one chunk overlap the
 // read-out of the previous one and the store of a finished unit.  Completion
@@ -341,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 for (int j = 0; j < 4; ++j) {
                     uint32_t v[32];
                     tc5::ld32(lane_base + buf * TBN + j * 32, v);
-                    // every chunk sum is an integer-valued f32 with |x| <= 2^23:
+                    // every chunk sum is an integer-valued f32 with |x| <= 2^24:
                     // the conversion is exact (one instruction each)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) acc[j * 32 + i] += __float2int_rz(__uint_as_float(v[i]));

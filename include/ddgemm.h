@@ -353,8 +353,9 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
  *     (least significant first, D = ((X + 128) mod 256) - 128, the top digit
  *     the rest): every part is an integer in [-128, 128], exact in bf16;
  *   - P_d = sum_{s+t=d} A_s B_t for d = 0..12 (91 pairs) with tcgen05.mma
- *     (bf16 in, f32 accumulators in tensor memory), exact: 512 products of at
- *     most 2^14 are summed in f32 and then added into exact int32 totals;
+ *     (bf16 in, f32 accumulators in tensor memory), exact: 1024 products of
+ *     at most 2^14 are summed in f32 (every partial sum an integer of at most
+ *     2^24) and then added into exact int32 totals;
  *   - Z = sum_d P_d 2^(8 (12 - d)) (exact) rounded once to the nearest double
  *     double of Z 2^(e'_i + f'_j - 112) (ties to even; zeros are +0).
  * Its result is not bit-identical to dd_gemm's (other parts, one rounding);

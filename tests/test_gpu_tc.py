@@ -236,9 +236,12 @@ def _extreme_element():
     return hi, lo
 
 
-def test_largest_parts_accumulate_exactly():
+@pytest.mark.parametrize("K", [512, 1024, 2048])
+def test_largest_parts_accumulate_exactly(K):
+    # with K = 1024 a chunk of one pair (s, t >= 1) sums 1024 products of
+    # 128 x 128: exactly 2^24 in the f32 accumulator
     hi, lo = _extreme_element()
-    M, N, K = 128, 256, 512
+    M, N = 128, 256
     A_hi, A_lo = np.full((M, K), hi), np.full((M, K), lo)
     B_hi, B_lo = np.full((K, N), hi), np.full((K, N), lo)
     assert sb.digits_of(hi, lo, 0) == [-127] + [-128] * 12
