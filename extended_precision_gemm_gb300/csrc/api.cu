@@ -16,7 +16,7 @@ namespace {
 
 constexpr int64_t kAlign = 256;
 constexpr int kMaxSplits = 64;
-constexpr int64_t kMaxTiles = 0x7FFFFFFF;  // grid.x of the slice GEMM
+constexpr int64_t kMaxTiles = 0x7FFFFFFF;  // output tiles (grid.x of the FP64 and integer slice GEMMs)
 
 struct Layout {
     int64_t Mp, Np, Kp, KC;
@@ -688,14 +688,13 @@ int64_t busiest_pair(int64_t tiles, int64_t s, int np, int64_t KB, int64_t pairs
 // the extra part sums cost.  Model (microseconds): a pair passes one k-block
 // of a 256 x 256 block (2 x 256 x 256 x 64 flops) in about 0.37 us, and each
 // k-split's int32 part sums are written and read back once at about 6 TB/s.
-int choose_tc_splits_uncached(int64_t Mp, int64_t Np, int64_t Kp, int parts) {
+int choose_tc_splits_uncached(int64_t Mp, int64_t Np, int64_t Kp, int parts, int64_t pairs) {
     const int64_t KB = Kp / kTcK;
     const int64_t tiles = (Mp / kTcM) * (Np / kTcN);
     if (tiles == 0 || KB == 0) return 1;
     const int64_t per_split = tc_max_k_split(parts) / kTcK;
     const int64_t smin = std::max<int64_t>(1, (KB + per_split - 1) / per_split);
     const int64_t smax = std::min<int64_t>(KB, std::max<int64_t>(4 * smin, 64));
-    const int64_t pairs = tc_resident_pairs();
     const double t_pass = 0.37;
     const double t_split = 2.0 * parts * (double)Mp * (double)Np * 4.0 / 6.0e6;
     int64_t best = smin, evaluated = 0;
@@ -715,19 +714,21 @@ int choose_tc_splits_uncached(int64_t Mp, int64_t Np, int64_t Kp, int parts) {
 // The choice above, remembered for the last few shapes (layouts are asked for
 // on every call).
 int choose_tc_splits(int64_t Mp, int64_t Np, int64_t Kp, int parts) {
-    struct Entry { int64_t Mp, Np, Kp; int parts, splits; };
+    struct Entry { int64_t Mp, Np, Kp, pairs; int parts, splits; };
     static std::mutex mu;
     static Entry cache[16];
     static int next = 0, used = 0;
+    const int64_t pairs = tc_resident_pairs();  // of the current device
     {
         std::lock_guard<std::mutex> lock(mu);
         for (int i = 0; i < used; ++i)
-            if (cache[i].Mp == Mp && cache[i].Np == Np && cache[i].Kp == Kp && cache[i].parts == parts)
+            if (cache[i].Mp == Mp && cache[i].Np == Np && cache[i].Kp == Kp && cache[i].parts == parts &&
+                cache[i].pairs == pairs)
                 return cache[i].splits;
     }
-    const int s = choose_tc_splits_uncached(Mp, Np, Kp, parts);
+    const int s = choose_tc_splits_uncached(Mp, Np, Kp, parts, pairs);
     std::lock_guard<std::mutex> lock(mu);
-    cache[next] = Entry{Mp, Np, Kp, parts, s};
+    cache[next] = Entry{Mp, Np, Kp, pairs, parts, s};
     next = (next + 1) % 16;
     used = std::min(used + 1, 16);
     return s;

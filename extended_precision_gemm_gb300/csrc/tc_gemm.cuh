@@ -382,8 +382,13 @@ int num_sms_tc() {
 // both SMs in one GPC, so this can be below half the SM count.
 template <int NP>
 int resident_pairs() {
-    static int cached = 0;
-    if (cached > 0) return cached;
+    static int cached[64] = {};  // per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        dev = 0;
+    }
+    if (cached[dev] > 0) return cached[dev];
     int n = 0;
     if (cudaFuncSetAttribute(slice_gemm_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) ==
         cudaSuccess) {
@@ -401,8 +406,8 @@ int resident_pairs() {
         if (cudaOccupancyMaxActiveClusters(&n, slice_gemm_tc_kernel<NP>, &cfg) != cudaSuccess) n = 0;
     }
     if (n <= 0) (void)cudaGetLastError();  // no device: fall back to half the SMs
-    cached = n > 0 ? n : std::max(1, num_sms_tc() / 2);
-    return cached;
+    cached[dev] = n > 0 ? n : std::max(1, num_sms_tc() / 2);
+    return cached[dev];
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
