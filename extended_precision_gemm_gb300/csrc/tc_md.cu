@@ -254,47 +254,66 @@ __global__ void __launch_bounds__(256) split_bf16_md_kernel(TcMdSplitGrid g) {
 }
 
 // Sum over the k-splits of part sum d of one output.
-__device__ __forceinline__ long long part_sum(const int32_t* p, int64_t plane, int NP, int splits, int d) {
-    long long v = 0;
-    for (int zz = 0; zz < splits; ++zz) v += __ldg(p + ((int64_t)zz * NP + d) * plane);
-    return v;
-}
-
 struct PlanePtrs {
     double* c[16];  // the output planes (device pointers), passed by value
 };
 
+// Adds a group value h (|h| < 2^63) at bit offset o of Z into the 64-bit
+// column sums of Z's 32-bit words (deferred carries).
+template <int NW>
+__device__ __forceinline__ void add_at(long long (&acc)[NW + 2], long long h, int o) {
+    const int w = o >> 5, r = o & 31;
+    const __int128 G = (__int128)h << r;  // |G| < 2^87
+    acc[w] += (long long)(uint32_t)G;
+    acc[w + 1] += (long long)(uint32_t)(G >> 32);
+    acc[w + 2] += (long long)(G >> 64);
+}
+
+// Z = sum_d v_d 256^(NP-1-d) with v_d = sum over the k-splits, formed as
+// column sums of 32-bit words, split by split (the sum is linear, so each
+// split's int32 part sums are grouped by three and placed on their own; all
+// loads of a split are independent), then one carry pass; rounded once into
+// NIN doubles.
 template <int NIN>
 __global__ void __launch_bounds__(256) recombine_tc_md_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
                                                               int64_t Np, const int32_t* __restrict__ e,
                                                               const int32_t* __restrict__ f, int64_t M, int64_t N,
                                                               PlanePtrs C, int64_t ldc) {
-    constexpr int NP = MdShape<NIN>::NP, W = MdShape<NIN>::WZ;
+    constexpr int NP = MdShape<NIN>::NP, W = MdShape<NIN>::WZ, NW = 2 * W;
     constexpr int G = NP / 3, R = NP % 3;
+    static_assert(8 * (NP - 3) + 63 + 24 < 32 * (NW + 2), "column sums cover the top group");
     const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= N) return;
     const int64_t plane = Mp * Np;
     const int fj = effective_exponent(f[j]) + 1;
     for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
-        const int32_t* p = P + i * Np + j;
-        // Horner over groups of three parts, the parts read group by group
-        uint64_t z[W];
-        {
-            const long long h0 = (part_sum(p, plane, NP, splits, 0) * 256 + part_sum(p, plane, NP, splits, 1)) * 256 +
-                                 part_sum(p, plane, NP, splits, 2);
-            z[0] = (uint64_t)h0;
+        long long acc[NW + 2];
 #pragma unroll
-            for (int w = 1; w < W; ++w) z[w] = (uint64_t)(h0 >> 63);
+        for (int w = 0; w < NW + 2; ++w) acc[w] = 0;
+        for (int zz = 0; zz < splits; ++zz) {
+            const int32_t* p = P + ((int64_t)zz * NP) * plane + i * Np + j;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const long long h = ((long long)__ldg(p + (int64_t)(3 * g) * plane) * 256 +
+                                     __ldg(p + (int64_t)(3 * g + 1) * plane)) * 256 +
+                                    __ldg(p + (int64_t)(3 * g + 2) * plane);
+                add_at<NW>(acc, h, 8 * (NP - 3 - 3 * g));
+            }
+            if (R == 1) add_at<NW>(acc, __ldg(p + (int64_t)(NP - 1) * plane), 0);
+            if (R == 2)
+                add_at<NW>(acc, (long long)__ldg(p + (int64_t)(NP - 2) * plane) * 256 + __ldg(p + (int64_t)(NP - 1) * plane),
+                           0);
         }
-#pragma unroll 1
-        for (int gi = 1; gi < G; ++gi) {
-            const long long h = (part_sum(p, plane, NP, splits, 3 * gi) * 256 + part_sum(p, plane, NP, splits, 3 * gi + 1)) *
-                                    256 + part_sum(p, plane, NP, splits, 3 * gi + 2);
-            xr::horner<W, 24>(z, h);
+        // one carry pass: Z in NW 32-bit words (two's complement; |Z| < 2^(32 NW - 1))
+        uint64_t z[W];
+        long long carry = 0;
+#pragma unroll
+        for (int w = 0; w < NW; w += 2) {
+            const long long t0 = acc[w] + carry;
+            const long long t1 = acc[w + 1] + (t0 >> 32);
+            carry = t1 >> 32;
+            z[w / 2] = (uint64_t)(uint32_t)t0 | ((uint64_t)(uint32_t)t1 << 32);
         }
-        if (R == 1) xr::horner<W, 8>(z, part_sum(p, plane, NP, splits, NP - 1));
-        if (R == 2)
-            xr::horner<W, 16>(z, part_sum(p, plane, NP, splits, NP - 2) * 256 + part_sum(p, plane, NP, splits, NP - 1));
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (NP + 1);
         double out[NIN];
         xr::round_parts_general<W>(z, q, out, NIN);
