@@ -27,12 +27,14 @@ struct MdShape<8> {
     static constexpr int NP = DDGEMM_TC_OD_SLICES;  // 54 parts
     static constexpr int WX = 7;                    // limbs of X and Y (|X| < 2^431)
     static constexpr int WZ = 8;                    // limbs of Z (|Z| < 2^467)
+    static constexpr int SPLIT_MINB = 1;            // blocks per SM the split kernels are built for
 };
 template <>
 struct MdShape<16> {
     static constexpr int NP = DDGEMM_TC_HD_SLICES;  // 107 parts
     static constexpr int WX = 14;                   // |X| < 2^855
     static constexpr int WZ = 14;                   // |Z| < 2^891
+    static constexpr int SPLIT_MINB = 2;            // 128 registers: two blocks per SM beat one of 169
 };
 
 constexpr uint64_t ABS = 0x7FFFFFFFFFFFFFFFULL;
@@ -148,6 +150,7 @@ struct TcMdSplitGrid {
     const double* B[16]; int64_t ldb, N; int32_t* f; int64_t b_tasks;
     int64_t K, KB;
     uint16_t* planesA; uint16_t* planesB;
+    bool a_vec;  // every plane of A 16-byte aligned and lda even: 16-byte loads
 };
 
 // Part s of a biased value Y as an f32 bit pattern (upper half = bf16).
@@ -174,86 +177,134 @@ __device__ __forceinline__ uint32_t md_part(const uint64_t (&y)[W], int s) {
     return __float_as_uint(__fsub_rn(__uint_as_float(0x4B000000u | E), 8388736.0f));
 }
 
-// One warp per task of 256 elements (4 rows of A, or 4 columns of B, x 64 k;
-// lane = row or column (lane/8), 8 consecutive k (lane%8)), as for the other
-// bf16 variants; each lane forms Y for its 8 elements, then writes one 16-byte
-// chunk of each of the NP part rows (a warp writes whole 128-byte rows).
+// Y = X + 128 (256^(NP-2) + ... + 1) for one element (NIN doubles) against
+// e': its low NP - 1 bytes are the balanced digits + 128, its top the first.
 template <int NIN>
-__global__ void __launch_bounds__(256) split_bf16_md_kernel(TcMdSplitGrid g) {
+__device__ __forceinline__ void biased_md(const double (&x)[NIN], int ep, uint64_t (&y)[MdShape<NIN>::WX]) {
     constexpr int NP = MdShape<NIN>::NP, W = MdShape<NIN>::WX;
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int64_t nw = (int64_t)gridDim.x * 8;
-    const int64_t tasks = g.a_tasks + g.b_tasks;
-    for (int64_t task = gw; task < tasks; task += nw) {
-        const bool is_a = task < g.a_tasks;
-        int64_t r, kb;
-        int kc;
-        if (is_a) {
-            kb = task % g.KB;
-            r = (task / g.KB) * 4 + (lane >> 3);
-            kc = lane & 7;
-        } else {
-            // 4 columns x one k-block, consecutive tasks on neighbouring columns
-            const int64_t local = task - g.a_tasks;
-            const int64_t groups = g.b_tasks / g.KB;
-            kb = local / groups;
-            r = (local % groups) * 4 + (lane >> 3);
-            kc = lane & 7;
-        }
-        const int64_t rows = is_a ? g.M : g.N;
-        int ep = 1;
-        if (r < rows) {
-            int32_t* ex = is_a ? g.e : g.f;
-            const int32_t er = ex[r];
-            if (kb == 0 && kc == 0 && er == EXP_NONE) ex[r] = 0;
-            ep = effective_exponent(er) + 1;
-        }
-        const int64_t k0 = kb * TBK + kc * 8;
-        uint64_t y[8][W];
-#pragma unroll 1
-        for (int j = 0; j < 8; ++j) {
-            double x[NIN];
+    uint64_t sign;
+    fixed_point_n<NIN, W>(x, ep, 8 * NP, y, sign);
+    if (sign) xr::negate(y);
+    uint64_t c = 0;
 #pragma unroll
-            for (int q = 0; q < NIN; ++q) x[q] = 0.0;
-            if (r < rows && k0 + j < g.K) {
-#pragma unroll
-                for (int q = 0; q < NIN; ++q)
-                    x[q] = is_a ? __ldg(g.A[q] + r * g.lda + k0 + j) : __ldg(g.B[q] + (k0 + j) * g.ldb + r);
-            }
-            uint64_t X[W];
-            uint64_t sign;
-            fixed_point_n<NIN, W>(x, ep, 8 * NP, X, sign);
-            if (sign) xr::negate(X);
-            // + 128 in each of the NP - 1 low bytes
-            uint64_t c = 0;
-#pragma unroll
-            for (int i = 0; i < W; ++i) {
-                const int lo_byte = 8 * i, n = NP - 1 - lo_byte;  // bytes of C in this limb
-                const uint64_t Ci = n >= 8 ? 0x8080808080808080ULL : n > 0 ? (0x8080808080808080ULL >> (64 - 8 * n)) : 0;
-                const uint64_t u = X[i] + Ci;
-                const uint64_t c1 = u < X[i];
-                const uint64_t u2 = u + c;
-                c = c1 | (u2 < u);
-                y[j][i] = u2;
-            }
-        }
-        uint16_t* planes = is_a ? g.planesA : g.planesB;
-        const int brows = is_a ? TBM : TBN;
-        const int64_t blk = r / brows;
-        const int rin = (int)(r % brows);
-#pragma unroll 1
-        for (int s = 0; s < NP; ++s) {
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) w[j >> 1] = pack_bf16(md_part<NP, W>(y[j], s), md_part<NP, W>(y[j + 1], s));
-            uint8_t* base = reinterpret_cast<uint8_t*>(planes + ((blk * NP + s) * g.KB + kb) * ((int64_t)brows * TBK));
-            *reinterpret_cast<uint4*>(base + swizzled(rin, kc)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+    for (int i = 0; i < W; ++i) {
+        const int n = NP - 1 - 8 * i;  // bytes of the bias in this limb
+        const uint64_t Ci = n >= 8 ? 0x8080808080808080ULL : n > 0 ? (0x8080808080808080ULL >> (64 - 8 * n)) : 0;
+        const uint64_t u = y[i] + Ci;
+        const uint64_t c1 = u < y[i];
+        const uint64_t u2 = u + c;
+        c = c1 | (u2 < u);
+        y[i] = u2;
     }
 }
 
-// Sum over the k-splits of part sum d of one output.
+// The NP parts of two consecutive elements (k, k + 1) of one part row: the
+// lane writes word jj of 16-byte chunk kc of every part row, so the 32 lanes
+// of a warp (kc = lane / 4, jj = lane % 4) write whole 128-byte rows.
+template <int NIN>
+__device__ __forceinline__ void store_parts2(uint16_t* planes, int64_t blk, int64_t KB, int64_t kb, int brows,
+                                             int rin, int kc, int jj, const uint64_t (&y0)[MdShape<NIN>::WX],
+                                             const uint64_t (&y1)[MdShape<NIN>::WX]) {
+    constexpr int NP = MdShape<NIN>::NP, W = MdShape<NIN>::WX;
+    uint8_t* base = reinterpret_cast<uint8_t*>(planes + (blk * NP * KB + kb) * ((int64_t)brows * TBK)) +
+                    swizzled(rin, kc) + 4 * jj;
+    const int64_t part_stride = KB * (int64_t)brows * TBK * 2;  // bytes from part s to s + 1
+#pragma unroll
+    for (int s = 0; s < NP; ++s)
+        *reinterpret_cast<uint32_t*>(base + s * part_stride) =
+            pack_bf16(md_part<NP, W>(y0, s), md_part<NP, W>(y1, s));
+}
+
+// A: one warp per row of A and k-block (64 k); lane (kc = lane / 4, jj =
+// lane % 4) splits k = 64 kb + 8 kc + 2 jj and the next, loading both with
+// 16-byte loads where aligned.  Rows up to Mp and k up to Kp are written (as
+// 0 beyond the matrix).
+template <int NIN>
+__global__ void __launch_bounds__(256, MdShape<NIN>::SPLIT_MINB) split_md_rows_kernel(TcMdSplitGrid g) {
+    constexpr int W = MdShape<NIN>::WX;
+    const int lane = threadIdx.x & 31, kc = lane >> 2, jj = lane & 3;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gridDim.x * 8;
+    for (int64_t task = gw; task < g.a_tasks; task += nw) {
+        const int64_t r = task / g.KB, kb = task % g.KB;
+        int ep = 1;
+        double x0[NIN], x1[NIN];
+#pragma unroll
+        for (int q = 0; q < NIN; ++q) x0[q] = x1[q] = 0.0;
+        const int64_t k = kb * TBK + kc * 8 + 2 * jj;
+        if (r < g.M) {
+            const int32_t er = g.e[r];
+            if (kb == 0 && lane == 0 && er == EXP_NONE) g.e[r] = 0;
+            ep = effective_exponent(er) + 1;
+            if (g.a_vec && k + 1 < g.K) {
+#pragma unroll
+                for (int q = 0; q < NIN; ++q) {
+                    const double2 v = __ldg(reinterpret_cast<const double2*>(g.A[q] + r * g.lda + k));
+                    x0[q] = v.x;
+                    x1[q] = v.y;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < NIN; ++q) {
+                    if (k < g.K) x0[q] = __ldg(g.A[q] + r * g.lda + k);
+                    if (k + 1 < g.K) x1[q] = __ldg(g.A[q] + r * g.lda + k + 1);
+                }
+            }
+        }
+        uint64_t y0[W], y1[W];
+        biased_md<NIN>(x0, ep, y0);
+        biased_md<NIN>(x1, ep, y1);
+        store_parts2<NIN>(g.planesA, r / TBM, g.KB, kb, TBM, (int)(r % TBM), kc, jj, y0, y1);
+    }
+}
+
+// B: one block per 8 columns of B and k-block.  The block stages the 64 x 8
+// doubles of every plane in shared memory (each row of 8 columns is 64
+// contiguous bytes of B), then warp w splits column 8 cg + w along k as the
+// row kernel does (a column of B is a row of its part blocks).
+constexpr int MD_COLS = 8;
+constexpr int MD_TILE_LD = MD_COLS + 1;  // padded row of the staged tile
+template <int NIN>
+constexpr int md_cols_smem() { return NIN * TBK * MD_TILE_LD * 8; }
+
+template <int NIN>
+__global__ void __launch_bounds__(256, MdShape<NIN>::SPLIT_MINB) split_md_cols_kernel(TcMdSplitGrid g) {
+    constexpr int W = MdShape<NIN>::WX;
+    extern __shared__ double tile[];  // [NIN][64][MD_TILE_LD]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, kc = lane >> 2, jj = lane & 3;
+    const int64_t groups = g.b_tasks / g.KB;
+    for (int64_t task = blockIdx.x; task < g.b_tasks; task += gridDim.x) {
+        const int64_t kb = task / groups, cg = task % groups;
+        const int64_t n0 = cg * MD_COLS, k0 = kb * TBK;
+        for (int idx = threadIdx.x; idx < NIN * TBK * MD_COLS; idx += blockDim.x) {
+            const int q = idx / (TBK * MD_COLS), rem = idx % (TBK * MD_COLS);
+            const int kk = rem / MD_COLS, c = rem % MD_COLS;
+            const int64_t n = n0 + c, k = k0 + kk;
+            tile[(q * TBK + kk) * MD_TILE_LD + c] = (n < g.N && k < g.K) ? __ldg(g.B[q] + k * g.ldb + n) : 0.0;
+        }
+        __syncthreads();
+        const int64_t n = n0 + warp;
+        int ep = 1;
+        if (n < g.N) {
+            const int32_t fr = g.f[n];
+            if (kb == 0 && lane == 0 && fr == EXP_NONE) g.f[n] = 0;
+            ep = effective_exponent(fr) + 1;
+        }
+        const int kk = kc * 8 + 2 * jj;
+        double x0[NIN], x1[NIN];
+#pragma unroll
+        for (int q = 0; q < NIN; ++q) {
+            x0[q] = tile[(q * TBK + kk) * MD_TILE_LD + warp];
+            x1[q] = tile[(q * TBK + kk + 1) * MD_TILE_LD + warp];
+        }
+        __syncthreads();  // the tile is free for the next task
+        uint64_t y0[W], y1[W];
+        biased_md<NIN>(x0, ep, y0);
+        biased_md<NIN>(x1, ep, y1);
+        store_parts2<NIN>(g.planesB, n / TBN, g.KB, kb, TBN, (int)(n % TBN), kc, jj, y0, y1);
+    }
+}
+
 struct PlanePtrs {
     double* c[16];  // the output planes (device pointers), passed by value
 };
@@ -331,22 +382,38 @@ cudaError_t split_md(const double* const* A, int64_t lda, int64_t M, int32_t* e,
     g.K = K;
     g.KB = Kp / TBK;
     if (A && M > 0) {
-        for (int q = 0; q < NIN; ++q) g.A[q] = A[q];
+        bool vec = lda % 2 == 0;
+        for (int q = 0; q < NIN; ++q) {
+            g.A[q] = A[q];
+            vec = vec && (uintptr_t)A[q] % 16 == 0;
+        }
         g.lda = lda; g.M = M; g.e = e;
-        g.a_tasks = (round_up(M, PAIR_M) / 4) * g.KB;
+        g.a_tasks = round_up(M, PAIR_M) * g.KB;
+        g.a_vec = vec;
     }
     if (B && N > 0) {
         for (int q = 0; q < NIN; ++q) g.B[q] = B[q];
         g.ldb = ldb; g.N = N; g.f = f;
-        g.b_tasks = (round_up(N, TBN) / 4) * g.KB;
+        g.b_tasks = (round_up(N, TBN) / MD_COLS) * g.KB;
     }
     g.planesA = planesA;
     g.planesB = planesB;
-    const int64_t tasks = g.a_tasks + g.b_tasks;
-    if (tasks == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms_tc() * 8));
-    split_bf16_md_kernel<NIN><<<blocks, 256, 0, st>>>(g);
-    return cudaGetLastError();
+    const int64_t sms = num_sms_tc();
+    if (g.a_tasks > 0) {
+        const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((g.a_tasks + 7) / 8, sms * 8));
+        split_md_rows_kernel<NIN><<<blocks, 256, 0, st>>>(g);
+        const cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    if (g.b_tasks > 0) {
+        cudaError_t err = cudaFuncSetAttribute(split_md_cols_kernel<NIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               md_cols_smem<NIN>());
+        if (err != cudaSuccess) return err;
+        const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(g.b_tasks, sms * 4));
+        split_md_cols_kernel<NIN><<<blocks, 256, md_cols_smem<NIN>(), st>>>(g);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
 }
 
 template <int NIN>
