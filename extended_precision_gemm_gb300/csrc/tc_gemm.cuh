@@ -133,10 +133,11 @@ __device__ __forceinline__ Unit unit_of(const TcGemmArgs& g, int64_t u, int np) 
 }
 
 // The r-th unit of CTA pair p: units are dealt out in rounds of one unit per
-// pair, the order of the pairs reversed every other round.  Unit weights only
-// fall along the numbering, so the pairs' totals stay within about one light
-// unit of each other, and in every round the pairs work on neighbouring
-// output blocks at the same diagonal (their copies share L2).
+// pair, the order of the pairs reversed every other round.  Unit weights fall
+// along the numbering (a shorter last k-split aside), so the pairs' totals
+// stay within about one light unit of each other, and in every round the
+// pairs work on neighbouring output blocks at the same diagonal (their copies
+// share L2).
 __device__ __forceinline__ int64_t unit_index(const TcGemmArgs& g, int64_t p, int64_t r) {
     return r * g.pairs + ((r & 1) ? g.pairs - 1 - p : p);
 }
