@@ -197,6 +197,112 @@ __device__ __forceinline__ void round_parts(const uint64_t (&z)[W], int q, doubl
 }
 
 
+// ---- sums as 64-bit column sums of 32-bit words (deferred carries) ----
+
+// Adds h (|h| < 2^63) at bit offset o (a compile-time constant after
+// unrolling) of a number kept as column sums acc[w] of its 32-bit words.
+template <int NC>
+__device__ __forceinline__ void add_at(long long (&acc)[NC], long long h, int o) {
+    const int w = o >> 5, r = o & 31;
+    const __int128 G = (__int128)h << r;  // |G| < 2^87
+    acc[w] += (long long)(uint32_t)G;
+    acc[w + 1] += (long long)(uint32_t)(G >> 32);
+    acc[w + 2] += (long long)(G >> 64);
+}
+
+// One carry pass over the column sums: the number in W 64-bit limbs (two's
+// complement; the caller guarantees it fits).
+template <int W, int NC>
+__device__ __forceinline__ void carry_to_limbs(const long long (&acc)[NC], uint64_t (&z)[W]) {
+    static_assert(NC >= 2 * W, "column sums cover the limbs");
+    long long carry = 0;
+#pragma unroll
+    for (int w = 0; w < 2 * W; w += 2) {
+        const long long t0 = acc[w] + carry;
+        const long long t1 = acc[w + 1] + (t0 >> 32);
+        carry = t1 >> 32;
+        z[w / 2] = (uint64_t)(uint32_t)t0 | ((uint64_t)(uint32_t)t1 << 32);
+    }
+}
+
+// ---- rounding by normalising shifts ----
+
+// Limb j of m, or 0 for j < 0 (j dynamic).
+template <int W>
+__device__ __forceinline__ uint64_t limb_or_zero(const uint64_t (&m)[W], int j) {
+    uint64_t v = 0;
+#pragma unroll
+    for (int i = 0; i < W; ++i)
+        if (i == j) v = m[i];
+    return v;
+}
+
+// r = m << n for 0 <= n < 64 W (bits shifted out at the top are dropped).
+template <int W>
+__device__ __forceinline__ void shift_left(const uint64_t (&m)[W], int n, uint64_t (&r)[W]) {
+    const int k = n >> 6, b = n & 63;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        const uint64_t hi = limb_or_zero(m, i - k), lo = limb_or_zero(m, i - k - 1);
+        r[i] = b ? (hi << b) | (lo >> (64 - b)) : hi;
+    }
+}
+
+// Z 2^q rounded into NOUT doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0),
+// ... (ties to even; +0 for zeros), when every part is a normal double or
+// zero: q >= -1022 and the leading bit of Z 2^q at most 2^1022; otherwise
+// false (nothing written).  Each part shifts the remainder up to the top bit,
+// keeps the top 53 bits, rounds on the next bit and the sticky rest, and
+// leaves the bits below (or 2^(64 W - 53) minus them after rounding up, with
+// the sign flipped) as the next remainder.
+template <int W, int NOUT>
+__device__ __forceinline__ bool round_parts_norm(const uint64_t (&z)[W], int q, double (&out)[NOUT]) {
+    uint64_t m[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) m[i] = z[i];
+    uint64_t sign = m[W - 1] >> 63;
+    if (sign) negate(m);
+    if (is_zero(m)) {
+#pragma unroll
+        for (int p = 0; p < NOUT; ++p) out[p] = 0.0;
+        return true;
+    }
+    if (q < -1022 || msb(m) + q > 1022) return false;
+    constexpr int TOP = 64 * W - 1;
+    int e0 = q;  // exponent of bit 0 of m
+    bool zero = false;
+#pragma unroll
+    for (int p = 0; p < NOUT; ++p) {
+        zero = zero || is_zero(m);
+        if (zero) {
+            out[p] = 0.0;
+            continue;
+        }
+        const int n = TOP - msb(m);
+        uint64_t N[W];
+        shift_left(m, n, N);
+        const uint64_t keep = N[W - 1] >> 11;  // the leading 53 bits
+        uint64_t sticky = N[W - 1] & 0x3FFULL;
+#pragma unroll
+        for (int i = 0; i < W - 1; ++i) sticky |= N[i];
+        const bool up = ((N[W - 1] >> 10) & 1) && (sticky != 0 || (keep & 1));
+        const int E = e0 - n + TOP;  // exponent of the leading bit
+        // keep + up lies in [2^52, 2^53]: added to the exponent field minus
+        // one it carries into the exponent when it reaches 2^53
+        out[p] = __longlong_as_double(
+            (long long)((sign << 63) | (((uint64_t)(E + 1022) << 52) + keep + (up ? 1 : 0))));
+        N[W - 1] &= 0x7FFULL;  // the tail below the kept bits
+        if (up) {
+            complement_to(N, TOP - 52);
+            sign ^= 1;
+        }
+#pragma unroll
+        for (int i = 0; i < W; ++i) m[i] = N[i];
+        e0 -= n;
+    }
+    return true;
+}
+
 // Z 2^q rounded into nout doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0), ...
 // for any q: gradual underflow (a part below half the smallest subnormal is
 // 0) and overflow (an infinite part) end the expansion, and the remaining

@@ -43,6 +43,7 @@ constexpr int QFIX = QS * TD;               // 216 fraction bits
 static_assert(TS * TD == fxp::FIX_BITS, "13 parts of 8 bits cover the 104-bit fixed-point value");
 static_assert((long long)TS * ksplit_max(TS) * 128 * 128 < (1LL << 31), "int32 totals per k-split");
 static_assert((long long)QS * ksplit_max(QS) * 128 * 128 < (1LL << 31), "int32 totals per k-split");
+static_assert(QS % 3 == 0, "quad-double parts come in groups of three");
 
 // ---------------------------------------------------------------------------
 // Step 1: bf16 parts.
@@ -435,22 +436,27 @@ __global__ void __launch_bounds__(256, 2) recombine_tc_qd_kernel(const int32_t* 
     const int fj = effective_exponent(f[j]) + 1;
     double* Cs[4] = {C0, C1, C2, C3};
     for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
-        const int32_t* p = P + i * Np + j;
-        // all loads of a split are issued before any is used
-        long long v[QS];
+        // Z = sum_d v_d 256^(26 - d) as column sums of 32-bit words: each
+        // k-split's part sums in groups of three at their offsets (all loads of
+        // a split independent), then one carry pass (|Z| < 2^250)
+        long long acc[10];
 #pragma unroll
-        for (int d = 0; d < QS; ++d) v[d] = __ldg(p + (int64_t)d * plane);
-        for (int zz = 1; zz < splits; ++zz) {
+        for (int w = 0; w < 10; ++w) acc[w] = 0;
+        for (int zz = 0; zz < splits; ++zz) {
+            const int32_t* p = P + ((int64_t)zz * QS) * plane + i * Np + j;
 #pragma unroll
-            for (int d = 0; d < QS; ++d) v[d] += __ldg(p + ((int64_t)zz * QS + d) * plane);
+            for (int g = 0; g < QS / 3; ++g) {
+                const long long h = ((long long)__ldg(p + (int64_t)(3 * g) * plane) * 256 +
+                                     __ldg(p + (int64_t)(3 * g + 1) * plane)) * 256 +
+                                    __ldg(p + (int64_t)(3 * g + 2) * plane);
+                xr::add_at(acc, h, TD * (QS - 3 - 3 * g));
+            }
         }
-        const int q = effective_exponent(e[i]) + 1 + fj - TD * (QS + 1);
         uint64_t z[4];
-        xr::exact_sum<QS, 4>(v, z);
+        xr::carry_to_limbs(acc, z);
+        const int q = effective_exponent(e[i]) + 1 + fj - TD * (QS + 1);
         double out[4];
-        if (xr::fast_path_ok(z, q)) {
-            xr::round_parts<4, 4>(z, q, out);
-        } else {
+        if (!xr::round_parts_norm<4, 4>(z, q, out)) {
             wide::U256 Z;
             Z.lo = ((wide::u128)z[1] << 64) | z[0];
             Z.hi = ((wide::u128)z[3] << 64) | z[2];

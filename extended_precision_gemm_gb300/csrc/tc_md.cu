@@ -309,17 +309,6 @@ struct PlanePtrs {
     double* c[16];  // the output planes (device pointers), passed by value
 };
 
-// Adds a group value h (|h| < 2^63) at bit offset o of Z into the 64-bit
-// column sums of Z's 32-bit words (deferred carries).
-template <int NW>
-__device__ __forceinline__ void add_at(long long (&acc)[NW + 2], long long h, int o) {
-    const int w = o >> 5, r = o & 31;
-    const __int128 G = (__int128)h << r;  // |G| < 2^87
-    acc[w] += (long long)(uint32_t)G;
-    acc[w + 1] += (long long)(uint32_t)(G >> 32);
-    acc[w + 2] += (long long)(G >> 64);
-}
-
 // Z = sum_d v_d 256^(NP-1-d) with v_d = sum over the k-splits, formed as
 // column sums of 32-bit words, split by split (the sum is linear, so each
 // split's int32 part sums are grouped by three and placed on their own; all
@@ -348,23 +337,16 @@ __global__ void __launch_bounds__(256) recombine_tc_md_kernel(const int32_t* __r
                 const long long h = ((long long)__ldg(p + (int64_t)(3 * g) * plane) * 256 +
                                      __ldg(p + (int64_t)(3 * g + 1) * plane)) * 256 +
                                     __ldg(p + (int64_t)(3 * g + 2) * plane);
-                add_at<NW>(acc, h, 8 * (NP - 3 - 3 * g));
+                xr::add_at(acc, h, 8 * (NP - 3 - 3 * g));
             }
-            if (R == 1) add_at<NW>(acc, __ldg(p + (int64_t)(NP - 1) * plane), 0);
+            if (R == 1) xr::add_at(acc, __ldg(p + (int64_t)(NP - 1) * plane), 0);
             if (R == 2)
-                add_at<NW>(acc, (long long)__ldg(p + (int64_t)(NP - 2) * plane) * 256 + __ldg(p + (int64_t)(NP - 1) * plane),
+                xr::add_at(acc, (long long)__ldg(p + (int64_t)(NP - 2) * plane) * 256 + __ldg(p + (int64_t)(NP - 1) * plane),
                            0);
         }
-        // one carry pass: Z in NW 32-bit words (two's complement; |Z| < 2^(32 NW - 1))
+        // one carry pass: Z in W limbs (two's complement; |Z| < 2^(64 W - 1))
         uint64_t z[W];
-        long long carry = 0;
-#pragma unroll
-        for (int w = 0; w < NW; w += 2) {
-            const long long t0 = acc[w] + carry;
-            const long long t1 = acc[w + 1] + (t0 >> 32);
-            carry = t1 >> 32;
-            z[w / 2] = (uint64_t)(uint32_t)t0 | ((uint64_t)(uint32_t)t1 << 32);
-        }
+        xr::carry_to_limbs(acc, z);
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (NP + 1);
         double out[NIN];
         xr::round_parts_general<W>(z, q, out, NIN);

@@ -114,11 +114,12 @@ def test_recombine_tc_rounding_cases():
     the 128-bit path (|v_0| = 2^30) and scales at the ends of the normal range;
     then random int32 part sums with one and two k-splits."""
     crafted = [
-        (2**53 + 1) * 2**60 + 2**59,        # tie, odd: up
-        2**53 * 2**60 + 2**59,              # tie, even: down
-        (2**53 + 1) * 2**60 + 2**59 + 1,    # just above the tie
-        2**120 + (2**53 + 1) * 8 + 4,       # exact leading double, tie in the trailing one
-        2**120 + 2**53 * 8 + 4,
+        (2**52 + 1) * 2**60 + 2**59,        # tie, odd 53-bit significand: up
+        2**52 * 2**60 + 2**59,              # tie, even: down
+        (2**52 + 1) * 2**60 + 2**59 + 1,    # just above the tie
+        (2**53 + 1) * 2**60 + 2**59,        # above half an ulp
+        2**120 + (2**52 + 1) * 8 + 4,       # exact leading double, tie in the trailing one
+        2**120 + 2**52 * 8 + 4,
         2**124 - 1,                         # rounds up to 2^124, trailing -1
         12345, 1, 0,
         (2**30 - 1) * 2**96 + 2**95 + 12345,

@@ -79,3 +79,50 @@ def test_qd_gemm_tc_k_split_bound_and_errors():
     lib = ddg.load()
     assert lib.qd_gemm_tc(2, 2, ddg.QD_MAX_K + 1, None, ddg.QD_MAX_K + 1, None, 2, None, 2, None, 0, None) == 2
     assert ddg.wait_timeouts() == 0
+
+
+def _qd_digits_of_sum(Z):
+    """27 part sums whose exact sum sum_d v_d 256^(26-d) is Z (v_0 = the bits
+    above 208, base-256 digits below; negated for a negative Z)."""
+    s, a = (-1, -Z) if Z < 0 else (1, Z)
+    return [s * (a >> 208)] + [s * ((a >> (8 * (26 - d))) & 0xFF) for d in range(1, S)]
+
+
+def test_qd_recombine_rounding_cases():
+    """Crafted part sums against the oracle's rounding into four doubles: a
+    tie in each of the four (to even, either way), carries to the next power
+    of two, remainders of both signs, exact small values, zero, both signs and
+    scales at the ends of the normal range; then random int32 part sums with
+    one and two k-splits."""
+    crafted = [
+        (2**52 + 1) * 2**180 + 2**179,                       # tie in x0, odd: up
+        2**52 * 2**180 + 2**179,                             # tie in x0, even: down
+        (2**53 + 1) * 2**180 + 2**179,                       # above half an ulp
+        2**236 + (2**52 + 1) * 2**100 + 2**99,               # tie in x1
+        2**236 + 2**170 + (2**52 + 1) * 2**50 + 2**49,       # tie in x2
+        2**236 + 2**170 + 2**110 + (2**52 + 1) * 4 + 2,      # tie in x3
+        2**236 + 2**170 + 2**110 + 2**52 * 4 + 2,            # tie in x3, even
+        2**237 - 1,                                          # carries all the way up
+        2**236 - 2**100 + 3,                                 # remainders change sign
+        (2**53 - 1) * 2**150 + 2**149 + 1,                   # rounds up to 2^203
+        12345, 1, 0,
+    ]
+    crafted += [-z for z in crafted if z]
+    rng = np.random.default_rng(22)
+    E = [0, -800, -801, 700, 1000, 1010, -990]  # q = e + f - 222: -1022 and -1023 at f = 0
+    M, Nc, Nr = len(E), len(crafted), 150
+    N = Nc + Nr
+    Mp, Np = pad(M, ddg.TC_TILE_M), pad(N, ddg.TC_TILE_N)
+    e = np.array(E, dtype=np.int32)
+    f = np.concatenate([np.zeros(Nc), rng.integers(-6, 7, Nr)]).astype(np.int32)
+    for splits in (1, 2):
+        P = np.zeros((splits, S, Mp, Np), dtype=np.int32)
+        for c, Z in enumerate(crafted):
+            P[0, :, :M, c] = np.array(_qd_digits_of_sum(Z), dtype=np.int64)[:, None]
+        lim = np.iinfo(np.int32)
+        P[:, :, :M, Nc:N] = rng.integers(lim.min, lim.max, (splits, S, M, Nr), endpoint=True)
+        R = bm.recombine(P.astype(np.int64).sum(axis=0)[:, :M, :N], e + 1, f + 1, 4)
+        C = [host(c) for c in ddg.qd_recombine_tc(M, N, dev(P), dev(e), dev(f))]
+        for p in range(4):
+            assert np.array_equal(C[p].view(np.int64), R[p].view(np.int64)), (splits, p)
+    assert ddg.wait_timeouts() == 0
