@@ -411,7 +411,12 @@ ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K,
  * dd_slice_gemm_tc: P, splits x 13 x Mp x Np int32 (row-major Mp x Np per
  *   split and part): the exact part sums of each k-split; splits as given by
  *   dd_gemm_tc_layout (1 <= splits, and ceil(Kp/64 / splits) * 64 <= 8192).
- * dd_recombine_tc: C from P and the exponents of dd_split_bf16.
+ *   planesA, planesB and P must be 16-byte aligned (tensor copies read the
+ *   parts, 16-byte stores write P); any split count in that range gives the
+ *   same sums.
+ * dd_recombine_tc: C from P and the exponents of dd_split_bf16 (P of any
+ *   alignment; 16-byte aligned P and C are read and written 16 bytes at a
+ *   time).
  * Errors as for the dd_gemm steps.
  */
 ddgemm_status dd_split_bf16(int64_t M, int64_t N, int64_t K,
