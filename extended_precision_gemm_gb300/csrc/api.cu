@@ -641,7 +641,7 @@ namespace {
 
 constexpr int64_t kTcM = DDGEMM_TC_TILE_M, kTcN = DDGEMM_TC_TILE_N, kTcK = DDGEMM_TC_CHUNK_K;
 constexpr int kTcParts = DDGEMM_TC_SLICES;
-constexpr int kTcMaxSplits = 65535;  // grid.y of the slice GEMM
+constexpr int kTcMaxSplits = 65535;  // k-splits accepted by the tensor-core step entry points
 
 struct TcLayout {
     int64_t Mp, Np, Kp;
