@@ -303,6 +303,98 @@ __device__ __forceinline__ bool round_parts_norm(const uint64_t (&z)[W], int q, 
     return true;
 }
 
+// ---- rounding by scanning the bits of |Z| (many limbs, many parts) ----
+//
+// With L the lowest set bit of |Z|, every remainder R of the expansion keeps
+// L as its lowest set bit, and below the position reached so far its bits are
+// either those of |Z| or, after an odd number of roundings up, those of |Z|
+// inverted above L (2^p - T = ~(T - 1) for T with lowest set bit L, and the
+// bits at and below L of ~(T - 1) are those of T).  So no remainder is ever
+// formed: each part reads 54 bits of |Z| at its leading bit, inverts them
+// above L when needed, and the sticky bit is simply L < (round-bit position).
+
+// Bits [lo, lo + 64) of m (lo may be negative: zeros below bit 0; m is held
+// in local memory for the dynamic limb index).
+template <int W>
+__device__ __forceinline__ uint64_t bits_from(const uint64_t* m, int lo) {
+    if (lo < 0) return m[0] << (-lo);  // only used with lo > -64
+    const int i = lo >> 6, o = lo & 63;
+    const uint64_t a = m[i], b = i + 1 < W ? m[i + 1] : 0;
+    return o ? (a >> o) | (b << (64 - o)) : a;
+}
+
+// Leading bit of the remainder below position pos: the highest set bit of m
+// below pos, or with inv the highest clear bit of m in (L, pos), else L.
+// -1 if the remainder is 0.
+template <int W>
+__device__ __forceinline__ int remainder_top(const uint64_t* m, int pos, bool inv, int L) {
+    if (pos <= L) return -1;
+    const int lL = L >> 6;
+    int i = (pos - 1) >> 6;
+    uint64_t v = inv ? ~m[i] : m[i];
+    if (pos & 63) v &= (1ULL << (pos & 63)) - 1;
+#pragma unroll 1
+    for (;;) {
+        if (i == lL) {
+            v &= ~((2ULL << (L & 63)) - 1);  // only bits above L (the bit at L is always set)
+            if (v) return 64 * i + 63 - __clzll((long long)v);
+            return L;
+        }
+        if (v) return 64 * i + 63 - __clzll((long long)v);
+        --i;
+        v = inv ? ~m[i] : m[i];
+    }
+}
+
+// Z 2^q rounded into nout doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0), ...
+// (ties to even; +0 for zeros) when every part is a normal double or zero:
+// q >= -1022 and the leading bit of Z 2^q at most 2^1022; otherwise false.
+template <int W>
+__device__ __forceinline__ bool round_parts_scan(const uint64_t (&z)[W], int q, double* out, int nout) {
+    uint64_t m[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) m[i] = z[i];
+    uint64_t sign = m[W - 1] >> 63;
+    if (sign) negate(m);
+    int L = -1;
+#pragma unroll
+    for (int i = W - 1; i >= 0; --i)
+        if (m[i] != 0) L = 64 * i + __ffsll((long long)m[i]) - 1;
+    if (L < 0) {
+        for (int p = 0; p < nout; ++p) out[p] = 0.0;
+        return true;
+    }
+    const int t = msb(m);
+    if (q < -1022 || t + q > 1022) return false;
+    int pos = t + 1;  // the remainder is the part of |Z| below pos
+    bool inv = false, zero = false;
+#pragma unroll 1
+    for (int p = 0; p < nout; ++p) {
+        const int tr = zero ? -1 : remainder_top<W>(m, pos, inv, L);
+        if (tr < 0) {
+            zero = true;
+            out[p] = 0.0;
+            continue;
+        }
+        const int lo = tr - 53;  // round bit
+        uint64_t w = bits_from<W>(m, lo) & ((1ULL << 54) - 1);
+        if (inv) {  // invert the window above L
+            const int b = L - lo;
+            w ^= b < 0 ? ((1ULL << 54) - 1) : (((1ULL << 54) - 1) & ~((2ULL << b) - 1));
+        }
+        const uint64_t keep = w >> 1;  // 53 bits, leading bit set
+        const bool up = (w & 1) && (L < lo || (keep & 1));
+        out[p] = __longlong_as_double(
+            (long long)((sign << 63) | (((uint64_t)(tr + q + 1022) << 52) + keep + (up ? 1 : 0))));
+        pos = tr - 52;
+        if (up) {
+            inv = !inv;
+            sign ^= 1;
+        }
+    }
+    return true;
+}
+
 // Z 2^q rounded into nout doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0), ...
 // for any q: gradual underflow (a part below half the smallest subnormal is
 // 0) and overflow (an infinite part) end the expansion, and the remaining

@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(256) recombine_tc_md_kernel(const int32_t* __r
         xr::carry_to_limbs(acc, z);
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (NP + 1);
         double out[NIN];
-        xr::round_parts_general<W>(z, q, out, NIN);
+        if (!xr::round_parts_scan<W>(z, q, out, NIN)) xr::round_parts_general<W>(z, q, out, NIN);
 #pragma unroll
         for (int pq = 0; pq < NIN; ++pq) C.c[pq][i * ldc + j] = out[pq];
     }

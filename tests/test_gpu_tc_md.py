@@ -76,3 +76,51 @@ def test_md_tc_tiny_values_round_with_gradual_underflow():
     for p in range(n):
         assert np.array_equal(C[p].view(np.int64), C_ref[p].view(np.int64)), p
     assert ddg.wait_timeouts() == 0
+
+
+def _md_digits_of_sum(Z, S_):
+    s, a = (-1, -Z) if Z < 0 else (1, Z)
+    top = 8 * (S_ - 1)
+    return [s * (a >> top)] + [s * ((a >> (8 * (S_ - 1 - d))) & 0xFF) for d in range(1, S_)]
+
+
+@pytest.mark.parametrize("n", [8, 16])
+def test_md_recombine_rounding_cases(n):
+    """Crafted and random exact sums against the oracle's rounding into n
+    doubles: ties (to even, both ways) in the first, a middle and the last
+    part, long runs of ones and zeros (remainders that flip sign part after
+    part), both signs, small values, zero, and scales at the ends of the
+    normal range (q = -1022 and -1023); then random int32 part sums."""
+    S_ = ddg.MD_TC_PARTS[n]
+    top = 8 * (S_ - 1) + 28                       # |Z| < 2^top keeps v_0 in int32
+    crafted = [
+        (2**52 + 1) * 2**(top - 60) + 2**(top - 61),                  # tie in x0, odd
+        2**52 * 2**(top - 60) + 2**(top - 61),                        # tie in x0, even
+        2**top - 1,                                                   # ones: every part rounds up
+        2**top - 2**(top // 2) + 1,
+        2**(top - 2) + (2**52 + 1) * 2**(top - 150) + 2**(top - 151),  # tie in x1
+        2**(top - 2) + 2**(top - 70) + 2**(top - 140) + (2**52 + 1) * 2**60 + 2**59,
+        sum(2**(top - 2 - 57 * k) for k in range(n)) + 2**3,           # one bit per part
+        (2**52 + 1) * 2 + 1, 12345, 1, 0,
+    ]
+    crafted += [-z for z in crafted if z]
+    rng = np.random.default_rng(30 + n)
+    # q = e + f + 2 - 8 (S + 1): -1022 and -1023 at f = 0, and large scales
+    base = 8 * (S_ + 1) - 2
+    E = [0, -1022 + base, -1023 + base, 300, 1022 - top + base - 2, -900]
+    M, Nc, Nr = len(E), len(crafted), 100
+    N = Nc + Nr
+    Mp, Np = pad(M, ddg.TC_TILE_M), pad(N, ddg.TC_TILE_N)
+    e = np.array(E, dtype=np.int32)
+    f = np.concatenate([np.zeros(Nc), rng.integers(-6, 7, Nr)]).astype(np.int32)
+    for splits in (1, 2):
+        P = np.zeros((splits, S_, Mp, Np), dtype=np.int32)
+        for c, Z in enumerate(crafted):
+            P[0, :, :M, c] = np.array(_md_digits_of_sum(Z, S_), dtype=np.int64)[:, None]
+        lim = np.iinfo(np.int32)
+        P[:, :, :M, Nc:N] = rng.integers(lim.min, lim.max, (splits, S_, M, Nr), endpoint=True)
+        R = bm.recombine(P.astype(np.int64).sum(axis=0)[:, :M, :N], e + 1, f + 1, n)
+        C = [host(c) for c in ddg.md_recombine_tc(n, M, N, dev(P), dev(e), dev(f))]
+        for p in range(n):
+            assert np.array_equal(C[p].view(np.int64), R[p].view(np.int64)), (splits, p)
+    assert ddg.wait_timeouts() == 0
