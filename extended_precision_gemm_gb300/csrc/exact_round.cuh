@@ -1,16 +1,17 @@
 // exact_round.cuh -- the exact sum of part sums on a base-256 grid and its
-// rounding into non-overlapping doubles, with 64-bit limbs (the fast path of
-// the bf16 variants' recombination).
+// rounding into non-overlapping doubles, with 64-bit limbs (the bf16
+// variants' recombination).
 //
 //   Z = sum_{d=0}^{NP-1} v_d 256^(NP-1-d),   |v_d| < 2^46,
 //
-// is formed exactly in W 64-bit limbs (two's complement, least significant
-// first) by Horner's rule over groups of three parts (a group
-// v_a 2^16 + v_b 2^8 + v_c stays below 2^63), and Z 2^q is rounded into NOUT
-// doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0), ... (ties to even).  The
-// fast path needs every part to be a normal double: q >= -1022 (a nonzero
-// remainder is at least 2^q) and the result below 2^1023; the caller checks
-// fast_path_ok() and otherwise uses the general 256-bit routine.
+// is formed exactly either in W 64-bit limbs (two's complement, least
+// significant first) by Horner's rule over groups of three parts (a group
+// v_a 2^16 + v_b 2^8 + v_c stays below 2^63), or as 64-bit column sums of its
+// 32-bit words followed by one carry pass.  Z 2^q is rounded into NOUT
+// doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0), ... (ties to even) by the
+// limb routines below (the fast ones need every part to be a normal double:
+// q >= -1022, so that a nonzero remainder is at least 2^q, and the result
+// below 2^1023), or by the general routine with gradual underflow.
 #pragma once
 
 #include <cstdint>
@@ -225,85 +226,7 @@ __device__ __forceinline__ void carry_to_limbs(const long long (&acc)[NC], uint6
     }
 }
 
-// ---- rounding by normalising shifts ----
-
-// Limb j of m, or 0 for j < 0 (j dynamic).
-template <int W>
-__device__ __forceinline__ uint64_t limb_or_zero(const uint64_t (&m)[W], int j) {
-    uint64_t v = 0;
-#pragma unroll
-    for (int i = 0; i < W; ++i)
-        if (i == j) v = m[i];
-    return v;
-}
-
-// r = m << n for 0 <= n < 64 W (bits shifted out at the top are dropped).
-template <int W>
-__device__ __forceinline__ void shift_left(const uint64_t (&m)[W], int n, uint64_t (&r)[W]) {
-    const int k = n >> 6, b = n & 63;
-#pragma unroll
-    for (int i = 0; i < W; ++i) {
-        const uint64_t hi = limb_or_zero(m, i - k), lo = limb_or_zero(m, i - k - 1);
-        r[i] = b ? (hi << b) | (lo >> (64 - b)) : hi;
-    }
-}
-
-// Z 2^q rounded into NOUT doubles x_0 = RN(Z 2^q), x_1 = RN(Z 2^q - x_0),
-// ... (ties to even; +0 for zeros), when every part is a normal double or
-// zero: q >= -1022 and the leading bit of Z 2^q at most 2^1022; otherwise
-// false (nothing written).  Each part shifts the remainder up to the top bit,
-// keeps the top 53 bits, rounds on the next bit and the sticky rest, and
-// leaves the bits below (or 2^(64 W - 53) minus them after rounding up, with
-// the sign flipped) as the next remainder.
-template <int W, int NOUT>
-__device__ __forceinline__ bool round_parts_norm(const uint64_t (&z)[W], int q, double (&out)[NOUT]) {
-    uint64_t m[W];
-#pragma unroll
-    for (int i = 0; i < W; ++i) m[i] = z[i];
-    uint64_t sign = m[W - 1] >> 63;
-    if (sign) negate(m);
-    if (is_zero(m)) {
-#pragma unroll
-        for (int p = 0; p < NOUT; ++p) out[p] = 0.0;
-        return true;
-    }
-    if (q < -1022 || msb(m) + q > 1022) return false;
-    constexpr int TOP = 64 * W - 1;
-    int e0 = q;  // exponent of bit 0 of m
-    bool zero = false;
-#pragma unroll
-    for (int p = 0; p < NOUT; ++p) {
-        zero = zero || is_zero(m);
-        if (zero) {
-            out[p] = 0.0;
-            continue;
-        }
-        const int n = TOP - msb(m);
-        uint64_t N[W];
-        shift_left(m, n, N);
-        const uint64_t keep = N[W - 1] >> 11;  // the leading 53 bits
-        uint64_t sticky = N[W - 1] & 0x3FFULL;
-#pragma unroll
-        for (int i = 0; i < W - 1; ++i) sticky |= N[i];
-        const bool up = ((N[W - 1] >> 10) & 1) && (sticky != 0 || (keep & 1));
-        const int E = e0 - n + TOP;  // exponent of the leading bit
-        // keep + up lies in [2^52, 2^53]: added to the exponent field minus
-        // one it carries into the exponent when it reaches 2^53
-        out[p] = __longlong_as_double(
-            (long long)((sign << 63) | (((uint64_t)(E + 1022) << 52) + keep + (up ? 1 : 0))));
-        N[W - 1] &= 0x7FFULL;  // the tail below the kept bits
-        if (up) {
-            complement_to(N, TOP - 52);
-            sign ^= 1;
-        }
-#pragma unroll
-        for (int i = 0; i < W; ++i) m[i] = N[i];
-        e0 -= n;
-    }
-    return true;
-}
-
-// ---- rounding by scanning the bits of |Z| (many limbs, many parts) ----
+// ---- rounding by scanning the bits of |Z| ----
 //
 // With L the lowest set bit of |Z|, every remainder R of the expansion keeps
 // L as its lowest set bit, and below the position reached so far its bits are

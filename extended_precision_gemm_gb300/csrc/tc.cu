@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(256, 2) recombine_tc_qd_kernel(const int32_t* 
         xr::carry_to_limbs(acc, z);
         const int q = effective_exponent(e[i]) + 1 + fj - TD * (QS + 1);
         double out[4];
-        if (!xr::round_parts_norm<4, 4>(z, q, out)) {
+        if (!xr::round_parts_scan<4>(z, q, out, 4)) {
             wide::U256 Z;
             Z.lo = ((wide::u128)z[1] << 64) | z[0];
             Z.hi = ((wide::u128)z[3] << 64) | z[2];
