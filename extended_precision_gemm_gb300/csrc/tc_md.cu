@@ -53,42 +53,6 @@ __device__ __forceinline__ UnpM unpack_m(uint64_t bits) {
     return u;
 }
 
-// X += (neg ? -1 : 1) m 2^sh for m < 2^53, 0 <= sh <= 64 W - 53.
-template <int W>
-__device__ __forceinline__ void add_shifted(uint64_t (&X)[W], uint64_t m, int sh, bool neg) {
-    const int i = sh >> 6, o = sh & 63;
-    const uint64_t lo = m << o, hi = o ? (m >> (64 - o)) : 0;
-    uint64_t t[W];
-#pragma unroll
-    for (int j = 0; j < W; ++j) t[j] = (j == i) ? lo : (j == i + 1) ? hi : 0;
-    if (neg) xr::negate(t);
-    uint64_t c = 0;
-#pragma unroll
-    for (int j = 0; j < W; ++j) {
-        const uint64_t u = X[j] + t[j];
-        const uint64_t c1 = u < X[j];
-        const uint64_t u2 = u + c;
-        c = c1 | (u2 < u);
-        X[j] = u2;
-    }
-}
-
-// X += F for a small signed F.
-template <int W>
-__device__ __forceinline__ void add_small(uint64_t (&X)[W], long long F) {
-    const uint64_t s = (uint64_t)(F >> 63);
-    uint64_t c = 0;
-#pragma unroll
-    for (int j = 0; j < W; ++j) {
-        const uint64_t add = j == 0 ? (uint64_t)F : s;
-        const uint64_t u = X[j] + add;
-        const uint64_t c1 = u < X[j];
-        const uint64_t u2 = u + c;
-        c = c1 | (u2 < u);
-        X[j] = u2;
-    }
-}
-
 // X = floor(|x_0 + ... + x_(NIN-1)| 2^(FIXB - e)) for a normalised multiple
 // double (|x_(p+1)| <= ulp(x_p) / 2) and the sign of the element.  With every
 // double signed relative to the leading one, the doubles that are integers at
@@ -99,6 +63,12 @@ __device__ __forceinline__ void add_small(uint64_t (&X)[W], long long F) {
 template <int NIN, int W>
 __device__ __forceinline__ void fixed_point_n(const double (&x)[NIN], int e, int FIXB, uint64_t (&X)[W],
                                               uint64_t& sign_out) {
+    // the integer parts of the doubles are added as 64-bit column sums of
+    // 32-bit words (dynamic positions, so the sums live in local memory), and
+    // one carry pass gives the limbs: the value is nonnegative
+    long long acc[2 * W + 2];
+#pragma unroll
+    for (int w = 0; w < 2 * W + 2; ++w) acc[w] = 0;
 #pragma unroll
     for (int j = 0; j < W; ++j) X[j] = 0;
     int lead = -1;
@@ -121,7 +91,20 @@ __device__ __forceinline__ void fixed_point_n(const double (&x)[NIN], int e, int
         const UnpM u = unpack_m(b);
         const int sh = u.E + FIXB - e;
         if (sh >= 0) {
-            add_shifted(X, u.m, min(sh, 64 * W - 53), negp);  // clamped only out of contract
+            const int s = min(sh, 64 * W - 53);  // clamped only out of contract
+            const int w = s >> 5;
+            const unsigned __int128 G = (unsigned __int128)u.m << (s & 31);  // < 2^85
+            const long long p0 = (long long)(uint32_t)G, p1 = (long long)(uint32_t)(G >> 32),
+                            p2 = (long long)(uint32_t)(G >> 64);
+            if (negp) {
+                acc[w] -= p0;
+                acc[w + 1] -= p1;
+                acc[w + 2] -= p2;
+            } else {
+                acc[w] += p0;
+                acc[w + 1] += p1;
+                acc[w + 2] += p2;
+            }
             continue;
         }
         const int rs = -sh;
@@ -140,9 +123,10 @@ __device__ __forceinline__ void fixed_point_n(const double (&x)[NIN], int e, int
                 }
             }
         }
-        add_small(X, F);
+        acc[0] += F;  // |F| < 2^53: the column sums absorb it before the carry pass
         done = true;
     }
+    xr::carry_to_limbs(acc, X);
 }
 
 struct TcMdSplitGrid {
