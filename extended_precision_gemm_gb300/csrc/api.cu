@@ -1016,6 +1016,7 @@ ddgemm_status qd_slice_gemm_tc(int64_t M, int64_t N, int64_t K, const uint16_t* 
     if (splits < 1 || splits > kTcMaxSplits || (KB > 0 && splits > KB) || (KB == 0 && splits != 1))
         return DDGEMM_ERR_INVALID_ARG;
     if (KB > 0 && ((KB + splits - 1) / splits) * kTcK > DDGEMM_TC_QD_MAX_K_SPLIT) return DDGEMM_ERR_INVALID_ARG;
+    if (!tc_part_rows_ok(M, N, K, kTcQdParts)) return DDGEMM_ERR_UNSUPPORTED;
     if (P == nullptr || (K > 0 && (planesA == nullptr || planesB == nullptr))) return DDGEMM_ERR_INVALID_ARG;
     if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0 || (uintptr_t)P % 16 != 0)
         return DDGEMM_ERR_INVALID_ARG;
@@ -1167,6 +1168,7 @@ ddgemm_status md_slice_gemm_tc(int nparts, int64_t M, int64_t N, int64_t K, cons
     if (splits < 1 || splits > kTcMaxSplits || (KB > 0 && splits > KB) || (KB == 0 && splits != 1))
         return DDGEMM_ERR_INVALID_ARG;
     if (KB > 0 && ((KB + splits - 1) / splits) * kTcK > tc_max_k_split(md_parts(nparts))) return DDGEMM_ERR_INVALID_ARG;
+    if (!tc_part_rows_ok(M, N, K, md_parts(nparts))) return DDGEMM_ERR_UNSUPPORTED;
     if (P == nullptr || (K > 0 && (planesA == nullptr || planesB == nullptr))) return DDGEMM_ERR_INVALID_ARG;
     if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0 || (uintptr_t)P % 16 != 0)
         return DDGEMM_ERR_INVALID_ARG;

@@ -117,3 +117,33 @@ def test_tc_layouts_splits_and_limits(lib):
     assert lib.qd_gemm_tc_layout(1 << 20, 256, 1 << 23, *refs) == 2
     assert lib.md_gemm_tc_layout(16, 1 << 16, 256, 1 << 20, *refs) == 2
     assert lib.md_gemm_tc_layout(8, 4096, 4096, 4096, *refs) == 0
+
+
+def test_tc_argument_errors_are_host_side(lib):
+    """The tensor-core entry points refuse bad arguments before any launch:
+    negative sizes, unknown part counts, bad k-splits, missing or misaligned
+    pointers, and shapes beyond the tensor copies' coordinates."""
+    P = ctypes.c_void_p(1 << 40)
+    A = ctypes.c_void_p(1 << 30)
+    odd = ctypes.c_void_p((1 << 30) + 8)
+    # dd
+    assert lib.dd_slice_gemm_tc(-1, 4, 64, A, A, 1, P, None) == 1
+    assert lib.dd_slice_gemm_tc(4, 4, 64, A, A, 2, P, None) == 1              # 2 splits > 1 k-block
+    assert lib.dd_slice_gemm_tc(4, 4, 64, odd, A, 1, P, None) == 1            # misaligned parts
+    assert lib.dd_slice_gemm_tc(4, 4, 64, A, A, 1, odd, None) == 1            # misaligned P
+    assert lib.dd_slice_gemm_tc(4, 4, 64, A, A, 1, None, None) == 1           # no P
+    assert lib.dd_slice_gemm_tc(4, 4, 16384, A, A, 1, P, None) == 1          # one split over 8192 of k
+    assert lib.dd_recombine_tc(4, 4, P, 0, A, A, A, A, 4, None) == 1          # splits < 1
+    assert lib.dd_recombine_tc(4, 4, P, 1, A, A, A, A, 3, None) == 1          # ldc < N
+    # quad doubles
+    assert lib.qd_slice_gemm_tc(4, 4, -1, A, A, 1, P, None) == 1
+    assert lib.qd_slice_gemm_tc(4, 4, 8192, A, A, 1, P, None) == 1           # one split over 4096 of k
+    assert lib.qd_slice_gemm_tc(4, 4, (1 << 23) + 1, A, A, 4096, P, None) == 2  # K beyond the bound
+    assert lib.qd_slice_gemm_tc(1 << 20, 256, 1 << 23, A, A, 2048, P, None) == 2  # part rows >= 2^31
+    assert lib.qd_recombine_tc(4, 4, P, 1, A, A, None, 4, None) == 1          # no output planes
+    # octo / hexa doubles
+    assert lib.md_slice_gemm_tc(5, 4, 4, 64, A, A, 1, P, None) == 2           # 5 doubles: unsupported
+    assert lib.md_slice_gemm_tc(16, 4, 4, 2048, A, A, 1, P, None) == 1        # one split over 1024 of k
+    assert lib.md_slice_gemm_tc(16, 1 << 16, 256, 1 << 20, A, A, 1024, P, None) == 2  # part rows >= 2^31
+    assert lib.md_recombine_tc(12, 4, 4, P, 1, A, A, None, 4, None) == 2      # 12 doubles: unsupported
+    assert lib.md_recombine_tc(8, 4, 4, P, 0, A, A, None, 4, None) == 1
