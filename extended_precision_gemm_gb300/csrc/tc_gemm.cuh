@@ -9,6 +9,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "async_copy.cuh"
@@ -383,13 +384,14 @@ int num_sms_tc() {
 // both SMs in one GPC, so this can be below half the SM count.
 template <int NP>
 int resident_pairs() {
-    static int cached[64] = {};  // per device
+    static std::atomic<int> cached[64];  // per device; 0 = not asked yet
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         (void)cudaGetLastError();
         dev = 0;
     }
-    if (cached[dev] > 0) return cached[dev];
+    const int known = cached[dev].load(std::memory_order_relaxed);
+    if (known > 0) return known;
     int n = 0;
     if (cudaFuncSetAttribute(slice_gemm_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) ==
         cudaSuccess) {
@@ -407,8 +409,9 @@ int resident_pairs() {
         if (cudaOccupancyMaxActiveClusters(&n, slice_gemm_tc_kernel<NP>, &cfg) != cudaSuccess) n = 0;
     }
     if (n <= 0) (void)cudaGetLastError();  // no device: fall back to half the SMs
-    cached[dev] = n > 0 ? n : std::max(1, num_sms_tc() / 2);
-    return cached[dev];
+    const int pairs = n > 0 ? n : std::max(1, num_sms_tc() / 2);
+    cached[dev].store(pairs, std::memory_order_relaxed);
+    return pairs;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -416,16 +419,19 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
+    static std::atomic<EncodeTiledFn> cached{nullptr};
+    EncodeTiledFn fn = cached.load(std::memory_order_acquire);
     if (fn == nullptr) {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+            q == cudaDriverEntryPointSuccess) {
             fn = reinterpret_cast<EncodeTiledFn>(ptr);
-        else
+            cached.store(fn, std::memory_order_release);
+        } else {
             (void)cudaGetLastError();
+        }
     }
     return fn;
 }
