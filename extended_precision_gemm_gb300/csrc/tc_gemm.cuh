@@ -229,12 +229,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                 }
             }
-            // copies still in flight (of both CTAs) must land before either
-            // CTA exits: the even CTA waits for its last stages to fill
+            // copies still in flight must land before the CTA exits: the even
+            // CTA waits for its last stages to fill (its barriers count the
+            // bytes of both CTAs); the odd CTA, whose copies complete on the
+            // even CTA's barriers, waits for its last stages to be consumed
+            // (fill j is consumed when phase j / STAGES of its stage's empty
+            // barrier completes)
             const int64_t first = issued > STAGES ? issued - STAGES : 0;
-            for (int64_t j = first; leader && j < issued; ++j)
-                if (!mbar_wait_bounded(full0 + 8 * (uint32_t)(j % STAGES), (uint32_t)((j / STAGES) & 1), WAIT_NS))
-                    note_timeout(&abort_flag);
+            for (int64_t j = first; j < issued; ++j) {
+                const uint32_t bar = (leader ? full0 : empty0) + 8 * (uint32_t)(j % STAGES);
+                if (!mbar_wait_bounded(bar, (uint32_t)((j / STAGES) & 1), WAIT_NS)) {
+                    if (!abort_flag) note_timeout(&abort_flag);
+                    break;
+                }
+            }
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
