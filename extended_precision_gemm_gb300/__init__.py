@@ -27,7 +27,8 @@ __all__ = [
     "dd_gemm", "dd_gemm_ws", "dd_gemm_host", "dd_gemm_noalloc", "layout", "workspace_size",
     "split_rows", "split_cols", "slice_gemm", "recombine", "wait_timeouts", "fp64_tensor_roof",
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
-    "split", "split_i16", "dd_gemm_simt",
+    "split", "split_i16", "dd_gemm_simt", "EXP_NONE", "exponents", "split_with_exponents",
+    "split_bf16_with_exponents", "dd_gemm_tc_host", "DDGemmOpts", "dd_gemm_ex", "ex_plan", "slice_gemm_fused",
     "QD_MAX_K", "qd_gemm", "qd_layout", "qd_workspace_size", "qd_split", "qd_slice_gemm", "qd_recombine",
     "TC_SLICES", "TC_TILE_M", "TC_BLOCK_M", "TC_TILE_N", "TC_CHUNK_K", "TC_MAX_K_SPLIT",
     "dd_gemm_tc", "tc_layout", "tc_workspace_size", "split_bf16", "slice_gemm_tc", "recombine_tc",
@@ -42,6 +43,7 @@ MAX_K = 1 << 24
 TILE_M = 32
 TILE_N = 32
 CHUNK_K = 8
+EXP_NONE = -4096
 STATUS = {0: "DDGEMM_OK", 1: "DDGEMM_ERR_INVALID_ARG", 2: "DDGEMM_ERR_UNSUPPORTED",
           3: "DDGEMM_ERR_ALLOC", 4: "DDGEMM_ERR_CUDA", 5: "DDGEMM_ERR_TOO_LARGE"}
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -82,6 +84,17 @@ _SIGNATURES = {
     "dd_split": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
     "dd_split_i16": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr, _ptr], _int),
     "dd_gemm_simt": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
+    "dd_exponents": ([_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr, _ptr], _int),
+    "dd_split_with_exponents": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr, _ptr,
+                                 _ptr], _int),
+    "dd_split_bf16_with_exponents": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _ptr,
+                                      _ptr, _ptr], _int),
+    "dd_gemm_ex_plan": ([_i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr], _int),
+    "dd_gemm_ex": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr,
+                    ctypes.c_size_t, _ptr], _int),
+    "dd_slice_gemm_fused": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _int, _ptr, _ptr],
+                            _int),
+    "dd_gemm_tc_host": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
     "qd_gemm_layout": ([_i64, _i64, _i64, _ptr], _int),
     "qd_gemm_workspace_size": ([_i64, _i64, _i64, _ptr], _int),
     "qd_gemm": ([_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, ctypes.c_size_t, _ptr], _int),
@@ -445,6 +458,111 @@ def split_i16(A_hi, A_lo, B_hi, B_lo, planesA=None, e=None, planesB=None, f=None
     return _split_both("dd_split_i16", A_hi, A_lo, B_hi, B_lo, planesA, e, planesB, f, _torch().int16, stream)
 
 
+class DDGemmOpts(ctypes.Structure):
+    """ddgemm_opts of ddgemm.h (all zero = what dd_gemm does)."""
+    _fields_ = [("slices", ctypes.c_int), ("pairs", ctypes.c_int), ("split_k", ctypes.c_int),
+                ("fuse_recombine", ctypes.c_int), ("fuse_split", ctypes.c_int)]
+
+
+def _opts(split_k=0, fuse_split=False, fuse_recombine=False, slices=0, pairs=0):
+    return DDGemmOpts(slices=slices, pairs=pairs, split_k=split_k, fuse_recombine=int(bool(fuse_recombine)),
+                      fuse_split=int(bool(fuse_split)))
+
+
+def ex_plan(M: int, N: int, K: int, split_k=0, fuse_split=False, fuse_recombine=False, slices=0, pairs=0):
+    """(workspace bytes, k-splits, recombination fused) of dd_gemm_ex for
+    these options and this shape on the current device."""
+    o = _opts(split_k, fuse_split, fuse_recombine, slices, pairs)
+    n, sp, fr = ctypes.c_size_t(), _int(), _int()
+    _check("dd_gemm_ex_plan", load().dd_gemm_ex_plan(M, N, K, ctypes.byref(o), ctypes.byref(n), ctypes.byref(sp),
+                                                     ctypes.byref(fr)))
+    return n.value, sp.value, bool(fr.value)
+
+
+def dd_gemm_ex(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, split_k=0, fuse_split=False, fuse_recombine=False,
+               workspace=None, stream=None, slices=0, pairs=0):
+    """dd_gemm with options: the k-split count (0 = automatic), the split
+    fused into the slice GEMM (parts formed from hi/lo tiles, no part planes),
+    the recombination fused into its epilogue (no part-sum planes).  Every
+    combination gives dd_gemm's result bit for bit.  `workspace` (uint8
+    tensor of ex_plan()[0] bytes) is optional."""
+    M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
+    o = _opts(split_k, fuse_split, fuse_recombine, slices, pairs)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("dd_gemm_ex", load().dd_gemm_ex(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                           B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
+                                           C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi), ctypes.byref(o), wp, wn,
+                                           _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def slice_gemm_fused(A_hi, A_lo, B_hi, B_lo, e, f, splits: int, P=None, stream=None):
+    """Step 2 with the split fused in: P (splits x 8 x Mp x Np) straight from
+    hi/lo and the exponents e, f."""
+    torch = _torch()
+    M, N, K = _pair(A_hi, A_lo, B_hi, B_lo)
+    Mp, Np = -(-M // TILE_M) * TILE_M, -(-N // TILE_N) * TILE_N
+    if P is None:
+        P = torch.empty((splits, SLICES, Mp, Np), dtype=torch.float64, device=A_hi.device)
+    if P.numel() < splits * SLICES * Mp * Np or e.numel() < M or f.numel() < N:
+        raise ValueError("buffers too small")
+    _check("dd_slice_gemm_fused",
+           load().dd_slice_gemm_fused(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi), B_hi.data_ptr(),
+                                      B_lo.data_ptr(), _ld(B_hi), e.data_ptr(), f.data_ptr(), splits, P.data_ptr(),
+                                      _stream_handle(stream)))
+    return P
+
+
+def _pair(A_hi, A_lo, B_hi, B_lo):
+    for t, n in ((A_hi, "A_hi"), (A_lo, "A_lo"), (B_hi, "B_hi"), (B_lo, "B_lo")):
+        _mat(t, n)
+    M, K = A_hi.shape
+    K2, N = B_hi.shape
+    if K2 != K or A_lo.shape != A_hi.shape or B_lo.shape != B_hi.shape:
+        raise ValueError("shape mismatch")
+    if A_hi.stride() != A_lo.stride() or B_hi.stride() != B_lo.stride():
+        raise ValueError("hi and lo planes must share strides")
+    return M, N, K
+
+
+def exponents(A_hi, B_hi, e=None, f=None, stream=None):
+    """Raw shared exponents (e of the rows of A, f of the columns of B, int32),
+    EXP_NONE for a row / column without a nonzero element: the form whose
+    elementwise maximum over k-slabs is the exponent of the whole row."""
+    torch = _torch()
+    _mat(A_hi, "A_hi"), _mat(B_hi, "B_hi")
+    M, K = A_hi.shape
+    K2, N = B_hi.shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    e = torch.empty(M, dtype=torch.int32, device=A_hi.device) if e is None else e
+    f = torch.empty(N, dtype=torch.int32, device=A_hi.device) if f is None else f
+    if e.numel() < M or f.numel() < N:
+        raise ValueError("output buffers too small")
+    _check("dd_exponents", load().dd_exponents(M, N, K, A_hi.data_ptr(), _ld(A_hi), B_hi.data_ptr(), _ld(B_hi),
+                                               e.data_ptr(), f.data_ptr(), _stream_handle(stream)))
+    return e, f
+
+
+def split_with_exponents(A_hi, A_lo, B_hi, B_lo, e, f, planesA=None, planesB=None, stream=None):
+    """FP64 part planes of a k-slab against given exponents (e.g. the maximum
+    over all slabs of `exponents`): (planesA, planesB) in dd_split's layout."""
+    torch = _torch()
+    M, N, K = _pair(A_hi, A_lo, B_hi, B_lo)
+    Mp, Np, Kp = -(-M // TILE_M) * TILE_M, -(-N // TILE_N) * TILE_N, -(-K // CHUNK_K) * CHUNK_K
+    dev = A_hi.device
+    pA = torch.empty(SLICES * Mp * Kp, dtype=torch.float64, device=dev) if planesA is None else planesA
+    pB = torch.empty(SLICES * Np * Kp, dtype=torch.float64, device=dev) if planesB is None else planesB
+    if pA.numel() < SLICES * Mp * Kp or pB.numel() < SLICES * Np * Kp or e.numel() < M or f.numel() < N:
+        raise ValueError("buffers too small")
+    _check("dd_split_with_exponents",
+           load().dd_split_with_exponents(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi), B_hi.data_ptr(),
+                                          B_lo.data_ptr(), _ld(B_hi), e.data_ptr(), f.data_ptr(), pA.data_ptr(),
+                                          pB.data_ptr(), _stream_handle(stream)))
+    return pA, pB
+
+
 def dd_gemm_simt(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, stream=None):
     """The comparator: plain double-double arithmetic on the FP64 ALUs, one
     accumulator per output (no splitting)."""
@@ -638,6 +756,39 @@ def recombine_tc(M: int, N: int, P, e, f, splits=None, C_hi=None, C_lo=None, str
     _check("dd_recombine_tc", load().dd_recombine_tc(M, N, P.data_ptr(), splits, e.data_ptr(), f.data_ptr(),
                                                      C_hi.data_ptr(), C_lo.data_ptr(), _ld(C_hi),
                                                      _stream_handle(stream)))
+    return C_hi, C_lo
+
+
+def split_bf16_with_exponents(A_hi, A_lo, B_hi, B_lo, e, f, planesA=None, planesB=None, stream=None):
+    """bf16 part blocks of a k-slab against given exponents (the maximum over
+    the slabs of `exponents`): (planesA, planesB) in split_bf16's layout."""
+    torch = _torch()
+    M, N, K = _pair(A_hi, A_lo, B_hi, B_lo)
+    Mp, Np, Kp = -(-M // TC_TILE_M) * TC_TILE_M, -(-N // TC_TILE_N) * TC_TILE_N, -(-K // TC_CHUNK_K) * TC_CHUNK_K
+    dev = A_hi.device
+    pA = torch.empty(TC_SLICES * Mp * Kp, dtype=torch.int16, device=dev) if planesA is None else planesA
+    pB = torch.empty(TC_SLICES * Np * Kp, dtype=torch.int16, device=dev) if planesB is None else planesB
+    if pA.numel() < TC_SLICES * Mp * Kp or pB.numel() < TC_SLICES * Np * Kp or e.numel() < M or f.numel() < N:
+        raise ValueError("buffers too small")
+    _check("dd_split_bf16_with_exponents",
+           load().dd_split_bf16_with_exponents(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
+                                               B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi), e.data_ptr(),
+                                               f.data_ptr(), pA.data_ptr(), pB.data_ptr(), _stream_handle(stream)))
+    return pA, pB
+
+
+def dd_gemm_tc_host(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, stream=None):
+    """dd_gemm_tc with HOST operands and result (C-contiguous float64 numpy
+    arrays or CPU torch tensors, ideally pinned); returns when C is written."""
+    def ptr(x):
+        return x.data_ptr() if hasattr(x, "data_ptr") else x.ctypes.data
+    M, K = A_hi.shape
+    K2, N = B_hi.shape
+    if K2 != K or tuple(C_hi.shape) != (M, N) or tuple(C_lo.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _check("dd_gemm_tc_host", load().dd_gemm_tc_host(M, N, K, ptr(A_hi), ptr(A_lo), max(K, 1),
+                                                     ptr(B_hi), ptr(B_lo), max(N, 1),
+                                                     ptr(C_hi), ptr(C_lo), max(N, 1), _stream_handle(stream)))
     return C_hi, C_lo
 
 

@@ -1,6 +1,6 @@
 """Build the dd GEMM library (libddgemm.so) for GB300 (sm_103a) with nvcc.
 
-The four translation units compile in parallel, then link into a shared
+The translation units compile in parallel, then link into a shared
 library in ``extended_precision_gemm_gb300/_build/``.  Rebuilds only when a
 source or header is newer than the library.  Usage: ``python -m
 extended_precision_gemm_gb300.build [--force]``.
@@ -20,7 +20,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = BUILD / "libddgemm.so"
-SOURCES = ["split.cu", "slice_gemm.cu", "slice_gemm_i64.cu", "recombine.cu", "simt.cu", "md.cu", "tc.cu", "tc_md.cu", "api.cu"]
+SOURCES = ["split.cu", "slice_gemm.cu", "slice_gemm_fused.cu", "slice_gemm_i64.cu", "recombine.cu", "simt.cu", "md.cu", "tc.cu", "tc_md.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",

@@ -182,6 +182,61 @@ ddgemm_status run_gemm_i64(const Layout& L, int64_t M, int64_t N, int64_t K, con
     return DDGEMM_OK;
 }
 
+// A product with HOST operands and result: one stream-ordered device block
+// holds A_hi, A_lo (M x K dense), B_hi, B_lo (K x N), C_hi, C_lo (M x N) and
+// `ws_bytes` of workspace; the operands are copied in, `run` launches the
+// product on the dense device copies, C is copied back, the block is freed,
+// and the stream is synchronised before returning.
+// `peek` reads the slice GEMM's count of bounded waits that gave up: a count
+// that grew during the call makes it return DDGEMM_ERR_CUDA.
+template <class Run, class Peek>
+ddgemm_status host_product(int64_t M, int64_t N, int64_t K, const double* h_A_hi, const double* h_A_lo,
+                           int64_t lda, const double* h_B_hi, const double* h_B_lo, int64_t ldb, double* h_C_hi,
+                           double* h_C_lo, int64_t ldc, int64_t ws_bytes, cudaStream_t st, Run run, Peek peek) {
+    unsigned int timeouts_before = 0;
+    if (peek(&timeouts_before, st) != cudaSuccess) return DDGEMM_ERR_CUDA;
+    const int64_t a = round_up(M * K * 8, kAlign), b = round_up(K * N * 8, kAlign), c = round_up(M * N * 8, kAlign);
+    const int64_t total = 2 * a + 2 * b + 2 * c + ws_bytes;
+    char* dev = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&dev), (size_t)total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    double* dA_hi = reinterpret_cast<double*>(dev);
+    double* dA_lo = reinterpret_cast<double*>(dev + a);
+    double* dB_hi = reinterpret_cast<double*>(dev + 2 * a);
+    double* dB_lo = reinterpret_cast<double*>(dev + 2 * a + b);
+    double* dC_hi = reinterpret_cast<double*>(dev + 2 * a + 2 * b);
+    double* dC_lo = reinterpret_cast<double*>(dev + 2 * a + 2 * b + c);
+    char* ws = dev + 2 * a + 2 * b + 2 * c;
+    cudaError_t err = cudaSuccess;
+    auto copy_in = [&](double* dst, const double* src, int64_t rows, int64_t cols, int64_t ld) {
+        if (err != cudaSuccess || rows == 0 || cols == 0) return;
+        err = cudaMemcpy2DAsync(dst, (size_t)cols * 8, src, (size_t)ld * 8, (size_t)cols * 8, (size_t)rows,
+                                cudaMemcpyHostToDevice, st);
+    };
+    copy_in(dA_hi, h_A_hi, M, K, lda);
+    copy_in(dA_lo, h_A_lo, M, K, lda);
+    copy_in(dB_hi, h_B_hi, K, N, ldb);
+    copy_in(dB_lo, h_B_lo, K, N, ldb);
+    ddgemm_status s = err == cudaSuccess ? run(dA_hi, dA_lo, dB_hi, dB_lo, dC_hi, dC_lo, ws, st) : DDGEMM_ERR_CUDA;
+    if (s == DDGEMM_OK) {
+        err = cudaMemcpy2DAsync(h_C_hi, (size_t)ldc * 8, dC_hi, (size_t)N * 8, (size_t)N * 8, (size_t)M,
+                                cudaMemcpyDeviceToHost, st);
+        if (err == cudaSuccess)
+            err = cudaMemcpy2DAsync(h_C_lo, (size_t)ldc * 8, dC_lo, (size_t)N * 8, (size_t)N * 8, (size_t)M,
+                                    cudaMemcpyDeviceToHost, st);
+        if (err != cudaSuccess) s = DDGEMM_ERR_CUDA;
+    }
+    cudaError_t fe = cudaFreeAsync(dev, st);
+    cudaError_t se = cudaStreamSynchronize(st);
+    if (s == DDGEMM_OK && (fe != cudaSuccess || se != cudaSuccess)) s = DDGEMM_ERR_CUDA;
+    unsigned int timeouts_after = 0;
+    if (s == DDGEMM_OK && (peek(&timeouts_after, st) != cudaSuccess || timeouts_after != timeouts_before))
+        s = DDGEMM_ERR_CUDA;
+    return s;
+}
+
 }  // namespace
 
 extern "C" {
@@ -261,51 +316,15 @@ ddgemm_status dd_gemm_host(int64_t M, int64_t N, int64_t K, const double* h_A_hi
                                       h_C_lo, ldc);
     if (s != DDGEMM_OK) return s;
     if (M == 0 || N == 0) return DDGEMM_OK;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     Layout L = make_layout(M, N, K);
-    // One device block: A_hi, A_lo (M x K dense), B_hi, B_lo (K x N), C_hi,
-    // C_lo (M x N), then the workspace.
-    const int64_t a = round_up(M * K * 8, kAlign), b = round_up(K * N * 8, kAlign),
-                  c = round_up(M * N * 8, kAlign);
-    const int64_t total = 2 * a + 2 * b + 2 * c + L.total;
-    char* dev = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&dev), (size_t)total, st) != cudaSuccess) {
-        cudaGetLastError();
-        return DDGEMM_ERR_ALLOC;
-    }
-    double* dA_hi = reinterpret_cast<double*>(dev);
-    double* dA_lo = reinterpret_cast<double*>(dev + a);
-    double* dB_hi = reinterpret_cast<double*>(dev + 2 * a);
-    double* dB_lo = reinterpret_cast<double*>(dev + 2 * a + b);
-    double* dC_hi = reinterpret_cast<double*>(dev + 2 * a + 2 * b);
-    double* dC_lo = reinterpret_cast<double*>(dev + 2 * a + 2 * b + c);
-    char* ws = dev + 2 * a + 2 * b + 2 * c;
-    cudaError_t err = cudaSuccess;
-    auto copy_in = [&](double* dst, const double* src, int64_t rows, int64_t cols, int64_t ld) {
-        if (err != cudaSuccess || rows == 0 || cols == 0) return;
-        err = cudaMemcpy2DAsync(dst, (size_t)cols * 8, src, (size_t)ld * 8, (size_t)cols * 8, (size_t)rows,
-                                cudaMemcpyHostToDevice, st);
-    };
-    copy_in(dA_hi, h_A_hi, M, K, lda);
-    copy_in(dA_lo, h_A_lo, M, K, lda);
-    copy_in(dB_hi, h_B_hi, K, N, ldb);
-    copy_in(dB_lo, h_B_lo, K, N, ldb);
-    if (err == cudaSuccess)
-        s = run_gemm(L, M, N, K, dA_hi, dA_lo, std::max<int64_t>(K, 1), dB_hi, dB_lo, N, dC_hi, dC_lo, N, ws, st);
-    else
-        s = DDGEMM_ERR_CUDA;
-    if (s == DDGEMM_OK) {
-        err = cudaMemcpy2DAsync(h_C_hi, (size_t)ldc * 8, dC_hi, (size_t)N * 8, (size_t)N * 8, (size_t)M,
-                                cudaMemcpyDeviceToHost, st);
-        if (err == cudaSuccess)
-            err = cudaMemcpy2DAsync(h_C_lo, (size_t)ldc * 8, dC_lo, (size_t)N * 8, (size_t)N * 8, (size_t)M,
-                                    cudaMemcpyDeviceToHost, st);
-        if (err != cudaSuccess) s = DDGEMM_ERR_CUDA;
-    }
-    cudaError_t fe = cudaFreeAsync(dev, st);
-    cudaError_t se = cudaStreamSynchronize(st);
-    if (s == DDGEMM_OK && (fe != cudaSuccess || se != cudaSuccess)) s = DDGEMM_ERR_CUDA;
-    return s;
+    return host_product(M, N, K, h_A_hi, h_A_lo, lda, h_B_hi, h_B_lo, ldb, h_C_hi, h_C_lo, ldc, L.total,
+                        static_cast<cudaStream_t>(stream),
+                        [&](const double* a_hi, const double* a_lo, const double* b_hi, const double* b_lo,
+                            double* c_hi, double* c_lo, char* ws, cudaStream_t st) {
+                            return run_gemm(L, M, N, K, a_hi, a_lo, std::max<int64_t>(K, 1), b_hi, b_lo, N,
+                                            c_hi, c_lo, N, ws, st);
+                        },
+                        peek_wait_timeouts);
 }
 
 ddgemm_status dd_split_rows(int64_t M, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
@@ -362,6 +381,39 @@ ddgemm_status dd_split_i16(int64_t M, int64_t N, int64_t K, const double* A_hi, 
                            const double* B_hi, const double* B_lo, int64_t ldb, int16_t* planesA, int32_t* e,
                            int16_t* planesB, int32_t* f, void* stream) {
     return split_both(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, planesA, e, planesB, f, true, stream);
+}
+
+ddgemm_status dd_exponents(int64_t M, int64_t N, int64_t K, const double* A_hi, int64_t lda, const double* B_hi,
+                           int64_t ldb, int32_t* e, int32_t* f, void* stream) {
+    ddgemm_status s = check_shapes(M, N, K, lda, ldb, std::max<int64_t>(1, N));
+    if (s != DDGEMM_OK) return s;
+    if ((M > 0 && (e == nullptr || (K > 0 && A_hi == nullptr))) || (N > 0 && (f == nullptr || (K > 0 && B_hi == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SplitOperand a{A_hi, nullptr, lda, M, e, false}, b{B_hi, nullptr, ldb, N, f, false};
+    const SplitOperand* pa = M > 0 ? &a : nullptr;
+    const SplitOperand* pb = N > 0 ? &b : nullptr;
+    DDG_TRY(launch_reset_exponents(pa ? e : nullptr, M, pb ? f : nullptr, N, EXP_NONE, st));
+    DDG_TRY(launch_exponents(pa, pb, K, st));
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_split_with_exponents(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                                      int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb,
+                                      const int32_t* e, const int32_t* f, double* planesA, double* planesB,
+                                      void* stream) {
+    ddgemm_status s = check_shapes(M, N, K, lda, ldb, std::max<int64_t>(1, N));
+    if (s != DDGEMM_OK) return s;
+    if (M > 0 && (e == nullptr || (K > 0 && (A_hi == nullptr || A_lo == nullptr || planesA == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (N > 0 && (f == nullptr || (K > 0 && (B_hi == nullptr || B_lo == nullptr || planesB == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    // exp_given: the kernels only read the exponents
+    SplitOperand a{A_hi, A_lo, lda, M, const_cast<int32_t*>(e), true};
+    SplitOperand b{B_hi, B_lo, ldb, N, const_cast<int32_t*>(f), true};
+    return from_cuda(launch_split_f64(M > 0 ? &a : nullptr, N > 0 ? &b : nullptr, K, round_up(K, BK), planesA,
+                                      planesB, static_cast<cudaStream_t>(stream)));
 }
 
 ddgemm_status dd_slice_gemm(int64_t M, int64_t N, int64_t K, const double* planesA,
@@ -634,6 +686,149 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// dd_gemm_ex: the FP64 path with options (k-split, fused split, fused
+// recombination).
+// ---------------------------------------------------------------------------
+
+namespace {
+
+struct ExPlan {
+    int64_t Mp, Np, Kp;
+    int splits;
+    bool fuse_split, fuse_recombine;
+    int64_t off_e, off_f, off_A, off_B, off_P, total;
+};
+
+ddgemm_status make_ex_plan(int64_t M, int64_t N, int64_t K, const ddgemm_opts* opts, ExPlan& X) {
+    ddgemm_opts o{};
+    if (opts != nullptr) o = *opts;
+    if (M < 0 || N < 0 || K < 0) return DDGEMM_ERR_INVALID_ARG;
+    if (K > DDGEMM_MAX_K) return DDGEMM_ERR_UNSUPPORTED;
+    if ((o.slices != 0 && o.slices != S) || (o.pairs != 0 && o.pairs != S * (S + 1) / 2))
+        return DDGEMM_ERR_UNSUPPORTED;
+    if (o.split_k < 0 || (o.fuse_recombine != 0 && o.fuse_recombine != 1) || (o.fuse_split != 0 && o.fuse_split != 1))
+        return DDGEMM_ERR_INVALID_ARG;
+    X.Mp = round_up(M, TM);
+    X.Np = round_up(N, TN);
+    X.Kp = round_up(K, BK);
+    const int64_t KC = X.Kp / BK;
+    if (o.split_k > 0) {
+        if (o.split_k > kMaxSplits || (KC > 0 && o.split_k > KC) || (KC == 0 && o.split_k != 1))
+            return DDGEMM_ERR_INVALID_ARG;
+        if (o.fuse_recombine && o.split_k > 1) return DDGEMM_ERR_UNSUPPORTED;
+        X.splits = o.split_k;
+    } else {
+        X.splits = choose_splits(X.Mp, X.Np, KC, Engine::kFp64Tensor);
+    }
+    X.fuse_split = o.fuse_split == 1;
+    X.fuse_recombine = o.fuse_recombine == 1 && X.splits == 1;
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) { int64_t at = off; off = round_up(off + bytes, kAlign); return at; };
+    X.off_e = take(X.Mp * 4);
+    X.off_f = take(X.Np * 4);
+    X.off_A = X.fuse_split ? -1 : take(S * X.Mp * X.Kp * 8);
+    X.off_B = X.fuse_split ? -1 : take(S * X.Np * X.Kp * 8);
+    X.off_P = X.fuse_recombine ? -1 : take((int64_t)X.splits * S * X.Mp * X.Np * 8);
+    X.total = off;
+    return DDGEMM_OK;
+}
+
+ddgemm_status run_gemm_ex(const ExPlan& X, int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                          int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb, double* C_hi,
+                          double* C_lo, int64_t ldc, char* ws, cudaStream_t st) {
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    int32_t* e = reinterpret_cast<int32_t*>(ws + X.off_e);
+    int32_t* f = reinterpret_cast<int32_t*>(ws + X.off_f);
+    double* P = X.fuse_recombine ? nullptr : reinterpret_cast<double*>(ws + X.off_P);
+    if (X.fuse_split) {
+        SplitOperand a{A_hi, A_lo, lda, M, e, false}, b{B_hi, B_lo, ldb, N, f, false};
+        DDG_TRY(launch_init_exponents(e, M, f, N, K, st));
+        DDG_TRY(launch_exponents(&a, &b, K, st));
+        const FusedSrc g = make_fused_src(A_hi, A_lo, lda, B_hi, B_lo, ldb, e, f, M, N, K);
+        if (X.fuse_recombine) {
+            DDG_TRY(launch_slice_gemm_fused_recombine(g, X.Mp, X.Np, X.Kp, C_hi, C_lo, ldc, st));
+            return DDGEMM_OK;
+        }
+        DDG_TRY(launch_slice_gemm_fused(g, X.Mp, X.Np, X.Kp, X.splits, P, st));
+    } else {
+        double* pA = reinterpret_cast<double*>(ws + X.off_A);
+        double* pB = reinterpret_cast<double*>(ws + X.off_B);
+        DDG_TRY(run_split(M, N, K, X.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, false, st));
+        if (X.fuse_recombine) {
+            DDG_TRY(launch_slice_gemm_recombine(pA, pB, X.Mp, X.Np, X.Kp, e, f, M, N, C_hi, C_lo, ldc, st));
+            return DDGEMM_OK;
+        }
+        DDG_TRY(launch_slice_gemm(pA, pB, X.Mp, X.Np, X.Kp, X.splits, P, st));
+    }
+    DDG_TRY(launch_recombine(P, X.splits, X.Mp, X.Np, e, f, M, N, C_hi, C_lo, ldc, st));
+    return DDGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ddgemm_status dd_gemm_ex_plan(int64_t M, int64_t N, int64_t K, const ddgemm_opts* opts, size_t* workspace_bytes,
+                              int* splits, int* fused_recombine) {
+    ExPlan X;
+    ddgemm_status s = make_ex_plan(M, N, K, opts, X);
+    if (s != DDGEMM_OK) return s;
+    if (workspace_bytes) *workspace_bytes = (size_t)X.total;
+    if (splits) *splits = X.splits;
+    if (fused_recombine) *fused_recombine = X.fuse_recombine ? 1 : 0;
+    return DDGEMM_OK;
+}
+
+ddgemm_status dd_gemm_ex(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
+                         const double* B_hi, const double* B_lo, int64_t ldb, double* C_hi, double* C_lo,
+                         int64_t ldc, const ddgemm_opts* opts, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc);
+    if (s != DDGEMM_OK) return s;
+    ExPlan X;
+    s = make_ex_plan(M, N, K, opts, X);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t c = span_bytes(M, N, ldc);
+    if (workspace != nullptr) {
+        if ((uintptr_t)workspace % kAlign != 0 || workspace_bytes < (size_t)X.total) return DDGEMM_ERR_INVALID_ARG;
+        if (ranges_overlap(workspace, X.total, C_hi, c) || ranges_overlap(workspace, X.total, C_lo, c))
+            return DDGEMM_ERR_INVALID_ARG;
+        return run_gemm_ex(X, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc,
+                           static_cast<char*>(workspace), st);
+    }
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, (size_t)X.total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    s = run_gemm_ex(X, M, N, K, A_hi, A_lo, lda, B_hi, B_lo, ldb, C_hi, C_lo, ldc, static_cast<char*>(ws), st);
+    cudaError_t fe = cudaFreeAsync(ws, st);
+    if (s == DDGEMM_OK && fe != cudaSuccess) s = DDGEMM_ERR_CUDA;
+    return s;
+}
+
+ddgemm_status dd_slice_gemm_fused(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                                  int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb, const int32_t* e,
+                                  const int32_t* f, int splits, double* P, void* stream) {
+    ddgemm_status s = check_shapes(M, N, K, lda, ldb, std::max<int64_t>(1, N));
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    const int64_t Mp = round_up(M, TM), Np = round_up(N, TN), Kp = round_up(K, BK), KC = Kp / BK;
+    if (splits < 1 || splits > kMaxSplits || (KC > 0 && splits > KC) || (KC == 0 && splits != 1))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (P == nullptr || e == nullptr || f == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (A_hi == nullptr || A_lo == nullptr || B_hi == nullptr || B_lo == nullptr))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)P % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    const FusedSrc g = make_fused_src(A_hi, A_lo, lda, B_hi, B_lo, ldb, e, f, M, N, K);
+    return from_cuda(launch_slice_gemm_fused(g, Mp, Np, Kp, splits, P, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
 // Double doubles with 8-bit parts on the bf16 tensor cores.
 // ---------------------------------------------------------------------------
 
@@ -849,6 +1044,24 @@ ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K, const double* A_hi, co
     return s;
 }
 
+ddgemm_status dd_gemm_tc_host(int64_t M, int64_t N, int64_t K, const double* h_A_hi, const double* h_A_lo,
+                              int64_t lda, const double* h_B_hi, const double* h_B_lo, int64_t ldb, double* h_C_hi,
+                              double* h_C_lo, int64_t ldc, void* stream) {
+    ddgemm_status s = check_gemm_args(M, N, K, h_A_hi, h_A_lo, lda, h_B_hi, h_B_lo, ldb, h_C_hi, h_C_lo, ldc);
+    if (s == DDGEMM_OK) s = check_tc_shapes(M, N, K);
+    if (s != DDGEMM_OK) return s;
+    if (M == 0 || N == 0) return DDGEMM_OK;
+    TcLayout L = make_tc_layout(M, N, K);
+    return host_product(M, N, K, h_A_hi, h_A_lo, lda, h_B_hi, h_B_lo, ldb, h_C_hi, h_C_lo, ldc, L.total,
+                        static_cast<cudaStream_t>(stream),
+                        [&](const double* a_hi, const double* a_lo, const double* b_hi, const double* b_lo,
+                            double* c_hi, double* c_lo, char* ws, cudaStream_t st) {
+                            return run_gemm_tc(L, M, N, K, a_hi, a_lo, std::max<int64_t>(K, 1), b_hi, b_lo, N,
+                                               c_hi, c_lo, N, ws, st);
+                        },
+                        peek_wait_timeouts_tc);
+}
+
 ddgemm_status dd_split_bf16(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo, int64_t lda,
                             const double* B_hi, const double* B_lo, int64_t ldb, uint16_t* planesA, int32_t* e,
                             uint16_t* planesB, int32_t* f, void* stream) {
@@ -863,6 +1076,25 @@ ddgemm_status dd_split_bf16(int64_t M, int64_t N, int64_t K, const double* A_hi,
     const int64_t Kp = round_up(K, kTcK);
     return from_cuda(run_split_tc(M, N, K, Kp, A_hi, A_lo, lda, M > 0 ? e : nullptr, planesA, B_hi, B_lo, ldb,
                                   N > 0 ? f : nullptr, planesB, static_cast<cudaStream_t>(stream)));
+}
+
+ddgemm_status dd_split_bf16_with_exponents(int64_t M, int64_t N, int64_t K, const double* A_hi, const double* A_lo,
+                                           int64_t lda, const double* B_hi, const double* B_lo, int64_t ldb,
+                                           const int32_t* e, const int32_t* f, uint16_t* planesA, uint16_t* planesB,
+                                           void* stream) {
+    ddgemm_status s = check_shapes(M, N, K, lda, ldb, std::max<int64_t>(1, N));
+    if (s == DDGEMM_OK) s = check_tc_shapes(M, N, K);
+    if (s != DDGEMM_OK) return s;
+    if (M > 0 && (e == nullptr || (K > 0 && (A_hi == nullptr || A_lo == nullptr || planesA == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if (N > 0 && (f == nullptr || (K > 0 && (B_hi == nullptr || B_lo == nullptr || planesB == nullptr))))
+        return DDGEMM_ERR_INVALID_ARG;
+    if ((uintptr_t)planesA % 16 != 0 || (uintptr_t)planesB % 16 != 0) return DDGEMM_ERR_INVALID_ARG;
+    SplitOperand a{A_hi, A_lo, lda, M, const_cast<int32_t*>(e), true};
+    SplitOperand b{B_hi, B_lo, ldb, N, const_cast<int32_t*>(f), true};
+    return from_cuda(launch_split_bf16(M > 0 ? &a : nullptr, N > 0 ? &b : nullptr, K, round_up(K, kTcK),
+                                       M > 0 ? planesA : nullptr, N > 0 ? planesB : nullptr,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 ddgemm_status dd_slice_gemm_tc(int64_t M, int64_t N, int64_t K, const uint16_t* planesA, const uint16_t* planesB,
@@ -1211,7 +1443,11 @@ void* g_noalloc_addr[kMaxDevices] = {};
 // the first call for that device).
 ddgemm_status noalloc_scratch(char** addr) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DDGEMM_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();  // leave no error behind for the caller's next CUDA call
+        return DDGEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return DDGEMM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     if (g_noalloc_addr[dev] == nullptr) {
         void* p = nullptr;

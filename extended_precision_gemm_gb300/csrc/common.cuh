@@ -15,7 +15,7 @@ constexpr int TM = DDGEMM_TILE_M;          // 32
 constexpr int TN = DDGEMM_TILE_N;          // 32
 constexpr int BK = DDGEMM_CHUNK_K;         // 8
 constexpr int CHUNK_DOUBLES = S * BK * TM; // one (tile, k-chunk) block of all 8 planes: 2048 doubles
-constexpr int EXP_NONE = -4096;            // "no nonzero element seen" exponent sentinel
+constexpr int EXP_NONE = DDGEMM_EXP_NONE;  // "no nonzero element seen" exponent sentinel
 
 static_assert(TM == TN, "tiles of A and B share one layout");
 static_assert(BK % 4 == 0, "k-chunk holds whole k4 groups of the m8n8k4 fragments");

@@ -10,16 +10,23 @@ namespace ddg {
 // columns); `rows` counts rows of A or columns of B; element (r, k) is
 // hi[r * ld + k] for A and hi[k * ld + r] for B.  Exponent arrays are
 // accumulated with atomicMax and must be reset by launch_init_exponents
-// first.  Either operand may be null.
+// first.  Either operand may be null.  The split kernels turn the sentinel
+// EXP_NONE of an all-zero row into its final exponent 0 in place, unless
+// exp_given is set (exponents supplied by the caller, read only).
 struct SplitOperand {
     const double* hi;
     const double* lo;
     int64_t ld;
     int64_t rows;
     int32_t* exp;
+    bool exp_given;
 };
 cudaError_t launch_init_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int64_t K,
                                   cudaStream_t st);
+// Set every exponent to `value` (EXP_NONE before launch_exponents when the
+// raw maxima, sentinel included, are wanted).
+cudaError_t launch_reset_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int32_t value,
+                                   cudaStream_t st);
 cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, cudaStream_t st);
 // FP64 parts in the tiled layout of the mma.sync slice GEMM.
 cudaError_t launch_split_f64(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
@@ -33,6 +40,30 @@ cudaError_t launch_split_i16(const SplitOperand* A, const SplitOperand* B, int64
 cudaError_t launch_slice_gemm(const double* planesA, const double* planesB, int64_t Mp,
                               int64_t Np, int64_t Kp, int splits, double* P, cudaStream_t st);
 int slice_gemm_ctas_per_sm();
+
+// Step 2 with the recombination in the epilogue (one k-split): C directly.
+cudaError_t launch_slice_gemm_recombine(const double* planesA, const double* planesB, int64_t Mp, int64_t Np,
+                                        int64_t Kp, const int32_t* e, const int32_t* f, int64_t M, int64_t N,
+                                        double* C_hi, double* C_lo, int64_t ldc, cudaStream_t st);
+
+// Step 2 with step 1's split fused into the prologue: the parts are formed
+// from hi/lo tiles of A (rows, leading dimension lda) and B (K x N, ldb)
+// against the exponents e, f (EXP_NONE reads as 0); no part planes.
+struct FusedSrc {
+    const double* A_hi; const double* A_lo; int64_t lda;
+    const double* B_hi; const double* B_lo; int64_t ldb;
+    const int32_t* e; const int32_t* f;
+    int64_t M, N, K;
+    bool a_vec;  // A_hi, A_lo 16-byte aligned and lda even: 16-byte loads
+};
+FusedSrc make_fused_src(const double* A_hi, const double* A_lo, int64_t lda, const double* B_hi, const double* B_lo,
+                        int64_t ldb, const int32_t* e, const int32_t* f, int64_t M, int64_t N, int64_t K);
+cudaError_t launch_slice_gemm_fused(const FusedSrc& g, int64_t Mp, int64_t Np, int64_t Kp, int splits, double* P,
+                                    cudaStream_t st);
+// ... and the recombination in the epilogue as well (one k-split): C directly.
+cudaError_t launch_slice_gemm_fused_recombine(const FusedSrc& g, int64_t Mp, int64_t Np, int64_t Kp,
+                                              double* C_hi, double* C_lo, int64_t ldc, cudaStream_t st);
+int slice_gemm_fused_ctas_per_sm();
 
 // Step 2 on the integer pipe: the same P from int16 parts, exact int64 sums.
 cudaError_t launch_slice_gemm_i64(const int16_t* planesA, const int16_t* planesB, int64_t Mp,
@@ -106,5 +137,9 @@ cudaError_t read_and_reset_wait_timeouts_tc_md(unsigned int* count);
 
 // Diagnostics of the bounded waits inside the slice GEMM.
 cudaError_t read_and_reset_wait_timeouts(unsigned int* count);
+// The counts of the FP64 slice GEMM / the bf16 dd slice GEMM without
+// clearing them, read after the work on `st` (synchronises `st`).
+cudaError_t peek_wait_timeouts(unsigned int* count, cudaStream_t st);
+cudaError_t peek_wait_timeouts_tc(unsigned int* count, cudaStream_t st);
 
 }  // namespace ddg

@@ -17,6 +17,7 @@
 //     non-overlapping doubles, x_0 = RN(X), x_1 = RN(X - x_0), ... (the page
 //     fixes double-double summation only for double doubles; the exact sum
 //     rounded once is the plain reading for more parts).
+#include <atomic>
 #include <algorithm>
 
 #include "async_copy.cuh"
@@ -306,15 +307,17 @@ cudaError_t launch_split_qd(const double* const* A, int64_t lda, int64_t M, cons
 }
 
 int slice_gemm_qd_ctas_per_sm() {
-    static int cached = 0;
-    if (cached > 0) return cached;
+    static std::atomic<int> cached{0};  // per-SM count of this kernel (the same on every device)
+    if (const int c = cached.load(std::memory_order_relaxed); c > 0) return c;
     int n = 0;
     if (cudaFuncSetAttribute(slice_gemm_qd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QSMEM) !=
             cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, slice_gemm_qd_kernel, QTHREADS, QSMEM) != cudaSuccess ||
-        n <= 0)
+        n <= 0) {
+        cudaGetLastError();
         return 1;
-    cached = n;
+    }
+    cached.store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -25,11 +25,13 @@
 //    layout [part][k4][row][k%4] makes each fragment 32 consecutive doubles.
 // Every wait on an mbarrier is bounded in time; a block that gives up counts
 // itself in a device counter (see dd_wait_timeouts) and stops.
+#include <atomic>
 #include <algorithm>
 
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.cuh"
+#include "slice_mma.cuh"
 
 namespace ddg {
 namespace {
@@ -40,7 +42,6 @@ constexpr int STAGE_DOUBLES = 2 * CHUNK_DOUBLES;            // A block + B block
 constexpr uint32_t COPY_BYTES = CHUNK_DOUBLES * sizeof(double);  // 16 KB per operand
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_DOUBLES * sizeof(double) + 64;
 constexpr unsigned long long WAIT_BUDGET_NS = 2000000000ULL;  // 2 s per wait
-constexpr int64_t TILE_GROUP = 16;
 
 static_assert(COPY_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 
@@ -55,60 +56,16 @@ __device__ __forceinline__ void issue_stage(uint32_t bar, double* dst, const dou
     bulk_load(dst + CHUNK_DOUBLES, srcB, COPY_BYTES, bar);
 }
 
-__device__ __forceinline__ void dmma(double& c0, double& c1, double a, double b) {
-    asm("mma.sync.aligned.m8n8k4.row.col.f64.f64.f64.f64 {%0,%1}, {%2}, {%3}, {%0,%1};"
-        : "+d"(c0), "+d"(c1)
-        : "d"(a), "d"(b));
-}
-
-// One k-chunk (8 values of k) of all 36 pairs for the warp's 16x16 quadrant
-// of the tile: rows mq*16 + {0..15}, columns nq*16 + {0..15}, i.e. m8n8
-// blocks mb in {2mq, 2mq+1} and nb in {2nq, 2nq+1}.  acc[d][i][j][2] holds
-// index sum d of block (2mq+i, 2nq+j).  Every warp runs the same instruction
-// stream.  Within a k4 step the B fragments of all 8 parts are loaded once;
-// then for each part s of A the 8-s pairs (s, t) are issued, so consecutive
-// updates of one accumulator are at least 4 * (8 - s) >= 4 MMAs apart.
-__device__ __forceinline__ void chunk_products(const double* __restrict__ As,
-                                               const double* __restrict__ Bs, int lane, int mq,
-                                               int nq, double (&acc)[S][2][2][2]) {
-#pragma unroll
-    for (int q = 0; q < BK / 4; ++q) {
-        double b[S][2];
-#pragma unroll
-        for (int t = 0; t < S; ++t)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) b[t][j] = Bs[((t * (BK / 4) + q) * TN + (2 * nq + j) * 8) * 4 + lane];
-#pragma unroll
-        for (int s = 0; s < S; ++s) {
-            double a[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) a[i] = As[((s * (BK / 4) + q) * TM + (2 * mq + i) * 8) * 4 + lane];
-#pragma unroll
-            for (int t = 0; t + s < S; ++t)
-#pragma unroll
-                for (int i = 0; i < 2; ++i)
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) dmma(acc[s + t][i][j][0], acc[s + t][i][j][1], a[i], b[t][j]);
-        }
-    }
-}
-
+template <bool RECOMBINE>
 __global__ void __launch_bounds__(THREADS, 2)
     slice_gemm_kernel(const double* __restrict__ planesA, const double* __restrict__ planesB,
-                      int64_t KC, int splits, double* __restrict__ P, int64_t Mp, int64_t Np) {
+                      int64_t KC, int splits, TileOut out) {
     extern __shared__ __align__(128) double smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_DOUBLES);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // Tile order: groups of TILE_GROUP row tiles, column-major inside a group,
-    // so the blocks resident at one time share few A and B blocks (L2 reuse).
-    const int64_t MT = Mp / TM, NT = Np / TN;
-    const int64_t t = blockIdx.x;
-    const int64_t group = t / (TILE_GROUP * NT);
-    const int64_t first = group * TILE_GROUP;
-    const int64_t rows = min((int64_t)TILE_GROUP, MT - first);
-    const int64_t local = t - group * TILE_GROUP * NT;
-    const int64_t mt = first + local % rows, nt = local / rows;
+    int64_t mt, nt;
+    tile_of(blockIdx.x, out.Mp / TM, out.Np / TN, mt, nt);
     const int z = blockIdx.y;
     const int64_t kc0 = (int64_t)z * KC / splits, kc1 = (int64_t)(z + 1) * KC / splits;
     const int nk = (int)(kc1 - kc0);
@@ -160,22 +117,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         chunk_products(As, As + CHUNK_DOUBLES, lane, mq, nq, acc);
     }
 
-    // Epilogue: for block (mb, nb) the thread holds row mb*8 + lane/4 and
-    // columns nb*8 + 2(lane%4) + {0, 1}.
-    const int64_t plane = Mp * Np;
-#pragma unroll
-    for (int d = 0; d < S; ++d) {
-        double* out = P + ((int64_t)z * S + d) * plane;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int64_t row = mt * TM + (2 * mq + i) * 8 + (lane >> 2);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int64_t col = nt * TN + (2 * nq + j) * 8 + 2 * (lane & 3);
-                *reinterpret_cast<double2*>(out + row * Np + col) = make_double2(acc[d][i][j][0], acc[d][i][j][1]);
-            }
-        }
-    }
+    store_tile<RECOMBINE>(acc, out, lane, mq, nq, mt, nt, z);
 }
 
 // Register-only throughput loop of the same mma.sync.m8n8k4.f64 instruction:
@@ -224,28 +166,54 @@ cudaError_t measure_dmma_roof(double* tflops, cudaStream_t st) {
 }
 
 int slice_gemm_ctas_per_sm() {
-    static int cached = 0;
-    if (cached > 0) return cached;
+    static std::atomic<int> cached{0};  // per-SM count of this kernel (the same on every device)
+    if (const int c = cached.load(std::memory_order_relaxed); c > 0) return c;
     int n = 0;
-    if (cudaFuncSetAttribute(slice_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(slice_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, slice_gemm_kernel, THREADS, SMEM_BYTES) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, slice_gemm_kernel<false>, THREADS, SMEM_BYTES) !=
             cudaSuccess ||
-        n <= 0)
+        n <= 0) {
+        cudaGetLastError();
         return 1;
-    cached = n;
+    }
+    cached.store(n, std::memory_order_relaxed);
     return n;
 }
 
 cudaError_t launch_slice_gemm(const double* planesA, const double* planesB, int64_t Mp,
                               int64_t Np, int64_t Kp, int splits, double* P, cudaStream_t st) {
     if (Mp == 0 || Np == 0) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(slice_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(slice_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
+    TileOut out{};
+    out.P = P;
+    out.Mp = Mp;
+    out.Np = Np;
     dim3 grid((unsigned)((Mp / TM) * (Np / TN)), (unsigned)splits);
-    slice_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(planesA, planesB, Kp / BK, splits, P, Mp, Np);
+    slice_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(planesA, planesB, Kp / BK, splits, out);
     return cudaGetLastError();
+}
+
+cudaError_t launch_slice_gemm_recombine(const double* planesA, const double* planesB, int64_t Mp, int64_t Np,
+                                        int64_t Kp, const int32_t* e, const int32_t* f, int64_t M, int64_t N,
+                                        double* C_hi, double* C_lo, int64_t ldc, cudaStream_t st) {
+    if (Mp == 0 || Np == 0) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(slice_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    const TileOut out = recombine_out(Mp, Np, e, f, M, N, C_hi, C_lo, ldc);
+    dim3 grid((unsigned)((Mp / TM) * (Np / TN)), 1u);
+    slice_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(planesA, planesB, Kp / BK, 1, out);
+    return cudaGetLastError();
+}
+
+cudaError_t peek_wait_timeouts(unsigned int* count, cudaStream_t st) {
+    cudaError_t err = cudaMemcpyFromSymbolAsync(count, g_wait_timeouts, sizeof(unsigned int), 0,
+                                                cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    return err;
 }
 
 cudaError_t read_and_reset_wait_timeouts(unsigned int* count) {

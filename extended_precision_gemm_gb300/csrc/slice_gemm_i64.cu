@@ -21,6 +21,7 @@
 // 4 KB of B per k-chunk) with bounded mbarrier waits feeds shared memory;
 // each k costs four 128-bit shared loads (broadcast inside the warp), 32
 // unpacks and 144 multiply-adds per thread.
+#include <atomic>
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.cuh"
@@ -182,16 +183,18 @@ __global__ void __launch_bounds__(THREADS, 3)
 }  // namespace
 
 int slice_gemm_i64_ctas_per_sm() {
-    static int cached = 0;
-    if (cached > 0) return cached;
+    static std::atomic<int> cached{0};  // per-SM count of this kernel (the same on every device)
+    if (const int c = cached.load(std::memory_order_relaxed); c > 0) return c;
     int n = 0;
     if (cudaFuncSetAttribute(slice_gemm_i64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, slice_gemm_i64_kernel, THREADS, SMEM_BYTES) !=
             cudaSuccess ||
-        n <= 0)
+        n <= 0) {
+        cudaGetLastError();
         return 1;
-    cached = n;
+    }
+    cached.store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -12,6 +12,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "digits.cuh"
 #include "fixed_point.cuh"
 #include "launch.cuh"
 
@@ -120,31 +121,10 @@ __global__ void __launch_bounds__(256) exponents_kernel(ExpGrid g) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// Digits.  X = floor(|hi + lo| * 2^(104 - e)) < 2^104 (fixed_point.cuh); the
-// parts are its 13-bit fields, most significant first, with the sign of the
-// element.
-// ---------------------------------------------------------------------------
-
-using fxp::fixed_point;
-
-// 13-bit field s of X, most significant first.
-__device__ __forceinline__ uint32_t digit_field(unsigned __int128 X, int s) {
-    return (uint32_t)(X >> (DIGIT * (S - 1 - s))) & ((1u << DIGIT) - 1);
-}
-
-// The 8 parts as doubles (exact small integers).
-__device__ __forceinline__ void split_digits(double hi, double lo, int e, double out[S]) {
-    uint64_t sign;
-    const unsigned __int128 X = fixed_point(hi, lo, e, sign);
-#pragma unroll
-    for (int s = 0; s < S; ++s) out[s] = small_int_to_double(digit_field(X, s), sign);
-}
-
 // The 8 parts as int16, packed two per 32-bit word (part 2j in the low half).
 __device__ __forceinline__ uint4 split_digits_i16(double hi, double lo, int e) {
     uint64_t sign;
-    const unsigned __int128 X = fixed_point(hi, lo, e, sign);
+    const unsigned __int128 X = fxp::fixed_point(hi, lo, e, sign);
     uint32_t w[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -177,6 +157,7 @@ struct SplitGrid {
     const double* B_hi; const double* B_lo; int64_t ldb, N, b_tiles;
     int64_t K, Kp, KT;  // KT = k-items per tile
     int32_t* e; int32_t* f;
+    bool a_given, b_given;  // exponents supplied by the caller: never written
     void* planesA; void* planesB;
 };
 
@@ -196,7 +177,7 @@ __device__ __forceinline__ int load_item(const SplitGrid& g, bool is_a, int64_t 
     if (is_a) {
         if (rr >= g.M) return 0;
         const int32_t er = g.e[rr];
-        if (kt == 0 && w == 0 && er == EXP_NONE) g.e[rr] = 0;
+        if (!g.a_given && kt == 0 && w == 0 && er == EXP_NONE) g.e[rr] = 0;
         const double* ph = g.A_hi + rr * g.lda + k0;
         const double* pl = g.A_lo + rr * g.lda + k0;
         if (VEC == 2 && k0 + 3 < g.K) {
@@ -215,7 +196,7 @@ __device__ __forceinline__ int load_item(const SplitGrid& g, bool is_a, int64_t 
     }
     if (rr >= g.N) return 0;
     const int32_t fr = g.f[rr];
-    if (kt == 0 && w == 0 && fr == EXP_NONE) g.f[rr] = 0;
+    if (!g.b_given && kt == 0 && w == 0 && fr == EXP_NONE) g.f[rr] = 0;
 #pragma unroll
     for (int r = 0; r < 4; ++r)
         if (k0 + r < g.K) {
@@ -370,6 +351,14 @@ cudaError_t launch_init_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, 
     return cudaGetLastError();
 }
 
+cudaError_t launch_reset_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int32_t value,
+                                   cudaStream_t st) {
+    int64_t n = std::max(e ? M : 0, f ? N : 0);
+    if (n == 0) return cudaSuccess;
+    init_exponents_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(e, M, f, N, value);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, cudaStream_t st) {
     if (K == 0) return cudaSuccess;
     ExpGrid g{};
@@ -407,8 +396,14 @@ static SplitGrid make_split_grid(const SplitOperand* A, const SplitOperand* B, i
     g.K = K;
     g.Kp = Kp;
     g.KT = (Kp / BK + SPLIT_CHUNKS - 1) / SPLIT_CHUNKS;
-    if (A) { g.A_hi = A->hi; g.A_lo = A->lo; g.lda = A->ld; g.M = A->rows; g.a_tiles = (A->rows + TM - 1) / TM; g.e = A->exp; }
-    if (B) { g.B_hi = B->hi; g.B_lo = B->lo; g.ldb = B->ld; g.N = B->rows; g.b_tiles = (B->rows + TN - 1) / TN; g.f = B->exp; }
+    if (A) {
+        g.A_hi = A->hi; g.A_lo = A->lo; g.lda = A->ld; g.M = A->rows; g.a_tiles = (A->rows + TM - 1) / TM;
+        g.e = A->exp; g.a_given = A->exp_given;
+    }
+    if (B) {
+        g.B_hi = B->hi; g.B_lo = B->lo; g.ldb = B->ld; g.N = B->rows; g.b_tiles = (B->rows + TN - 1) / TN;
+        g.f = B->exp; g.b_given = B->exp_given;
+    }
     g.planesA = planesA;
     g.planesB = planesB;
     return g;

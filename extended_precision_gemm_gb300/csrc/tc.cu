@@ -79,6 +79,7 @@ struct TcSplitGrid {
     int64_t K, KB;  // KB = k-blocks of 64
     uint16_t* planesA; uint16_t* planesB;
     bool a_vec;     // A_hi, A_lo 16-byte aligned and lda even: 128-bit loads
+    bool a_given, b_given;  // exponents supplied by the caller: never written
 };
 
 // One warp per task, 256 elements each: 4 rows of A, or 4 columns of B, x
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
             int ep = 1;
             if (r < g.M) {
                 const int32_t er = g.e[r];
-                if (kb == 0 && kc == 0 && er == EXP_NONE) g.e[r] = 0;
+                if (!g.a_given && kb == 0 && kc == 0 && er == EXP_NONE) g.e[r] = 0;
                 ep = effective_exponent(er) + 1;
                 const double* ph = g.A_hi + r * g.lda + k0;
                 const double* pl = g.A_lo + r * g.lda + k0;
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
             int ep = 1;
             if (n < g.N) {
                 const int32_t fr = g.f[n];
-                if (kb == 0 && kc == 0 && fr == EXP_NONE) g.f[n] = 0;
+                if (!g.b_given && kb == 0 && kc == 0 && fr == EXP_NONE) g.f[n] = 0;
                 ep = effective_exponent(fr) + 1;
             }
             const int64_t k0 = kb * TBK + kc * 8;
@@ -476,12 +477,12 @@ cudaError_t launch_split_bf16(const SplitOperand* A, const SplitOperand* B, int6
     g.K = K;
     g.KB = Kp / TBK;
     if (A) {
-        g.A_hi = A->hi; g.A_lo = A->lo; g.lda = A->ld; g.M = A->rows; g.e = A->exp;
+        g.A_hi = A->hi; g.A_lo = A->lo; g.lda = A->ld; g.M = A->rows; g.e = A->exp; g.a_given = A->exp_given;
         g.a_tasks = (round_up(A->rows, PAIR_M) / 4) * g.KB;
         g.a_vec = (uintptr_t)A->hi % 16 == 0 && (uintptr_t)A->lo % 16 == 0 && A->ld % 2 == 0;
     }
     if (B) {
-        g.B_hi = B->hi; g.B_lo = B->lo; g.ldb = B->ld; g.N = B->rows; g.f = B->exp;
+        g.B_hi = B->hi; g.B_lo = B->lo; g.ldb = B->ld; g.N = B->rows; g.f = B->exp; g.b_given = B->exp_given;
         g.b_tasks = (round_up(B->rows, TBN) / 4) * g.KB;
     }
     g.planesA = planesA;
@@ -560,6 +561,8 @@ cudaError_t launch_recombine_tc_qd(const int32_t* P, int splits, int64_t Mp, int
 }
 
 cudaError_t read_and_reset_wait_timeouts_tc(unsigned int* count) { return reset_tc_timeouts(count); }
+
+cudaError_t peek_wait_timeouts_tc(unsigned int* count, cudaStream_t st) { return peek_tc_timeouts(count, st); }
 
 int tc_resident_pairs() { return resident_pairs<TS>(); }
 

@@ -416,10 +416,14 @@ int resident_pairs() {
         cfg.numAttrs = 1;
         if (cudaOccupancyMaxActiveClusters(&n, slice_gemm_tc_kernel<NP>, &cfg) != cudaSuccess) n = 0;
     }
-    if (n <= 0) (void)cudaGetLastError();  // no device: fall back to half the SMs
-    const int pairs = n > 0 ? n : std::max(1, num_sms_tc() / 2);
-    cached[dev].store(pairs, std::memory_order_relaxed);
-    return pairs;
+    if (n <= 0) {
+        // no answer (no device, or a failure that may pass): half the SMs,
+        // not remembered, so that a later call asks again
+        (void)cudaGetLastError();
+        return std::max(1, num_sms_tc() / 2);
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -493,6 +497,15 @@ cudaError_t launch_slice_gemm_parts(const uint16_t* planesA, const uint16_t* pla
     dim3 grid((unsigned)(2 * g.pairs), 1);  // clusters of 2 along x
     slice_gemm_tc_kernel<NP><<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(g, tmA, tmB);
     return cudaGetLastError();
+}
+
+// This translation unit's count of bounded waits that gave up, read once the
+// work on `st` before it has finished (synchronises `st`).
+cudaError_t peek_tc_timeouts(unsigned int* count, cudaStream_t st) {
+    cudaError_t err = cudaMemcpyFromSymbolAsync(count, g_wait_timeouts_tc, sizeof(unsigned int), 0,
+                                                cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    return err;
 }
 
 // Read and clear this translation unit's count of bounded waits that gave up.

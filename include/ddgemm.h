@@ -28,6 +28,14 @@
  *     is exact (the argument of eq. (5) of the paper, for 13-bit parts and
  *     8 index sums).  Larger K returns DDGEMM_ERR_UNSUPPORTED.
  *   - M, N or K = 0 is valid; K = 0 writes C = +0.
+ *   - Every wait inside a slice GEMM on its operand copies is bounded in
+ *     time.  A block that gives up stops early, leaves its part of the result
+ *     incomplete and counts itself in a device counter; the asynchronous
+ *     entry points cannot see this and still return DDGEMM_OK.  A result
+ *     counts only if dd_wait_timeouts (which synchronises) reads 0 after it;
+ *     the blocking host-buffer entry points (dd_gemm_host, dd_gemm_tc_host)
+ *     check the counter themselves and return DDGEMM_ERR_CUDA when it is not
+ *     0.  (It stays 0 in normal operation.)
  */
 #ifndef DDGEMM_H
 #define DDGEMM_H
@@ -45,6 +53,7 @@ extern "C" {
 #define DDGEMM_TILE_M 32         /* row tile of the part planes of A / of P */
 #define DDGEMM_TILE_N 32         /* column tile of the part planes of B / of P */
 #define DDGEMM_CHUNK_K 8         /* k-chunk of the part planes */
+#define DDGEMM_EXP_NONE (-4096)  /* raw exponent of an all-zero row / column (dd_exponents) */
 
 typedef enum {
     DDGEMM_OK = 0,
@@ -115,6 +124,60 @@ ddgemm_status dd_gemm_host(int64_t M, int64_t N, int64_t K,
                            double* h_C_hi, double* h_C_lo, int64_t ldc, void* stream);
 
 /*
+ * Options of dd_gemm_ex.  A zero-initialised struct (or a NULL pointer) asks
+ * for what dd_gemm does.
+ *   slices:         parts per double double: 0 or 8 (the only count built;
+ *                   other values return DDGEMM_ERR_UNSUPPORTED).
+ *   pairs:          part pairs kept: 0 or 36, every pair with index sum
+ *                   s + t <= 7 (others: DDGEMM_ERR_UNSUPPORTED).
+ *   split_k:        k-splits of the slice GEMM: 0 = automatic (as
+ *                   dd_gemm_layout), else 1 .. min(64, Kp / 8) (1 when K = 0);
+ *                   any count gives the same result bit for bit.
+ *   fuse_recombine: 1 = the recombination (steps 4-5 of Section 2) runs in
+ *                   the slice GEMM's epilogue, which writes C directly: no
+ *                   part-sum planes P.  It needs all of k in one block: with
+ *                   split_k = 1 it always applies; with split_k = 0 it applies
+ *                   when the automatic choice is one split (dd_gemm_ex_plan
+ *                   tells); split_k > 1 returns DDGEMM_ERR_UNSUPPORTED.
+ *   fuse_split:     1 = the 13-bit parts are formed inside the slice GEMM from
+ *                   hi/lo tiles of A and B (the conversion pipelined behind
+ *                   the MMAs; "Ozaki 2.5: Engineering the Deconstruction Path
+ *                   of fp64-Emulated Dense Matrix Multiplication on FP8 Tensor
+ *                   Cores", summary): no part planes.  The exponents are still
+ *                   found first (one pass over A_hi and B_hi).
+ * Every combination gives C identical bit for bit to dd_gemm's.
+ */
+typedef struct {
+    int slices;
+    int pairs;
+    int split_k;
+    int fuse_recombine;
+    int fuse_split;
+} ddgemm_opts;
+
+/*
+ * What dd_gemm_ex does with these options for this shape on the current
+ * device: its workspace bytes, its k-split count, and whether the
+ * recombination runs in the slice GEMM (1) or as its own kernel (0).  Any
+ * output pointer may be NULL.  Errors as dd_gemm_ex's option checks.
+ */
+ddgemm_status dd_gemm_ex_plan(int64_t M, int64_t N, int64_t K, const ddgemm_opts* opts,
+                              size_t* workspace_bytes, int* splits, int* fused_recombine);
+
+/*
+ * C = A * B (double double) with options (ddgemm_opts; NULL = defaults).
+ * `workspace` (dd_gemm_ex_plan's bytes, 256-byte aligned) may be NULL: then
+ * it comes from the stream-ordered allocator (DDGEMM_ERR_ALLOC on failure).
+ * With both fusions the workspace holds only the exponents (4 (Mp + Np)
+ * bytes).  Otherwise as dd_gemm_ws.
+ */
+ddgemm_status dd_gemm_ex(int64_t M, int64_t N, int64_t K,
+                         const double* A_hi, const double* A_lo, int64_t lda,
+                         const double* B_hi, const double* B_lo, int64_t ldb,
+                         double* C_hi, double* C_lo, int64_t ldc,
+                         const ddgemm_opts* opts, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * C = A * B (double double) without allocating any memory.
  *
  * The paper has no counterpart to this entry point; it exists for callers
@@ -137,7 +200,8 @@ ddgemm_status dd_gemm_host(int64_t M, int64_t N, int64_t K,
  * reading it, so leftovers never change a result and nothing needs clearing;
  * but calls whose work can overlap on the same GPU (issued on different
  * streams, or from different host threads) race on the buffer: order them,
- * for example by issuing them on one stream.
+ * for example by issuing them on one stream.  Device ordinals 0..63 are
+ * served; a current device of 64 or more returns DDGEMM_ERR_CUDA.
  */
 #define DDGEMM_NOALLOC_SCRATCH_BYTES (64u << 20)
 ddgemm_status dd_gemm_noalloc(int64_t M, int64_t N, int64_t K,
@@ -191,6 +255,42 @@ ddgemm_status dd_split(int64_t M, int64_t N, int64_t K,
                        double* planesA, int32_t* e, double* planesB, int32_t* f, void* stream);
 
 /*
+ * The k-split of the product across devices or passes (each holds a slab of
+ * the inner dimension: columns k0..k1-1 of A and the same rows of B).  The
+ * paper's method splits each row of A / column of B on one exponent grid
+ * (Section 2; Problems 3.2 and 3.4 of Section 3); for the slab products to add
+ * up to the unsplit ones every slab must use the exponents of the WHOLE row /
+ * column, the maximum over the slabs.  Pattern: dd_exponents on each slab ->
+ * elementwise MAX of the e (and f) arrays over the slabs (an all-reduce MAX
+ * across devices) -> dd_split_with_exponents on each slab with those maxima
+ * -> dd_slice_gemm on each slab -> the P of all slabs, side by side as
+ * k-splits (or summed: an all-reduce SUM, exact because every partial sum is
+ * an integer below 2^53) -> one dd_recombine with the same maxima.  The
+ * result is identical bit for bit to dd_gemm on the unsplit operands.
+ *
+ * dd_exponents: the raw shared exponents of the rows of A (e, M int32) and
+ *   the columns of B (f, N int32): e[i] = smallest integer with
+ *   max_k |A_hi[i,k]| < 2^e[i], and DDGEMM_EXP_NONE (below every other value)
+ *   for a row without a nonzero element, including every row when K = 0, so
+ *   that the elementwise maximum over slabs is the exponent of the whole row.
+ *   M = 0 (N = 0) skips A (B); A_hi / B_hi may then be NULL.
+ * dd_split_with_exponents: the part planes of dd_split_rows / dd_split_cols
+ *   (same layouts) against caller-supplied exponents e, f (read only; a value
+ *   of DDGEMM_EXP_NONE stands for 0).  Every e[i] must be at least the
+ *   exponent of row i of this slab (the maximum over slabs is), otherwise the
+ *   parts are unspecified (no fault).  M = 0 (N = 0) skips A (B).
+ * Errors as for dd_split.  Both are asynchronous on `stream`.
+ */
+ddgemm_status dd_exponents(int64_t M, int64_t N, int64_t K,
+                           const double* A_hi, int64_t lda, const double* B_hi, int64_t ldb,
+                           int32_t* e, int32_t* f, void* stream);
+ddgemm_status dd_split_with_exponents(int64_t M, int64_t N, int64_t K,
+                                      const double* A_hi, const double* A_lo, int64_t lda,
+                                      const double* B_hi, const double* B_lo, int64_t ldb,
+                                      const int32_t* e, const int32_t* f,
+                                      double* planesA, double* planesB, void* stream);
+
+/*
  * Step 2 (slice-pair GEMM, eqs. (3)-(4) of the paper grouped by index sum):
  *   P[z][d][i][j] = sum_{s+t=d} sum_{k in split z} A_s[i,k] * B_t[k,j],
  *   d = 0..7, for the 36 pairs s + t <= 7, on the FP64 tensor pipe
@@ -203,6 +303,21 @@ ddgemm_status dd_split(int64_t M, int64_t N, int64_t K,
 ddgemm_status dd_slice_gemm(int64_t M, int64_t N, int64_t K,
                             const double* planesA, const double* planesB,
                             int splits, double* P, void* stream);
+
+/*
+ * Step 2 with step 1's split fused in: P exactly as dd_slice_gemm produces
+ * from dd_split's planes, but the parts are formed inside the GEMM from the
+ * hi/lo of A (M x K, lda) and B (K x N, ldb) against the exponents e (M) and
+ * f (N) -- from dd_split, dd_exponents, or the maximum over k-slabs of
+ * dd_exponents (DDGEMM_EXP_NONE reads as 0; see dd_split_with_exponents for
+ * the contract on slab exponents).  P: splits x 8 x Mp x Np doubles, 16-byte
+ * aligned; splits as for dd_slice_gemm.  No part planes are read or written.
+ */
+ddgemm_status dd_slice_gemm_fused(int64_t M, int64_t N, int64_t K,
+                                  const double* A_hi, const double* A_lo, int64_t lda,
+                                  const double* B_hi, const double* B_lo, int64_t ldb,
+                                  const int32_t* e, const int32_t* f,
+                                  int splits, double* P, void* stream);
 
 /*
  * Step 3 (recombination, steps 4-5 of the paper's algorithm):
@@ -397,6 +512,18 @@ ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K,
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dd_gemm_tc with HOST operands and result, as dd_gemm_host: copies A and B
+ * to the current device, runs dd_gemm_tc on a stream-ordered workspace,
+ * copies C back, frees what it allocated, and returns after the result is in
+ * h_C_hi / h_C_lo (it synchronises `stream`).  Pinned host buffers make the
+ * copies faster.
+ */
+ddgemm_status dd_gemm_tc_host(int64_t M, int64_t N, int64_t K,
+                              const double* h_A_hi, const double* h_A_lo, int64_t lda,
+                              const double* h_B_hi, const double* h_B_lo, int64_t ldb,
+                              double* h_C_hi, double* h_C_lo, int64_t ldc, void* stream);
+
+/*
  * The steps of dd_gemm_tc (all device pointers; used by the parity tests).
  *
  * dd_split_bf16: e (M int32) and f (N int32) receive the exponents e, f of
@@ -423,6 +550,19 @@ ddgemm_status dd_split_bf16(int64_t M, int64_t N, int64_t K,
                             const double* A_hi, const double* A_lo, int64_t lda,
                             const double* B_hi, const double* B_lo, int64_t ldb,
                             uint16_t* planesA, int32_t* e, uint16_t* planesB, int32_t* f, void* stream);
+/*
+ * The k-split of the bf16 variant across slabs (see dd_exponents): the parts
+ * of dd_split_bf16 (same layouts; exponents plus one bit of headroom) against
+ * caller-supplied exponents e, f in the form dd_exponents returns (the
+ * maximum over the slabs; DDGEMM_EXP_NONE stands for 0).  The int32 part sums
+ * of the slabs, side by side as k-splits, go to one dd_recombine_tc with the
+ * same e, f; the result equals dd_gemm_tc's bit for bit.
+ */
+ddgemm_status dd_split_bf16_with_exponents(int64_t M, int64_t N, int64_t K,
+                                           const double* A_hi, const double* A_lo, int64_t lda,
+                                           const double* B_hi, const double* B_lo, int64_t ldb,
+                                           const int32_t* e, const int32_t* f,
+                                           uint16_t* planesA, uint16_t* planesB, void* stream);
 ddgemm_status dd_slice_gemm_tc(int64_t M, int64_t N, int64_t K, const uint16_t* planesA,
                                const uint16_t* planesB, int splits, int32_t* P, void* stream);
 ddgemm_status dd_recombine_tc(int64_t M, int64_t N, const int32_t* P, int splits, const int32_t* e,

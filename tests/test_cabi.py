@@ -147,3 +147,59 @@ def test_tc_argument_errors_are_host_side(lib):
     assert lib.md_slice_gemm_tc(16, 1 << 16, 256, 1 << 20, A, A, 1024, P, None) == 2  # part rows >= 2^31
     assert lib.md_recombine_tc(12, 4, 4, P, 1, A, A, None, 4, None) == 2      # 12 doubles: unsupported
     assert lib.md_recombine_tc(8, 4, 4, P, 0, A, A, None, 4, None) == 1
+
+
+def test_options_and_sharding_entry_points_validate_host_side(lib):
+    """dd_gemm_ex's options, its plan, and the k-split / fused step entry
+    points refuse bad arguments before anything is launched."""
+    A = ctypes.c_void_p(1 << 30)
+    P = ctypes.c_void_p(1 << 40)
+    odd = ctypes.c_void_p((1 << 40) + 8)
+    n, sp, fr = ctypes.c_size_t(), ctypes.c_int(), ctypes.c_int()
+    refs = (ctypes.byref(n), ctypes.byref(sp), ctypes.byref(fr))
+
+    def plan(**kw):
+        return lib.dd_gemm_ex_plan(64, 64, 64, ctypes.byref(ddg.DDGemmOpts(**kw)), *refs)
+
+    assert plan(slices=7) == 2 and plan(slices=16) == 2     # only 8 parts are built
+    assert plan(pairs=28) == 2                               # only the 36 pairs s + t <= 7
+    assert plan(split_k=-1) == 1 and plan(split_k=9) == 1    # 9 splits > 8 k-chunks
+    assert plan(split_k=65) == 1
+    assert plan(fuse_recombine=2) == 1 and plan(fuse_split=-1) == 1
+    assert plan(split_k=2, fuse_recombine=1) == 2            # the epilogue needs all of k
+    assert plan(slices=8, pairs=36, split_k=2) == 0 and sp.value == 2 and fr.value == 0
+    # workspace: exponents, then planes and P unless fused away
+    e_f = 256 + 256
+    planes = 8 * 64 * 64 * 8 * 2
+    p1 = 8 * 64 * 64 * 8
+    assert plan(split_k=1) == 0 and n.value == e_f + planes + p1 and fr.value == 0
+    assert plan(split_k=1, fuse_split=1) == 0 and n.value == e_f + p1
+    assert plan(split_k=1, fuse_recombine=1) == 0 and n.value == e_f + planes and fr.value == 1
+    assert plan(split_k=1, fuse_split=1, fuse_recombine=1) == 0 and n.value == e_f and fr.value == 1
+    assert lib.dd_gemm_ex_plan(64, 64, ddg.MAX_K + 1, None, *refs) == 2
+    assert lib.dd_gemm_ex_plan(-1, 64, 64, None, *refs) == 1
+    # dd_gemm_ex: argument checks of dd_gemm plus the options
+    o = ddg.DDGemmOpts(split_k=3, fuse_recombine=1)
+    assert lib.dd_gemm_ex(4, 4, 64, 1 << 20, 1 << 30, 64, 1 << 32, 1 << 33, 4, 1 << 40, 1 << 41, 4,
+                          ctypes.byref(o), None, 0, None) == 2
+    assert lib.dd_gemm_ex(4, 4, 4, 1 << 20, 1 << 30, 3, 1 << 32, 1 << 33, 4, 1 << 40, 1 << 41, 4,
+                          None, None, 0, None) == 1                               # lda < K
+    assert lib.dd_gemm_ex(0, 4, 4, None, None, 4, None, None, 4, None, None, 4, None, None, 0, None) == 0
+    # exponents and splits against given exponents
+    assert lib.dd_exponents(-1, 4, 4, A, 4, A, 4, P, P, None) == 1
+    assert lib.dd_exponents(4, 4, 4, None, 4, A, 4, P, P, None) == 1             # no A_hi
+    assert lib.dd_exponents(4, 4, 4, A, 4, A, 4, None, P, None) == 1             # no e
+    assert lib.dd_exponents(0, 0, 4, None, 4, None, 1, None, None, None) == 0    # nothing to do
+    assert lib.dd_split_with_exponents(4, 4, 4, A, A, 4, A, A, 4, None, P, P, P, None) == 1   # no e
+    assert lib.dd_split_with_exponents(4, 4, 4, A, A, 4, A, A, 4, P, P, odd, P, None) == 1    # misaligned
+    assert lib.dd_split_with_exponents(4, 4, ddg.MAX_K + 1, A, A, 1 << 25, A, A, 4, P, P, P, P, None) == 2
+    assert lib.dd_split_bf16_with_exponents(4, 4, 4, A, A, 4, A, A, 4, P, None, P, P, None) == 1  # no f
+    assert lib.dd_split_bf16_with_exponents(4, 4, 4, A, A, 4, A, A, 4, P, P, P, odd, None) == 1
+    # the fused slice GEMM
+    assert lib.dd_slice_gemm_fused(4, 4, 64, A, A, 64, A, A, 4, P, P, 0, P, None) == 1       # splits < 1
+    assert lib.dd_slice_gemm_fused(4, 4, 64, A, A, 64, A, A, 4, P, P, 9, P, None) == 1       # splits > KC
+    assert lib.dd_slice_gemm_fused(4, 4, 64, A, A, 64, A, A, 4, None, P, 1, P, None) == 1    # no e
+    assert lib.dd_slice_gemm_fused(4, 4, 64, A, A, 64, A, A, 4, P, P, 1, odd, None) == 1     # misaligned P
+    assert lib.dd_slice_gemm_fused(4, 4, 64, None, A, 64, A, A, 4, P, P, 1, P, None) == 1    # no A_hi
+    # host-buffer variant of the bf16 path: dd_gemm's checks
+    assert lib.dd_gemm_tc_host(-1, 4, 4, A, A, 4, A, A, 4, P, P, 4, None) == 1

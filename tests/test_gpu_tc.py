@@ -270,3 +270,29 @@ def test_rejects_bad_arguments():
     lib = ddg.load()
     assert lib.dd_gemm_tc(4, 4, ddg.MAX_K + 1, 1, 1, ddg.MAX_K + 1, 1, 1, 4, 1, 1, 4, None, 0, None) == 2
     assert lib.dd_slice_gemm_tc(4, 4, 64, 16, 16, 0, 16, None) == 1       # splits < 1
+
+
+def test_dd_gemm_tc_host_matches_device_and_model():
+    # host operands and result: copies in, the product, the copy back, with
+    # leading dimensions of the host arrays larger than their widths
+    M, N, K = 130, 260, 200
+    A_hi, A_lo, B_hi, B_lo = workloads.make_dd(M, N, K, "normal_rowcol30", 24)
+    D_hi, D_lo = ddg.dd_gemm_tc(dev(A_hi), dev(A_lo), dev(B_hi), dev(B_lo))
+    H_hi = np.zeros((M, N))
+    H_lo = np.zeros((M, N))
+    ddg.dd_gemm_tc_host(A_hi, A_lo, B_hi, B_lo, H_hi, H_lo)
+    assert np.array_equal(H_hi.view(np.int64), host(D_hi).view(np.int64))
+    assert np.array_equal(H_lo.view(np.int64), host(D_lo).view(np.int64))
+    R_hi, R_lo, *_ = sb.sliced_dd_gemm(A_hi, A_lo, B_hi, B_lo)
+    assert np.array_equal(H_hi.view(np.int64), R_hi.view(np.int64))
+    assert np.array_equal(H_lo.view(np.int64), R_lo.view(np.int64))
+    lib = ddg.load()
+    wide = np.zeros((M, K + 3))
+    widel = np.zeros((M, K + 3))
+    wide[:, :K], widel[:, :K] = A_hi, A_lo
+    Cw = np.full((M, N + 2), 5.0)
+    Cwl = np.full((M, N + 2), 5.0)
+    assert lib.dd_gemm_tc_host(M, N, K, wide.ctypes.data, widel.ctypes.data, K + 3, B_hi.ctypes.data,
+                               B_lo.ctypes.data, N, Cw.ctypes.data, Cwl.ctypes.data, N + 2, None) == 0
+    assert np.array_equal(Cw[:, :N], H_hi) and np.array_equal(Cwl[:, :N], H_lo)
+    assert (Cw[:, N:] == 5.0).all() and (Cwl[:, N:] == 5.0).all()
