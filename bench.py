@@ -11,14 +11,23 @@ Prints ONE JSON line (rank 0).
 Timed regions (CUDA events on the launching stream, synchronised on both
 sides, max over ranks):
   * value:  K calls of dd_gemm_ws with inputs resident in HBM;
-  * per-kernel durations (roofline): K more passes through the step entry
-    points (split rows/cols, slice GEMM, recombine) with events between them;
-  * e2e:    K calls of dd_gemm_host (host buffers, copies inside the region).
+  * per-kernel durations (roofline): min(K, 3) more passes through the step
+    entry points (split rows/cols, slice GEMM, recombine) with events between;
+  * e2e:    min(K, 3) calls of dd_gemm_host (host buffers, copies inside the
+    region, host wall clock);
+  * variants beside the headline (the fused split/recombination, the integer
+    pipe, the bf16 tensor cores with their own e2e, quad/octo/hexa doubles,
+    the plain dd comparator), each on the same inputs;
+  * per_config (one GPU): every workload of the suite on the FP64 path and the
+    bf16 variant -- throughput, roof fractions, k-splits, the oracle timed on
+    a row sample and the normwise error of both results on those rows.
 Inputs (512 MB) and the part planes (2 GB) are larger than the 126 MB L2, so
 no flush is needed between steps.
 
 --impl reference times the oracle (exact superaccumulator, all host cores) on
 a bounded sample of the same workload per step.
+--only V --shape M N K runs warmup + steps products of one kind and nothing
+else (the command under the ncu captures in profiles/).
 N > 1 (torchrun): every rank multiplies its own copy of the workload (weak
 scaling, no collective on the data path); value = all ranks' work / max time.
 """
@@ -52,6 +61,7 @@ RECOMB_BYTES = 80   # per output element: 8 part sums * 8 B read + 16 B written
 FP64_NOMINAL_TF = 1.25
 BF16_NOMINAL_TF = 2250.0
 FALLBACK_BF16_TF = 1900.0
+FALLBACK_BF16_SUSTAINED_TF = 1700.0
 FALLBACK_HBM_GBS = 6800.0
 LAUNCHES_PER_STEP = 5  # exponent reset, exponents, split, slice GEMM, recombine
 SIMT_OPS = 17          # FP64 operations per k of the comparator's dd multiply-add
@@ -59,10 +69,19 @@ FP64_PER_CLK_SM = 2    # FP64 (DFMA/DADD/DMUL) instructions per clock per SM (GB
 IMAD_PER_CLK_SM = 64   # 32-bit integer multiply-add (also 32x32->64 wide) per clock per SM
 SM_COUNT = 152
 SM_MAX_GHZ = 2.07
-TRAFFIC_FILE = ROOT / "profiles" / "slice_gemm_kernel_dram_traffic.txt"
-KERNEL_SOURCES = ["extended_precision_gemm_gb300/csrc/slice_gemm.cu",
-                  "extended_precision_gemm_gb300/csrc/common.cuh",
-                  "extended_precision_gemm_gb300/csrc/async_copy.cuh"]
+ONLY_VARIANTS = ("dd", "dd_fused", "dd_int", "dd_tc", "qd_tc", "od_tc", "hd_tc")
+CSRC = "extended_precision_gemm_gb300/csrc/"
+# DRAM bytes per launch of a kernel, from a committed ncu summary; valid while
+# the sources the kernel is compiled from hash to the recorded value
+TRAFFIC = {
+    "fp64": ("profiles/slice_gemm_kernel_dram_traffic.txt",
+             ["slice_gemm.cu", "slice_mma.cuh", "dd_arith.cuh", "common.cuh", "async_copy.cuh"]),
+    "fused": ("profiles/slice_gemm_fused_kernel_dram_traffic.txt",
+              ["slice_gemm_fused.cu", "slice_mma.cuh", "dd_arith.cuh", "digits.cuh", "fixed_point.cuh",
+               "common.cuh"]),
+    "bf16": ("profiles/slice_gemm_tc_kernel_dram_traffic.txt",
+             ["tc_gemm.cuh", "tcgen05.cuh", "async_copy.cuh", "common.cuh"]),
+}
 
 
 # ----------------------------------------------------------------------------
@@ -118,34 +137,38 @@ def aggregate(dist, elapsed_s: float, units: float, device=None):
 # ----------------------------------------------------------------------------
 
 def load_peaks():
+    """(HBM GB/s, bf16 burst TF/s, bf16 sustained TF/s, 'measured' | 'fallback')."""
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
         try:
             d = json.loads(p.read_text())
-            return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+            return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                    float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
         except Exception:
             pass
-    return FALLBACK_HBM_GBS, FALLBACK_BF16_TF, "fallback"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TF, FALLBACK_BF16_SUSTAINED_TF, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        h.update((ROOT / rel).read_bytes())
+    for rel in sources:
+        h.update((ROOT / CSRC / rel).read_bytes())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name: str):
-    """DRAM bytes per slice-GEMM launch from a committed ncu summary, or None
-    when the kernel's sources changed since the capture."""
-    if not TRAFFIC_FILE.exists():
+def recorded_traffic(kernel: str, workload_name: str):
+    """DRAM bytes per launch of `kernel` on this workload from a committed ncu
+    summary, or None when its sources changed since the capture."""
+    path, sources = TRAFFIC[kernel]
+    f = ROOT / path
+    if not f.exists():
         return None
     fields = {}
-    for line in TRAFFIC_FILE.read_text().splitlines():
+    for line in f.read_text().splitlines():
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("kernel_source_sha256") != kernel_source_hash():
+    if fields.get("kernel_source_sha256") != kernel_source_hash(sources):
         return None
     if fields.get("workload") != workload_name:
         return None
@@ -227,6 +250,8 @@ def oracle_md_rows(A_parts, B_parts, rows):
 
 
 def cpu_baseline(w, A_hi, A_lo, B_hi, B_lo, target_s: float = 12.0):
+    """The oracle timed on rows 0.. of C (about target_s of CPU work on all
+    host cores); returns the baseline dict, the rows and the oracle's rows."""
     import oracle
     r0 = list(range(min(16, w.M)))   # one row per core or so: calibrates the parallel rate
     t1, _, _ = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, r0)
@@ -235,13 +260,38 @@ def cpu_baseline(w, A_hi, A_lo, B_hi, B_lo, target_s: float = 12.0):
     t, C_hi, C_lo = oracle_rows_timed(A_hi, A_lo, B_hi, B_lo, rows)
     value = 2.0 * nrows * w.N * w.K / t / 1e9
     return {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"rows 0..{nrows - 1} of C ({nrows} x {w.N} outputs, K = {w.K}), exact "
+            "sample": f"rows 0..{nrows - 1} of C ({nrows} x {w.N} outputs, K = {w.K}) of {w.name}, exact "
                       f"superaccumulator, {t:.1f} s"}, rows, C_hi, C_lo
+
+
+def normwise_rows(G_hi, G_lo, R_hi, R_lo, A_hi, A_lo, B_hi, B_lo, rows):
+    """||C - C_exact||_F / (||A||_F ||B||_F) over the given rows of C."""
+    import numpy as np
+    d = (G_hi - R_hi) + (G_lo - R_lo)
+    den = np.linalg.norm(A_hi[rows] + A_lo[rows]) * np.linalg.norm(B_hi + B_lo)
+    return float(np.linalg.norm(d) / den) if den > 0 else float(np.linalg.norm(d))
 
 
 # ----------------------------------------------------------------------------
 # the two arms
 # ----------------------------------------------------------------------------
+
+def config_of(w, world, splits):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dist": w.dist, "seed": w.seed,
+            "slices": 8, "pairs": PAIRS, "k_splits": splits,
+            "parallelism": f"independent problem per GPU x{world}",
+            "l2": "no flush: inputs 512 MB and part planes 2 GB exceed the 126 MB L2"}
+
+
+def fp64_k_splits(w):
+    """The k-split dd_gemm_layout chooses for this shape on this device (the
+    reference arm reports it too, so both lines name the same workload)."""
+    try:
+        import extended_precision_gemm_gb300 as ddg
+        return ddg.layout(w.M, w.N, w.K)[3]
+    except Exception:
+        return None
+
 
 def run_reference(args, w):
     rank, world, _ = dist_env()
@@ -266,18 +316,210 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(w, world, None),
+        "data": "synthetic", "config": config_of(w, world, fp64_k_splits(w)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def config_of(w, world, splits):
-    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dist": w.dist, "seed": w.seed,
-            "slices": 8, "pairs": PAIRS, "k_splits": splits,
-            "parallelism": f"independent problem per GPU x{world}",
-            "l2": "no flush: inputs 512 MB and part planes 2 GB exceed the 126 MB L2"}
+class Timer:
+    """CUDA-event timing on one stream, synchronised on both sides."""
+
+    def __init__(self, torch, stream, dev, dist):
+        self.torch, self.stream, self.dev, self.dist = torch, stream, dev, dist
+
+    def steps(self, fn, steps, warmup):
+        """Seconds for `steps` calls of fn after `warmup` untimed ones."""
+        torch = self.torch
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(self.dev)
+        barrier(self.dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(steps):
+            fn()
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1) / 1e3
+
+    def phases(self, phases, steps):
+        """Average seconds of each phase (a list of callables run in order,
+        events between them) over `steps` passes."""
+        torch = self.torch
+        n = len(phases)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+        torch.cuda.synchronize(self.dev)
+        barrier(self.dist)
+        for i in range(steps):
+            evs[i][0].record(self.stream)
+            for j, ph in enumerate(phases):
+                ph()
+                evs[i][j + 1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / steps / 1e3 for j in range(n)]
+
+
+def gemm_roof(flops, seconds, peak, unit="TFLOP/s"):
+    achieved = flops / seconds / 1e12
+    return {"achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak}
+
+
+def run_only(args, w):
+    """A few products of one kind, no timing of their own: the command under
+    the ncu launch lists and captures in profiles/."""
+    import torch
+    import extended_precision_gemm_gb300 as ddg
+    M, N, K = w.M, w.N, w.K
+    dev = torch.device("cuda", 0)
+
+    def to(x):
+        return torch.from_numpy(x).to(dev)
+
+    v = args.only
+    if v in ("dd", "dd_fused", "dd_int", "dd_tc"):
+        A_hi, A_lo, B_hi, B_lo = (to(x) for x in workloads.make_dd(M, N, K, w.dist, w.seed))
+        C_hi = torch.empty((M, N), dtype=torch.float64, device=dev)
+        C_lo = torch.empty_like(C_hi)
+        if v == "dd":
+            ws = torch.empty(ddg.workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+            run = lambda: ddg.dd_gemm_ws(A_hi, A_lo, B_hi, B_lo, ws, C_hi, C_lo)
+        elif v == "dd_fused":
+            ws = torch.empty(ddg.ex_plan(M, N, K, fuse_split=True, fuse_recombine=True)[0], dtype=torch.uint8,
+                             device=dev)
+            run = lambda: ddg.dd_gemm_ex(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, fuse_split=True,
+                                         fuse_recombine=True, workspace=ws)
+        elif v == "dd_int":
+            ws = torch.empty(ddg.workspace_size_i64(M, N, K), dtype=torch.uint8, device=dev)
+            run = lambda: ddg.dd_gemm_i64(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, ws)
+        else:
+            ws = torch.empty(ddg.tc_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+            run = lambda: ddg.dd_gemm_tc(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, ws)
+    else:
+        parts = {"qd_tc": 4, "od_tc": 8, "hd_tc": 16}[v]
+        A, B = workloads.make_md(M, N, K, w.dist, w.seed, parts)
+        tA, tB = [to(a) for a in A], [to(b) for b in B]
+        C = [torch.empty((M, N), dtype=torch.float64, device=dev) for _ in range(parts)]
+        if parts == 4:
+            ws = torch.empty(ddg.qd_tc_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+            run = lambda: ddg.qd_gemm_tc(tA, tB, C, ws)
+        else:
+            ws = torch.empty(ddg.md_tc_workspace_size(parts, M, N, K), dtype=torch.uint8, device=dev)
+            run = lambda: ddg.md_gemm_tc(tA, tB, C, ws)
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize(dev)
+    if ddg.wait_timeouts() != 0:
+        raise SystemExit("bounded waits gave up")
+    return {"only": v, "workload": w.name, "products": args.warmup + args.steps}
+
+
+# per-configuration legs: (warm-up, timed) steps of the FP64 path and of the
+# bf16 variant; the 8192^3 FP64 product takes about 36 s
+CONFIG_STEPS = {0: ((3, 10), (3, 10)), 1: ((3, 5), (3, 10)), 2: ((3, 3), (3, 5)), 3: ((2, 3), (3, 5)),
+                4: ((1, 1), (2, 3))}
+CONFIG_ORACLE_S = {0: 1.0, 1: 3.0, 2: 3.0, 3: 3.0, 4: 4.0}
+
+
+def measure_config(idx, T, ddg, torch, dev, peaks, fp64_peak, head=None):
+    """One workload's throughput and roof fractions on both paths, with the
+    oracle timed on a row sample and the normwise error of both results on
+    those rows.  `head` carries the headline's own measurements when idx is
+    the headline workload (its FP64 numbers are not measured twice)."""
+    import numpy as np
+    hbm_gbs, bf16_tf, bf16_sus = peaks
+    wc = workloads.WORKLOADS[idx]
+    M, N, K = wc.M, wc.N, wc.K
+    (fw, fs), (tw, ts) = CONFIG_STEPS[idx]
+    A_hi, A_lo, B_hi, B_lo = workloads.make_workload(idx)
+    tA_hi, tA_lo, tB_hi, tB_lo = (torch.from_numpy(x).to(dev) for x in (A_hi, A_lo, B_hi, B_lo))
+    C_hi = torch.empty((M, N), dtype=torch.float64, device=dev)
+    C_lo = torch.empty_like(C_hi)
+    out = {"workload": wc.name, "M": M, "N": N, "K": K}
+
+    # ---- FP64 tensor-pipe path ----
+    Mp, Np, Kp, splits = ddg.layout(M, N, K)
+    if head is None:
+        e = torch.empty(M, dtype=torch.int32, device=dev)
+        f = torch.empty(N, dtype=torch.int32, device=dev)
+        pA = torch.empty(8 * Mp * Kp, dtype=torch.float64, device=dev)
+        pB = torch.empty(8 * Np * Kp, dtype=torch.float64, device=dev)
+        P = torch.empty((splits, 8, Mp, Np), dtype=torch.float64, device=dev)
+        phases = [lambda: ddg.split(tA_hi, tA_lo, tB_hi, tB_lo, pA, e, pB, f),
+                  lambda: ddg.slice_gemm(M, N, K, pA, pB, splits, P),
+                  lambda: ddg.recombine(M, N, P, e, f, splits, C_hi, C_lo)]
+        for _ in range(fw):   # warm-up: the whole product through the step entry points
+            for ph in phases:
+                ph()
+        t_split, t_gemm, t_rec = T.phases(phases, fs)
+        t_step = t_split + t_gemm + t_rec
+        timed_through = "step entry points (dd_split, dd_slice_gemm, dd_recombine: the kernels of dd_gemm_ws)"
+        if t_step < 2.0:   # short steps: time the one-call product as well
+            ws = torch.empty(ddg.workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+            t_step = T.steps(lambda: ddg.dd_gemm_ws(tA_hi, tA_lo, tB_hi, tB_lo, ws, C_hi, C_lo), fs, fw) / fs
+            timed_through = "dd_gemm_ws (step); step entry points (per-kernel times)"
+            del ws
+        del pA, pB, P
+        assert ddg.wait_timeouts() == 0
+    else:
+        t_step, t_split, t_gemm, t_rec = head["t_step"], head["t_split"], head["t_gemm"], head["t_rec"]
+        fw, fs = head["warmup"], head["steps"]
+        C_hi, C_lo = head["C_hi"], head["C_lo"]
+        timed_through = "dd_gemm_ws (the headline's timed steps)"
+    gemm = gemm_roof(PAIRS * 2.0 * M * N * K, t_gemm, fp64_peak)
+    out["fp64"] = {
+        "value": 2.0 * M * N * K / t_step / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_step,
+        "warmup": fw, "steps": fs, "k_splits": splits, "timed_through": timed_through,
+        "slice_gemm": {"ms": 1e3 * t_gemm, **gemm, "bound": "tensor (FP64 pipe)"},
+        "split": {"ms": 1e3 * t_split, **gemm_roof(SPLIT_BYTES * (M * K + K * N) / 1e3, t_split, hbm_gbs, "GB/s"),
+                  "kernels": "exponent reset + exponents + split (A and B)"},
+        "recombine_ms": 1e3 * t_rec,
+    }
+
+    # ---- bf16 tensor-core variant ----
+    T_hi = torch.empty_like(C_hi)
+    T_lo = torch.empty_like(C_lo)
+    ws_t = torch.empty(ddg.tc_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    tt = T.steps(lambda: ddg.dd_gemm_tc(tA_hi, tA_lo, tB_hi, tB_lo, T_hi, T_lo, workspace=ws_t), ts, tw) / ts
+    del ws_t
+    _, _, _, splits_t = ddg.tc_layout(M, N, K)
+    pA8, e8, pB8, f8 = ddg.split_bf16(tA_hi, tA_lo, tB_hi, tB_lo)
+    Pt = ddg.slice_gemm_tc(M, N, K, pA8, pB8, splits_t)
+    U_hi = torch.empty_like(C_hi)
+    U_lo = torch.empty_like(C_lo)
+    tt_split, tt_gemm, tt_rec = T.phases(
+        [lambda: ddg.split_bf16(tA_hi, tA_lo, tB_hi, tB_lo, pA8, e8, pB8, f8),
+         lambda: ddg.slice_gemm_tc(M, N, K, pA8, pB8, splits_t, Pt),
+         lambda: ddg.recombine_tc(M, N, Pt, e8, f8, splits_t, U_hi, U_lo)], ts)
+    del pA8, pB8, Pt
+    sustained = tt_gemm > 0.02   # launches of tens of ms run under the power cap
+    peak_t = bf16_sus if sustained else bf16_tf
+    out["bf16"] = {
+        "value": 2.0 * M * N * K / tt / 1e9, "unit": UNIT, "ms_per_step": 1e3 * tt, "warmup": tw, "steps": ts,
+        "k_splits": splits_t,
+        "slice_gemm": {"ms": 1e3 * tt_gemm, **gemm_roof(TC_PAIRS * 2.0 * M * N * K, tt_gemm, peak_t),
+                       "peak_kind": "bf16 sustained (launch of tens of ms)" if sustained else "bf16 burst"},
+        "split_ms": 1e3 * tt_split, "recombine_ms": 1e3 * tt_rec,
+        "identical_to_step_entry_points": bool(torch.equal(T_hi, U_hi) and torch.equal(T_lo, U_lo)),
+    }
+    assert ddg.wait_timeouts() == 0
+
+    # ---- oracle on a row sample: CPU baseline and accuracy of both results ----
+    cpu, rows, R_hi, R_lo = cpu_baseline(wc, A_hi, A_lo, B_hi, B_lo, CONFIG_ORACLE_S[idx])
+    ridx = torch.as_tensor(rows, device=dev)
+    out["fp64"]["normwise_vs_exact_oracle"] = normwise_rows(
+        C_hi[ridx].cpu().numpy(), C_lo[ridx].cpu().numpy(), R_hi, R_lo, A_hi, A_lo, B_hi, B_lo, rows)
+    out["bf16"]["normwise_vs_exact_oracle"] = normwise_rows(
+        T_hi[ridx].cpu().numpy(), T_lo[ridx].cpu().numpy(), R_hi, R_lo, A_hi, A_lo, B_hi, B_lo, rows)
+    out["rows_checked"] = len(rows)
+    out["normwise_bound"] = 1e-26
+    out["cpu_baseline"] = cpu
+    del tA_hi, tA_lo, tB_hi, tB_lo, T_hi, T_lo, U_hi, U_lo
+    if head is None:
+        del C_hi, C_lo
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, w):
@@ -292,6 +534,7 @@ def run_ours(args, w):
     dist = dist_init("nccl")
     dev = torch.device("cuda", local)
     M, N, K = w.M, w.N, w.K
+    VSTEPS = max(1, min(args.steps, 3))   # passes of the per-kernel and variant legs
 
     A_hi, A_lo, B_hi, B_lo = workloads.make_dd(M, N, K, w.dist, w.seed)
     pinned = [torch.from_numpy(x).pin_memory() for x in (A_hi, A_lo, B_hi, B_lo)]
@@ -302,6 +545,7 @@ def run_ours(args, w):
     ws = torch.empty(ddg.workspace_size(M, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
+    T = Timer(torch, stream, dev, dist)
 
     dmma_tf = ddg.fp64_tensor_roof()
 
@@ -335,24 +579,14 @@ def run_ours(args, w):
     pA = torch.empty(8 * Mp * Kp, dtype=torch.float64, device=dev)
     pB = torch.empty(8 * Np * Kp, dtype=torch.float64, device=dev)
     P = torch.empty((splits, 8, Mp, Np), dtype=torch.float64, device=dev)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    barrier(dist)
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        ddg.split(dA_hi, dA_lo, dB_hi, dB_lo, pA, e_buf, pB, f_buf, stream=stream)
-        evs[i][1].record(stream)
-        ddg.slice_gemm(M, N, K, pA, pB, splits, P, stream=stream)
-        evs[i][2].record(stream)
-        ddg.recombine(M, N, P, e_buf, f_buf, splits, C_hi, C_lo, stream=stream)
-        evs[i][3].record(stream)
-    torch.cuda.synchronize(dev)
-    t_split = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1e3
-    t_gemm = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1e3
-    t_recomb = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1e3
+    t_split, t_gemm, t_recomb = T.phases(
+        [lambda: ddg.split(dA_hi, dA_lo, dB_hi, dB_lo, pA, e_buf, pB, f_buf, stream=stream),
+         lambda: ddg.slice_gemm(M, N, K, pA, pB, splits, P, stream=stream),
+         lambda: ddg.recombine(M, N, P, e_buf, f_buf, splits, C_hi, C_lo, stream=stream)], VSTEPS)
     t_gemm = allreduce_max(dist, t_gemm, dev)
     t_split = allreduce_max(dist, t_split, dev)
     t_recomb = allreduce_max(dist, t_recomb, dev)
+    del pA, pB, P
 
     # ---- end to end through the C ABI with host buffers ----
     h_C_hi = torch.empty((M, N), dtype=torch.float64).pin_memory()
@@ -360,103 +594,79 @@ def run_ours(args, w):
     ddg.dd_gemm_host(*pinned, h_C_hi, h_C_lo, stream=stream)
     barrier(dist)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(VSTEPS):
         ddg.dd_gemm_host(*pinned, h_C_hi, h_C_lo, stream=stream)
     t_e2e = time.perf_counter() - t0
-    e2e_units, t_e2e = aggregate(dist, t_e2e, args.steps * w.dd_flops, dev)
+    e2e_units, t_e2e = aggregate(dist, t_e2e, VSTEPS * w.dd_flops, dev)
     same = bool(torch.equal(h_C_hi, C_hi.cpu()) and torch.equal(h_C_lo, C_lo.cpu()))
+
+    # ---- the split fused into the slice GEMM, the recombination into its epilogue ----
+    ws_f = torch.empty(ddg.ex_plan(M, N, K, fuse_split=True, fuse_recombine=True)[0], dtype=torch.uint8, device=dev)
+    _, splits_f, fused_rec = ddg.ex_plan(M, N, K, fuse_split=True, fuse_recombine=True)
+    F_hi = torch.empty_like(C_hi)
+    F_lo = torch.empty_like(C_lo)
+    t_f = T.steps(lambda: ddg.dd_gemm_ex(dA_hi, dA_lo, dB_hi, dB_lo, F_hi, F_lo, fuse_split=True,
+                                         fuse_recombine=True, workspace=ws_f, stream=stream), VSTEPS, 1)
+    units_f, t_f = aggregate(dist, t_f, VSTEPS * w.dd_flops, dev)
+    same_f = bool(torch.equal(F_hi, C_hi) and torch.equal(F_lo, C_lo))
+    ws_f_bytes = ws_f.numel()
+    del ws_f, F_hi, F_lo
+    assert ddg.wait_timeouts() == 0
 
     # ---- the integer-pipe variant of the slice GEMM (same parts, exact int64 sums) ----
     ws_i = torch.empty(ddg.workspace_size_i64(M, N, K), dtype=torch.uint8, device=dev)
     I_hi = torch.empty_like(C_hi)
     I_lo = torch.empty_like(C_lo)
-
-    def step_i64():
-        ddg.dd_gemm_i64(dA_hi, dA_lo, dB_hi, dB_lo, I_hi, I_lo, workspace=ws_i, stream=stream)
-
-    for _ in range(args.warmup):
-        step_i64()
-    barrier(dist)
-    torch.cuda.synchronize(dev)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step_i64()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(dist)
-    units_i, t_i = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    t_i = T.steps(lambda: ddg.dd_gemm_i64(dA_hi, dA_lo, dB_hi, dB_lo, I_hi, I_lo, workspace=ws_i, stream=stream),
+                  VSTEPS, 1)
+    units_i, t_i = aggregate(dist, t_i, VSTEPS * w.dd_flops, dev)
     same_i = bool(torch.equal(I_hi, C_hi) and torch.equal(I_lo, C_lo))
     splits_i = ddg.layout_i64(M, N, K)
     pA16 = torch.empty(8 * Mp * Kp, dtype=torch.int16, device=dev)
     pB16 = torch.empty(8 * Np * Kp, dtype=torch.int16, device=dev)
     Pi = torch.empty((splits_i, 8, Mp, Np), dtype=torch.float64, device=dev)
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        ddg.split_i16(dA_hi, dA_lo, dB_hi, dB_lo, pA16, e_buf, pB16, f_buf, stream=stream)
-        evs[i][1].record(stream)
-        ddg.slice_gemm_i64(M, N, K, pA16, pB16, splits_i, Pi, stream=stream)
-        evs[i][2].record(stream)
-        ddg.recombine(M, N, Pi, e_buf, f_buf, splits_i, I_hi, I_lo, stream=stream)
-        evs[i][3].record(stream)
-    torch.cuda.synchronize(dev)
-    ti_split = allreduce_max(dist, sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1e3, dev)
-    ti_gemm = allreduce_max(dist, sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1e3, dev)
-    ti_recomb = allreduce_max(dist, sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1e3, dev)
-    del ws_i, pA16, pB16, Pi
+    ti_split, ti_gemm, ti_recomb = (allreduce_max(dist, x, dev) for x in T.phases(
+        [lambda: ddg.split_i16(dA_hi, dA_lo, dB_hi, dB_lo, pA16, e_buf, pB16, f_buf, stream=stream),
+         lambda: ddg.slice_gemm_i64(M, N, K, pA16, pB16, splits_i, Pi, stream=stream),
+         lambda: ddg.recombine(M, N, Pi, e_buf, f_buf, splits_i, I_hi, I_lo, stream=stream)], VSTEPS))
+    del ws_i, pA16, pB16, Pi, I_hi, I_lo
     assert ddg.wait_timeouts() == 0
 
     # ---- 8-bit parts on the bf16 tensor cores (tcgen05), exact sums rounded once ----
     ws_t = torch.empty(ddg.tc_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
     T_hi = torch.empty_like(C_hi)
     T_lo = torch.empty_like(C_lo)
-
-    def step_tc():
-        ddg.dd_gemm_tc(dA_hi, dA_lo, dB_hi, dB_lo, T_hi, T_lo, workspace=ws_t, stream=stream)
-
-    for _ in range(args.warmup):
-        step_tc()
-    barrier(dist)
-    torch.cuda.synchronize(dev)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step_tc()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(dist)
-    units_t, t_t = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    TC_STEPS = max(args.steps, 3)
+    t_t = T.steps(lambda: ddg.dd_gemm_tc(dA_hi, dA_lo, dB_hi, dB_lo, T_hi, T_lo, workspace=ws_t, stream=stream),
+                  TC_STEPS, args.warmup)
+    units_t, t_t = aggregate(dist, t_t, TC_STEPS * w.dd_flops, dev)
     del ws_t
     _, _, _, splits_t = ddg.tc_layout(M, N, K)
     pA8, e8, pB8, f8 = ddg.split_bf16(dA_hi, dA_lo, dB_hi, dB_lo, stream=stream)
     Pt = ddg.slice_gemm_tc(M, N, K, pA8, pB8, splits_t, stream=stream)
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        ddg.split_bf16(dA_hi, dA_lo, dB_hi, dB_lo, pA8, e8, pB8, f8, stream=stream)
-        evs[i][1].record(stream)
-        ddg.slice_gemm_tc(M, N, K, pA8, pB8, splits_t, Pt, stream=stream)
-        evs[i][2].record(stream)
-        ddg.recombine_tc(M, N, Pt, e8, f8, splits_t, T_hi, T_lo, stream=stream)
-        evs[i][3].record(stream)
-    torch.cuda.synchronize(dev)
-    tt_split = allreduce_max(dist, sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps / 1e3, dev)
-    tt_gemm = allreduce_max(dist, sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps / 1e3, dev)
-    tt_recomb = allreduce_max(dist, sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps / 1e3, dev)
+    tt_split, tt_gemm, tt_recomb = (allreduce_max(dist, x, dev) for x in T.phases(
+        [lambda: ddg.split_bf16(dA_hi, dA_lo, dB_hi, dB_lo, pA8, e8, pB8, f8, stream=stream),
+         lambda: ddg.slice_gemm_tc(M, N, K, pA8, pB8, splits_t, Pt, stream=stream),
+         lambda: ddg.recombine_tc(M, N, Pt, e8, f8, splits_t, T_hi, T_lo, stream=stream)], TC_STEPS))
     del pA8, pB8, Pt
+    # end to end with host buffers
+    h_T_hi = torch.empty((M, N), dtype=torch.float64).pin_memory()
+    h_T_lo = torch.empty((M, N), dtype=torch.float64).pin_memory()
+    ddg.dd_gemm_tc_host(*pinned, h_T_hi, h_T_lo, stream=stream)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(TC_STEPS):
+        ddg.dd_gemm_tc_host(*pinned, h_T_hi, h_T_lo, stream=stream)
+    t_te2e = time.perf_counter() - t0
+    te2e_units, t_te2e = aggregate(dist, t_te2e, TC_STEPS * w.dd_flops, dev)
+    same_t = bool(torch.equal(h_T_hi, T_hi.cpu()) and torch.equal(h_T_lo, T_lo.cpu()))
     assert ddg.wait_timeouts() == 0
 
     # ---- the comparator: plain double-double arithmetic on the FP64 ALUs ----
     S_hi = torch.empty_like(C_hi)
     S_lo = torch.empty_like(C_lo)
-    ddg.dd_gemm_simt(dA_hi, dA_lo, dB_hi, dB_lo, S_hi, S_lo, stream=stream)
-    barrier(dist)
-    torch.cuda.synchronize(dev)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        ddg.dd_gemm_simt(dA_hi, dA_lo, dB_hi, dB_lo, S_hi, S_lo, stream=stream)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    units_s, t_s = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    t_s = T.steps(lambda: ddg.dd_gemm_simt(dA_hi, dA_lo, dB_hi, dB_lo, S_hi, S_lo, stream=stream), VSTEPS, 1)
+    units_s, t_s = aggregate(dist, t_s, VSTEPS * w.dd_flops, dev)
     Sr_hi = S_hi[:8].cpu().numpy()
     Sr_lo = S_lo[:8].cpu().numpy()
     del S_hi, S_lo
@@ -467,28 +677,14 @@ def run_ours(args, w):
     tQB = [torch.from_numpy(x).to(dev) for x in QB]
     QC = [torch.empty((M, N), dtype=torch.float64, device=dev) for _ in range(4)]
     ws_q = torch.empty(ddg.qd_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
-    ddg.qd_gemm(tQA, tQB, QC, workspace=ws_q, stream=stream)
-    barrier(dist)
-    torch.cuda.synchronize(dev)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        ddg.qd_gemm(tQA, tQB, QC, workspace=ws_q, stream=stream)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    units_q, t_q = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    t_q = T.steps(lambda: ddg.qd_gemm(tQA, tQB, QC, workspace=ws_q, stream=stream), VSTEPS, 1)
+    units_q, t_q = aggregate(dist, t_q, VSTEPS * w.dd_flops, dev)
     qd_rows = [QC[p][:2].cpu().numpy() for p in range(4)]
     del ws_q
     # the same quad-double product with 27 bf16 parts on the tensor cores
     ws_qt = torch.empty(ddg.qd_tc_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
-    ddg.qd_gemm_tc(tQA, tQB, QC, workspace=ws_qt, stream=stream)
-    barrier(dist)
-    torch.cuda.synchronize(dev)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        ddg.qd_gemm_tc(tQA, tQB, QC, workspace=ws_qt, stream=stream)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    units_qt, t_qt = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * w.dd_flops, dev)
+    t_qt = T.steps(lambda: ddg.qd_gemm_tc(tQA, tQB, QC, workspace=ws_qt, stream=stream), TC_STEPS, 1)
+    units_qt, t_qt = aggregate(dist, t_qt, TC_STEPS * w.dd_flops, dev)
     qdt_rows = [QC[p][:2].cpu().numpy() for p in range(4)]
     splits_qt = ddg.qd_tc_layout(M, N, K)[3]
     del tQA, tQB, QC, ws_qt
@@ -504,49 +700,52 @@ def run_ours(args, w):
         del MA, MB
         MC = [torch.empty((Mm, Nm), dtype=torch.float64, device=dev) for _ in range(n_md)]
         ws_m = torch.empty(ddg.md_tc_workspace_size(n_md, Mm, Nm, Km), dtype=torch.uint8, device=dev)
-        ddg.md_gemm_tc(tMA, tMB, MC, workspace=ws_m, stream=stream)
-        barrier(dist)
-        torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            ddg.md_gemm_tc(tMA, tMB, MC, workspace=ws_m, stream=stream)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        units_m, t_m = aggregate(dist, ev0.elapsed_time(ev1) / 1e3, args.steps * 2.0 * Mm * Nm * Km, dev)
+        t_m = T.steps(lambda: ddg.md_gemm_tc(tMA, tMB, MC, workspace=ws_m, stream=stream), VSTEPS, 1)
+        units_m, t_m = aggregate(dist, t_m, VSTEPS * 2.0 * Mm * Nm * Km, dev)
         parts_m = ddg.MD_TC_PARTS[n_md]
         md_results[{8: "octo_double", 16: "hexa_double"}[n_md]] = {
             "workload": f"{'od' if n_md == 8 else 'hd'}_gemm_2048x2048x2048_{w.dist}",
-            "value": units_m / t_m / 1e9, "unit": "GFLOP/s (2MNK/s)", "ms_per_step": 1e3 * t_m / args.steps,
-            "parts": parts_m, "slice_pairs": parts_m * (parts_m + 1) // 2,
+            "value": units_m / t_m / 1e9, "unit": "GFLOP/s (2MNK/s)", "ms_per_step": 1e3 * t_m / VSTEPS,
+            "steps": VSTEPS, "parts": parts_m, "slice_pairs": parts_m * (parts_m + 1) // 2,
             "k_splits": ddg.md_tc_layout(n_md, Mm, Nm, Km)[3],
-            "bf16_tflops_whole_product": parts_m * (parts_m + 1) // 2 * 2.0 * Mm * Nm * Km / (t_m / args.steps) / 1e12,
+            "bf16_tflops_whole_product": parts_m * (parts_m + 1) // 2 * 2.0 * Mm * Nm * Km / (t_m / VSTEPS) / 1e12,
         }
         del tMA, tMB, MC, ws_m
         torch.cuda.empty_cache()
     assert ddg.wait_timeouts() == 0
 
+    hbm_gbs, bf16_tf, bf16_sus, peak_src = load_peaks()
+    fp64_derived = bf16_tf * FP64_NOMINAL_TF / BF16_NOMINAL_TF
+    fp64_peak = max(fp64_derived, dmma_tf)
+
+    # ---- every workload of the suite, on both paths (one GPU only) ----
+    per_config = None
+    if world == 1 and not args.no_per_config and not args.shape:
+        head = {"t_step": t_max / args.steps, "t_split": t_split, "t_gemm": t_gemm, "t_rec": t_recomb,
+                "warmup": args.warmup, "steps": args.steps, "C_hi": C_hi, "C_lo": C_lo}
+        per_config = {}
+        for idx in sorted(workloads.WORKLOADS):
+            per_config[str(idx)] = measure_config(idx, T, ddg, torch, dev, (hbm_gbs, bf16_tf, bf16_sus), fp64_peak,
+                                                  head if w == workloads.WORKLOADS[idx] else None)
+
     if rank != 0:
         return None
 
-    hbm_gbs, bf16_tf, peak_src = load_peaks()
-    fp64_peak = bf16_tf * FP64_NOMINAL_TF / BF16_NOMINAL_TF
     gemm_flops = PAIRS * 2.0 * M * N * K
     achieved_tf = gemm_flops / t_gemm / 1e12
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic("fp64", w.name)
+    traffic_tc = recorded_traffic("bf16", w.name)
     split_gbs = SPLIT_BYTES * (M * K + K * N) / t_split / 1e9
     recomb_gbs = RECOMB_BYTES * M * N / t_recomb / 1e9
+    alg_bytes = 64.0 * (M * K + N * K) + 64.0 * M * N          # parts read once, P written once
+    alg_bytes_tc = 26.0 * (M * K + N * K) + 52.0 * M * N
 
     cpu, rows, R_hi, R_lo = cpu_baseline(w, A_hi, A_lo, B_hi, B_lo)
-    G_hi = C_hi[rows].cpu().numpy()
-    G_lo = C_lo[rows].cpu().numpy()
-    d = (G_hi - R_hi) + (G_lo - R_lo)
-    normwise = float(np.linalg.norm(d) / (np.linalg.norm(A_hi[rows] + A_lo[rows])
-                                          * np.linalg.norm(B_hi + B_lo)))
-
-    Tg_hi = T_hi[rows].cpu().numpy()
-    Tg_lo = T_lo[rows].cpu().numpy()
-    dt = (Tg_hi - R_hi) + (Tg_lo - R_lo)
-    tc_norm = float(np.linalg.norm(dt) / (np.linalg.norm(A_hi[rows] + A_lo[rows]) * np.linalg.norm(B_hi + B_lo)))
+    ridx = torch.as_tensor(rows, device=dev)
+    normwise = normwise_rows(C_hi[ridx].cpu().numpy(), C_lo[ridx].cpu().numpy(), R_hi, R_lo,
+                             A_hi, A_lo, B_hi, B_lo, rows)
+    tc_norm = normwise_rows(T_hi[ridx].cpu().numpy(), T_lo[ridx].cpu().numpy(), R_hi, R_lo,
+                            A_hi, A_lo, B_hi, B_lo, rows)
     tc_flops = TC_PAIRS * 2.0 * M * N * K
     tc_tf = tc_flops / tt_gemm / 1e12
 
@@ -556,9 +755,10 @@ def run_ours(args, w):
     dqt = sum(qdt_rows[p] - QR[p] for p in range(4))
     qdt_norm = float(np.linalg.norm(dqt) / (np.linalg.norm(sum(a[:2] for a in QA)) * np.linalg.norm(sum(QB))))
     n8 = min(8, len(rows))
-    ds = (Sr_hi[:n8] - R_hi[:n8]) + (Sr_lo[:n8] - R_lo[:n8])
-    simt_norm = float(np.linalg.norm(ds) / (np.linalg.norm(A_hi[:n8] + A_lo[:n8]) * np.linalg.norm(B_hi + B_lo)))
+    simt_norm = normwise_rows(Sr_hi[:n8], Sr_lo[:n8], R_hi[:n8], R_lo[:n8], A_hi, A_lo, B_hi, B_lo, list(range(n8)))
     value = units / t_max / 1e9
+    imad_peak = IMAD_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3
+    simt_peak = FP64_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
@@ -567,11 +767,13 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "kernel": "slice_gemm_kernel (FP64 mma.sync m8n8k4)",
                      "achieved": achieved_tf, "peak": fp64_peak, "unit": "TFLOP/s",
                      "frac": achieved_tf / fp64_peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 burst {bf16_tf} TF/s x nominal FP64/bf16 "
-                                    f"{FP64_NOMINAL_TF}/{BF16_NOMINAL_TF}",
-                     "flops_per_launch": gemm_flops, "ms_per_launch": 1e3 * t_gemm,
-                     "fp64_tensor_loop_measured_tflops": dmma_tf,
-                     "frac_of_measured_loop": achieved_tf / dmma_tf},
+                     "traffic_over_algorithmic": traffic / alg_bytes if traffic else None,
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "peak_source": "max of the in-run mma.sync f64 loop and the FP64 rate derived from the "
+                                    f"{peak_src} bf16 burst ({bf16_tf} TF/s x nominal FP64/bf16 "
+                                    f"{FP64_NOMINAL_TF}/{BF16_NOMINAL_TF})",
+                     "fp64_derived_peak_tflops": fp64_derived, "fp64_tensor_loop_measured_tflops": dmma_tf,
+                     "flops_per_launch": gemm_flops, "ms_per_launch": 1e3 * t_gemm, "launches_timed": VSTEPS},
         "roofline_split": {"bound": "hbm", "achieved": split_gbs, "peak": hbm_gbs, "unit": "GB/s",
                            "frac": split_gbs / hbm_gbs, "bytes_per_step": SPLIT_BYTES * (M * K + K * N),
                            "ms": 1e3 * t_split, "kernels": "exponent reset + exponents + split (A and B)"},
@@ -579,22 +781,31 @@ def run_ours(args, w):
                                "frac": recomb_gbs / hbm_gbs, "ms": 1e3 * t_recomb},
         "frac_of_fp64_tensor_roof_end_to_end": (units / t_max * PAIRS) / (fp64_peak * 1e12),
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_units / t_e2e / 1e9, "unit": UNIT,
+        "e2e": {"value": e2e_units / t_e2e / 1e9, "unit": UNIT, "steps": VSTEPS,
                 "h2d_bytes_per_step": 16 * (M * K + K * N), "d2h_bytes_per_step": 16 * M * N,
-                "matches_device_result": same},
+                "api": "dd_gemm_host", "matches_device_result": same},
         "accuracy": {"normwise_vs_exact_oracle": normwise, "rows_checked": len(rows), "bound": 1e-26},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clock_info,
+        "fused_variant": {
+            "what": "dd_gemm_ex with the split fused into the slice GEMM's prologue (13-bit parts formed from "
+                    "hi/lo tiles) and the recombination in its epilogue: exponents, then one GEMM kernel; no "
+                    "part planes, no part-sum planes",
+            "value": units_f / t_f / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_f / VSTEPS, "steps": VSTEPS,
+            "k_splits": splits_f, "recombination_fused": fused_rec, "workspace_bytes": ws_f_bytes,
+            "workspace_bytes_unfused": ws.numel(), "identical_to_dd_gemm": same_f,
+            "frac_of_fp64_roof_end_to_end": (units_f / t_f * PAIRS) / (fp64_peak * 1e12),
+            "traffic": recorded_traffic("fused", w.name),
+        },
         "int_pipe_variant": {
             "what": "same 13-bit parts and 36 pairs; products as 32-bit integer multiply-adds into int32 "
                     "partial sums flushed into exact int64 totals; C identical bit for bit to the FP64 "
                     "tensor-pipe path",
-            "value": units_i / t_i / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_i / args.steps,
+            "value": units_i / t_i / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_i / VSTEPS, "steps": VSTEPS,
             "identical_to_fp64_path": same_i, "k_splits": splits_i,
             "roofline": {"bound": "alu", "kernel": "slice_gemm_i64_kernel (32-bit IMAD)",
-                         "achieved": PAIRS * M * N * K / ti_gemm / 1e12,
-                         "peak": IMAD_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3, "unit": "Tops/s",
-                         "frac": (PAIRS * M * N * K / ti_gemm / 1e12) / (IMAD_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3),
+                         "achieved": PAIRS * M * N * K / ti_gemm / 1e12, "peak": imad_peak, "unit": "Tops/s",
+                         "frac": (PAIRS * M * N * K / ti_gemm / 1e12) / imad_peak,
                          "peak_source": f"{IMAD_PER_CLK_SM} int32 multiply-adds/clk/SM x {SM_COUNT} SMs x "
                                         f"{SM_MAX_GHZ} GHz", "ms_per_launch": 1e3 * ti_gemm,
                          "ops_per_launch": PAIRS * M * N * K},
@@ -602,25 +813,30 @@ def run_ours(args, w):
         },
         "bf16_tensor_variant": {
             "what": "13 balanced 8-bit parts per element (exact in bf16), the 91 part pairs with index sum "
-                    "<= 12 as tcgen05.mma (bf16 in, f32 accumulators in tensor memory, flushed every 512 "
+                    "<= 12 as tcgen05.mma (bf16 in, f32 accumulators in tensor memory, flushed every 1024 "
                     "products into exact int32 totals), the exact part sums rounded once to a double double",
-            "value": units_t / t_t / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_t / args.steps,
+            "value": units_t / t_t / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_t / TC_STEPS, "steps": TC_STEPS,
             "k_splits": splits_t,
             "normwise_vs_exact_oracle": tc_norm, "rows_checked": len(rows),
             "roofline": {"bound": "tensor", "kernel": "slice_gemm_tc_kernel (tcgen05.mma kind::f16, bf16)",
                          "achieved": tc_tf, "peak": bf16_tf, "unit": "TFLOP/s", "frac": tc_tf / bf16_tf,
                          "peak_source": f"{peak_src} cuBLAS bf16 burst", "flops_per_launch": tc_flops,
-                         "ms_per_launch": 1e3 * tt_gemm},
+                         "ms_per_launch": 1e3 * tt_gemm, "traffic": traffic_tc,
+                         "traffic_over_algorithmic": traffic_tc / alg_bytes_tc if traffic_tc else None,
+                         "algorithmic_bytes_per_launch": alg_bytes_tc},
             "ms_split_bf16": 1e3 * tt_split, "ms_recombine": 1e3 * tt_recomb,
             "launches_per_step": 5,
+            "e2e": {"value": te2e_units / t_te2e / 1e9, "unit": UNIT, "steps": TC_STEPS,
+                    "h2d_bytes_per_step": 16 * (M * K + K * N), "d2h_bytes_per_step": 16 * M * N,
+                    "api": "dd_gemm_tc_host", "matches_device_result": same_t},
         },
         "qd_bf16_tensor_variant": {
             "what": "quad-double GEMM with 27 balanced 8-bit parts (exact in bf16), the 378 part pairs with "
                     "index sum <= 26 as tcgen05.mma on CTA pairs, exact sums rounded once into 4 doubles",
             "workload": w.name.replace("dd_gemm", "qd_gemm"),
             "value": units_qt / t_qt / 1e9, "unit": "qd-GFLOP/s (2MNK/s)",
-            "ms_per_step": 1e3 * t_qt / args.steps, "k_splits": splits_qt, "slice_pairs": 378,
-            "bf16_tflops_whole_product": 378 * 2.0 * M * N * K / (t_qt / args.steps) / 1e12,
+            "ms_per_step": 1e3 * t_qt / TC_STEPS, "steps": TC_STEPS, "k_splits": splits_qt, "slice_pairs": 378,
+            "bf16_tflops_whole_product": 378 * 2.0 * M * N * K / (t_qt / TC_STEPS) / 1e12,
             "normwise_vs_exact_oracle_2_rows": qdt_norm,
         },
         "md_bf16_tensor_variants": md_results,
@@ -628,24 +844,24 @@ def run_ours(args, w):
             "what": "quad-double GEMM (4 doubles per number): 16 parts of 13 bits, 136 pairs on the "
                     "integer pipe, exact sums rounded once into 4 doubles",
             "workload": w.name.replace("dd_gemm", "qd_gemm"),
-            "value": units_q / t_q / 1e9, "unit": "qd-GFLOP/s (2MNK/s)", "ms_per_step": 1e3 * t_q / args.steps,
-            "slice_pairs": 136,
-            "multiply_adds_per_s": 136 * M * N * K / (t_q / args.steps),
+            "value": units_q / t_q / 1e9, "unit": "qd-GFLOP/s (2MNK/s)", "ms_per_step": 1e3 * t_q / VSTEPS,
+            "steps": VSTEPS, "slice_pairs": 136,
+            "multiply_adds_per_s": 136 * M * N * K / (t_q / VSTEPS),
             "normwise_vs_exact_oracle_2_rows": qd_norm,
         },
         "simt_comparator": {
             "what": "plain double-double arithmetic on the FP64 ALUs, one accumulator per output "
                     "(17 FP64 operations per k), no splitting",
-            "value": units_s / t_s / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_s / args.steps,
+            "value": units_s / t_s / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_s / VSTEPS, "steps": VSTEPS,
             "roofline": {"bound": "alu", "kernel": "simt_dd_gemm_kernel (FP64 pipe)",
-                         "achieved": SIMT_OPS * M * N * K / (t_s / args.steps) / 1e12,
-                         "peak": FP64_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3, "unit": "T FP64 ops/s",
-                         "frac": (SIMT_OPS * M * N * K / (t_s / args.steps) / 1e12)
-                                 / (FP64_PER_CLK_SM * SM_COUNT * SM_MAX_GHZ / 1e3),
+                         "achieved": SIMT_OPS * M * N * K / (t_s / VSTEPS) / 1e12, "peak": simt_peak,
+                         "unit": "T FP64 ops/s",
+                         "frac": (SIMT_OPS * M * N * K / (t_s / VSTEPS) / 1e12) / simt_peak,
                          "peak_source": f"{FP64_PER_CLK_SM} FP64 instructions/clk/SM x {SM_COUNT} SMs x "
                                         f"{SM_MAX_GHZ} GHz"},
             "normwise_vs_exact_oracle_first_rows": simt_norm,
         },
+        "per_config": per_config,
     }
 
 
@@ -658,13 +874,20 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--shape", type=int, nargs=3, metavar=("M", "N", "K"),
                     help="profiling only: the workload's distribution and seed at another shape")
+    ap.add_argument("--only", choices=ONLY_VARIANTS,
+                    help="profiling only: warmup + steps products of one kind, no timing")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload legs")
     args = ap.parse_args(argv)
     w = workloads.WORKLOADS[args.workload]
     if args.shape:
         M, N, K = args.shape
         w = workloads.Workload(w.index, f"dd_gemm_{M}x{N}x{K}_{w.dist}", M, N, K, w.dist, w.seed)
-    args.w = w
-    out = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if args.only:
+        out = run_only(args, w)
+    elif args.impl == "reference":
+        out = run_reference(args, w)
+    else:
+        out = run_ours(args, w)
     if out is not None:
         print(json.dumps(out), flush=True)
 

@@ -226,8 +226,8 @@ def test_k_beyond_one_split_is_split_and_exact():
 
 def _extreme_element():
     """A double double whose parts (exponent e' = 0) are -127 then twelve times
-    -128: every product of two lower parts is 2^14, so a chunk of 512 of them
-    sums to exactly 2^23, the bound of the f32 accumulation."""
+    -128: every product of two lower parts is 2^14, so a chunk of 1024 of them
+    sums to exactly 2^24, the bound of the f32 accumulation."""
     from fractions import Fraction
     X = -(127 * 256**12 + 128 * (256**12 - 1) // 255)
     v = Fraction(X, 2**104)

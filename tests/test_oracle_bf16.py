@@ -135,9 +135,9 @@ def test_slice_products_bruteforce():
 
 def test_pair_count_and_bound():
     assert sb.PAIRS == 91 == sum(1 for s in range(13) for t in range(13) if s + t <= 12)
-    # parts of magnitude <= 128: a product is at most 2^14, so 512 products sum
-    # to at most 2^23 (exact in an fp32 accumulator, one bit of margin)
-    assert 128 * 128 == 2**14 and 512 * 2**14 == 2**23
+    # parts of magnitude <= 128: a product is at most 2^14, so a chunk of 1024
+    # products sums to at most 2^24, an integer an fp32 accumulator holds
+    assert 128 * 128 == 2**14 and 1024 * 2**14 == 2**24
 
 
 def check_recombine(fn):
