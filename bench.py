@@ -283,14 +283,24 @@ def config_of(w, world, splits):
             "l2": "no flush: inputs 512 MB and part planes 2 GB exceed the 126 MB L2"}
 
 
-def fp64_k_splits(w):
-    """The k-split dd_gemm_layout chooses for this shape on this device (the
-    reference arm reports it too, so both lines name the same workload)."""
-    try:
-        import extended_precision_gemm_gb300 as ddg
-        return ddg.layout(w.M, w.N, w.K)[3]
-    except Exception:
-        return None
+def fp64_k_splits(w, sms=SM_COUNT, per_sm=2):
+    """The k-split dd_gemm_layout chooses for this shape on a GB300 (152 SMs,
+    two slice-GEMM blocks resident per SM): the fewest splits whose waves of
+    blocks fill the GPU best.  Restated here so that the reference arm names
+    the same workload without loading the library."""
+    tiles = -(-w.M // 32) * -(-w.N // 32)
+    KC = -(-w.K // 8)
+    if tiles == 0 or KC <= 1:
+        return 1
+    slots = sms * per_sm
+    best, best_score = 1, -1.0
+    for s in range(1, min(64, max(1, KC // 4)) + 1):
+        blocks = tiles * s
+        waves = -(-blocks // slots)
+        score = blocks / (waves * slots) - 0.002 * s
+        if score > best_score + 1e-12:
+            best, best_score = s, score
+    return best
 
 
 def run_reference(args, w):
@@ -472,7 +482,7 @@ def measure_config(idx, T, ddg, torch, dev, peaks, fp64_peak, head=None):
         "value": 2.0 * M * N * K / t_step / 1e9, "unit": UNIT, "ms_per_step": 1e3 * t_step,
         "warmup": fw, "steps": fs, "k_splits": splits, "timed_through": timed_through,
         "slice_gemm": {"ms": 1e3 * t_gemm, **gemm, "bound": "tensor (FP64 pipe)"},
-        "split": {"ms": 1e3 * t_split, **gemm_roof(SPLIT_BYTES * (M * K + K * N) / 1e3, t_split, hbm_gbs, "GB/s"),
+        "split": {"ms": 1e3 * t_split, **gemm_roof(SPLIT_BYTES * (M * K + K * N) * 1e3, t_split, hbm_gbs, "GB/s"),
                   "kernels": "exponent reset + exponents + split (A and B)"},
         "recombine_ms": 1e3 * t_rec,
     }

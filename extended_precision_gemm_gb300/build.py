@@ -65,7 +65,7 @@ def build(force: bool = False, verbose: bool = False) -> pathlib.Path:
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = BUILD / f"libddgemm.{os.getpid()}.so"
-    cmd = [exe, *ARCH, "-shared", "-Xcompiler", "-fPIC", *map(str, objs), "-o", str(tmp)]
+    cmd = [exe, *ARCH, "-shared", "-Xcompiler", "-fPIC", *map(str, objs), "-ldl", "-o", str(tmp)]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")

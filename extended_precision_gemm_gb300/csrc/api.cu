@@ -7,6 +7,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "launch.cuh"
 
@@ -132,6 +134,23 @@ ddgemm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DDGEMM_OK : D
         if (err_ != cudaSuccess) return DDGEMM_ERR_CUDA; \
     } while (0)
 
+// An NVTX range around the launches of one step of a product ("dd/split",
+// "dd/slice_gemm", ...), so that a profiler can attribute and filter the
+// kernels by step (e.g. ncu --nvtx --nvtx-include "dd/slice_gemm/").  The
+// ranges cost nothing unless a tool is attached.
+struct StepRange {
+    explicit StepRange(const char* name) { nvtxRangePushA(name); }
+    ~StepRange() { nvtxRangePop(); }
+    StepRange(const StepRange&) = delete;
+    StepRange& operator=(const StepRange&) = delete;
+};
+
+#define DDG_STEP(name, call)        \
+    do {                            \
+        StepRange range_(name);     \
+        DDG_TRY(call);              \
+    } while (0)
+
 // Step 1 for any subset of the operands (null hi = operand absent): exponent
 // reset, exponents, split into FP64 or int16 part planes -- three launches.
 cudaError_t run_split(int64_t M, int64_t N, int64_t K, int64_t Kp, const double* A_hi, const double* A_lo,
@@ -159,9 +178,9 @@ ddgemm_status run_gemm(const Layout& L, int64_t M, int64_t N, int64_t K, const d
     double* pA = reinterpret_cast<double*>(ws + L.off_A);
     double* pB = reinterpret_cast<double*>(ws + L.off_B);
     double* P = reinterpret_cast<double*>(ws + L.off_P);
-    DDG_TRY(run_split(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, false, st));
-    DDG_TRY(launch_slice_gemm(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
-    DDG_TRY(launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
+    DDG_STEP("dd/split", run_split(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, false, st));
+    DDG_STEP("dd/slice_gemm", launch_slice_gemm(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_STEP("dd/recombine", launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
     return DDGEMM_OK;
 }
 
@@ -176,9 +195,9 @@ ddgemm_status run_gemm_i64(const Layout& L, int64_t M, int64_t N, int64_t K, con
     int16_t* pA = reinterpret_cast<int16_t*>(ws + L.off_A);
     int16_t* pB = reinterpret_cast<int16_t*>(ws + L.off_B);
     double* P = reinterpret_cast<double*>(ws + L.off_P);
-    DDG_TRY(run_split(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, true, st));
-    DDG_TRY(launch_slice_gemm_i64(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
-    DDG_TRY(launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
+    DDG_STEP("dd_i64/split", run_split(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, true, st));
+    DDG_STEP("dd_i64/slice_gemm", launch_slice_gemm_i64(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_STEP("dd_i64/recombine", launch_recombine(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
     return DDGEMM_OK;
 }
 
@@ -593,11 +612,11 @@ static ddgemm_status run_qd(const Layout& L, int64_t M, int64_t N, int64_t K, co
     int16_t* pB = reinterpret_cast<int16_t*>(ws + L.off_B);
     double* P = reinterpret_cast<double*>(ws + L.off_P);
     SplitOperand a{A[0], A[1], lda, M, e}, b{B[0], B[1], ldb, N, f};
-    DDG_TRY(launch_init_exponents(e, M, f, N, K, st));
-    DDG_TRY(launch_exponents(&a, &b, K, st));
-    DDG_TRY(launch_split_qd(A, lda, M, e, B, ldb, N, f, K, L.Kp, pA, pB, st));
-    DDG_TRY(launch_slice_gemm_qd(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
-    DDG_TRY(launch_recombine_qd(P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
+    DDG_STEP("qd/exponents", launch_init_exponents(e, M, f, N, K, st));
+    DDG_STEP("qd/exponents", launch_exponents(&a, &b, K, st));
+    DDG_STEP("qd/split", launch_split_qd(A, lda, M, e, B, ldb, N, f, K, L.Kp, pA, pB, st));
+    DDG_STEP("qd/slice_gemm", launch_slice_gemm_qd(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_STEP("qd/recombine", launch_recombine_qd(P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
     return DDGEMM_OK;
 }
 
@@ -742,25 +761,25 @@ ddgemm_status run_gemm_ex(const ExPlan& X, int64_t M, int64_t N, int64_t K, cons
     double* P = X.fuse_recombine ? nullptr : reinterpret_cast<double*>(ws + X.off_P);
     if (X.fuse_split) {
         SplitOperand a{A_hi, A_lo, lda, M, e, false}, b{B_hi, B_lo, ldb, N, f, false};
-        DDG_TRY(launch_init_exponents(e, M, f, N, K, st));
-        DDG_TRY(launch_exponents(&a, &b, K, st));
+        DDG_STEP("dd_ex/exponents", launch_init_exponents(e, M, f, N, K, st));
+        DDG_STEP("dd_ex/exponents", launch_exponents(&a, &b, K, st));
         const FusedSrc g = make_fused_src(A_hi, A_lo, lda, B_hi, B_lo, ldb, e, f, M, N, K);
         if (X.fuse_recombine) {
-            DDG_TRY(launch_slice_gemm_fused_recombine(g, X.Mp, X.Np, X.Kp, C_hi, C_lo, ldc, st));
+            DDG_STEP("dd_ex/slice_gemm", launch_slice_gemm_fused_recombine(g, X.Mp, X.Np, X.Kp, C_hi, C_lo, ldc, st));
             return DDGEMM_OK;
         }
-        DDG_TRY(launch_slice_gemm_fused(g, X.Mp, X.Np, X.Kp, X.splits, P, st));
+        DDG_STEP("dd_ex/slice_gemm", launch_slice_gemm_fused(g, X.Mp, X.Np, X.Kp, X.splits, P, st));
     } else {
         double* pA = reinterpret_cast<double*>(ws + X.off_A);
         double* pB = reinterpret_cast<double*>(ws + X.off_B);
-        DDG_TRY(run_split(M, N, K, X.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, false, st));
+        DDG_STEP("dd_ex/split", run_split(M, N, K, X.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, false, st));
         if (X.fuse_recombine) {
-            DDG_TRY(launch_slice_gemm_recombine(pA, pB, X.Mp, X.Np, X.Kp, e, f, M, N, C_hi, C_lo, ldc, st));
+            DDG_STEP("dd_ex/slice_gemm", launch_slice_gemm_recombine(pA, pB, X.Mp, X.Np, X.Kp, e, f, M, N, C_hi, C_lo, ldc, st));
             return DDGEMM_OK;
         }
-        DDG_TRY(launch_slice_gemm(pA, pB, X.Mp, X.Np, X.Kp, X.splits, P, st));
+        DDG_STEP("dd_ex/slice_gemm", launch_slice_gemm(pA, pB, X.Mp, X.Np, X.Kp, X.splits, P, st));
     }
-    DDG_TRY(launch_recombine(P, X.splits, X.Mp, X.Np, e, f, M, N, C_hi, C_lo, ldc, st));
+    DDG_STEP("dd_ex/recombine", launch_recombine(P, X.splits, X.Mp, X.Np, e, f, M, N, C_hi, C_lo, ldc, st));
     return DDGEMM_OK;
 }
 
@@ -986,9 +1005,9 @@ ddgemm_status run_gemm_tc(const TcLayout& L, int64_t M, int64_t N, int64_t K, co
     uint16_t* pA = reinterpret_cast<uint16_t*>(ws + L.off_A);
     uint16_t* pB = reinterpret_cast<uint16_t*>(ws + L.off_B);
     int32_t* P = reinterpret_cast<int32_t*>(ws + L.off_P);
-    DDG_TRY(run_split_tc(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, st));
-    DDG_TRY(launch_slice_gemm_tc(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
-    DDG_TRY(launch_recombine_tc(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
+    DDG_STEP("dd_tc/split", run_split_tc(M, N, K, L.Kp, A_hi, A_lo, lda, e, pA, B_hi, B_lo, ldb, f, pB, st));
+    DDG_STEP("dd_tc/slice_gemm", launch_slice_gemm_tc(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_STEP("dd_tc/recombine", launch_recombine_tc(P, L.splits, L.Mp, L.Np, e, f, M, N, C_hi, C_lo, ldc, st));
     return DDGEMM_OK;
 }
 
@@ -1173,9 +1192,9 @@ ddgemm_status run_qd_tc(const TcLayout& L, int64_t M, int64_t N, int64_t K, cons
     uint16_t* pA = reinterpret_cast<uint16_t*>(ws + L.off_A);
     uint16_t* pB = reinterpret_cast<uint16_t*>(ws + L.off_B);
     int32_t* P = reinterpret_cast<int32_t*>(ws + L.off_P);
-    DDG_TRY(run_split_tc_qd(M, N, K, L.Kp, A, lda, e, pA, B, ldb, f, pB, st));
-    DDG_TRY(launch_slice_gemm_tc_qd(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
-    DDG_TRY(launch_recombine_tc_qd(P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
+    DDG_STEP("qd_tc/split", run_split_tc_qd(M, N, K, L.Kp, A, lda, e, pA, B, ldb, f, pB, st));
+    DDG_STEP("qd_tc/slice_gemm", launch_slice_gemm_tc_qd(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_STEP("qd_tc/recombine", launch_recombine_tc_qd(P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
     return DDGEMM_OK;
 }
 
@@ -1321,9 +1340,9 @@ ddgemm_status run_md_tc(int nparts, const TcLayout& L, int64_t M, int64_t N, int
     uint16_t* pA = reinterpret_cast<uint16_t*>(ws + L.off_A);
     uint16_t* pB = reinterpret_cast<uint16_t*>(ws + L.off_B);
     int32_t* P = reinterpret_cast<int32_t*>(ws + L.off_P);
-    DDG_TRY(run_split_tc_md(nparts, M, N, K, L.Kp, A, lda, e, pA, B, ldb, f, pB, st));
-    DDG_TRY(launch_slice_gemm_tc_md(nparts, pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
-    DDG_TRY(launch_recombine_tc_md(nparts, P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
+    DDG_STEP("md_tc/split", run_split_tc_md(nparts, M, N, K, L.Kp, A, lda, e, pA, B, ldb, f, pB, st));
+    DDG_STEP("md_tc/slice_gemm", launch_slice_gemm_tc_md(nparts, pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
+    DDG_STEP("md_tc/recombine", launch_recombine_tc_md(nparts, P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
     return DDGEMM_OK;
 }
 
