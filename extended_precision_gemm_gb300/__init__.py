@@ -29,6 +29,7 @@ __all__ = [
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
     "split", "split_i16", "dd_gemm_simt", "EXP_NONE", "exponents", "split_with_exponents",
     "split_bf16_with_exponents", "dd_gemm_tc_host", "DDGemmOpts", "dd_gemm_ex", "ex_plan", "slice_gemm_fused",
+    "host_pool_trim",
     "QD_MAX_K", "qd_gemm", "qd_layout", "qd_workspace_size", "qd_split", "qd_slice_gemm", "qd_recombine",
     "TC_SLICES", "TC_TILE_M", "TC_BLOCK_M", "TC_TILE_N", "TC_CHUNK_K", "TC_MAX_K_SPLIT",
     "dd_gemm_tc", "tc_layout", "tc_workspace_size", "split_bf16", "slice_gemm_tc", "recombine_tc",
@@ -94,6 +95,7 @@ _SIGNATURES = {
                     ctypes.c_size_t, _ptr], _int),
     "dd_slice_gemm_fused": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _int, _ptr, _ptr],
                             _int),
+    "dd_host_pool_trim": ([], _int),
     "dd_gemm_tc_host": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
     "qd_gemm_layout": ([_i64, _i64, _i64, _ptr], _int),
     "qd_gemm_workspace_size": ([_i64, _i64, _i64, _ptr], _int),
@@ -775,6 +777,12 @@ def split_bf16_with_exponents(A_hi, A_lo, B_hi, B_lo, e, f, planesA=None, planes
                                                B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi), e.data_ptr(),
                                                f.data_ptr(), pA.data_ptr(), pB.data_ptr(), _stream_handle(stream)))
     return pA, pB
+
+
+def host_pool_trim():
+    """Return the device memory the host-buffer products keep in the
+    library's pool on the current device."""
+    _check("dd_host_pool_trim", load().dd_host_pool_trim())
 
 
 def dd_gemm_tc_host(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, stream=None):

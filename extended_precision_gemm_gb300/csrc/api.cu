@@ -159,8 +159,7 @@ cudaError_t run_split(int64_t M, int64_t N, int64_t K, int64_t Kp, const double*
     SplitOperand a{A_hi, A_lo, lda, M, e}, b{B_hi, B_lo, ldb, N, f};
     const SplitOperand* pa = (e != nullptr && M > 0) ? &a : nullptr;
     const SplitOperand* pb = (f != nullptr && N > 0) ? &b : nullptr;
-    cudaError_t err = launch_init_exponents(pa ? e : nullptr, M, pb ? f : nullptr, N, K, st);
-    if (err == cudaSuccess) err = launch_exponents(pa, pb, K, st);
+    cudaError_t err = launch_shared_exponents(pa, pb, K, 0, st);
     if (err == cudaSuccess)
         err = i16 ? launch_split_i16(pa, pb, K, Kp, static_cast<int16_t*>(pA), static_cast<int16_t*>(pB), st)
                   : launch_split_f64(pa, pb, K, Kp, static_cast<double*>(pA), static_cast<double*>(pB), st);
@@ -206,6 +205,42 @@ ddgemm_status run_gemm_i64(const Layout& L, int64_t M, int64_t N, int64_t K, con
 // `ws_bytes` of workspace; the operands are copied in, `run` launches the
 // product on the dense device copies, C is copied back, the block is freed,
 // and the stream is synchronised before returning.
+// The stream-ordered memory pool of the host-buffer entry points on the
+// current device: created on first use with no release threshold, so the
+// device memory of one call (operands, result, workspace) stays in the pool
+// for the next instead of being unmapped at every synchronisation and mapped
+// again (which costs more than the copies at 4096^3).  dd_host_pool_trim
+// gives it back.
+constexpr int kMaxPoolDevices = 64;
+std::mutex g_pool_mutex;
+cudaMemPool_t g_host_pool[kMaxPoolDevices] = {};
+
+cudaError_t host_pool(cudaMemPool_t* pool, bool create) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxPoolDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (g_host_pool[dev] == nullptr && create) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        err = cudaMemPoolCreate(&p, &props);
+        if (err != cudaSuccess) return err;
+        uint64_t keep = ~0ULL;
+        err = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (err != cudaSuccess) {
+            cudaMemPoolDestroy(p);
+            return err;
+        }
+        g_host_pool[dev] = p;
+    }
+    *pool = g_host_pool[dev];
+    return cudaSuccess;
+}
+
 // `peek` reads the slice GEMM's count of bounded waits that gave up: a count
 // that grew during the call makes it return DDGEMM_ERR_CUDA.
 template <class Run, class Peek>
@@ -216,8 +251,13 @@ ddgemm_status host_product(int64_t M, int64_t N, int64_t K, const double* h_A_hi
     if (peek(&timeouts_before, st) != cudaSuccess) return DDGEMM_ERR_CUDA;
     const int64_t a = round_up(M * K * 8, kAlign), b = round_up(K * N * 8, kAlign), c = round_up(M * N * 8, kAlign);
     const int64_t total = 2 * a + 2 * b + 2 * c + ws_bytes;
+    cudaMemPool_t pool = nullptr;
+    if (host_pool(&pool, true) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_CUDA;
+    }
     char* dev = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&dev), (size_t)total, st) != cudaSuccess) {
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dev), (size_t)total, pool, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }
@@ -412,8 +452,7 @@ ddgemm_status dd_exponents(int64_t M, int64_t N, int64_t K, const double* A_hi, 
     SplitOperand a{A_hi, nullptr, lda, M, e, false}, b{B_hi, nullptr, ldb, N, f, false};
     const SplitOperand* pa = M > 0 ? &a : nullptr;
     const SplitOperand* pb = N > 0 ? &b : nullptr;
-    DDG_TRY(launch_reset_exponents(pa ? e : nullptr, M, pb ? f : nullptr, N, EXP_NONE, st));
-    DDG_TRY(launch_exponents(pa, pb, K, st));
+    DDG_TRY(launch_shared_exponents(pa, pb, K, EXP_NONE, st));
     return DDGEMM_OK;
 }
 
@@ -479,6 +518,20 @@ ddgemm_status dd_wait_timeouts(unsigned int* count) {
     if (s == DDGEMM_OK) s = from_cuda(read_and_reset_wait_timeouts_tc_md(&m));
     *count = a + b + c + d + m;
     return s;
+}
+
+ddgemm_status dd_host_pool_trim(void) {
+    cudaMemPool_t pool = nullptr;
+    if (host_pool(&pool, false) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_CUDA;
+    }
+    if (pool == nullptr) return DDGEMM_OK;  // no host-buffer call on this device yet
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemPoolTrimTo(pool, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_CUDA;
+    }
+    return DDGEMM_OK;
 }
 
 // ---- the comparator ----
@@ -612,8 +665,7 @@ static ddgemm_status run_qd(const Layout& L, int64_t M, int64_t N, int64_t K, co
     int16_t* pB = reinterpret_cast<int16_t*>(ws + L.off_B);
     double* P = reinterpret_cast<double*>(ws + L.off_P);
     SplitOperand a{A[0], A[1], lda, M, e}, b{B[0], B[1], ldb, N, f};
-    DDG_STEP("qd/exponents", launch_init_exponents(e, M, f, N, K, st));
-    DDG_STEP("qd/exponents", launch_exponents(&a, &b, K, st));
+    DDG_STEP("qd/exponents", launch_shared_exponents(&a, &b, K, 0, st));
     DDG_STEP("qd/split", launch_split_qd(A, lda, M, e, B, ldb, N, f, K, L.Kp, pA, pB, st));
     DDG_STEP("qd/slice_gemm", launch_slice_gemm_qd(pA, pB, L.Mp, L.Np, L.Kp, L.splits, P, st));
     DDG_STEP("qd/recombine", launch_recombine_qd(P, L.splits, L.Mp, L.Np, e, f, M, N, C, ldc, st));
@@ -669,8 +721,7 @@ ddgemm_status qd_split(int64_t M, int64_t N, int64_t K, const double* const* A, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t Kp = round_up(K, BK);
     SplitOperand a{M > 0 ? A[0] : nullptr, nullptr, lda, M, e}, b{N > 0 ? B[0] : nullptr, nullptr, ldb, N, f};
-    DDG_TRY(launch_init_exponents(M > 0 ? e : nullptr, M, N > 0 ? f : nullptr, N, K, st));
-    DDG_TRY(launch_exponents(M > 0 ? &a : nullptr, N > 0 ? &b : nullptr, K, st));
+    DDG_TRY(launch_shared_exponents(M > 0 ? &a : nullptr, N > 0 ? &b : nullptr, K, 0, st));
     DDG_TRY(launch_split_qd(M > 0 ? A : nullptr, lda, M, e, N > 0 ? B : nullptr, ldb, N, f, K, Kp, planesA,
                             planesB, st));
     return DDGEMM_OK;
@@ -761,8 +812,7 @@ ddgemm_status run_gemm_ex(const ExPlan& X, int64_t M, int64_t N, int64_t K, cons
     double* P = X.fuse_recombine ? nullptr : reinterpret_cast<double*>(ws + X.off_P);
     if (X.fuse_split) {
         SplitOperand a{A_hi, A_lo, lda, M, e, false}, b{B_hi, B_lo, ldb, N, f, false};
-        DDG_STEP("dd_ex/exponents", launch_init_exponents(e, M, f, N, K, st));
-        DDG_STEP("dd_ex/exponents", launch_exponents(&a, &b, K, st));
+        DDG_STEP("dd_ex/exponents", launch_shared_exponents(&a, &b, K, 0, st));
         const FusedSrc g = make_fused_src(A_hi, A_lo, lda, B_hi, B_lo, ldb, e, f, M, N, K);
         if (X.fuse_recombine) {
             DDG_STEP("dd_ex/slice_gemm", launch_slice_gemm_fused_recombine(g, X.Mp, X.Np, X.Kp, C_hi, C_lo, ldc, st));
@@ -990,8 +1040,7 @@ cudaError_t run_split_tc(int64_t M, int64_t N, int64_t K, int64_t Kp, const doub
     SplitOperand a{A_hi, A_lo, lda, M, e}, b{B_hi, B_lo, ldb, N, f};
     const SplitOperand* pa = (e != nullptr && M > 0) ? &a : nullptr;
     const SplitOperand* pb = (f != nullptr && N > 0) ? &b : nullptr;
-    cudaError_t err = launch_init_exponents(pa ? e : nullptr, M, pb ? f : nullptr, N, K, st);
-    if (err == cudaSuccess) err = launch_exponents(pa, pb, K, st);
+    cudaError_t err = launch_shared_exponents(pa, pb, K, 0, st);
     if (err == cudaSuccess) err = launch_split_bf16(pa, pb, K, Kp, pa ? pA : nullptr, pb ? pB : nullptr, st);
     return err;
 }
@@ -1177,8 +1226,7 @@ cudaError_t run_split_tc_qd(int64_t M, int64_t N, int64_t K, int64_t Kp, const d
                             cudaStream_t st) {
     const bool has_a = A != nullptr && e != nullptr && M > 0, has_b = B != nullptr && f != nullptr && N > 0;
     SplitOperand a{has_a ? A[0] : nullptr, nullptr, lda, M, e}, b{has_b ? B[0] : nullptr, nullptr, ldb, N, f};
-    cudaError_t err = launch_init_exponents(has_a ? e : nullptr, M, has_b ? f : nullptr, N, K, st);
-    if (err == cudaSuccess) err = launch_exponents(has_a ? &a : nullptr, has_b ? &b : nullptr, K, st);
+    cudaError_t err = launch_shared_exponents(has_a ? &a : nullptr, has_b ? &b : nullptr, K, 0, st);
     if (err == cudaSuccess)
         err = launch_split_bf16_qd(has_a ? A : nullptr, lda, M, e, has_b ? B : nullptr, ldb, N, f, K, Kp, pA, pB, st);
     return err;
@@ -1324,8 +1372,7 @@ cudaError_t run_split_tc_md(int nparts, int64_t M, int64_t N, int64_t K, int64_t
                             uint16_t* pB, cudaStream_t st) {
     const bool has_a = A != nullptr && e != nullptr && M > 0, has_b = B != nullptr && f != nullptr && N > 0;
     SplitOperand a{has_a ? A[0] : nullptr, nullptr, lda, M, e}, b{has_b ? B[0] : nullptr, nullptr, ldb, N, f};
-    cudaError_t err = launch_init_exponents(has_a ? e : nullptr, M, has_b ? f : nullptr, N, K, st);
-    if (err == cudaSuccess) err = launch_exponents(has_a ? &a : nullptr, has_b ? &b : nullptr, K, st);
+    cudaError_t err = launch_shared_exponents(has_a ? &a : nullptr, has_b ? &b : nullptr, K, 0, st);
     if (err == cudaSuccess)
         err = launch_split_bf16_md(nparts, has_a ? A : nullptr, lda, M, e, has_b ? B : nullptr, ldb, N, f, K, Kp, pA,
                                    pB, st);

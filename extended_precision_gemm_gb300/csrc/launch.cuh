@@ -9,8 +9,8 @@ namespace ddg {
 // Step 1: exponents and part planes.  An operand is A (its rows) or B (its
 // columns); `rows` counts rows of A or columns of B; element (r, k) is
 // hi[r * ld + k] for A and hi[k * ld + r] for B.  Exponent arrays are
-// accumulated with atomicMax and must be reset by launch_init_exponents
-// first.  Either operand may be null.  The split kernels turn the sentinel
+// accumulated with atomicMax (launch_shared_exponents resets them first).
+// Either operand may be null.  The split kernels turn the sentinel
 // EXP_NONE of an all-zero row into its final exponent 0 in place, unless
 // exp_given is set (exponents supplied by the caller, read only).
 struct SplitOperand {
@@ -21,12 +21,16 @@ struct SplitOperand {
     int32_t* exp;
     bool exp_given;
 };
-cudaError_t launch_init_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int64_t K,
-                                  cudaStream_t st);
 // Set every exponent to `value` (EXP_NONE before launch_exponents when the
 // raw maxima, sentinel included, are wanted).
 cudaError_t launch_reset_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int32_t value,
                                    cudaStream_t st);
+// The shared exponents of A's rows and B's columns (either may be null):
+// e[i] = smallest e with max_k |A_hi[i,k]| < 2^e, EXP_NONE for a row without
+// a nonzero element (a reset, then the atomicMax kernel over k-chunks); with
+// K = 0 every exponent is set to zero_k_value.
+cudaError_t launch_shared_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, int32_t zero_k_value,
+                                    cudaStream_t st);
 cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, cudaStream_t st);
 // FP64 parts in the tiled layout of the mma.sync slice GEMM.
 cudaError_t launch_split_f64(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,

@@ -342,21 +342,23 @@ int num_sms() {
 
 }  // namespace
 
-cudaError_t launch_init_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int64_t K,
-                                  cudaStream_t st) {
-    int64_t n = std::max(e ? M : 0, f ? N : 0);
-    if (n == 0) return cudaSuccess;
-    // K = 0 has no elements to take a maximum over: every exponent is final 0.
-    init_exponents_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(e, M, f, N, K == 0 ? 0 : EXP_NONE);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_reset_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int32_t value,
                                    cudaStream_t st) {
     int64_t n = std::max(e ? M : 0, f ? N : 0);
     if (n == 0) return cudaSuccess;
     init_exponents_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(e, M, f, N, value);
     return cudaGetLastError();
+}
+
+cudaError_t launch_shared_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, int32_t zero_k_value,
+                                    cudaStream_t st) {
+    int32_t* e = A ? A->exp : nullptr;
+    int32_t* f = B ? B->exp : nullptr;
+    const int64_t M = A ? A->rows : 0, N = B ? B->rows : 0;
+    if (K == 0) return launch_reset_exponents(e, M, f, N, zero_k_value, st);
+    cudaError_t err = launch_reset_exponents(e, M, f, N, EXP_NONE, st);
+    if (err != cudaSuccess) return err;
+    return launch_exponents(A, B, K, st);
 }
 
 cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, cudaStream_t st) {

@@ -113,10 +113,14 @@ ddgemm_status dd_gemm(int64_t M, int64_t N, int64_t K,
 
 /*
  * C = A * B with HOST operands and result: copies A and B to the current
- * device, runs dd_gemm, copies C back, frees what it allocated, and returns
- * only after the result is in h_C_hi / h_C_lo (it synchronises `stream`).
- * Host buffers are read and written as dense row-major arrays with the given
- * leading dimensions; page-locked (pinned) buffers make the copies faster.
+ * device, runs dd_gemm, copies C back, and returns only after the result is
+ * in h_C_hi / h_C_lo (it synchronises `stream`).  Host buffers are read and
+ * written as dense row-major arrays with the given leading dimensions;
+ * page-locked (pinned) buffers make the copies faster.  The device memory of
+ * the call (dense copies of A, B and C plus the workspace) comes from a
+ * stream-ordered pool of the library on the current device, which keeps it
+ * after the call for the next one (mapping gigabytes anew on every call costs
+ * more than the copies); dd_host_pool_trim returns it to the device.
  */
 ddgemm_status dd_gemm_host(int64_t M, int64_t N, int64_t K,
                            const double* h_A_hi, const double* h_A_lo, int64_t lda,
@@ -208,6 +212,13 @@ ddgemm_status dd_gemm_noalloc(int64_t M, int64_t N, int64_t K,
                               const double* A_hi, const double* A_lo, int64_t lda,
                               const double* B_hi, const double* B_lo, int64_t ldb,
                               double* C_hi, double* C_lo, int64_t ldc, void* stream);
+
+/*
+ * Return the device memory that dd_gemm_host / dd_gemm_tc_host keep in the
+ * library's pool on the current device (synchronises the device).  DDGEMM_OK
+ * also when no such call has run on it.
+ */
+ddgemm_status dd_host_pool_trim(void);
 
 /* ------------------------------------------------------------------ */
 /* The steps of the path, one entry point each                          */
@@ -513,10 +524,10 @@ ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K,
 
 /*
  * dd_gemm_tc with HOST operands and result, as dd_gemm_host: copies A and B
- * to the current device, runs dd_gemm_tc on a stream-ordered workspace,
- * copies C back, frees what it allocated, and returns after the result is in
- * h_C_hi / h_C_lo (it synchronises `stream`).  Pinned host buffers make the
- * copies faster.
+ * to the current device (memory from the library's pool, see dd_gemm_host),
+ * runs dd_gemm_tc, copies C back, and returns after the result is in h_C_hi /
+ * h_C_lo (it synchronises `stream`).  Pinned host buffers make the copies
+ * faster.
  */
 ddgemm_status dd_gemm_tc_host(int64_t M, int64_t N, int64_t K,
                               const double* h_A_hi, const double* h_A_lo, int64_t lda,

@@ -296,3 +296,12 @@ def test_dd_gemm_tc_host_matches_device_and_model():
                                B_lo.ctypes.data, N, Cw.ctypes.data, Cwl.ctypes.data, N + 2, None) == 0
     assert np.array_equal(Cw[:, :N], H_hi) and np.array_equal(Cwl[:, :N], H_lo)
     assert (Cw[:, N:] == 5.0).all() and (Cwl[:, N:] == 5.0).all()
+    # the pool that keeps the calls' device memory can be emptied, and the
+    # next call refills it
+    ddg.host_pool_trim()
+    G_hi = np.zeros((M, N))
+    G_lo = np.zeros((M, N))
+    ddg.dd_gemm_tc_host(A_hi, A_lo, B_hi, B_lo, G_hi, G_lo)
+    ddg.dd_gemm_host(A_hi, A_lo, B_hi, B_lo, np.zeros((M, N)), np.zeros((M, N)))
+    assert np.array_equal(G_hi, H_hi) and np.array_equal(G_lo, H_lo)
+    ddg.host_pool_trim()
