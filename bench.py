@@ -65,6 +65,7 @@ FALLBACK_BF16_SUSTAINED_TF = 1700.0
 FALLBACK_HBM_GBS = 6800.0
 LAUNCHES_PER_STEP = 5  # exponent reset, exponents, split, slice GEMM, recombine
 SIMT_OPS = 17          # FP64 operations per k of the comparator's dd multiply-add
+RECOMB_FP64_OPS = 70   # FP64 operations per output of the recombination: 7 x (two_sum 6 + 1 + quick_two_sum 3)
 FP64_PER_CLK_SM = 2    # FP64 (DFMA/DADD/DMUL) instructions per clock per SM (GB300)
 IMAD_PER_CLK_SM = 64   # 32-bit integer multiply-add (also 32x32->64 wide) per clock per SM
 SM_COUNT = 152
@@ -339,6 +340,13 @@ class Timer:
     def __init__(self, torch, stream, dev, dist):
         self.torch, self.stream, self.dev, self.dist = torch, stream, dev, dist
 
+    def lead(self):
+        """Queue about 1 ms of device work ahead of the first timed event, so
+        that the timed launches are enqueued while the GPU is busy and no
+        host launch latency falls inside the timed region."""
+        with self.torch.cuda.stream(self.stream):
+            self.torch.cuda._sleep(2_000_000)
+
     def steps(self, fn, steps, warmup):
         """Seconds for `steps` calls of fn after `warmup` untimed ones."""
         torch = self.torch
@@ -347,6 +355,7 @@ class Timer:
         torch.cuda.synchronize(self.dev)
         barrier(self.dist)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.lead()
         e0.record(self.stream)
         for _ in range(steps):
             fn()
@@ -362,6 +371,7 @@ class Timer:
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
         torch.cuda.synchronize(self.dev)
         barrier(self.dist)
+        self.lead()
         for i in range(steps):
             evs[i][0].record(self.stream)
             for j, ph in enumerate(phases):
@@ -572,6 +582,7 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     clocks.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    T.lead()
     ev0.record(stream)
     for _ in range(args.steps):
         step()
@@ -787,8 +798,13 @@ def run_ours(args, w):
         "roofline_split": {"bound": "hbm", "achieved": split_gbs, "peak": hbm_gbs, "unit": "GB/s",
                            "frac": split_gbs / hbm_gbs, "bytes_per_step": SPLIT_BYTES * (M * K + K * N),
                            "ms": 1e3 * t_split, "kernels": "exponent reset + exponents + split (A and B)"},
-        "roofline_recombine": {"bound": "hbm", "achieved": recomb_gbs, "peak": hbm_gbs, "unit": "GB/s",
-                               "frac": recomb_gbs / hbm_gbs, "ms": 1e3 * t_recomb},
+        "roofline_recombine": {"bound": "alu", "kernel": "recombine_kernel (FP64 pipe)",
+                               "achieved": RECOMB_FP64_OPS * M * N / t_recomb / 1e12, "peak": simt_peak,
+                               "unit": "T FP64 ops/s",
+                               "frac": RECOMB_FP64_OPS * M * N / t_recomb / 1e12 / simt_peak,
+                               "peak_source": f"{FP64_PER_CLK_SM} FP64 instructions/clk/SM x {SM_COUNT} SMs x "
+                                              f"{SM_MAX_GHZ} GHz",
+                               "ms": 1e3 * t_recomb, "hbm_gbs": recomb_gbs, "hbm_frac": recomb_gbs / hbm_gbs},
         "frac_of_fp64_tensor_roof_end_to_end": (units / t_max * PAIRS) / (fp64_peak * 1e12),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_units / t_e2e / 1e9, "unit": UNIT, "steps": VSTEPS,

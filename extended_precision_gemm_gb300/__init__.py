@@ -16,6 +16,7 @@ added back into a double double.
 from __future__ import annotations
 
 import ctypes
+import os
 import pathlib
 import threading
 
@@ -29,7 +30,7 @@ __all__ = [
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
     "split", "split_i16", "dd_gemm_simt", "EXP_NONE", "exponents", "split_with_exponents",
     "split_bf16_with_exponents", "dd_gemm_tc_host", "DDGemmOpts", "dd_gemm_ex", "ex_plan", "slice_gemm_fused",
-    "host_pool_trim",
+    "host_pool_trim", "checked_build", "check_report",
     "QD_MAX_K", "qd_gemm", "qd_layout", "qd_workspace_size", "qd_split", "qd_slice_gemm", "qd_recombine",
     "TC_SLICES", "TC_TILE_M", "TC_BLOCK_M", "TC_TILE_N", "TC_CHUNK_K", "TC_MAX_K_SPLIT",
     "dd_gemm_tc", "tc_layout", "tc_workspace_size", "split_bf16", "slice_gemm_tc", "recombine_tc",
@@ -96,6 +97,8 @@ _SIGNATURES = {
     "dd_slice_gemm_fused": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _int, _ptr, _ptr],
                             _int),
     "dd_host_pool_trim": ([], _int),
+    "dd_checked_build": ([], _int),
+    "dd_check_report": ([_ptr, _ptr, _ptr], _int),
     "dd_gemm_tc_host": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
     "qd_gemm_layout": ([_i64, _i64, _i64, _ptr], _int),
     "qd_gemm_workspace_size": ([_i64, _i64, _i64, _ptr], _int),
@@ -125,8 +128,14 @@ _SIGNATURES = {
 }
 
 
+def _checked_requested() -> bool:
+    return os.environ.get("DDGEMM_CHECKED", "") not in ("", "0")
+
+
 def library_path() -> pathlib.Path:
-    return _build.LIB
+    """The library this process loads: libddgemm.so, or the bounds-checked
+    libddgemm_checked.so when the environment sets DDGEMM_CHECKED=1."""
+    return _build.LIB_CHECKED if _checked_requested() else _build.LIB
 
 
 def exported_symbols():
@@ -135,15 +144,16 @@ def exported_symbols():
 
 
 def load(build_if_missing: bool = True):
-    """Load libddgemm.so (building it with nvcc first if it is missing)."""
+    """Load the library (building it with nvcc first if it is missing)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
-            if not _build.up_to_date():
+            checked = _checked_requested()
+            path = library_path()
+            if not _build.up_to_date(checked):
                 if not build_if_missing and not path.exists():
                     raise RuntimeError(f"{path} is not built")
-                _build.build()
+                _build.build(checked=checked)
             lib = ctypes.CDLL(str(path))
             for name, (args, res) in _SIGNATURES.items():
                 fn = getattr(lib, name)
@@ -777,6 +787,19 @@ def split_bf16_with_exponents(A_hi, A_lo, B_hi, B_lo, e, f, planesA=None, planes
                                                B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi), e.data_ptr(),
                                                f.data_ptr(), pA.data_ptr(), pB.data_ptr(), _stream_handle(stream)))
     return pA, pB
+
+
+def checked_build() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(load().dd_checked_build())
+
+
+def check_report():
+    """(count, site, index) of the accesses the bounds-checked build refused
+    since the last call (synchronises the device; zeros in the normal build)."""
+    n, site, idx = ctypes.c_uint(), ctypes.c_uint(), _i64()
+    _check("dd_check_report", load().dd_check_report(ctypes.byref(n), ctypes.byref(site), ctypes.byref(idx)))
+    return n.value, site.value, idx.value
 
 
 def host_pool_trim():

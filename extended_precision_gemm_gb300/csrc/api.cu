@@ -520,6 +520,36 @@ ddgemm_status dd_wait_timeouts(unsigned int* count) {
     return s;
 }
 
+int dd_checked_build(void) {
+#ifdef DDGEMM_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+ddgemm_status dd_check_report(unsigned int* count, unsigned int* site, int64_t* index) {
+    if (count == nullptr || site == nullptr || index == nullptr) return DDGEMM_ERR_INVALID_ARG;
+    cudaError_t (*readers[])(CheckRecord*) = {check_record_split, check_record_slice_gemm, check_record_fused,
+                                              check_record_recombine, check_record_tc, check_record_tc_md};
+    *count = 0;
+    *site = 0;
+    *index = 0;
+    for (auto read : readers) {
+        CheckRecord r{};
+        if (read(&r) != cudaSuccess) {
+            cudaGetLastError();
+            return DDGEMM_ERR_CUDA;
+        }
+        if (r.count > 0 && *count == 0) {
+            *site = r.site;
+            *index = r.index;
+        }
+        *count += r.count;
+    }
+    return DDGEMM_OK;
+}
+
 ddgemm_status dd_host_pool_trim(void) {
     cudaMemPool_t pool = nullptr;
     if (host_pool(&pool, false) != cudaSuccess) {

@@ -45,4 +45,69 @@ __device__ __forceinline__ double small_int_to_double(uint32_t v, uint64_t sign)
     return __longlong_as_double((long long)bits);
 }
 
+// Bounds-checked build.  Compiled with -DDDGEMM_CHECKED (libddgemm_checked.so),
+// every global access the kernels guard with in_bounds() is tested against
+// the extent of its buffer first; a failing access is skipped, never trapped,
+// and the first failure of the translation unit is recorded (check site,
+// offending index) with a count of all failures.  dd_check_report reads and
+// clears the records.  In the normal build in_bounds() is the constant true
+// and the checks compile to nothing.
+struct CheckRecord {
+    unsigned int count;  // failures since the last read
+    unsigned int site;   // check site of the first failure
+    long long index;     // its index (element offset into the buffer)
+};
+
+#ifdef DDGEMM_CHECKED
+static __device__ CheckRecord g_check_record;  // one per translation unit
+
+__device__ __forceinline__ bool in_bounds(int64_t index, int64_t extent, unsigned int site) {
+    if (index >= 0 && index < extent) return true;
+    if (atomicAdd(&g_check_record.count, 1u) == 0) {
+        g_check_record.site = site;
+        g_check_record.index = (long long)index;
+    }
+    return false;
+}
+
+// Host function reading and clearing this translation unit's record.
+#define DDG_DEFINE_CHECK_READER(name)                                                          \
+    cudaError_t name(CheckRecord* out) {                                                       \
+        cudaError_t err_ = cudaDeviceSynchronize();                                            \
+        if (err_ == cudaSuccess) err_ = cudaMemcpyFromSymbol(out, g_check_record, sizeof(*out)); \
+        const CheckRecord zero_ = {0u, 0u, 0};                                                 \
+        if (err_ == cudaSuccess) err_ = cudaMemcpyToSymbol(g_check_record, &zero_, sizeof(zero_)); \
+        return err_;                                                                           \
+    }
+#else
+__device__ __forceinline__ constexpr bool in_bounds(int64_t, int64_t, unsigned int) { return true; }
+
+#define DDG_DEFINE_CHECK_READER(name)         \
+    cudaError_t name(CheckRecord* out) {      \
+        *out = CheckRecord{0u, 0u, 0};        \
+        return cudaSuccess;                   \
+    }
+#endif
+
+// Check sites (the site number a failure records).
+enum CheckSite : unsigned int {
+    kSiteSplitLoadA = 101, kSiteSplitLoadB = 102, kSiteSplitStore = 103,
+    kSiteGemmCopyA = 201, kSiteGemmCopyB = 202, kSiteGemmStoreP = 203, kSiteGemmStoreC = 204,
+    kSiteRecombineLoadP = 301, kSiteRecombineStoreC = 302,
+    kSiteFusedLoadA = 401, kSiteFusedLoadB = 402, kSiteFusedExp = 403,
+    kSiteTcSplitLoadA = 501, kSiteTcSplitLoadB = 502, kSiteTcSplitStore = 503,
+    kSiteTcRecombineLoadP = 601, kSiteTcRecombineStoreC = 602,
+    kSiteTcGemmStoreP = 701,
+    kSiteExpLoadA = 801, kSiteExpLoadB = 802,
+};
+
+// Programmatic dependent launch: a kernel launched with launch_pdl may be
+// scheduled while the work before it on the stream drains.  pdl_wait()
+// returns once the grids it depends on have completed and their writes are
+// visible: every such kernel calls it before its first access to global
+// memory (a no-op for an ordinary launch).  pdl_launch_dependents() lets the
+// next grid on the stream be scheduled as this one's blocks retire.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace ddg

@@ -4,7 +4,28 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "common.cuh"
+
 namespace ddg {
+
+// Launch `kernel` on `st` with programmatic stream serialisation: the grid
+// may be scheduled before the previous kernel on the stream has finished; the
+// kernel must call pdl_wait() (common.cuh) before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Step 1: exponents and part planes.  An operand is A (its rows) or B (its
 // columns); `rows` counts rows of A or columns of B; element (r, k) is
@@ -138,6 +159,16 @@ cudaError_t launch_recombine_tc_md(int nin, const int32_t* P, int splits, int64_
                                    const int32_t* f, int64_t M, int64_t N, double* const* C, int64_t ldc,
                                    cudaStream_t st);
 cudaError_t read_and_reset_wait_timeouts_tc_md(unsigned int* count);
+
+// The bounds-check records of the translation units with checks (all zero
+// unless the library was built with -DDDGEMM_CHECKED); each synchronises the
+// device, reads its record and clears it.
+cudaError_t check_record_split(CheckRecord* out);
+cudaError_t check_record_slice_gemm(CheckRecord* out);
+cudaError_t check_record_fused(CheckRecord* out);
+cudaError_t check_record_recombine(CheckRecord* out);
+cudaError_t check_record_tc(CheckRecord* out);
+cudaError_t check_record_tc_md(CheckRecord* out);
 
 // Diagnostics of the bounded waits inside the slice GEMM.
 cudaError_t read_and_reset_wait_timeouts(unsigned int* count);

@@ -28,12 +28,17 @@ __global__ void __launch_bounds__(256) recombine_kernel(const double* __restrict
                                                         const int32_t* __restrict__ f, int64_t M,
                                                         int64_t N, double* __restrict__ C_hi,
                                                         double* __restrict__ C_lo, int64_t ldc) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= N) return;
     const int64_t plane = Mp * Np;
     const int fj = effective_exponent(f[j]);
     for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
         const double* p = P + i * Np + j;
+        if (!in_bounds((int64_t)(splits * S - 1) * plane + i * Np + j, (int64_t)splits * S * plane, kSiteRecombineLoadP) ||
+            !in_bounds(i * ldc + j, (M - 1) * ldc + N, kSiteRecombineStoreC))
+            continue;
         double part[S];
 #pragma unroll
         for (int d = 0; d < S; ++d) part[d] = __ldg(p + d * plane);
@@ -54,14 +59,16 @@ __global__ void __launch_bounds__(256) recombine_kernel(const double* __restrict
 
 }  // namespace
 
+DDG_DEFINE_CHECK_READER(check_record_recombine)
+
 cudaError_t launch_recombine(const double* P, int splits, int64_t Mp, int64_t Np,
                              const int32_t* e, const int32_t* f, int64_t M, int64_t N,
                              double* C_hi, double* C_lo, int64_t ldc, cudaStream_t st) {
     if (M == 0 || N == 0) return cudaSuccess;
     const unsigned gx = (unsigned)((N + 255) / 256);
     const unsigned gy = (unsigned)(M < 65535 ? M : 65535);
-    recombine_kernel<<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc);
-    return cudaGetLastError();
+    return launch_pdl(recombine_kernel, dim3(gx, gy), dim3(256), 0, st, P, splits, Mp, Np, e, f, M, N, C_hi, C_lo,
+                      ldc);
 }
 
 }  // namespace ddg

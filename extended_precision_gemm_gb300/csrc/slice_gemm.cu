@@ -48,18 +48,27 @@ static_assert(COPY_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 __device__ unsigned int g_wait_timeouts = 0;
 
 // Post the expected byte count on the stage barrier and start the two bulk
-// copies (A block, B block) that complete it.
-__device__ __forceinline__ void issue_stage(uint32_t bar, double* dst, const double* srcA,
-                                            const double* srcB) {
+// copies (A block, B block) that complete it.  offA / offB are the blocks'
+// offsets in their planes (checked against extA / extB in the checked build;
+// a block out of bounds is not copied and the barrier completes without it).
+__device__ __forceinline__ void issue_stage(uint32_t bar, double* dst, const double* planesA, int64_t offA,
+                                            int64_t extA, const double* planesB, int64_t offB, int64_t extB) {
+    if (!in_bounds(offA + CHUNK_DOUBLES - 1, extA, kSiteGemmCopyA) ||
+        !in_bounds(offB + CHUNK_DOUBLES - 1, extB, kSiteGemmCopyB)) {
+        mbar_arrive(bar);
+        return;
+    }
     mbar_expect_tx(bar, 2u * COPY_BYTES);
-    bulk_load(dst, srcA, COPY_BYTES, bar);
-    bulk_load(dst + CHUNK_DOUBLES, srcB, COPY_BYTES, bar);
+    bulk_load(dst, planesA + offA, COPY_BYTES, bar);
+    bulk_load(dst + CHUNK_DOUBLES, planesB + offB, COPY_BYTES, bar);
 }
 
 template <bool RECOMBINE>
 __global__ void __launch_bounds__(THREADS, 2)
     slice_gemm_kernel(const double* __restrict__ planesA, const double* __restrict__ planesB,
                       int64_t KC, int splits, TileOut out) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ __align__(128) double smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_DOUBLES);
 
@@ -69,8 +78,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int z = blockIdx.y;
     const int64_t kc0 = (int64_t)z * KC / splits, kc1 = (int64_t)(z + 1) * KC / splits;
     const int nk = (int)(kc1 - kc0);
-    const double* srcA = planesA + (mt * KC + kc0) * CHUNK_DOUBLES;
-    const double* srcB = planesB + (nt * KC + kc0) * CHUNK_DOUBLES;
+    const int64_t offA = (mt * KC + kc0) * CHUNK_DOUBLES, offB = (nt * KC + kc0) * CHUNK_DOUBLES;
+    const int64_t extA = (out.Mp / TM) * KC * CHUNK_DOUBLES, extB = (out.Np / TN) * KC * CHUNK_DOUBLES;
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) mbar_init(smem_addr(&bars[i]), 1);
@@ -79,8 +88,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     __syncthreads();
     if (tid == 0)
         for (int i = 0; i < STAGES && i < nk; ++i)
-            issue_stage(smem_addr(&bars[i]), smem + i * STAGE_DOUBLES, srcA + (int64_t)i * CHUNK_DOUBLES,
-                        srcB + (int64_t)i * CHUNK_DOUBLES);
+            issue_stage(smem_addr(&bars[i]), smem + i * STAGE_DOUBLES, planesA, offA + (int64_t)i * CHUNK_DOUBLES,
+                        extA, planesB, offB + (int64_t)i * CHUNK_DOUBLES, extB);
 
     const int mq = warp >> 1, nq = warp & 1;
     double acc[S][2][2][2];
@@ -110,8 +119,8 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
         if (tid == 0 && it >= 1 && it - 1 + STAGES < nk) {
             const int nxt = it - 1 + STAGES, ns = (it - 1) % STAGES;
-            issue_stage(smem_addr(&bars[ns]), smem + ns * STAGE_DOUBLES,
-                        srcA + (int64_t)nxt * CHUNK_DOUBLES, srcB + (int64_t)nxt * CHUNK_DOUBLES);
+            issue_stage(smem_addr(&bars[ns]), smem + ns * STAGE_DOUBLES, planesA,
+                        offA + (int64_t)nxt * CHUNK_DOUBLES, extA, planesB, offB + (int64_t)nxt * CHUNK_DOUBLES, extB);
         }
         const double* As = smem + st * STAGE_DOUBLES;
         chunk_products(As, As + CHUNK_DOUBLES, lane, mq, nq, acc);
@@ -191,9 +200,10 @@ cudaError_t launch_slice_gemm(const double* planesA, const double* planesB, int6
     out.P = P;
     out.Mp = Mp;
     out.Np = Np;
+    out.p_extent = (int64_t)splits * S * Mp * Np;
     dim3 grid((unsigned)((Mp / TM) * (Np / TN)), (unsigned)splits);
-    slice_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(planesA, planesB, Kp / BK, splits, out);
-    return cudaGetLastError();
+    return launch_pdl(slice_gemm_kernel<false>, grid, dim3(THREADS), SMEM_BYTES, st, planesA, planesB, Kp / BK, splits,
+                      out);
 }
 
 cudaError_t launch_slice_gemm_recombine(const double* planesA, const double* planesB, int64_t Mp, int64_t Np,
@@ -205,8 +215,7 @@ cudaError_t launch_slice_gemm_recombine(const double* planesA, const double* pla
     if (err != cudaSuccess) return err;
     const TileOut out = recombine_out(Mp, Np, e, f, M, N, C_hi, C_lo, ldc);
     dim3 grid((unsigned)((Mp / TM) * (Np / TN)), 1u);
-    slice_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(planesA, planesB, Kp / BK, 1, out);
-    return cudaGetLastError();
+    return launch_pdl(slice_gemm_kernel<true>, grid, dim3(THREADS), SMEM_BYTES, st, planesA, planesB, Kp / BK, 1, out);
 }
 
 cudaError_t peek_wait_timeouts(unsigned int* count, cudaStream_t st) {
@@ -215,6 +224,8 @@ cudaError_t peek_wait_timeouts(unsigned int* count, cudaStream_t st) {
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
     return err;
 }
+
+DDG_DEFINE_CHECK_READER(check_record_slice_gemm)
 
 cudaError_t read_and_reset_wait_timeouts(unsigned int* count) {
     cudaError_t err = cudaDeviceSynchronize();

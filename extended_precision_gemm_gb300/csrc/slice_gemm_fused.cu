@@ -54,7 +54,7 @@ __device__ __forceinline__ void load_chunk(const FusedSrc& g, int64_t row, int64
                                            Pending& p) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) p.ah[r] = p.al[r] = p.bh[r] = p.bl[r] = 0.0;
-    if (row < g.M) {
+    if (row < g.M && in_bounds(row * g.lda + min(k0 + ak + 1, g.K - 1), (g.M - 1) * g.lda + g.K, kSiteFusedLoadA)) {
         const int64_t k = k0 + ak;
         const double* ph = g.A_hi + row * g.lda + k;
         const double* pl = g.A_lo + row * g.lda + k;
@@ -68,7 +68,7 @@ __device__ __forceinline__ void load_chunk(const FusedSrc& g, int64_t row, int64
                 if (k + r < g.K) { p.ah[r] = __ldg(ph + r); p.al[r] = __ldg(pl + r); }
         }
     }
-    if (col < g.N) {
+    if (col < g.N && in_bounds(min(k0 + bk + 1, g.K - 1) * g.ldb + col, (g.K - 1) * g.ldb + g.N, kSiteFusedLoadB)) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int64_t k = k0 + bk + r;
@@ -108,6 +108,8 @@ __device__ __forceinline__ void store_parts(double* stage, const Pending& p, int
 template <bool RECOMBINE>
 __global__ void __launch_bounds__(THREADS, 2) slice_gemm_fused_kernel(FusedSrc g, int64_t KC, int splits,
                                                                       TileOut out) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ __align__(128) double smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int64_t mt, nt;
@@ -117,13 +119,14 @@ __global__ void __launch_bounds__(THREADS, 2) slice_gemm_fused_kernel(FusedSrc g
     const int nk = (int)(kc1 - kc0);
 
     // element assignment: A row ar, k ak..ak+1 (4 threads per row, 64
-    // contiguous bytes of hi and of lo); B column bc (a warp reads 256
-    // contiguous bytes per k), k bk..bk+1
+    // contiguous bytes of hi and of lo); B column bc, k bk..bk+1, a warp
+    // covering 16 columns at two k (128 contiguous bytes of a row of B per
+    // load) so that its part stores fill 512 contiguous bytes of the stage
     const int ar = tid >> 2, ak = (tid & 3) * 2;
-    const int bc = lane, bk = warp * 2;
+    const int bc = 16 * (warp & 1) + (lane & 15), bk = 4 * (warp >> 1) + 2 * (lane >> 4);
     const int64_t row = mt * TM + ar, col = nt * TN + bc;
-    const int ea = row < g.M ? effective_exponent(g.e[row]) : 0;
-    const int fb = col < g.N ? effective_exponent(g.f[col]) : 0;
+    const int ea = row < g.M && in_bounds(row, g.M, kSiteFusedExp) ? effective_exponent(g.e[row]) : 0;
+    const int fb = col < g.N && in_bounds(col, g.N, kSiteFusedExp) ? effective_exponent(g.f[col]) : 0;
 
     const int mq = warp >> 1, nq = warp & 1;
     double acc[S][2][2][2];
@@ -163,8 +166,7 @@ cudaError_t launch_fused(const FusedSrc& g, int64_t Mp, int64_t Np, int64_t Kp, 
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
     dim3 grid((unsigned)((Mp / TM) * (Np / TN)), (unsigned)splits);
-    slice_gemm_fused_kernel<RECOMBINE><<<grid, THREADS, SMEM_BYTES, st>>>(g, Kp / BK, splits, out);
-    return cudaGetLastError();
+    return launch_pdl(slice_gemm_fused_kernel<RECOMBINE>, grid, dim3(THREADS), SMEM_BYTES, st, g, Kp / BK, splits, out);
 }
 
 }  // namespace
@@ -186,6 +188,7 @@ cudaError_t launch_slice_gemm_fused(const FusedSrc& g, int64_t Mp, int64_t Np, i
     out.P = P;
     out.Mp = Mp;
     out.Np = Np;
+    out.p_extent = (int64_t)splits * S * Mp * Np;
     return launch_fused<false>(g, Mp, Np, Kp, splits, out, st);
 }
 
@@ -194,6 +197,8 @@ cudaError_t launch_slice_gemm_fused_recombine(const FusedSrc& g, int64_t Mp, int
     const TileOut out = recombine_out(Mp, Np, g.e, g.f, g.M, g.N, C_hi, C_lo, ldc);
     return launch_fused<true>(g, Mp, Np, Kp, 1, out, st);
 }
+
+DDG_DEFINE_CHECK_READER(check_record_fused)
 
 int slice_gemm_fused_ctas_per_sm() {
     static std::atomic<int> cached{0};  // per-SM count of this kernel (the same on every device)

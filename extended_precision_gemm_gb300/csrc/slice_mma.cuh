@@ -75,6 +75,7 @@ __device__ __forceinline__ void tile_of(int64_t t, int64_t MT, int64_t NT, int64
 struct TileOut {
     double* P;
     int64_t Mp, Np;
+    int64_t p_extent;  // doubles in P (splits x 8 x Mp x Np)
     const int32_t* e;
     const int32_t* f;
     double* C_hi;
@@ -104,7 +105,7 @@ inline TileOut recombine_out(int64_t Mp, int64_t Np, const int32_t* e, const int
 template <bool RECOMBINE>
 __device__ __forceinline__ void store_tile(const double (&acc)[S][2][2][2], const TileOut& o, int lane, int mq,
                                            int nq, int64_t mt, int64_t nt, int z) {
-    if (!RECOMBINE) {
+    if constexpr (!RECOMBINE) {
         const int64_t plane = o.Mp * o.Np;
 #pragma unroll
         for (int d = 0; d < S; ++d) {
@@ -115,39 +116,42 @@ __device__ __forceinline__ void store_tile(const double (&acc)[S][2][2][2], cons
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int64_t col = nt * TN + (2 * nq + j) * 8 + 2 * (lane & 3);
-                    *reinterpret_cast<double2*>(out + row * o.Np + col) =
-                        make_double2(acc[d][i][j][0], acc[d][i][j][1]);
+                    if (in_bounds(((int64_t)z * S + d) * plane + row * o.Np + col + 1, o.p_extent, kSiteGemmStoreP))
+                        *reinterpret_cast<double2*>(out + row * o.Np + col) =
+                            make_double2(acc[d][i][j][0], acc[d][i][j][1]);
                 }
             }
         }
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int64_t row = mt * TM + (2 * mq + i) * 8 + (lane >> 2);
-        if (row >= o.M) continue;
-        const int ei = effective_exponent(o.e[row]);
+        for (int i = 0; i < 2; ++i) {
+            const int64_t row = mt * TM + (2 * mq + i) * 8 + (lane >> 2);
+            if (row >= o.M) continue;
+            const int ei = effective_exponent(o.e[row]);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int64_t col = nt * TN + (2 * nq + j) * 8 + 2 * (lane & 3);
-            double hi[2], lo[2];
+            for (int j = 0; j < 2; ++j) {
+                const int64_t col = nt * TN + (2 * nq + j) * 8 + 2 * (lane & 3);
+                double hi[2], lo[2];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                double part[S];
+                for (int c = 0; c < 2; ++c) {
+                    double part[S];
 #pragma unroll
-                for (int d = 0; d < S; ++d) part[d] = acc[d][i][j][c];
-                const int fc = col + c < o.N ? effective_exponent(o.f[col + c]) : 0;
-                recombine_parts(part, ei + fc, hi[c], lo[c]);
-            }
-            double* ph = o.C_hi + row * o.ldc + col;
-            double* pl = o.C_lo + row * o.ldc + col;
-            if (o.c_vec && col + 1 < o.N) {
-                *reinterpret_cast<double2*>(ph) = make_double2(hi[0], hi[1]);
-                *reinterpret_cast<double2*>(pl) = make_double2(lo[0], lo[1]);
-            } else {
+                    for (int d = 0; d < S; ++d) part[d] = acc[d][i][j][c];
+                    const int fc = col + c < o.N ? effective_exponent(o.f[col + c]) : 0;
+                    recombine_parts(part, ei + fc, hi[c], lo[c]);
+                }
+                if (!in_bounds(row * o.ldc + min(col + 1, o.N - 1), (o.M - 1) * o.ldc + o.N, kSiteGemmStoreC))
+                    continue;
+                double* ph = o.C_hi + row * o.ldc + col;
+                double* pl = o.C_lo + row * o.ldc + col;
+                if (o.c_vec && col + 1 < o.N) {
+                    *reinterpret_cast<double2*>(ph) = make_double2(hi[0], hi[1]);
+                    *reinterpret_cast<double2*>(pl) = make_double2(lo[0], lo[1]);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    if (col + c < o.N) { ph[c] = hi[c]; pl[c] = lo[c]; }
+                    for (int c = 0; c < 2; ++c)
+                        if (col + c < o.N) { ph[c] = hi[c]; pl[c] = lo[c]; }
+                }
             }
         }
     }

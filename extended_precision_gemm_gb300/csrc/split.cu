@@ -33,6 +33,8 @@ __device__ __forceinline__ uint64_t abs_bits(double x) {
 // ---------------------------------------------------------------------------
 
 __global__ void init_exponents_kernel(int32_t* e, int64_t M, int32_t* f, int64_t N, int32_t value) {
+    pdl_wait();
+    pdl_launch_dependents();
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e != nullptr && i < M) e[i] = value;
     if (f != nullptr && i < N) f[i] = value;
@@ -50,74 +52,89 @@ struct ExpGrid {
     int32_t* e; int32_t* f;
 };
 
+// A-item bid: the row maxima of 8 rows (one per warp) over one k-chunk.
+template <int VEC>
+__device__ __forceinline__ void exponents_a_item(const ExpGrid& g, int64_t bid) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (bid / g.a_ksplit) * 8 + (threadIdx.x >> 5);
+    if (row >= g.M) return;
+    const int64_t k0 = (bid % g.a_ksplit) * g.a_kchunk;
+    const int64_t k1 = min(g.K, k0 + g.a_kchunk);
+    // rows are read in [row * lda, row * lda + K): within the span of A
+    if (!in_bounds(row * g.lda + k1 - 1, (g.M - 1) * g.lda + g.K, kSiteExpLoadA)) return;
+    const double* p = g.A_hi + row * g.lda;
+    uint64_t m = 0;
+    if (VEC == 2) {
+        // four independent 128-bit loads in flight per lane
+        uint64_t m1 = 0, m2 = 0, m3 = 0;
+        int64_t k = k0 + 2 * lane;
+        for (; k + 193 < k1; k += 256) {
+            const double2 v0 = __ldg(reinterpret_cast<const double2*>(p + k));
+            const double2 v1 = __ldg(reinterpret_cast<const double2*>(p + k + 64));
+            const double2 v2 = __ldg(reinterpret_cast<const double2*>(p + k + 128));
+            const double2 v3 = __ldg(reinterpret_cast<const double2*>(p + k + 192));
+            m = max(m, max(abs_bits(v0.x), abs_bits(v0.y)));
+            m1 = max(m1, max(abs_bits(v1.x), abs_bits(v1.y)));
+            m2 = max(m2, max(abs_bits(v2.x), abs_bits(v2.y)));
+            m3 = max(m3, max(abs_bits(v3.x), abs_bits(v3.y)));
+        }
+        for (; k < k1; k += 64) {
+            if (k + 1 < k1) {
+                double2 v = __ldg(reinterpret_cast<const double2*>(p + k));
+                m = max(m, max(abs_bits(v.x), abs_bits(v.y)));
+            } else {
+                m = max(m, abs_bits(__ldg(p + k)));
+            }
+        }
+        m = max(max(m, m1), max(m2, m3));
+    } else {
+        for (int64_t k = k0 + lane; k < k1; k += 32) m = max(m, abs_bits(__ldg(p + k)));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        m = max(m, (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)m, off));
+    if (lane == 0 && m != 0) atomicMax(&g.e[row], exponent_from_abs_bits(m));
+}
+
+// B-item b: the column maxima of 256 columns (one per thread) over one k-chunk.
+__device__ __forceinline__ void exponents_b_item(const ExpGrid& g, int64_t b) {
+    const int64_t col = (b / g.b_ksplit) * 256 + threadIdx.x;
+    if (col >= g.N) return;
+    const int64_t k0 = (b % g.b_ksplit) * g.b_kchunk;
+    const int64_t k1 = min(g.K, k0 + g.b_kchunk);
+    if (!in_bounds((k1 - 1) * g.ldb + col, (g.K - 1) * g.ldb + g.N, kSiteExpLoadB)) return;
+    const double* p = g.B_hi + col;
+    const int64_t ldb = g.ldb;
+    uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+    int64_t k = k0;
+    for (; k + 7 < k1; k += 8) {  // eight loads in flight per thread
+        const double x0 = __ldg(p + (k + 0) * ldb), x1 = __ldg(p + (k + 1) * ldb);
+        const double x2 = __ldg(p + (k + 2) * ldb), x3 = __ldg(p + (k + 3) * ldb);
+        const double x4 = __ldg(p + (k + 4) * ldb), x5 = __ldg(p + (k + 5) * ldb);
+        const double x6 = __ldg(p + (k + 6) * ldb), x7 = __ldg(p + (k + 7) * ldb);
+        m0 = max(m0, max(abs_bits(x0), abs_bits(x4)));
+        m1 = max(m1, max(abs_bits(x1), abs_bits(x5)));
+        m2 = max(m2, max(abs_bits(x2), abs_bits(x6)));
+        m3 = max(m3, max(abs_bits(x3), abs_bits(x7)));
+    }
+    for (; k < k1; ++k) m0 = max(m0, abs_bits(__ldg(p + k * ldb)));
+    const uint64_t m = max(max(m0, m1), max(m2, m3));
+    if (m != 0) atomicMax(&g.f[col], exponent_from_abs_bits(m));
+}
+
+// Blocks alternate between the operands (even block: A-item, odd block:
+// B-item), so that neither operand forms a tail.
 template <int VEC>
 __global__ void __launch_bounds__(256) exponents_kernel(ExpGrid g) {
+    pdl_wait();
+    pdl_launch_dependents();
     const bool both = g.a_items > 0 && g.b_items > 0;
     const bool is_a = both ? (blockIdx.x & 1) == 0 : g.a_items > 0;
     const int64_t bid = both ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
     if (is_a) {
-        if (bid >= g.a_items) return;
-        const int lane = threadIdx.x & 31;
-        const int64_t row = (bid / g.a_ksplit) * 8 + (threadIdx.x >> 5);
-        if (row >= g.M) return;
-        const int64_t k0 = (bid % g.a_ksplit) * g.a_kchunk;
-        const int64_t k1 = min(g.K, k0 + g.a_kchunk);
-        const double* p = g.A_hi + row * g.lda;
-        uint64_t m = 0;
-        if (VEC == 2) {
-            // four independent 128-bit loads in flight per lane
-            uint64_t m1 = 0, m2 = 0, m3 = 0;
-            int64_t k = k0 + 2 * lane;
-            for (; k + 193 < k1; k += 256) {
-                const double2 v0 = __ldg(reinterpret_cast<const double2*>(p + k));
-                const double2 v1 = __ldg(reinterpret_cast<const double2*>(p + k + 64));
-                const double2 v2 = __ldg(reinterpret_cast<const double2*>(p + k + 128));
-                const double2 v3 = __ldg(reinterpret_cast<const double2*>(p + k + 192));
-                m = max(m, max(abs_bits(v0.x), abs_bits(v0.y)));
-                m1 = max(m1, max(abs_bits(v1.x), abs_bits(v1.y)));
-                m2 = max(m2, max(abs_bits(v2.x), abs_bits(v2.y)));
-                m3 = max(m3, max(abs_bits(v3.x), abs_bits(v3.y)));
-            }
-            for (; k < k1; k += 64) {
-                if (k + 1 < k1) {
-                    double2 v = __ldg(reinterpret_cast<const double2*>(p + k));
-                    m = max(m, max(abs_bits(v.x), abs_bits(v.y)));
-                } else {
-                    m = max(m, abs_bits(__ldg(p + k)));
-                }
-            }
-            m = max(max(m, m1), max(m2, m3));
-        } else {
-            for (int64_t k = k0 + lane; k < k1; k += 32) m = max(m, abs_bits(__ldg(p + k)));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            m = max(m, (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)m, off));
-        if (lane == 0 && m != 0) atomicMax(&g.e[row], exponent_from_abs_bits(m));
-    } else {
-        if (bid >= g.b_items) return;
-        const int64_t b = bid;
-        const int64_t col = (b / g.b_ksplit) * 256 + threadIdx.x;
-        if (col >= g.N) return;
-        const int64_t k0 = (b % g.b_ksplit) * g.b_kchunk;
-        const int64_t k1 = min(g.K, k0 + g.b_kchunk);
-        const double* p = g.B_hi + col;
-        const int64_t ldb = g.ldb;
-        uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
-        int64_t k = k0;
-        for (; k + 7 < k1; k += 8) {  // eight loads in flight per thread
-            const double x0 = __ldg(p + (k + 0) * ldb), x1 = __ldg(p + (k + 1) * ldb);
-            const double x2 = __ldg(p + (k + 2) * ldb), x3 = __ldg(p + (k + 3) * ldb);
-            const double x4 = __ldg(p + (k + 4) * ldb), x5 = __ldg(p + (k + 5) * ldb);
-            const double x6 = __ldg(p + (k + 6) * ldb), x7 = __ldg(p + (k + 7) * ldb);
-            m0 = max(m0, max(abs_bits(x0), abs_bits(x4)));
-            m1 = max(m1, max(abs_bits(x1), abs_bits(x5)));
-            m2 = max(m2, max(abs_bits(x2), abs_bits(x6)));
-            m3 = max(m3, max(abs_bits(x3), abs_bits(x7)));
-        }
-        for (; k < k1; ++k) m0 = max(m0, abs_bits(__ldg(p + k * ldb)));
-        const uint64_t m = max(max(m0, m1), max(m2, m3));
-        if (m != 0) atomicMax(&g.f[col], exponent_from_abs_bits(m));
+        if (bid < g.a_items) exponents_a_item<VEC>(g, bid);
+    } else if (bid < g.b_items) {
+        exponents_b_item(g, bid);
     }
 }
 
@@ -180,6 +197,8 @@ __device__ __forceinline__ int load_item(const SplitGrid& g, bool is_a, int64_t 
         if (!g.a_given && kt == 0 && w == 0 && er == EXP_NONE) g.e[rr] = 0;
         const double* ph = g.A_hi + rr * g.lda + k0;
         const double* pl = g.A_lo + rr * g.lda + k0;
+        if (!in_bounds(rr * g.lda + min(k0 + 3, g.K - 1), (g.M - 1) * g.lda + g.K, kSiteSplitLoadA))
+            return effective_exponent(er);
         if (VEC == 2 && k0 + 3 < g.K) {
             double2 h0 = __ldg(reinterpret_cast<const double2*>(ph));
             double2 h1 = __ldg(reinterpret_cast<const double2*>(ph + 2));
@@ -197,6 +216,8 @@ __device__ __forceinline__ int load_item(const SplitGrid& g, bool is_a, int64_t 
     if (rr >= g.N) return 0;
     const int32_t fr = g.f[rr];
     if (!g.b_given && kt == 0 && w == 0 && fr == EXP_NONE) g.f[rr] = 0;
+    if (!in_bounds(min(k0 + 3, g.K - 1) * g.ldb + rr, (g.K - 1) * g.ldb + g.N, kSiteSplitLoadB))
+        return effective_exponent(fr);
 #pragma unroll
     for (int r = 0; r < 4; ++r)
         if (k0 + r < g.K) {
@@ -231,6 +252,8 @@ __device__ __forceinline__ Item item_of(const SplitGrid& g, int64_t item, int64_
 // its own previous stores have read it -- no block-wide barrier.
 template <int VEC>
 __global__ void __launch_bounds__(SPLIT_THREADS, 3) split_f64_kernel(SplitGrid g) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ __align__(128) double stage[];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t items = (g.a_tiles + g.b_tiles) * g.KT;
@@ -277,13 +300,17 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 3) split_f64_kernel(SplitGrid g
         __syncwarp();
         if (lane == 0) {
             // part s of this warp's (k-chunk, k4 group) is 1 KB contiguous in the plane block
-            double* base = static_cast<double*>(it.is_a ? g.planesA : g.planesB) +
-                           (it.tile * KC + it.kt * SPLIT_CHUNKS + (w >> 1)) * CHUNK_DOUBLES + (w & 1) * TM * 4;
+            const int64_t off = (it.tile * KC + it.kt * SPLIT_CHUNKS + (w >> 1)) * CHUNK_DOUBLES + (w & 1) * TM * 4;
+            double* base = static_cast<double*>(it.is_a ? g.planesA : g.planesB) + off;
+            const int64_t extent = (it.is_a ? g.a_tiles : g.b_tiles) * KC * CHUNK_DOUBLES;
+            if (in_bounds(off + (S - 1) * PART_STRIDE + TM * 4 - 1, extent, kSiteSplitStore)) {
 #pragma unroll
-            for (int s = 0; s < S; ++s)
-                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(base + s * PART_STRIDE),
-                             "r"(smem_u32(ws + s * TM * 4)), "r"((uint32_t)(TM * 4 * sizeof(double)))
-                             : "memory");
+                for (int s = 0; s < S; ++s)
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                                     base + s * PART_STRIDE),
+                                 "r"(smem_u32(ws + s * TM * 4)), "r"((uint32_t)(TM * 4 * sizeof(double)))
+                                 : "memory");
+            }
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
         pending = true;
@@ -342,12 +369,13 @@ int num_sms() {
 
 }  // namespace
 
+DDG_DEFINE_CHECK_READER(check_record_split)
+
 cudaError_t launch_reset_exponents(int32_t* e, int64_t M, int32_t* f, int64_t N, int32_t value,
                                    cudaStream_t st) {
     int64_t n = std::max(e ? M : 0, f ? N : 0);
     if (n == 0) return cudaSuccess;
-    init_exponents_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(e, M, f, N, value);
-    return cudaGetLastError();
+    return launch_pdl(init_exponents_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, e, M, f, N, value);
 }
 
 cudaError_t launch_shared_exponents(const SplitOperand* A, const SplitOperand* B, int64_t K, int32_t zero_k_value,
@@ -387,9 +415,8 @@ cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64
     const int64_t blocks = (g.a_items > 0 && g.b_items > 0) ? 2 * std::max(g.a_items, g.b_items)
                                                             : g.a_items + g.b_items;
     const bool vec = !A || (((uintptr_t)A->hi % 16 == 0) && (A->ld % 2 == 0));
-    if (vec) exponents_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(g);
-    else exponents_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(g);
-    return cudaGetLastError();
+    return vec ? launch_pdl(exponents_kernel<2>, dim3((unsigned)blocks), dim3(256), 0, st, g)
+               : launch_pdl(exponents_kernel<1>, dim3((unsigned)blocks), dim3(256), 0, st, g);
 }
 
 static SplitGrid make_split_grid(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
@@ -431,11 +458,11 @@ cudaError_t launch_split_f64(const SplitOperand* A, const SplitOperand* B, int64
     if (a_vec(A)) {
         err = cudaFuncSetAttribute(split_f64_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
         if (err != cudaSuccess) return err;
-        split_f64_kernel<2><<<split_blocks(items, 3), SPLIT_THREADS, SPLIT_SMEM, st>>>(g);
+        err = launch_pdl(split_f64_kernel<2>, dim3(split_blocks(items, 3)), dim3(SPLIT_THREADS), SPLIT_SMEM, st, g);
     } else {
         err = cudaFuncSetAttribute(split_f64_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
         if (err != cudaSuccess) return err;
-        split_f64_kernel<1><<<split_blocks(items, 3), SPLIT_THREADS, SPLIT_SMEM, st>>>(g);
+        err = launch_pdl(split_f64_kernel<1>, dim3(split_blocks(items, 3)), dim3(SPLIT_THREADS), SPLIT_SMEM, st, g);
     }
     return cudaGetLastError();
 }

@@ -90,6 +90,8 @@ struct TcSplitGrid {
 // 128-byte part rows: 512 contiguous bytes per part.  Rows / k beyond the
 // matrix are written as 0.
 __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * 8;
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) hi[j] = lo[j] = 0.0;
             int ep = 1;
-            if (r < g.M) {
+            if (r < g.M && in_bounds(r * g.lda + min(k0 + 7, g.K - 1), (g.M - 1) * g.lda + g.K, kSiteTcSplitLoadA)) {
                 const int32_t er = g.e[r];
                 if (!g.a_given && kb == 0 && kc == 0 && er == EXP_NONE) g.e[r] = 0;
                 ep = effective_exponent(er) + 1;
@@ -134,10 +136,14 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
             }
             const int64_t mt = r / TBM;
             const int rin = (int)(r % TBM);
+            const int64_t a_extent = (int64_t)TS * round_up(g.M, PAIR_M) * g.KB * TBK;  // bf16 elements of planesA
+            if (in_bounds(((mt * TS + TS - 1) * g.KB + kb) * (TBM * TBK) + (swizzled(rin, kc) + 15) / 2, a_extent,
+                          kSiteTcSplitStore)) {
 #pragma unroll
-            for (int s = 0; s < TS; ++s) {
-                uint8_t* blk = reinterpret_cast<uint8_t*>(g.planesA + ((mt * TS + s) * g.KB + kb) * (TBM * TBK));
-                *reinterpret_cast<uint4*>(blk + swizzled(rin, kc)) = make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
+                for (int s = 0; s < TS; ++s) {
+                    uint8_t* blk = reinterpret_cast<uint8_t*>(g.planesA + ((mt * TS + s) * g.KB + kb) * (TBM * TBK));
+                    *reinterpret_cast<uint4*>(blk + swizzled(rin, kc)) = make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
+                }
             }
         } else {
             // B task: 4 columns x one k-block (lane = column (lane/8), 8
@@ -155,9 +161,11 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
             }
             const int64_t k0 = kb * TBK + kc * 8;
             double hi[8], lo[8];
+            const bool n_ok = n < g.N && in_bounds(min(k0 + 7, g.K - 1) * g.ldb + n, (g.K - 1) * g.ldb + g.N,
+                                                   kSiteTcSplitLoadB);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const bool in = n < g.N && k0 + j < g.K;
+                const bool in = n_ok && k0 + j < g.K;
                 hi[j] = in ? __ldg(g.B_hi + (k0 + j) * g.ldb + n) : 0.0;
                 lo[j] = in ? __ldg(g.B_lo + (k0 + j) * g.ldb + n) : 0.0;
             }
@@ -172,10 +180,14 @@ __global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
             }
             const int64_t nt = n / TBN;
             const int nin = (int)(n % TBN);
+            const int64_t b_extent = (int64_t)TS * round_up(g.N, TBN) * g.KB * TBK;  // bf16 elements of planesB
+            if (in_bounds(((nt * TS + TS - 1) * g.KB + kb) * (TBN * TBK) + (swizzled(nin, kc) + 15) / 2, b_extent,
+                          kSiteTcSplitStore)) {
 #pragma unroll
-            for (int s = 0; s < TS; ++s) {
-                uint8_t* blk = reinterpret_cast<uint8_t*>(g.planesB + ((nt * TS + s) * g.KB + kb) * (TBN * TBK));
-                *reinterpret_cast<uint4*>(blk + swizzled(nin, kc)) = make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
+                for (int s = 0; s < TS; ++s) {
+                    uint8_t* blk = reinterpret_cast<uint8_t*>(g.planesB + ((nt * TS + s) * g.KB + kb) * (TBN * TBK));
+                    *reinterpret_cast<uint4*>(blk + swizzled(nin, kc)) = make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
+                }
             }
         }
     }
@@ -268,6 +280,8 @@ __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ f, int64_t M, int64_t N,
                                                            double* __restrict__ C_hi, double* __restrict__ C_lo,
                                                            int64_t ldc, bool vec_store) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * V;
     if (j0 >= N) return;
     const int64_t plane = Mp * Np;
@@ -276,6 +290,10 @@ __global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __rest
     for (int c = 0; c < V; ++c) fj[c] = j0 + c < N ? effective_exponent(f[j0 + c]) + 1 : 0;
     for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
         const int32_t* p = P + i * Np + j0;
+        if (!in_bounds((int64_t)(splits * TS - 1) * plane + i * Np + j0 + V - 1, (int64_t)splits * TS * plane,
+                       kSiteTcRecombineLoadP) ||
+            !in_bounds(i * ldc + min(j0 + V - 1, N - 1), (M - 1) * ldc + N, kSiteTcRecombineStoreC))
+            continue;
         const int qi = effective_exponent(e[i]) + 1 - TD * (TS + 1);
         double h[V], l[V];
         if (splits == 1) {
@@ -490,8 +508,7 @@ cudaError_t launch_split_bf16(const SplitOperand* A, const SplitOperand* B, int6
     const int64_t tasks = g.a_tasks + g.b_tasks;
     if (tasks == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms_tc() * 8));
-    split_bf16_kernel<<<blocks, 256, 0, st>>>(g);
-    return cudaGetLastError();
+    return launch_pdl(split_bf16_kernel, dim3(blocks), dim3(256), 0, st, g);
 }
 
 cudaError_t launch_slice_gemm_tc(const uint16_t* planesA, const uint16_t* planesB, int64_t Mp, int64_t Np,
@@ -515,13 +532,11 @@ cudaError_t launch_recombine_tc(const int32_t* P, int splits, int64_t Mp, int64_
     // planes are multiples of 256 columns, so every 4-column group is aligned)
     if (splits == 1 && (uintptr_t)P % 16 == 0) {
         const unsigned gx4 = (unsigned)((N + 1023) / 1024);
-        recombine_tc_kernel<4><<<dim3(gx4, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc,
-                                                                vec_store);
-    } else {
-        recombine_tc_kernel<1><<<dim3(gx, gy), 256, 0, st>>>(P, splits, Mp, Np, e, f, M, N, C_hi, C_lo, ldc,
-                                                               false);
+        return launch_pdl(recombine_tc_kernel<4>, dim3(gx4, gy), dim3(256), 0, st, P, splits, Mp, Np, e, f, M, N,
+                          C_hi, C_lo, ldc, vec_store);
     }
-    return cudaGetLastError();
+    return launch_pdl(recombine_tc_kernel<1>, dim3(gx, gy), dim3(256), 0, st, P, splits, Mp, Np, e, f, M, N, C_hi,
+                      C_lo, ldc, false);
 }
 
 cudaError_t launch_split_bf16_qd(const double* const* A, int64_t lda, int64_t M, int32_t* e, const double* const* B,
@@ -561,6 +576,8 @@ cudaError_t launch_recombine_tc_qd(const int32_t* P, int splits, int64_t Mp, int
 }
 
 cudaError_t read_and_reset_wait_timeouts_tc(unsigned int* count) { return reset_tc_timeouts(count); }
+
+DDG_DEFINE_CHECK_READER(check_record_tc)
 
 cudaError_t peek_wait_timeouts_tc(unsigned int* count, cudaStream_t st) { return peek_tc_timeouts(count, st); }
 

@@ -363,11 +363,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     else mbar_arrive_remote(acce0 + 8 * buf, 0);
                 }
             }
-            int32_t* dst = g.P + (((w.z * NP + d) * g.Mp + w.mt * PAIR_M + rank * TBM + row) * g.Np + w.nt * TBN +
-                                  half * 128);
+            const int64_t off = ((w.z * NP + d) * g.Mp + w.mt * PAIR_M + rank * TBM + row) * g.Np + w.nt * TBN +
+                                half * 128;
+            int32_t* dst = g.P + off;
+            if (in_bounds(off + 127, (int64_t)g.splits * NP * g.Mp * g.Np, kSiteTcGemmStoreP)) {
 #pragma unroll
-            for (int i = 0; i < 128; i += 4)
-                *reinterpret_cast<int4*>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                for (int i = 0; i < 128; i += 4)
+                    *reinterpret_cast<int4*>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+            }
         }
     }
 

@@ -421,4 +421,6 @@ cudaError_t launch_recombine_tc_md(int nin, const int32_t* P, int splits, int64_
 
 cudaError_t read_and_reset_wait_timeouts_tc_md(unsigned int* count) { return reset_tc_timeouts(count); }
 
+DDG_DEFINE_CHECK_READER(check_record_tc_md)
+
 }  // namespace ddg

@@ -651,6 +651,24 @@ ddgemm_status md_recombine_tc(int nparts, int64_t M, int64_t N, const int32_t* P
 ddgemm_status dd_fp64_tensor_roof(double* tflops, void* stream);
 
 /*
+ * The bounds-checked build.  libddgemm_checked.so (the same sources compiled
+ * with -DDDGEMM_CHECKED) tests the global accesses of the split, slice-GEMM
+ * and recombination kernels of the double-double paths (FP64 planes, fused,
+ * bf16 tensor cores) against the extents of their buffers before making
+ * them: an access out of bounds is skipped (its result is wrong, nothing
+ * faults) and counted, and the first one is recorded.  It stands in for a
+ * memory checker where none can run.  dd_checked_build returns 1 in that
+ * library and 0 in libddgemm.so.  dd_check_report synchronises the device
+ * and returns, since its previous call, the number of accesses refused
+ * (*count), the check site of the first one (*site: 1xx split, 2xx slice
+ * GEMM, 3xx recombination, 4xx fused GEMM, 5xx-7xx bf16 split, recombination
+ * and GEMM, 8xx exponents) and its element offset (*index); all zero in the
+ * normal build.
+ */
+int dd_checked_build(void);
+ddgemm_status dd_check_report(unsigned int* count, unsigned int* site, int64_t* index);
+
+/*
  * Number of times a slice-GEMM thread block (any variant) gave up waiting
  * for its operand copies on the current device (each wait is bounded in time; a block that
  * gives up stops early and its P tile is incomplete).  Synchronises the

@@ -203,3 +203,17 @@ def test_options_and_sharding_entry_points_validate_host_side(lib):
     assert lib.dd_slice_gemm_fused(4, 4, 64, None, A, 64, A, A, 4, P, P, 1, P, None) == 1    # no A_hi
     # host-buffer variant of the bf16 path: dd_gemm's checks
     assert lib.dd_gemm_tc_host(-1, 4, 4, A, A, 4, A, A, 4, P, P, 4, None) == 1
+
+
+def test_checked_library_exports_the_same_entry_points():
+    """The bounds-checked variant is the same C ABI; only dd_checked_build
+    tells the two apart (no GPU needed to load either)."""
+    from extended_precision_gemm_gb300 import build as lib_build
+    path = lib_build.build(checked=True)
+    checked = ctypes.CDLL(str(path))
+    for name in ddg.exported_symbols():
+        assert hasattr(checked, name), name
+    checked.dd_checked_build.restype = ctypes.c_int
+    assert checked.dd_checked_build() == 1
+    ddg.load().dd_checked_build.restype = ctypes.c_int
+    assert ddg.load().dd_checked_build() == 0
