@@ -50,6 +50,7 @@ struct ExpGrid {
     const double* B_hi; int64_t ldb, N, b_kchunk, b_ksplit, b_items;
     int64_t K;
     int32_t* e; int32_t* f;
+    bool b_vec;  // B_hi 16-byte aligned and ldb even: two columns per thread, 16-byte loads
 };
 
 // A-item bid: the row maxima of 8 rows (one per warp) over one k-chunk.
@@ -96,28 +97,52 @@ __device__ __forceinline__ void exponents_a_item(const ExpGrid& g, int64_t bid) 
     if (lane == 0 && m != 0) atomicMax(&g.e[row], exponent_from_abs_bits(m));
 }
 
-// B-item b: the column maxima of 256 columns (one per thread) over one k-chunk.
+// B-item b: the column maxima of 256 columns (one per thread; 512 with 16-byte
+// loads of two columns per thread) over one k-chunk.
 __device__ __forceinline__ void exponents_b_item(const ExpGrid& g, int64_t b) {
-    const int64_t col = (b / g.b_ksplit) * 256 + threadIdx.x;
+    const int per = g.b_vec ? 2 : 1;
+    const int64_t col = (b / g.b_ksplit) * 256 * per + (int64_t)threadIdx.x * per;
     if (col >= g.N) return;
     const int64_t k0 = (b % g.b_ksplit) * g.b_kchunk;
     const int64_t k1 = min(g.K, k0 + g.b_kchunk);
-    if (!in_bounds((k1 - 1) * g.ldb + col, (g.K - 1) * g.ldb + g.N, kSiteExpLoadB)) return;
+    const bool pair = g.b_vec && col + 1 < g.N;
+    if (!in_bounds((k1 - 1) * g.ldb + col + (pair ? 1 : 0), (g.K - 1) * g.ldb + g.N, kSiteExpLoadB)) return;
     const double* p = g.B_hi + col;
     const int64_t ldb = g.ldb;
-    uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+    uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;  // column col
+    uint64_t n0 = 0, n1 = 0, n2 = 0, n3 = 0;  // column col + 1
     int64_t k = k0;
-    for (; k + 7 < k1; k += 8) {  // eight loads in flight per thread
-        const double x0 = __ldg(p + (k + 0) * ldb), x1 = __ldg(p + (k + 1) * ldb);
-        const double x2 = __ldg(p + (k + 2) * ldb), x3 = __ldg(p + (k + 3) * ldb);
-        const double x4 = __ldg(p + (k + 4) * ldb), x5 = __ldg(p + (k + 5) * ldb);
-        const double x6 = __ldg(p + (k + 6) * ldb), x7 = __ldg(p + (k + 7) * ldb);
-        m0 = max(m0, max(abs_bits(x0), abs_bits(x4)));
-        m1 = max(m1, max(abs_bits(x1), abs_bits(x5)));
-        m2 = max(m2, max(abs_bits(x2), abs_bits(x6)));
-        m3 = max(m3, max(abs_bits(x3), abs_bits(x7)));
+    if (pair) {
+        for (; k + 3 < k1; k += 4) {  // four 16-byte loads in flight per thread
+            const double2 x0 = __ldg(reinterpret_cast<const double2*>(p + (k + 0) * ldb));
+            const double2 x1 = __ldg(reinterpret_cast<const double2*>(p + (k + 1) * ldb));
+            const double2 x2 = __ldg(reinterpret_cast<const double2*>(p + (k + 2) * ldb));
+            const double2 x3 = __ldg(reinterpret_cast<const double2*>(p + (k + 3) * ldb));
+            m0 = max(m0, abs_bits(x0.x)); n0 = max(n0, abs_bits(x0.y));
+            m1 = max(m1, abs_bits(x1.x)); n1 = max(n1, abs_bits(x1.y));
+            m2 = max(m2, abs_bits(x2.x)); n2 = max(n2, abs_bits(x2.y));
+            m3 = max(m3, abs_bits(x3.x)); n3 = max(n3, abs_bits(x3.y));
+        }
+        for (; k < k1; ++k) {
+            const double2 x = __ldg(reinterpret_cast<const double2*>(p + k * ldb));
+            m0 = max(m0, abs_bits(x.x));
+            n0 = max(n0, abs_bits(x.y));
+        }
+        const uint64_t n = max(max(n0, n1), max(n2, n3));
+        if (n != 0) atomicMax(&g.f[col + 1], exponent_from_abs_bits(n));
+    } else {
+        for (; k + 7 < k1; k += 8) {  // eight loads in flight per thread
+            const double x0 = __ldg(p + (k + 0) * ldb), x1 = __ldg(p + (k + 1) * ldb);
+            const double x2 = __ldg(p + (k + 2) * ldb), x3 = __ldg(p + (k + 3) * ldb);
+            const double x4 = __ldg(p + (k + 4) * ldb), x5 = __ldg(p + (k + 5) * ldb);
+            const double x6 = __ldg(p + (k + 6) * ldb), x7 = __ldg(p + (k + 7) * ldb);
+            m0 = max(m0, max(abs_bits(x0), abs_bits(x4)));
+            m1 = max(m1, max(abs_bits(x1), abs_bits(x5)));
+            m2 = max(m2, max(abs_bits(x2), abs_bits(x6)));
+            m3 = max(m3, max(abs_bits(x3), abs_bits(x7)));
+        }
+        for (; k < k1; ++k) m0 = max(m0, abs_bits(__ldg(p + k * ldb)));
     }
-    for (; k < k1; ++k) m0 = max(m0, abs_bits(__ldg(p + k * ldb)));
     const uint64_t m = max(max(m0, m1), max(m2, m3));
     if (m != 0) atomicMax(&g.f[col], exponent_from_abs_bits(m));
 }
@@ -393,8 +418,9 @@ cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64
     if (K == 0) return cudaSuccess;
     ExpGrid g{};
     g.K = K;
+    g.b_vec = B && (uintptr_t)B->hi % 16 == 0 && B->ld % 2 == 0;
     const int64_t a_rows = A ? (A->rows + 7) / 8 : 0;
-    const int64_t b_cols = B ? (B->rows + 255) / 256 : 0;
+    const int64_t b_cols = B ? (B->rows + (g.b_vec ? 511 : 255)) / (g.b_vec ? 512 : 256) : 0;
     if (a_rows + b_cols == 0) return cudaSuccess;
     // About 16 blocks per SM in total, at least 64 (A) / 16 (B) k per chunk.
     const int64_t want = std::max<int64_t>(1, 16LL * num_sms() / ((A ? 1 : 0) + (B ? 1 : 0)));
