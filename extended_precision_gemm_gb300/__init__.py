@@ -30,7 +30,7 @@ __all__ = [
     "dd_gemm_i64", "layout_i64", "workspace_size_i64", "split_rows_i16", "split_cols_i16", "slice_gemm_i64",
     "split", "split_i16", "dd_gemm_simt", "EXP_NONE", "exponents", "split_with_exponents",
     "split_bf16_with_exponents", "dd_gemm_tc_host", "DDGemmOpts", "dd_gemm_ex", "ex_plan", "slice_gemm_fused",
-    "host_pool_trim", "checked_build", "check_report",
+    "pool_trim", "checked_build", "check_report",
     "QD_MAX_K", "qd_gemm", "qd_layout", "qd_workspace_size", "qd_split", "qd_slice_gemm", "qd_recombine",
     "TC_SLICES", "TC_TILE_M", "TC_BLOCK_M", "TC_TILE_N", "TC_CHUNK_K", "TC_MAX_K_SPLIT",
     "dd_gemm_tc", "tc_layout", "tc_workspace_size", "split_bf16", "slice_gemm_tc", "recombine_tc",
@@ -96,7 +96,7 @@ _SIGNATURES = {
                     ctypes.c_size_t, _ptr], _int),
     "dd_slice_gemm_fused": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _int, _ptr, _ptr],
                             _int),
-    "dd_host_pool_trim": ([], _int),
+    "dd_pool_trim": ([], _int),
     "dd_checked_build": ([], _int),
     "dd_check_report": ([_ptr, _ptr, _ptr], _int),
     "dd_gemm_tc_host": ([_i64, _i64, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr, _ptr, _i64, _ptr], _int),
@@ -231,7 +231,7 @@ def _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo):
 
 def dd_gemm(A_hi, A_lo, B_hi, B_lo, C_hi=None, C_lo=None, stream=None):
     """(C_hi, C_lo) = (A_hi + A_lo) @ (B_hi + B_lo) on the GPU (workspace from the
-    stream-ordered allocator)."""
+    library's stream-ordered pool, kept between calls; pool_trim returns it)."""
     M, N, K, C_hi, C_lo = _gemm_args(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo)
     _check("dd_gemm", load().dd_gemm(M, N, K, A_hi.data_ptr(), A_lo.data_ptr(), _ld(A_hi),
                                      B_hi.data_ptr(), B_lo.data_ptr(), _ld(B_hi),
@@ -802,10 +802,11 @@ def check_report():
     return n.value, site.value, idx.value
 
 
-def host_pool_trim():
-    """Return the device memory the host-buffer products keep in the
-    library's pool on the current device."""
-    _check("dd_host_pool_trim", load().dd_host_pool_trim())
+def pool_trim():
+    """Return the device memory the library's pool keeps on the current
+    device (workspaces of calls without one, device copies of the host-buffer
+    products)."""
+    _check("dd_pool_trim", load().dd_pool_trim())
 
 
 def dd_gemm_tc_host(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, stream=None):

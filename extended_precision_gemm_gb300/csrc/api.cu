@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <nvtx3/nvToolsExt.h>
 
@@ -205,23 +206,24 @@ ddgemm_status run_gemm_i64(const Layout& L, int64_t M, int64_t N, int64_t K, con
 // `ws_bytes` of workspace; the operands are copied in, `run` launches the
 // product on the dense device copies, C is copied back, the block is freed,
 // and the stream is synchronised before returning.
-// The stream-ordered memory pool of the host-buffer entry points on the
-// current device: created on first use with no release threshold, so the
-// device memory of one call (operands, result, workspace) stays in the pool
-// for the next instead of being unmapped at every synchronisation and mapped
-// again (which costs more than the copies at 4096^3).  dd_host_pool_trim
-// gives it back.
+// The library's stream-ordered memory pool on the current device, from which
+// every entry point that is not given a workspace (and the host-buffer
+// entry points, for their device copies) allocates: created on first use
+// with no release threshold, so the memory of one call stays in the pool for
+// the next instead of being unmapped at every synchronisation and mapped
+// again (mapping the 1.7 GB workspace of a 4096^3 bf16 product costs more
+// than 10% of the product).  dd_pool_trim gives it back.
 constexpr int kMaxPoolDevices = 64;
 std::mutex g_pool_mutex;
-cudaMemPool_t g_host_pool[kMaxPoolDevices] = {};
+cudaMemPool_t g_pool[kMaxPoolDevices] = {};
 
-cudaError_t host_pool(cudaMemPool_t* pool, bool create) {
+cudaError_t library_pool(cudaMemPool_t* pool, bool create) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxPoolDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_pool_mutex);
-    if (g_host_pool[dev] == nullptr && create) {
+    if (g_pool[dev] == nullptr && create) {
         cudaMemPoolProps props = {};
         props.allocType = cudaMemAllocationTypePinned;
         props.location.type = cudaMemLocationTypeDevice;
@@ -235,10 +237,18 @@ cudaError_t host_pool(cudaMemPool_t* pool, bool create) {
             cudaMemPoolDestroy(p);
             return err;
         }
-        g_host_pool[dev] = p;
+        g_pool[dev] = p;
     }
-    *pool = g_host_pool[dev];
+    *pool = g_pool[dev];
     return cudaSuccess;
+}
+
+// Stream-ordered allocation from the library's pool (cudaFreeAsync returns it).
+cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t st) {
+    cudaMemPool_t pool = nullptr;
+    cudaError_t err = library_pool(&pool, true);
+    if (err != cudaSuccess) return err;
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, st);
 }
 
 // `peek` reads the slice GEMM's count of bounded waits that gave up: a count
@@ -251,13 +261,8 @@ ddgemm_status host_product(int64_t M, int64_t N, int64_t K, const double* h_A_hi
     if (peek(&timeouts_before, st) != cudaSuccess) return DDGEMM_ERR_CUDA;
     const int64_t a = round_up(M * K * 8, kAlign), b = round_up(K * N * 8, kAlign), c = round_up(M * N * 8, kAlign);
     const int64_t total = 2 * a + 2 * b + 2 * c + ws_bytes;
-    cudaMemPool_t pool = nullptr;
-    if (host_pool(&pool, true) != cudaSuccess) {
-        cudaGetLastError();
-        return DDGEMM_ERR_CUDA;
-    }
     char* dev = nullptr;
-    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dev), (size_t)total, pool, st) != cudaSuccess) {
+    if (pool_alloc(reinterpret_cast<void**>(&dev), (size_t)total, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }
@@ -357,7 +362,7 @@ ddgemm_status dd_gemm(int64_t M, int64_t N, int64_t K, const double* A_hi, const
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Layout L = make_layout(M, N, K);
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+    if (pool_alloc(&ws, (size_t)L.total, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }
@@ -550,13 +555,13 @@ ddgemm_status dd_check_report(unsigned int* count, unsigned int* site, int64_t* 
     return DDGEMM_OK;
 }
 
-ddgemm_status dd_host_pool_trim(void) {
+ddgemm_status dd_pool_trim(void) {
     cudaMemPool_t pool = nullptr;
-    if (host_pool(&pool, false) != cudaSuccess) {
+    if (library_pool(&pool, false) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_CUDA;
     }
-    if (pool == nullptr) return DDGEMM_OK;  // no host-buffer call on this device yet
+    if (pool == nullptr) return DDGEMM_OK;  // nothing allocated on this device yet
     if (cudaDeviceSynchronize() != cudaSuccess || cudaMemPoolTrimTo(pool, 0) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_CUDA;
@@ -610,7 +615,7 @@ ddgemm_status dd_gemm_i64(int64_t M, int64_t N, int64_t K, const double* A_hi, c
                             static_cast<char*>(workspace), st);
     }
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+    if (pool_alloc(&ws, (size_t)L.total, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }
@@ -728,7 +733,7 @@ ddgemm_status qd_gemm(int64_t M, int64_t N, int64_t K, const double* const* A, i
         return run_qd(L, M, N, K, A, lda, B, ldb, C, ldc, static_cast<char*>(workspace), st);
     }
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+    if (pool_alloc(&ws, (size_t)L.total, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }
@@ -898,7 +903,7 @@ ddgemm_status dd_gemm_ex(int64_t M, int64_t N, int64_t K, const double* A_hi, co
                            static_cast<char*>(workspace), st);
     }
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, (size_t)X.total, st) != cudaSuccess) {
+    if (pool_alloc(&ws, (size_t)X.total, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }
@@ -1090,6 +1095,143 @@ ddgemm_status run_gemm_tc(const TcLayout& L, int64_t M, int64_t N, int64_t K, co
     return DDGEMM_OK;
 }
 
+// The library's copy stream on the current device (non-blocking, created on
+// first use): the host-buffer products move data on it while the caller's
+// stream computes, joined to that stream through events.
+cudaError_t copy_stream(cudaStream_t* cs) {
+    static std::mutex mu;
+    static cudaStream_t streams[kMaxPoolDevices] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxPoolDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (streams[dev] == nullptr) {
+        err = cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+        if (err != cudaSuccess) return err;
+    }
+    *cs = streams[dev];
+    return cudaSuccess;
+}
+
+// dd_gemm_tc with host operands, its copies overlapped with the work: A goes
+// up in blocks of rows on the copy stream (the first block, then all of B,
+// then the other blocks); the caller's stream splits B once, then for each
+// block of rows splits it, multiplies it by B and recombines its rows of C,
+// and the copy stream brings each finished block of C back while the next
+// one is computed.  A row of C depends only on its row of A (whose exponent
+// is its own) and on all of B, so the blocks give the one-shot product's
+// result bit for bit.  Device memory from the library's pool; returns after
+// C is in the host buffers (synchronises `st`).
+ddgemm_status tc_host_pipelined(int64_t M, int64_t N, int64_t K, const double* h_A_hi, const double* h_A_lo,
+                                int64_t lda, const double* h_B_hi, const double* h_B_lo, int64_t ldb,
+                                double* h_C_hi, double* h_C_lo, int64_t ldc, cudaStream_t st) {
+    constexpr int kBlocks = 4;
+    const int64_t rows = round_up((M + kBlocks - 1) / kBlocks, kTcM);  // rows per block, a multiple of 256
+    const int64_t nb = (M + rows - 1) / rows;
+    const TcLayout LF = make_tc_layout(rows, N, K);                      // a full block
+    const TcLayout LL = make_tc_layout(M - (nb - 1) * rows, N, K);      // the last block
+    const int64_t Np = LF.Np, Kp = LF.Kp;
+    const int64_t a = round_up(M * K * 8, kAlign), b = round_up(K * N * 8, kAlign), c = round_up(M * N * 8, kAlign);
+    const int64_t ee = round_up(M * 4, kAlign), ff = round_up(Np * 4, kAlign);
+    const int64_t pb = round_up((int64_t)kTcParts * Np * Kp * 2, kAlign);
+    const int64_t pa = round_up((int64_t)kTcParts * LF.Mp * Kp * 2, kAlign);
+    const int64_t pp = round_up((int64_t)std::max(LF.splits, LL.splits) * kTcParts * LF.Mp * Np * 4, kAlign);
+    const int64_t total = 2 * a + 2 * b + 2 * c + ee + ff + pb + pa + pp;
+
+    unsigned int timeouts_before = 0;
+    if (peek_wait_timeouts_tc(&timeouts_before, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_CUDA;
+    }
+    cudaStream_t cs = nullptr;
+    if (copy_stream(&cs) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_CUDA;
+    }
+    char* dev = nullptr;
+    if (pool_alloc(reinterpret_cast<void**>(&dev), (size_t)total, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DDGEMM_ERR_ALLOC;
+    }
+    double* dA_hi = reinterpret_cast<double*>(dev);
+    double* dA_lo = reinterpret_cast<double*>(dev + a);
+    double* dB_hi = reinterpret_cast<double*>(dev + 2 * a);
+    double* dB_lo = reinterpret_cast<double*>(dev + 2 * a + b);
+    double* dC_hi = reinterpret_cast<double*>(dev + 2 * a + 2 * b);
+    double* dC_lo = reinterpret_cast<double*>(dev + 2 * a + 2 * b + c);
+    int32_t* e = reinterpret_cast<int32_t*>(dev + 2 * a + 2 * b + 2 * c);
+    int32_t* f = reinterpret_cast<int32_t*>(dev + 2 * a + 2 * b + 2 * c + ee);
+    uint16_t* pB = reinterpret_cast<uint16_t*>(dev + 2 * a + 2 * b + 2 * c + ee + ff);
+    uint16_t* pA = reinterpret_cast<uint16_t*>(dev + 2 * a + 2 * b + 2 * c + ee + ff + pb);
+    int32_t* P = reinterpret_cast<int32_t*>(dev + 2 * a + 2 * b + 2 * c + ee + ff + pb + pa);
+
+    // events: [0] start (st), [1] B up, [2 .. 2+nb) A blocks up, [2+nb .. 2+2nb) C blocks done, [2+2nb] all down
+    std::vector<cudaEvent_t> ev((size_t)(3 + 2 * nb), nullptr);
+    cudaError_t err = cudaSuccess;
+    for (auto& x : ev)
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+    auto up = [&](double* dst, const double* src, int64_t r, int64_t cols, int64_t ld) {
+        if (err == cudaSuccess && r > 0 && cols > 0)
+            err = cudaMemcpy2DAsync(dst, (size_t)cols * 8, src, (size_t)ld * 8, (size_t)cols * 8, (size_t)r,
+                                    cudaMemcpyHostToDevice, cs);
+    };
+    auto block_rows = [&](int64_t i) { return std::min(rows, M - i * rows); };
+    if (err == cudaSuccess) err = cudaEventRecord(ev[0], st);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(cs, ev[0], 0);
+    for (int64_t i = 0; i < nb; ++i) {
+        up(dA_hi + i * rows * K, h_A_hi + i * rows * lda, block_rows(i), K, lda);
+        up(dA_lo + i * rows * K, h_A_lo + i * rows * lda, block_rows(i), K, lda);
+        if (err == cudaSuccess) err = cudaEventRecord(ev[2 + i], cs);
+        if (i == 0) {
+            up(dB_hi, h_B_hi, K, N, ldb);
+            up(dB_lo, h_B_lo, K, N, ldb);
+            if (err == cudaSuccess) err = cudaEventRecord(ev[1], cs);
+        }
+    }
+    // the caller's stream: B's exponents and parts once, then block by block
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(st, ev[1], 0);
+    if (err == cudaSuccess) err = run_split_tc(0, N, K, Kp, nullptr, nullptr, 1, nullptr, nullptr, dB_hi, dB_lo, N, f, pB, st);
+    for (int64_t i = 0; i < nb && err == cudaSuccess; ++i) {
+        const int64_t r0 = i * rows, mb = block_rows(i);
+        const TcLayout& L = i + 1 < nb ? LF : LL;
+        err = cudaStreamWaitEvent(st, ev[2 + i], 0);
+        if (err == cudaSuccess)
+            err = run_split_tc(mb, 0, K, Kp, dA_hi + r0 * K, dA_lo + r0 * K, K, e + r0, pA, nullptr, nullptr, 1,
+                               nullptr, nullptr, st);
+        if (err == cudaSuccess) err = launch_slice_gemm_tc(pA, pB, L.Mp, Np, Kp, L.splits, P, st);
+        if (err == cudaSuccess)
+            err = launch_recombine_tc(P, L.splits, L.Mp, Np, e + r0, f, mb, N, dC_hi + r0 * N, dC_lo + r0 * N, N, st);
+        if (err == cudaSuccess) err = cudaEventRecord(ev[2 + nb + i], st);
+    }
+    // the copy stream: each block of C back as soon as it is done
+    for (int64_t i = 0; i < nb && err == cudaSuccess; ++i) {
+        const int64_t r0 = i * rows, mb = block_rows(i);
+        err = cudaStreamWaitEvent(cs, ev[2 + nb + i], 0);
+        if (err == cudaSuccess)
+            err = cudaMemcpy2DAsync(h_C_hi + r0 * ldc, (size_t)ldc * 8, dC_hi + r0 * N, (size_t)N * 8, (size_t)N * 8,
+                                    (size_t)mb, cudaMemcpyDeviceToHost, cs);
+        if (err == cudaSuccess)
+            err = cudaMemcpy2DAsync(h_C_lo + r0 * ldc, (size_t)ldc * 8, dC_lo + r0 * N, (size_t)N * 8, (size_t)N * 8,
+                                    (size_t)mb, cudaMemcpyDeviceToHost, cs);
+    }
+    // join, release, wait
+    cudaError_t je = ev[2 + 2 * nb] ? cudaEventRecord(ev[2 + 2 * nb], cs) : cudaErrorInvalidValue;
+    if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ev[2 + 2 * nb], 0);
+    if (je != cudaSuccess) je = cudaStreamSynchronize(cs);  // the copy stream must be idle before the memory goes
+    cudaError_t fe = cudaFreeAsync(dev, st);
+    cudaError_t se = cudaStreamSynchronize(st);
+    for (auto& x : ev)
+        if (x) cudaEventDestroy(x);
+    ddgemm_status s = (err == cudaSuccess && je == cudaSuccess && fe == cudaSuccess && se == cudaSuccess)
+                          ? DDGEMM_OK : DDGEMM_ERR_CUDA;
+    unsigned int timeouts_after = 0;
+    if (s == DDGEMM_OK && (peek_wait_timeouts_tc(&timeouts_after, st) != cudaSuccess || timeouts_after != timeouts_before))
+        s = DDGEMM_ERR_CUDA;
+    if (s != DDGEMM_OK) cudaGetLastError();
+    return s;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1132,7 +1274,7 @@ ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K, const double* A_hi, co
                            static_cast<char*>(workspace), st);
     }
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+    if (pool_alloc(&ws, (size_t)L.total, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }
@@ -1149,6 +1291,9 @@ ddgemm_status dd_gemm_tc_host(int64_t M, int64_t N, int64_t K, const double* h_A
     if (s == DDGEMM_OK) s = check_tc_shapes(M, N, K);
     if (s != DDGEMM_OK) return s;
     if (M == 0 || N == 0) return DDGEMM_OK;
+    if (M >= 4 * kTcM && K > 0)  // enough rows for blocks of at least 256 to overlap the copies
+        return tc_host_pipelined(M, N, K, h_A_hi, h_A_lo, lda, h_B_hi, h_B_lo, ldb, h_C_hi, h_C_lo, ldc,
+                                 static_cast<cudaStream_t>(stream));
     TcLayout L = make_tc_layout(M, N, K);
     return host_product(M, N, K, h_A_hi, h_A_lo, lda, h_B_hi, h_B_lo, ldb, h_C_hi, h_C_lo, ldc, L.total,
                         static_cast<cudaStream_t>(stream),
@@ -1311,7 +1456,7 @@ ddgemm_status qd_gemm_tc(int64_t M, int64_t N, int64_t K, const double* const* A
         return run_qd_tc(L, M, N, K, A, lda, B, ldb, C, ldc, static_cast<char*>(workspace), st);
     }
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+    if (pool_alloc(&ws, (size_t)L.total, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }
@@ -1460,7 +1605,7 @@ ddgemm_status md_gemm_tc(int nparts, int64_t M, int64_t N, int64_t K, const doub
         return run_md_tc(nparts, L, M, N, K, A, lda, B, ldb, C, ldc, static_cast<char*>(workspace), st);
     }
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, (size_t)L.total, st) != cudaSuccess) {
+    if (pool_alloc(&ws, (size_t)L.total, st) != cudaSuccess) {
         cudaGetLastError();
         return DDGEMM_ERR_ALLOC;
     }

@@ -103,8 +103,13 @@ ddgemm_status dd_gemm_ws(int64_t M, int64_t N, int64_t K,
 
 /*
  * C = A * B (double double).  As dd_gemm_ws, with the workspace taken from the
- * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
- * Returns DDGEMM_ERR_ALLOC when the allocation fails.
+ * library's stream-ordered memory pool on the current device (allocated and
+ * freed on `stream`).  The pool keeps freed memory for the next call instead
+ * of unmapping it at every synchronisation (mapping gigabytes anew on every
+ * call costs a visible part of a product); dd_pool_trim returns it to the
+ * device.  Every entry point below whose workspace may be NULL, and the
+ * host-buffer entry points, allocate from the same pool.  Returns
+ * DDGEMM_ERR_ALLOC when the allocation fails.
  */
 ddgemm_status dd_gemm(int64_t M, int64_t N, int64_t K,
                       const double* A_hi, const double* A_lo, int64_t lda,
@@ -117,10 +122,8 @@ ddgemm_status dd_gemm(int64_t M, int64_t N, int64_t K,
  * in h_C_hi / h_C_lo (it synchronises `stream`).  Host buffers are read and
  * written as dense row-major arrays with the given leading dimensions;
  * page-locked (pinned) buffers make the copies faster.  The device memory of
- * the call (dense copies of A, B and C plus the workspace) comes from a
- * stream-ordered pool of the library on the current device, which keeps it
- * after the call for the next one (mapping gigabytes anew on every call costs
- * more than the copies); dd_host_pool_trim returns it to the device.
+ * the call (dense copies of A, B and C plus the workspace) comes from the
+ * library's pool (see dd_gemm); dd_pool_trim returns it to the device.
  */
 ddgemm_status dd_gemm_host(int64_t M, int64_t N, int64_t K,
                            const double* h_A_hi, const double* h_A_lo, int64_t lda,
@@ -171,7 +174,7 @@ ddgemm_status dd_gemm_ex_plan(int64_t M, int64_t N, int64_t K, const ddgemm_opts
 /*
  * C = A * B (double double) with options (ddgemm_opts; NULL = defaults).
  * `workspace` (dd_gemm_ex_plan's bytes, 256-byte aligned) may be NULL: then
- * it comes from the stream-ordered allocator (DDGEMM_ERR_ALLOC on failure).
+ * it comes from the library's pool (see dd_gemm; DDGEMM_ERR_ALLOC on failure).
  * With both fusions the workspace holds only the exponents (4 (Mp + Np)
  * bytes).  Otherwise as dd_gemm_ws.
  */
@@ -214,11 +217,12 @@ ddgemm_status dd_gemm_noalloc(int64_t M, int64_t N, int64_t K,
                               double* C_hi, double* C_lo, int64_t ldc, void* stream);
 
 /*
- * Return the device memory that dd_gemm_host / dd_gemm_tc_host keep in the
- * library's pool on the current device (synchronises the device).  DDGEMM_OK
- * also when no such call has run on it.
+ * Return the device memory the library's pool keeps on the current device
+ * (workspaces of calls without one, device copies of the host-buffer entry
+ * points) to the device; synchronises the device.  DDGEMM_OK also when
+ * nothing was allocated on it.
  */
-ddgemm_status dd_host_pool_trim(void);
+ddgemm_status dd_pool_trim(void);
 
 /* ------------------------------------------------------------------ */
 /* The steps of the path, one entry point each                          */
@@ -378,7 +382,7 @@ ddgemm_status dd_gemm_simt(int64_t M, int64_t N, int64_t K,
  * dd_gemm's.
  *
  * dd_gemm_i64: as dd_gemm_ws; `workspace` may be NULL, in which case it is
- * taken from the stream-ordered allocator (DDGEMM_ERR_ALLOC on failure).
+ * taken from the library's pool (see dd_gemm; DDGEMM_ERR_ALLOC on failure).
  * dd_gemm_i64_workspace_size / dd_gemm_i64_layout: its workspace bytes and
  * automatic k-split for this shape on the current device.
  */
@@ -434,7 +438,7 @@ ddgemm_status dd_slice_gemm_i64(int64_t M, int64_t N, int64_t K,
  * the product summed exactly and rounded once into four doubles
  * (c0 = RN(X), c1 = RN(X - c0), ...).  K <= QDGEMM_MAX_K (2^23) keeps every
  * part sum below 2^53.  `workspace` (qd_gemm_workspace_size bytes, 256-byte
- * aligned) may be NULL: then it comes from the stream-ordered allocator.
+ * aligned) may be NULL: then it comes from the library's pool (see dd_gemm).
  */
 #define QDGEMM_MAX_K (1 << 23)
 ddgemm_status qd_gemm_layout(int64_t M, int64_t N, int64_t K, int* splits);
@@ -488,7 +492,7 @@ ddgemm_status qd_recombine(int64_t M, int64_t N, const double* P, int splits, co
  * both are within the same normwise bound of the exact product.
  * Same arguments and conventions as dd_gemm; K <= DDGEMM_MAX_K.  `workspace`
  * (dd_gemm_tc_workspace_size bytes, 256-byte aligned) may be NULL: then it
- * comes from the stream-ordered allocator (DDGEMM_ERR_ALLOC on failure).
+ * comes from the library's pool (see dd_gemm; DDGEMM_ERR_ALLOC on failure).
  */
 #define DDGEMM_TC_SLICES 13         /* parts per double double */
 #define DDGEMM_TC_DIGIT_BITS 8      /* bits per part */
@@ -524,7 +528,7 @@ ddgemm_status dd_gemm_tc(int64_t M, int64_t N, int64_t K,
 
 /*
  * dd_gemm_tc with HOST operands and result, as dd_gemm_host: copies A and B
- * to the current device (memory from the library's pool, see dd_gemm_host),
+ * to the current device (memory from the library's pool, see dd_gemm),
  * runs dd_gemm_tc, copies C back, and returns after the result is in h_C_hi /
  * h_C_lo (it synchronises `stream`).  Pinned host buffers make the copies
  * faster.

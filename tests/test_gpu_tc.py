@@ -298,10 +298,37 @@ def test_dd_gemm_tc_host_matches_device_and_model():
     assert (Cw[:, N:] == 5.0).all() and (Cwl[:, N:] == 5.0).all()
     # the pool that keeps the calls' device memory can be emptied, and the
     # next call refills it
-    ddg.host_pool_trim()
+    ddg.pool_trim()
     G_hi = np.zeros((M, N))
     G_lo = np.zeros((M, N))
     ddg.dd_gemm_tc_host(A_hi, A_lo, B_hi, B_lo, G_hi, G_lo)
     ddg.dd_gemm_host(A_hi, A_lo, B_hi, B_lo, np.zeros((M, N)), np.zeros((M, N)))
     assert np.array_equal(G_hi, H_hi) and np.array_equal(G_lo, H_lo)
-    ddg.host_pool_trim()
+    ddg.pool_trim()
+
+
+def test_dd_gemm_tc_host_pipelined_blocks():
+    # M >= 1024: A goes up in blocks of rows while earlier blocks compute and
+    # finished blocks of C come back (here blocks of 512, 512 and 76 rows);
+    # the result must be the one-shot device product's, and the oracle
+    # model's, bit for bit, with leading dimensions above the widths
+    M, N, K = 1100, 300, 200
+    A_hi, A_lo, B_hi, B_lo = workloads.make_dd(M, N, K, "uniform_exp20", 25)
+    D_hi, D_lo = ddg.dd_gemm_tc(dev(A_hi), dev(A_lo), dev(B_hi), dev(B_lo))
+    wide, widel = np.zeros((M, K + 5)), np.zeros((M, K + 5))
+    wide[:, :K], widel[:, :K] = A_hi, A_lo
+    Bw, Bwl = np.zeros((K, N + 3)), np.zeros((K, N + 3))
+    Bw[:, :N], Bwl[:, :N] = B_hi, B_lo
+    Cw = np.full((M, N + 2), 5.0)
+    Cwl = np.full((M, N + 2), 5.0)
+    lib = ddg.load()
+    for _ in range(2):  # twice: the second call reuses the pool's memory
+        assert lib.dd_gemm_tc_host(M, N, K, wide.ctypes.data, widel.ctypes.data, K + 5, Bw.ctypes.data,
+                                   Bwl.ctypes.data, N + 3, Cw.ctypes.data, Cwl.ctypes.data, N + 2, None) == 0
+        assert np.array_equal(Cw[:, :N].view(np.int64), host(D_hi).view(np.int64))
+        assert np.array_equal(Cwl[:, :N].view(np.int64), host(D_lo).view(np.int64))
+        assert (Cw[:, N:] == 5.0).all() and (Cwl[:, N:] == 5.0).all()
+    R_hi, R_lo, *_ = sb.sliced_dd_gemm(A_hi, A_lo, B_hi, B_lo)
+    assert np.array_equal(Cw[:, :N].view(np.int64), R_hi.view(np.int64))
+    assert np.array_equal(Cwl[:, :N].view(np.int64), R_lo.view(np.int64))
+    assert ddg.wait_timeouts() == 0
