@@ -22,6 +22,17 @@ static_assert(BK % 4 == 0, "k-chunk holds whole k4 groups of the m8n8k4 fragment
 
 __host__ __device__ inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// The IEEE 754 bits of x, moved through an opaque instruction.  Masked tests
+// and maxima of the bits then stay integer instructions: a compiler may
+// otherwise fold a test of the magnitude bits back into a floating-point
+// comparison or absolute value, which runs on the FP64 pipe (the narrowest
+// unit of GB300).
+__device__ __forceinline__ uint64_t f64_bits(double x) {
+    uint64_t b;
+    asm("mov.b64 %0, %1;" : "=l"(b) : "d"(x));
+    return b;
+}
+
 // Smallest integer e with |x| < 2^e for the magnitude bits of a finite double
 // (sign bit cleared); EXP_NONE for zero.  IEEE 754 binary64 layout.
 __device__ __forceinline__ int exponent_from_abs_bits(uint64_t a) {

@@ -33,7 +33,7 @@ __device__ __forceinline__ void quick_two_sum(double a, double b, double& s, dou
 
 // An integer-valued double of magnitude below 2^53 as int64.
 __device__ __forceinline__ long long to_int(double v) {
-    const uint64_t b = (uint64_t)__double_as_longlong(v);
+    const uint64_t b = f64_bits(v);
     const uint64_t a = b & 0x7FFFFFFFFFFFFFFFULL;
     if (a == 0) return 0;
     const int E = (int)(a >> 52) - 1075;
@@ -55,7 +55,7 @@ __device__ __forceinline__ double to_double(long long x) {
 // x * 2^k for x = 0 or 1 <= |x| < 2^53 and -117 <= k <= 0: the result is a
 // normal double (or 0), so only the exponent field changes.
 __device__ __forceinline__ double scale_part(double x, int k) {
-    const long long b = __double_as_longlong(x);
+    const long long b = (long long)f64_bits(x);
     if ((b & 0x7FFFFFFFFFFFFFFFLL) == 0) return 0.0;
     return __longlong_as_double(b + ((long long)k << 52));
 }
@@ -63,7 +63,7 @@ __device__ __forceinline__ double scale_part(double x, int k) {
 // ldexp(x, k), correctly rounded: an exponent-field add when x and the
 // result are normal, the library ldexp otherwise (zero, subnormal, overflow).
 __device__ __forceinline__ double scale_result(double x, int k) {
-    const long long b = __double_as_longlong(x);
+    const long long b = (long long)f64_bits(x);
     const int biased = (int)((b >> 52) & 0x7FF);
     if (biased != 0 && biased != 0x7FF && biased + k >= 1 && biased + k <= 2046)
         return __longlong_as_double(b + ((long long)k << 52));
@@ -72,7 +72,7 @@ __device__ __forceinline__ double scale_result(double x, int k) {
 
 // +0 for a zero of either sign.
 __device__ __forceinline__ double plus_zero(double x) {
-    return (__double_as_longlong(x) << 1) == 0 ? 0.0 : x;
+    return (f64_bits(x) << 1) == 0 ? 0.0 : x;
 }
 
 // (c_hi, c_lo) from the 8 part sums of one output: from d = 7 down to 0,

@@ -18,6 +18,8 @@
 
 #include <cstdint>
 
+#include "common.cuh"
+
 namespace ddg {
 namespace fxp {
 
@@ -55,8 +57,8 @@ __device__ __forceinline__ bool scaled_frac_zero(uint64_t m, int sh) {
 
 // X = floor(|hi + lo| * 2^(104 - e)) and the sign of the element.
 __device__ __forceinline__ unsigned __int128 fixed_point(double hi, double lo, int e, uint64_t& sign_out) {
-    uint64_t hb = (uint64_t)__double_as_longlong(hi);
-    uint64_t lb = (uint64_t)__double_as_longlong(lo);
+    uint64_t hb = f64_bits(hi);
+    uint64_t lb = f64_bits(lo);
     if ((hb & ABS_MASK) == 0) { hb = lb; lb = 0; }  // hi = 0: the element is lo alone
     const uint64_t sign = hb >> 63;
     unsigned __int128 X = 0;

@@ -42,16 +42,16 @@ __device__ __forceinline__ U256 fixed_point_qd(const double (&x)[4], int e, uint
     int lead = -1;
 #pragma unroll
     for (int p = 3; p >= 0; --p)
-        if (((uint64_t)__double_as_longlong(x[p]) & 0x7FFFFFFFFFFFFFFFULL) != 0) lead = p;
+        if ((f64_bits(x[p]) & 0x7FFFFFFFFFFFFFFFULL) != 0) lead = p;
     sign_out = 0;
     if (lead < 0) return u256_zero();
-    const uint64_t sign = (uint64_t)__double_as_longlong(x[lead]) >> 63;
+    const uint64_t sign = f64_bits(x[lead]) >> 63;
     sign_out = sign;
     U256 X = u256_zero();
     bool done = false;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        const uint64_t b = (uint64_t)__double_as_longlong(x[p]);
+        const uint64_t b = f64_bits(x[p]);
         if (done || (b & 0x7FFFFFFFFFFFFFFFULL) == 0) continue;
         const bool negp = ((b >> 63) != sign);  // part sign relative to the element
         const UnpQ u = unpack_abs_q(b);
@@ -72,7 +72,7 @@ __device__ __forceinline__ U256 fixed_point_qd(const double (&x)[4], int e, uint
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 if (r <= p) continue;
-                const uint64_t c = (uint64_t)__double_as_longlong(x[r]);
+                const uint64_t c = f64_bits(x[r]);
                 if ((c & 0x7FFFFFFFFFFFFFFFULL) != 0) {
                     if ((c >> 63) != sign) F -= 1;
                     break;

@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(QTHREADS, 3)
 
 // An integer-valued double of magnitude below 2^63 as int64 (exact).
 __device__ __forceinline__ long long exact_double_to_int(double v) {
-    const uint64_t b = (uint64_t)__double_as_longlong(v);
+    const uint64_t b = f64_bits(v);
     const uint64_t a = b & ABS_MASK;
     if (a == 0) return 0;
     const int E = (int)(a >> 52) - 1075;  // v = m 2^E, E >= -52 for integers >= 1

@@ -22,7 +22,7 @@ namespace {
 constexpr uint64_t ABS_MASK = 0x7FFFFFFFFFFFFFFFULL;
 
 __device__ __forceinline__ uint64_t abs_bits(double x) {
-    return (uint64_t)__double_as_longlong(x) & ABS_MASK;
+    return f64_bits(x) & ABS_MASK;
 }
 
 // ---------------------------------------------------------------------------

@@ -74,18 +74,18 @@ __device__ __forceinline__ void fixed_point_n(const double (&x)[NIN], int e, int
     int lead = -1;
 #pragma unroll
     for (int p = NIN - 1; p >= 0; --p)
-        if (((uint64_t)__double_as_longlong(x[p]) & ABS) != 0) lead = p;
+        if ((f64_bits(x[p]) & ABS) != 0) lead = p;
     sign_out = 0;
     if (lead < 0) return;
     uint64_t sign = 0;
 #pragma unroll
     for (int p = 0; p < NIN; ++p)
-        if (p == lead) sign = (uint64_t)__double_as_longlong(x[p]) >> 63;
+        if (p == lead) sign = f64_bits(x[p]) >> 63;
     sign_out = sign;
     bool done = false;
 #pragma unroll
     for (int p = 0; p < NIN; ++p) {
-        const uint64_t b = (uint64_t)__double_as_longlong(x[p]);
+        const uint64_t b = f64_bits(x[p]);
         if (done || (b & ABS) == 0) continue;
         const bool negp = (b >> 63) != sign;
         const UnpM u = unpack_m(b);
@@ -116,7 +116,7 @@ __device__ __forceinline__ void fixed_point_n(const double (&x)[NIN], int e, int
 #pragma unroll
             for (int r = 0; r < NIN; ++r) {
                 if (r <= p || seen) continue;
-                const uint64_t c = (uint64_t)__double_as_longlong(x[r]);
+                const uint64_t c = f64_bits(x[r]);
                 if ((c & ABS) != 0) {
                     if ((c >> 63) != sign) F -= 1;
                     seen = true;

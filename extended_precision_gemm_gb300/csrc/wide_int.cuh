@@ -6,6 +6,8 @@
 
 #include <cstdint>
 
+#include "common.cuh"
+
 namespace ddg {
 namespace wide {
 
@@ -151,7 +153,7 @@ __device__ __forceinline__ void round_into_doubles(U256 X, int q, double (&out)[
             stop = true;
         }
         // +0 for a zero of either sign (integer test: no FP64 operation)
-        out[p] = (__double_as_longlong(v) << 1) == 0 ? 0.0 : v;
+        out[p] = (f64_bits(v) << 1) == 0 ? 0.0 : v;
     }
 }
 
