@@ -280,13 +280,6 @@ __global__ void __launch_bounds__(256) recombine_qd_kernel(const double* __restr
     }
 }
 
-int num_sms_md() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 152;
-    return sms;
-}
-
 }  // namespace
 
 cudaError_t launch_split_qd(const double* const* A, int64_t lda, int64_t M, const int32_t* e,
@@ -301,7 +294,7 @@ cudaError_t launch_split_qd(const double* const* A, int64_t lda, int64_t M, cons
     const int64_t a_items = ((a.rows + TM - 1) / TM) * KT;
     const int64_t items = a_items + ((b.rows + TN - 1) / TN) * KT;
     if (items == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)num_sms_md() * 16));
+    const unsigned blocks = (unsigned)std::min<int64_t>(items, 0x7FFFFFFF);  // one item per block
     split_qd_kernel<<<blocks, 256, 0, st>>>(a, b, K, Kp, KT, a_items, items, planesA, planesB);
     return cudaGetLastError();
 }

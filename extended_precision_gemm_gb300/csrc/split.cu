@@ -182,16 +182,14 @@ __device__ __forceinline__ uint4 split_digits_i16(double hi, double lo, int e) {
 // consecutive k (4 k-chunks): 32 lanes = rows (columns) x 8 warps = groups
 // of 4 consecutive k.  Items [0, a_items) are A's, the rest B's.
 // FP64 parts: the item's parts form one contiguous 64 KB block of the plane
-// array ([chunk][part][k4 group][row in tile][k % 4]), assembled in shared
-// memory and written by one bulk asynchronous copy (TMA engine), so every
-// DRAM line is written whole.
+// array ([chunk][part][k4 group][row in tile][k % 4]), written straight from
+// registers in whole 32-byte DRAM sectors.
 // int16 parts: layout [tile][k-chunk][k in chunk][row in tile][part]; each
 // lane writes the 16 bytes of one element, a warp 512 contiguous bytes.
 // ---------------------------------------------------------------------------
 
 constexpr int SPLIT_THREADS = 256;
 constexpr int SPLIT_CHUNKS = 32 / BK;                                                // k-chunks per item
-constexpr size_t SPLIT_SMEM = (size_t)SPLIT_CHUNKS * CHUNK_DOUBLES * sizeof(double);  // 64 KB
 constexpr int PART_STRIDE = (BK / 4) * TM * 4;                                       // doubles between parts
 
 struct SplitGrid {
@@ -269,25 +267,25 @@ __device__ __forceinline__ Item item_of(const SplitGrid& g, int64_t item, int64_
     return it;
 }
 
-// Each block walks its items with a stride of the grid; the loads of the next
-// item are issued before the current one is split, so their latency overlaps
-// the digit arithmetic and the stores.  Each warp stages its own 8 parts x
-// (32 rows x 4 k) = 8 KB in shared memory and writes them with eight 1 KB
-// bulk stores (TMA engine); before refilling its stage it only waits until
-// its own previous stores have read it -- no block-wide barrier.
+// One item per block (a grid-stride walk only past 2^31 - 1 items, with the
+// next item's loads issued before the current one is split).  A lane keeps the fixed-point values
+// of its 4 elements (one row, 4 consecutive k) and forms the parts one plane
+// at a time: part s of the 4 elements is 32 contiguous bytes of the plane
+// block, written by one 256-bit store, so a warp writes 1 KB per part and
+// every DRAM sector is written whole, straight from registers.
+__device__ __forceinline__ void st_global_v4(double* p, double a, double b, double c, double d) {
+    asm volatile("st.global.v4.f64 [%0], {%1, %2, %3, %4};" ::"l"(p), "d"(a), "d"(b), "d"(c), "d"(d) : "memory");
+}
+
 template <int VEC>
-__global__ void __launch_bounds__(SPLIT_THREADS, 3) split_f64_kernel(SplitGrid g) {
+__global__ void __launch_bounds__(SPLIT_THREADS, 4) split_f64_kernel(SplitGrid g) {
     pdl_wait();
     pdl_launch_dependents();
-    extern __shared__ __align__(128) double stage[];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t items = (g.a_tiles + g.b_tiles) * g.KT;
     const int64_t KC = g.Kp / BK;
-    constexpr int WARP_STAGE = S * TM * 4;  // 1024 doubles
-    double* ws = stage + w * WARP_STAGE;    // [part][row][k % 4]
     double nhi[4] = {0, 0, 0, 0}, nlo[4] = {0, 0, 0, 0};
     int nex = 0;
-    bool pending = false;
     int64_t item = blockIdx.x;
     Item nit;
     if (item < items) {
@@ -297,10 +295,10 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 3) split_f64_kernel(SplitGrid g
     }
     for (; item < items; item += gridDim.x) {
         const Item it = nit;
-        double hi[4], lo[4];
+        unsigned __int128 X[4];
+        uint64_t sign[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) { hi[r] = nhi[r]; lo[r] = nlo[r]; }
-        const int ex = nex;
+        for (int r = 0; r < 4; ++r) X[r] = fxp::fixed_point(nhi[r], nlo[r], nex, sign[r]);
         const int64_t next = item + gridDim.x;
         if (next < items) {
             nit = item_of(g, next, KC);
@@ -308,41 +306,19 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 3) split_f64_kernel(SplitGrid g
                 nex = load_item<VEC>(g, nit.is_a, nit.tile, nit.kt * 32 + 4 * w, lane, w, nit.kt, nhi, nlo);
         }
         if ((w >> 1) >= it.chunks) continue;  // this warp's k-chunk does not exist
-        if (pending) {
-            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            __syncwarp();
-        }
+        // part s of this warp's (k-chunk, k4 group): 32 rows x 4 k, 1 KB contiguous
+        const int64_t off = (it.tile * KC + it.kt * SPLIT_CHUNKS + (w >> 1)) * CHUNK_DOUBLES + (w & 1) * TM * 4;
+        const int64_t extent = (it.is_a ? g.a_tiles : g.b_tiles) * KC * CHUNK_DOUBLES;
+        if (!in_bounds(off + (S - 1) * PART_STRIDE + TM * 4 - 1, extent, kSiteSplitStore)) continue;
+        double* out = static_cast<double*>(it.is_a ? g.planesA : g.planesB) + off + lane * 4;
 #pragma unroll
-        for (int r = 0; r < 4; r += 2) {
-            double d0[S], d1[S];
-            split_digits(hi[r], lo[r], ex, d0);
-            split_digits(hi[r + 1], lo[r + 1], ex, d1);
+        for (int s = 0; s < S; ++s) {
+            double d[4];
 #pragma unroll
-            for (int s = 0; s < S; ++s)
-                *reinterpret_cast<double2*>(ws + (s * TM + lane) * 4 + r) = make_double2(d0[s], d1[s]);
+            for (int r = 0; r < 4; ++r) d[r] = small_int_to_double(digit_field(X[r], s), sign[r]);
+            st_global_v4(out + s * PART_STRIDE, d[0], d[1], d[2], d[3]);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-            // part s of this warp's (k-chunk, k4 group) is 1 KB contiguous in the plane block
-            const int64_t off = (it.tile * KC + it.kt * SPLIT_CHUNKS + (w >> 1)) * CHUNK_DOUBLES + (w & 1) * TM * 4;
-            double* base = static_cast<double*>(it.is_a ? g.planesA : g.planesB) + off;
-            const int64_t extent = (it.is_a ? g.a_tiles : g.b_tiles) * KC * CHUNK_DOUBLES;
-            if (in_bounds(off + (S - 1) * PART_STRIDE + TM * 4 - 1, extent, kSiteSplitStore)) {
-#pragma unroll
-                for (int s = 0; s < S; ++s)
-                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                                     base + s * PART_STRIDE),
-                                 "r"(smem_u32(ws + s * TM * 4)), "r"((uint32_t)(TM * 4 * sizeof(double)))
-                                 : "memory");
-            }
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-        pending = true;
     }
-    // the stage must stay valid until the last stores have read it
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-    __syncwarp();
 }
 
 __device__ __forceinline__ int64_t i16_offset(int64_t tile, int64_t KC, int64_t k, int ti) {
@@ -468,10 +444,13 @@ static bool a_vec(const SplitOperand* A) {
     return !A || (((uintptr_t)A->hi % 16 == 0) && ((uintptr_t)A->lo % 16 == 0) && (A->ld % 2 == 0));
 }
 
-// One resident wave of blocks: each block walks many items (prefetching).
-static unsigned split_blocks(int64_t items, int per_sm) {
-    const int64_t cap = (int64_t)num_sms() * per_sm;
-    return (unsigned)std::max<int64_t>(1, std::min(items, cap));
+// FP64 split: one block per item.  The block scheduler hands out the items in
+// order as blocks finish, so the blocks in flight write one compact range of
+// the planes; a persistent grid drifts apart and spreads its writes over
+// many DRAM pages (on GB300 a grid-stride loop of 256-bit stores reaches
+// about 6.5 TB/s, the same stores from a one-item-per-block grid 7.7 TB/s).
+static unsigned split_grid(int64_t items) {
+    return (unsigned)std::min<int64_t>(items, 0x7FFFFFFF);
 }
 
 cudaError_t launch_split_f64(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
@@ -480,16 +459,11 @@ cudaError_t launch_split_f64(const SplitOperand* A, const SplitOperand* B, int64
     SplitGrid g = make_split_grid(A, B, K, Kp, planesA, planesB);
     const int64_t items = (g.a_tiles + g.b_tiles) * g.KT;
     if (items == 0) return cudaSuccess;
-    cudaError_t err;
-    if (a_vec(A)) {
-        err = cudaFuncSetAttribute(split_f64_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
-        if (err != cudaSuccess) return err;
-        err = launch_pdl(split_f64_kernel<2>, dim3(split_blocks(items, 3)), dim3(SPLIT_THREADS), SPLIT_SMEM, st, g);
-    } else {
-        err = cudaFuncSetAttribute(split_f64_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
-        if (err != cudaSuccess) return err;
-        err = launch_pdl(split_f64_kernel<1>, dim3(split_blocks(items, 3)), dim3(SPLIT_THREADS), SPLIT_SMEM, st, g);
-    }
+    const cudaError_t err = a_vec(A) ? launch_pdl(split_f64_kernel<2>, dim3(split_grid(items)), dim3(SPLIT_THREADS),
+                                                  0, st, g)
+                                     : launch_pdl(split_f64_kernel<1>, dim3(split_grid(items)), dim3(SPLIT_THREADS),
+                                                  0, st, g);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
@@ -499,7 +473,7 @@ cudaError_t launch_split_i16(const SplitOperand* A, const SplitOperand* B, int64
     SplitGrid g = make_split_grid(A, B, K, Kp, planesA, planesB);
     const int64_t items = (g.a_tiles + g.b_tiles) * g.KT;
     if (items == 0) return cudaSuccess;
-    const unsigned blocks = split_blocks(items, 4 * 4);  // several resident waves: no shared memory to share
+    const unsigned blocks = split_grid(items);
     if (a_vec(A)) split_i16_kernel<2><<<blocks, SPLIT_THREADS, 0, st>>>(g);
     else split_i16_kernel<1><<<blocks, SPLIT_THREADS, 0, st>>>(g);
     return cudaGetLastError();

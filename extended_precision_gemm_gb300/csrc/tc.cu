@@ -507,7 +507,8 @@ cudaError_t launch_split_bf16(const SplitOperand* A, const SplitOperand* B, int6
     g.planesB = planesB;
     const int64_t tasks = g.a_tasks + g.b_tasks;
     if (tasks == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms_tc() * 8));
+    // one task per warp, no grid-stride: blocks in flight write one compact range
+    const unsigned blocks = (unsigned)std::min<int64_t>((tasks + 7) / 8, 0x7FFFFFFF);
     return launch_pdl(split_bf16_kernel, dim3(blocks), dim3(256), 0, st, g);
 }
 
@@ -560,7 +561,7 @@ cudaError_t launch_split_bf16_qd(const double* const* A, int64_t lda, int64_t M,
     g.planesB = planesB;
     const int64_t tasks = g.a_tasks + g.b_tasks;
     if (tasks == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms_tc() * 8));
+    const unsigned blocks = (unsigned)std::min<int64_t>((tasks + 7) / 8, 0x7FFFFFFF);  // one task per warp
     split_bf16_qd_kernel<<<blocks, 256, 0, st>>>(g);
     return cudaGetLastError();
 }

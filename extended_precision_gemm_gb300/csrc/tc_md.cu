@@ -364,9 +364,8 @@ cudaError_t split_md(const double* const* A, int64_t lda, int64_t M, int32_t* e,
     }
     g.planesA = planesA;
     g.planesB = planesB;
-    const int64_t sms = num_sms_tc();
     if (g.a_tasks > 0) {
-        const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((g.a_tasks + 7) / 8, sms * 8));
+        const unsigned blocks = (unsigned)std::min<int64_t>((g.a_tasks + 7) / 8, 0x7FFFFFFF);  // one task per warp
         split_md_rows_kernel<NIN><<<blocks, 256, 0, st>>>(g);
         const cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
@@ -375,7 +374,7 @@ cudaError_t split_md(const double* const* A, int64_t lda, int64_t M, int32_t* e,
         cudaError_t err = cudaFuncSetAttribute(split_md_cols_kernel<NIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                md_cols_smem<NIN>());
         if (err != cudaSuccess) return err;
-        const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(g.b_tasks, sms * 4));
+        const unsigned blocks = (unsigned)std::min<int64_t>(g.b_tasks, 0x7FFFFFFF);  // one task per block
         split_md_cols_kernel<NIN><<<blocks, 256, md_cols_smem<NIN>(), st>>>(g);
         return cudaGetLastError();
     }
