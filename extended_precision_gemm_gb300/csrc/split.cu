@@ -40,126 +40,130 @@ __global__ void init_exponents_kernel(int32_t* e, int64_t M, int32_t* f, int64_t
     if (f != nullptr && i < N) f[i] = value;
 }
 
-// Work split of the exponent grid.  A-items: 8 rows of A (one warp per row)
-// x one k-chunk; B-items: 256 columns of B (one thread per column) x one
-// k-chunk.  Chunks are sized so both operands have about the same number of
-// items of about the same size, and blocks alternate between the two
-// (even block: A-item, odd block: B-item), so neither operand forms a tail.
+// Work split of the exponent grid: one item per block, each thread issuing
+// all its loads (8 x 16 bytes) before it reduces, so a block has 32 KB in
+// flight, and the blocks in flight read one compact range (a grid-stride loop
+// with fewer loads in flight reads at half the DRAM rate on GB300).
+//   A-item: one row x EXP_A_SEG consecutive k (256 threads x 2 k x 8 loads);
+//           block maximum, one atomicMax.
+//   B-item: EXP_B_COLS columns x EXP_B_ROWS k (8 warps x 8 rows; a lane two
+//           columns with 16-byte loads, or one); the 8 warps' maxima are
+//           combined in shared memory, one atomicMax per column.
+// Items are ordered so that neighbouring blocks read neighbouring memory:
+// A by (row, k-segment), B by (k-segment, column group).
+constexpr int EXP_THREADS = 256;
+constexpr int EXP_LOADS = 8;
+constexpr int64_t EXP_A_SEG = (int64_t)EXP_THREADS * 2 * EXP_LOADS;  // 4096 k
+constexpr int EXP_B_ROWS = (EXP_THREADS / 32) * EXP_LOADS;           // 64 k
+
 struct ExpGrid {
-    const double* A_hi; int64_t lda, M, a_kchunk, a_ksplit, a_items;
-    const double* B_hi; int64_t ldb, N, b_kchunk, b_ksplit, b_items;
+    const double* A_hi; int64_t lda, M, a_segs, a_items;
+    const double* B_hi; int64_t ldb, N, b_groups, b_items;
     int64_t K;
     int32_t* e; int32_t* f;
-    bool b_vec;  // B_hi 16-byte aligned and ldb even: two columns per thread, 16-byte loads
+    bool b_vec;  // B_hi 16-byte aligned and ldb even: two columns per lane, 16-byte loads
 };
 
-// A-item bid: the row maxima of 8 rows (one per warp) over one k-chunk.
 template <int VEC>
-__device__ __forceinline__ void exponents_a_item(const ExpGrid& g, int64_t bid) {
-    const int lane = threadIdx.x & 31;
-    const int64_t row = (bid / g.a_ksplit) * 8 + (threadIdx.x >> 5);
-    if (row >= g.M) return;
-    const int64_t k0 = (bid % g.a_ksplit) * g.a_kchunk;
-    const int64_t k1 = min(g.K, k0 + g.a_kchunk);
-    // rows are read in [row * lda, row * lda + K): within the span of A
-    if (!in_bounds(row * g.lda + k1 - 1, (g.M - 1) * g.lda + g.K, kSiteExpLoadA)) return;
+__device__ __forceinline__ void exponents_a_item(const ExpGrid& g, int64_t item, uint64_t* red) {
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int64_t row = item / g.a_segs;
+    const int64_t k0 = (item % g.a_segs) * EXP_A_SEG;
+    const int64_t k1 = min(g.K, k0 + EXP_A_SEG);
+    // the row is read in [row * lda + k0, row * lda + k1): within the span of A
+    const bool live = in_bounds(row * g.lda + k1 - 1, (g.M - 1) * g.lda + g.K, kSiteExpLoadA);
     const double* p = g.A_hi + row * g.lda;
     uint64_t m = 0;
-    if (VEC == 2) {
-        // four independent 128-bit loads in flight per lane
-        uint64_t m1 = 0, m2 = 0, m3 = 0;
-        int64_t k = k0 + 2 * lane;
-        for (; k + 193 < k1; k += 256) {
-            const double2 v0 = __ldg(reinterpret_cast<const double2*>(p + k));
-            const double2 v1 = __ldg(reinterpret_cast<const double2*>(p + k + 64));
-            const double2 v2 = __ldg(reinterpret_cast<const double2*>(p + k + 128));
-            const double2 v3 = __ldg(reinterpret_cast<const double2*>(p + k + 192));
-            m = max(m, max(abs_bits(v0.x), abs_bits(v0.y)));
-            m1 = max(m1, max(abs_bits(v1.x), abs_bits(v1.y)));
-            m2 = max(m2, max(abs_bits(v2.x), abs_bits(v2.y)));
-            m3 = max(m3, max(abs_bits(v3.x), abs_bits(v3.y)));
-        }
-        for (; k < k1; k += 64) {
-            if (k + 1 < k1) {
-                double2 v = __ldg(reinterpret_cast<const double2*>(p + k));
-                m = max(m, max(abs_bits(v.x), abs_bits(v.y)));
-            } else {
-                m = max(m, abs_bits(__ldg(p + k)));
+    if (live) {
+        if (VEC == 2) {
+            double2 v[EXP_LOADS];
+#pragma unroll
+            for (int j = 0; j < EXP_LOADS; ++j) {
+                const int64_t k = k0 + 2 * t + 2 * EXP_THREADS * j;
+                v[j] = make_double2(0.0, 0.0);
+                if (k + 1 < k1) v[j] = __ldg(reinterpret_cast<const double2*>(p + k));
+                else if (k < k1) v[j].x = __ldg(p + k);
             }
+#pragma unroll
+            for (int j = 0; j < EXP_LOADS; ++j) m = max(m, max(abs_bits(v[j].x), abs_bits(v[j].y)));
+        } else {
+            double v[2 * EXP_LOADS];
+#pragma unroll
+            for (int j = 0; j < 2 * EXP_LOADS; ++j) {
+                const int64_t k = k0 + t + EXP_THREADS * j;
+                v[j] = k < k1 ? __ldg(p + k) : 0.0;
+            }
+#pragma unroll
+            for (int j = 0; j < 2 * EXP_LOADS; ++j) m = max(m, abs_bits(v[j]));
         }
-        m = max(max(m, m1), max(m2, m3));
-    } else {
-        for (int64_t k = k0 + lane; k < k1; k += 32) m = max(m, abs_bits(__ldg(p + k)));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         m = max(m, (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)m, off));
-    if (lane == 0 && m != 0) atomicMax(&g.e[row], exponent_from_abs_bits(m));
-}
-
-// B-item b: the column maxima of 256 columns (one per thread; 512 with 16-byte
-// loads of two columns per thread) over one k-chunk.
-__device__ __forceinline__ void exponents_b_item(const ExpGrid& g, int64_t b) {
-    const int per = g.b_vec ? 2 : 1;
-    const int64_t col = (b / g.b_ksplit) * 256 * per + (int64_t)threadIdx.x * per;
-    if (col >= g.N) return;
-    const int64_t k0 = (b % g.b_ksplit) * g.b_kchunk;
-    const int64_t k1 = min(g.K, k0 + g.b_kchunk);
-    const bool pair = g.b_vec && col + 1 < g.N;
-    if (!in_bounds((k1 - 1) * g.ldb + col + (pair ? 1 : 0), (g.K - 1) * g.ldb + g.N, kSiteExpLoadB)) return;
-    const double* p = g.B_hi + col;
-    const int64_t ldb = g.ldb;
-    uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;  // column col
-    uint64_t n0 = 0, n1 = 0, n2 = 0, n3 = 0;  // column col + 1
-    int64_t k = k0;
-    if (pair) {
-        for (; k + 3 < k1; k += 4) {  // four 16-byte loads in flight per thread
-            const double2 x0 = __ldg(reinterpret_cast<const double2*>(p + (k + 0) * ldb));
-            const double2 x1 = __ldg(reinterpret_cast<const double2*>(p + (k + 1) * ldb));
-            const double2 x2 = __ldg(reinterpret_cast<const double2*>(p + (k + 2) * ldb));
-            const double2 x3 = __ldg(reinterpret_cast<const double2*>(p + (k + 3) * ldb));
-            m0 = max(m0, abs_bits(x0.x)); n0 = max(n0, abs_bits(x0.y));
-            m1 = max(m1, abs_bits(x1.x)); n1 = max(n1, abs_bits(x1.y));
-            m2 = max(m2, abs_bits(x2.x)); n2 = max(n2, abs_bits(x2.y));
-            m3 = max(m3, abs_bits(x3.x)); n3 = max(n3, abs_bits(x3.y));
-        }
-        for (; k < k1; ++k) {
-            const double2 x = __ldg(reinterpret_cast<const double2*>(p + k * ldb));
-            m0 = max(m0, abs_bits(x.x));
-            n0 = max(n0, abs_bits(x.y));
-        }
-        const uint64_t n = max(max(n0, n1), max(n2, n3));
-        if (n != 0) atomicMax(&g.f[col + 1], exponent_from_abs_bits(n));
-    } else {
-        for (; k + 7 < k1; k += 8) {  // eight loads in flight per thread
-            const double x0 = __ldg(p + (k + 0) * ldb), x1 = __ldg(p + (k + 1) * ldb);
-            const double x2 = __ldg(p + (k + 2) * ldb), x3 = __ldg(p + (k + 3) * ldb);
-            const double x4 = __ldg(p + (k + 4) * ldb), x5 = __ldg(p + (k + 5) * ldb);
-            const double x6 = __ldg(p + (k + 6) * ldb), x7 = __ldg(p + (k + 7) * ldb);
-            m0 = max(m0, max(abs_bits(x0), abs_bits(x4)));
-            m1 = max(m1, max(abs_bits(x1), abs_bits(x5)));
-            m2 = max(m2, max(abs_bits(x2), abs_bits(x6)));
-            m3 = max(m3, max(abs_bits(x3), abs_bits(x7)));
-        }
-        for (; k < k1; ++k) m0 = max(m0, abs_bits(__ldg(p + k * ldb)));
+    if (lane == 0) red[w] = m;
+    __syncthreads();
+    if (t == 0) {
+        uint64_t mm = red[0];
+#pragma unroll
+        for (int j = 1; j < EXP_THREADS / 32; ++j) mm = max(mm, red[j]);
+        if (mm != 0) atomicMax(&g.e[row], exponent_from_abs_bits(mm));
     }
-    const uint64_t m = max(max(m0, m1), max(m2, m3));
-    if (m != 0) atomicMax(&g.f[col], exponent_from_abs_bits(m));
 }
 
-// Blocks alternate between the operands (even block: A-item, odd block:
-// B-item), so that neither operand forms a tail.
+__device__ __forceinline__ void exponents_b_item(const ExpGrid& g, int64_t item, uint64_t* red) {
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int per = g.b_vec ? 2 : 1;  // columns per lane
+    const int64_t col = (item % g.b_groups) * 32 * per + (int64_t)lane * per;
+    const int64_t k0 = (item / g.b_groups) * EXP_B_ROWS + (int64_t)w * EXP_LOADS;
+    const int64_t k1 = min(g.K, k0 + EXP_LOADS);
+    uint64_t m0 = 0, m1 = 0;
+    if (col < g.N && k0 < g.K) {
+        const bool pair = g.b_vec && col + 1 < g.N;
+        if (in_bounds((k1 - 1) * g.ldb + col + (pair ? 1 : 0), (g.K - 1) * g.ldb + g.N, kSiteExpLoadB)) {
+            const double* p = g.B_hi + col;
+            if (pair) {
+                double2 v[EXP_LOADS];
+#pragma unroll
+                for (int j = 0; j < EXP_LOADS; ++j)
+                    v[j] = k0 + j < k1 ? __ldg(reinterpret_cast<const double2*>(p + (k0 + j) * g.ldb))
+                                       : make_double2(0.0, 0.0);
+#pragma unroll
+                for (int j = 0; j < EXP_LOADS; ++j) {
+                    m0 = max(m0, abs_bits(v[j].x));
+                    m1 = max(m1, abs_bits(v[j].y));
+                }
+            } else {
+                double v[EXP_LOADS];
+#pragma unroll
+                for (int j = 0; j < EXP_LOADS; ++j) v[j] = k0 + j < k1 ? __ldg(p + (k0 + j) * g.ldb) : 0.0;
+#pragma unroll
+                for (int j = 0; j < EXP_LOADS; ++j) m0 = max(m0, abs_bits(v[j]));
+            }
+        }
+    }
+    // red: [warp][64 columns]
+    red[w * 64 + lane * per] = m0;
+    if (per == 2) red[w * 64 + lane * 2 + 1] = m1;
+    __syncthreads();
+    if (t < 32 * per) {
+        uint64_t mm = red[t];
+#pragma unroll
+        for (int j = 1; j < EXP_THREADS / 32; ++j) mm = max(mm, red[j * 64 + t]);
+        const int64_t c = (item % g.b_groups) * 32 * per + t;
+        if (mm != 0 && c < g.N) atomicMax(&g.f[c], exponent_from_abs_bits(mm));
+    }
+}
+
 template <int VEC>
-__global__ void __launch_bounds__(256) exponents_kernel(ExpGrid g) {
+__global__ void __launch_bounds__(EXP_THREADS) exponents_kernel(ExpGrid g) {
     pdl_wait();
     pdl_launch_dependents();
-    const bool both = g.a_items > 0 && g.b_items > 0;
-    const bool is_a = both ? (blockIdx.x & 1) == 0 : g.a_items > 0;
-    const int64_t bid = both ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
-    if (is_a) {
-        if (bid < g.a_items) exponents_a_item<VEC>(g, bid);
-    } else if (bid < g.b_items) {
-        exponents_b_item(g, bid);
+    __shared__ uint64_t red[(EXP_THREADS / 32) * 64];
+    const int64_t items = g.a_items + g.b_items;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+        if (item < g.a_items) exponents_a_item<VEC>(g, item, red);
+        else exponents_b_item(g, item - g.a_items, red);
+        __syncthreads();  // red is reused by the next item
     }
 }
 
@@ -394,31 +398,23 @@ cudaError_t launch_exponents(const SplitOperand* A, const SplitOperand* B, int64
     if (K == 0) return cudaSuccess;
     ExpGrid g{};
     g.K = K;
-    g.b_vec = B && (uintptr_t)B->hi % 16 == 0 && B->ld % 2 == 0;
-    const int64_t a_rows = A ? (A->rows + 7) / 8 : 0;
-    const int64_t b_cols = B ? (B->rows + (g.b_vec ? 511 : 255)) / (g.b_vec ? 512 : 256) : 0;
-    if (a_rows + b_cols == 0) return cudaSuccess;
-    // About 16 blocks per SM in total, at least 64 (A) / 16 (B) k per chunk.
-    const int64_t want = std::max<int64_t>(1, 16LL * num_sms() / ((A ? 1 : 0) + (B ? 1 : 0)));
-    if (A) {
-        int64_t ks = std::max<int64_t>(1, std::min<int64_t>((want + a_rows - 1) / a_rows, (K + 63) / 64));
-        g.a_kchunk = round_up((K + ks - 1) / ks, 64);
-        g.a_ksplit = (K + g.a_kchunk - 1) / g.a_kchunk;
+    if (A && A->rows > 0) {
         g.A_hi = A->hi; g.lda = A->ld; g.M = A->rows; g.e = A->exp;
-        g.a_items = a_rows * g.a_ksplit;
+        g.a_segs = (K + EXP_A_SEG - 1) / EXP_A_SEG;
+        g.a_items = A->rows * g.a_segs;
     }
-    if (B) {
-        int64_t ks = std::max<int64_t>(1, std::min<int64_t>((want + b_cols - 1) / b_cols, (K + 15) / 16));
-        g.b_kchunk = (K + ks - 1) / ks;
-        g.b_ksplit = (K + g.b_kchunk - 1) / g.b_kchunk;
+    if (B && B->rows > 0) {
+        g.b_vec = (uintptr_t)B->hi % 16 == 0 && B->ld % 2 == 0;
         g.B_hi = B->hi; g.ldb = B->ld; g.N = B->rows; g.f = B->exp;
-        g.b_items = b_cols * g.b_ksplit;
+        g.b_groups = (B->rows + (g.b_vec ? 63 : 31)) / (g.b_vec ? 64 : 32);
+        g.b_items = g.b_groups * ((K + EXP_B_ROWS - 1) / EXP_B_ROWS);
     }
-    const int64_t blocks = (g.a_items > 0 && g.b_items > 0) ? 2 * std::max(g.a_items, g.b_items)
-                                                            : g.a_items + g.b_items;
+    const int64_t items = g.a_items + g.b_items;
+    if (items == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::min<int64_t>(items, 0x7FFFFFFF);
     const bool vec = !A || (((uintptr_t)A->hi % 16 == 0) && (A->ld % 2 == 0));
-    return vec ? launch_pdl(exponents_kernel<2>, dim3((unsigned)blocks), dim3(256), 0, st, g)
-               : launch_pdl(exponents_kernel<1>, dim3((unsigned)blocks), dim3(256), 0, st, g);
+    return vec ? launch_pdl(exponents_kernel<2>, dim3(blocks), dim3(EXP_THREADS), 0, st, g)
+               : launch_pdl(exponents_kernel<1>, dim3(blocks), dim3(EXP_THREADS), 0, st, g);
 }
 
 static SplitGrid make_split_grid(const SplitOperand* A, const SplitOperand* B, int64_t K, int64_t Kp,
