@@ -70,7 +70,7 @@ FP64_PER_CLK_SM = 2    # FP64 (DFMA/DADD/DMUL) instructions per clock per SM (GB
 IMAD_PER_CLK_SM = 64   # 32-bit integer multiply-add (also 32x32->64 wide) per clock per SM
 SM_COUNT = 152
 SM_MAX_GHZ = 2.07
-ONLY_VARIANTS = ("dd", "dd_fused", "dd_int", "dd_tc", "qd_tc", "od_tc", "hd_tc")
+ONLY_VARIANTS = ("dd", "dd_fused", "dd_int", "dd_tc", "qd", "qd_tc", "od_tc", "hd_tc")
 CSRC = "extended_precision_gemm_gb300/csrc/"
 # DRAM bytes per launch of a kernel, from a committed ncu summary; valid while
 # the sources the kernel is compiled from hash to the recorded value
@@ -416,6 +416,12 @@ def run_only(args, w):
         else:
             ws = torch.empty(ddg.tc_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
             run = lambda: ddg.dd_gemm_tc(A_hi, A_lo, B_hi, B_lo, C_hi, C_lo, ws)
+    elif v == "qd":  # quad double on the integer pipe (int16 parts, int64 sums)
+        A, B = workloads.make_md(M, N, K, w.dist, w.seed, 4)
+        tA, tB = [to(a) for a in A], [to(b) for b in B]
+        C = [torch.empty((M, N), dtype=torch.float64, device=dev) for _ in range(4)]
+        ws = torch.empty(ddg.qd_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+        run = lambda: ddg.qd_gemm(tA, tB, C, workspace=ws)
     else:
         parts = {"qd_tc": 4, "od_tc": 8, "hd_tc": 16}[v]
         A, B = workloads.make_md(M, N, K, w.dist, w.seed, parts)
