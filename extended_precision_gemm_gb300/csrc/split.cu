@@ -440,7 +440,7 @@ static bool a_vec(const SplitOperand* A) {
     return !A || (((uintptr_t)A->hi % 16 == 0) && ((uintptr_t)A->lo % 16 == 0) && (A->ld % 2 == 0));
 }
 
-// FP64 split: one block per item.  The block scheduler hands out the items in
+// Split grids: one block per item.  The block scheduler hands out the items in
 // order as blocks finish, so the blocks in flight write one compact range of
 // the planes; a persistent grid drifts apart and spreads its writes over
 // many DRAM pages (on GB300 a grid-stride loop of 256-bit stores reaches

@@ -148,3 +148,42 @@ def test_output_blocks_equal_full_product(gemm):
             G_hi, G_lo = fn(tA_hi[r0:r1], tA_lo[r0:r1], tB_hi[:, c0:c1], tB_lo[:, c0:c1])
             assert np.array_equal(_bits(host(G_hi)), _bits(F_hi[r0:r1, c0:c1]))
             assert np.array_equal(_bits(host(G_lo)), _bits(F_lo[r0:r1, c0:c1]))
+
+
+def _window(X, offset):
+    """X as a column window of a wider device matrix starting `offset`
+    elements in (offset 1: rows off the 16-byte grid, odd leading dimension)."""
+    import torch
+    r, c = X.shape
+    big = torch.full((r, c + offset + 1), 7.0, dtype=torch.float64, device="cuda")
+    big[:, offset:offset + c] = torch.from_numpy(np.ascontiguousarray(X)).cuda()
+    return big[:, offset:offset + c]
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 65, 4095), (4, 64, 4097), (5, 130, 8200), (6, 33, 63), (7, 129, 65),
+                                   (2, 3, 1)])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_exponents_across_work_items(M, N, K, offset):
+    """The exponent pass reduces a row of A in segments of 4096 k and a column
+    of B in segments of 64 k (maxima combined across blocks), two columns per
+    lane when B is 16-byte aligned with an even leading dimension, one
+    otherwise.  Each row's / column's largest element sits at a segment edge
+    (first or last k of a segment, or K - 1); one row and one column are all
+    zero (the sentinel); one row holds only subnormals."""
+    rng = np.random.default_rng(1000 * M + K + offset)
+    A_hi = rng.uniform(-1, 1, (M, K)) * 2.0 ** rng.integers(-40, -20, (M, K)).astype(np.float64)
+    B_hi = rng.uniform(-1, 1, (K, N)) * 2.0 ** rng.integers(-40, -20, (K, N)).astype(np.float64)
+    edges_a = sorted({0, min(4095, K - 1), min(4096, K - 1), K - 1})
+    edges_b = sorted({0, min(63, K - 1), min(64, K - 1), K - 1})
+    for i in range(M):
+        A_hi[i, edges_a[i % len(edges_a)]] = (-1) ** i * 2.0 ** (i % 5) * 1.5
+    for j in range(N):
+        B_hi[edges_b[j % len(edges_b)], j] = (-1) ** j * 2.0 ** (j % 7) * 1.25
+    A_hi[M - 1] = 0.0
+    B_hi[:, N - 1] = 0.0
+    if M > 2:
+        A_hi[1] = rng.uniform(-1, 1, K) * 2.0**-1060  # subnormal row
+    e, f = ddg.exponents(_window(A_hi, offset), _window(B_hi, offset))
+    assert np.array_equal(host(e), _raw_exponents_ref(A_hi, 1))
+    assert np.array_equal(host(f), _raw_exponents_ref(B_hi, 0))
+    assert ddg.wait_timeouts() == 0
