@@ -4,7 +4,8 @@ afford: a block of sampled rows x columns bit for bit against the oracle's
 model of the method (row / column exponents depend only on that row /
 column, so the block is the model's product of the sampled rows and
 columns), and whole sampled rows against the exact product (normwise bound
-1e-26 on those rows).  Plus the maximum inner dimension K = 2^24 with the
+1e-26 on those rows), for the FP64 tensor-pipe path and for the bf16
+tensor-core variant.  Plus the maximum inner dimension K = 2^24 with the
 largest digits, whose part sums sit just below 2^53 and have a closed form."""
 from fractions import Fraction
 
@@ -45,6 +46,38 @@ def test_full_size_workload(idx):
     err = normwise(G_hi[:2], G_lo[:2], R_hi, R_lo, A_hi[r2], A_lo[r2], B_hi, B_lo)
     assert err <= 1e-26, err
 
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_full_size_workload_bf16_variant(idx):
+    """The bf16 tensor-core variant (dd_gemm_tc) on the full-size workloads, in
+    the layout and k-split bench.py times: a sampled block bit for bit against
+    the oracle's model of that variant (13 balanced 8-bit parts, exact sums
+    rounded once; the k-splits do not change an exact sum), and two whole
+    rows against the exact product."""
+    import torch
+    from oracle import slices_bf16
+    w = workloads.WORKLOADS[idx]
+    A_hi, A_lo, B_hi, B_lo = workloads.make_workload(idx)
+    t = [dev(x) for x in (A_hi, A_lo, B_hi, B_lo)]
+    ws = torch.empty(ddg.tc_workspace_size(w.M, w.N, w.K), dtype=torch.uint8, device="cuda")
+    C_hi = torch.empty((w.M, w.N), dtype=torch.float64, device="cuda")
+    C_lo = torch.empty_like(C_hi)
+    ddg.dd_gemm_tc(*t, C_hi, C_lo, ws)
+    torch.cuda.synchronize()
+    assert ddg.wait_timeouts() == 0
+    rng = np.random.default_rng(200 + idx)
+    rows = np.unique(np.concatenate([[0, w.M // 2, w.M - 1], rng.integers(0, w.M, 3)]))
+    cols = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, 14)]))
+    G_hi = host(C_hi[torch.from_numpy(rows).cuda()])
+    G_lo = host(C_lo[torch.from_numpy(rows).cuda()])
+    M_hi, M_lo, *_ = slices_bf16.sliced_dd_gemm(A_hi[rows], A_lo[rows], B_hi[:, cols], B_lo[:, cols])
+    assert np.array_equal(G_hi[:, cols].view(np.int64), M_hi.view(np.int64))
+    assert np.array_equal(G_lo[:, cols].view(np.int64), M_lo.view(np.int64))
+    r2 = rows[:2]
+    R_hi, R_lo = oracle.exact_dd_gemm(A_hi, A_lo, B_hi, B_lo, rows=r2)
+    err = normwise(G_hi[:2], G_lo[:2], R_hi, R_lo, A_hi[r2], A_lo[r2], B_hi, B_lo)
+    assert err <= 1e-26, err
 
 def test_maximum_k_closed_form():
     import torch
