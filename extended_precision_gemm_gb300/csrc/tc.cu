@@ -89,7 +89,7 @@ struct TcSplitGrid {
 // Each lane writes one 16-byte chunk of each part, so a warp writes whole
 // 128-byte part rows: 512 contiguous bytes per part.  Rows / k beyond the
 // matrix are written as 0.
-__global__ void __launch_bounds__(256, 3) split_bf16_kernel(TcSplitGrid g) {
+__global__ void __launch_bounds__(256, 4) split_bf16_kernel(TcSplitGrid g) {
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -275,7 +275,7 @@ __device__ __forceinline__ void recombine_one(const long long (&v)[TS], bool one
 // V consecutive outputs of a row per thread (V = 4: 16-byte loads of every
 // part plane; vec_store: 16-byte stores of C when aligned).
 template <int V>
-__global__ void __launch_bounds__(256) recombine_tc_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
+__global__ void __launch_bounds__(256, 3) recombine_tc_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
                                                            int64_t Np, const int32_t* __restrict__ e,
                                                            const int32_t* __restrict__ f, int64_t M, int64_t N,
                                                            double* __restrict__ C_hi, double* __restrict__ C_lo,
@@ -388,7 +388,7 @@ __device__ __forceinline__ uint32_t qd_part(const uint32_t (&y)[8], int s) {
 // columns of B, x 64 k (lane = row or column (lane/8), 8 consecutive k
 // (lane%8)).  Each lane forms Y for its 8 elements, then writes one 16-byte
 // chunk of each of the 27 part rows (a warp writes whole 128-byte rows).
-__global__ void __launch_bounds__(256) split_bf16_qd_kernel(TcQdSplitGrid g) {
+__global__ void __launch_bounds__(256, 3) split_bf16_qd_kernel(TcQdSplitGrid g) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * 8;
