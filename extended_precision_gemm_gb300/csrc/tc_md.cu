@@ -299,7 +299,7 @@ struct PlanePtrs {
 // loads of a split are independent), then one carry pass; rounded once into
 // NIN doubles.
 template <int NIN>
-__global__ void __launch_bounds__(256, 3) recombine_tc_md_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
+__global__ void __launch_bounds__(256) recombine_tc_md_kernel(const int32_t* __restrict__ P, int splits, int64_t Mp,
                                                               int64_t Np, const int32_t* __restrict__ e,
                                                               const int32_t* __restrict__ f, int64_t M, int64_t N,
                                                               PlanePtrs C, int64_t ldc) {
