@@ -620,10 +620,13 @@ def run_ours(args, w):
     h_C_lo = torch.empty((M, N), dtype=torch.float64).pin_memory()
     ddg.dd_gemm_host(*pinned, h_C_hi, h_C_lo, stream=stream)
     barrier(dist)
+    e2e_clocks = ClockSampler(local)
+    e2e_clocks.start()
     t0 = time.perf_counter()
     for _ in range(VSTEPS):
         ddg.dd_gemm_host(*pinned, h_C_hi, h_C_lo, stream=stream)
     t_e2e = time.perf_counter() - t0
+    e2e_clock_info = e2e_clocks.stop()
     e2e_units, t_e2e = aggregate(dist, t_e2e, VSTEPS * w.dd_flops, dev)
     same = bool(torch.equal(h_C_hi, C_hi.cpu()) and torch.equal(h_C_lo, C_lo.cpu()))
 
@@ -815,7 +818,7 @@ def run_ours(args, w):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_units / t_e2e / 1e9, "unit": UNIT, "steps": VSTEPS,
                 "h2d_bytes_per_step": 16 * (M * K + K * N), "d2h_bytes_per_step": 16 * M * N,
-                "api": "dd_gemm_host", "matches_device_result": same},
+                "api": "dd_gemm_host", "matches_device_result": same, "clocks": e2e_clock_info},
         "accuracy": {"normwise_vs_exact_oracle": normwise, "rows_checked": len(rows), "bound": 1e-26},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clock_info,
