@@ -667,6 +667,8 @@ def run_ours(args, w):
     T_hi = torch.empty_like(C_hi)
     T_lo = torch.empty_like(C_lo)
     TC_STEPS = max(args.steps, 3)
+    tc_clocks = ClockSampler(local)
+    tc_clocks.start()
     t_t = T.steps(lambda: ddg.dd_gemm_tc(dA_hi, dA_lo, dB_hi, dB_lo, T_hi, T_lo, workspace=ws_t, stream=stream),
                   TC_STEPS, args.warmup)
     units_t, t_t = aggregate(dist, t_t, TC_STEPS * w.dd_flops, dev)
@@ -678,6 +680,7 @@ def run_ours(args, w):
         [lambda: ddg.split_bf16(dA_hi, dA_lo, dB_hi, dB_lo, pA8, e8, pB8, f8, stream=stream),
          lambda: ddg.slice_gemm_tc(M, N, K, pA8, pB8, splits_t, Pt, stream=stream),
          lambda: ddg.recombine_tc(M, N, Pt, e8, f8, splits_t, T_hi, T_lo, stream=stream)], TC_STEPS))
+    tc_clock_info = tc_clocks.stop()
     del pA8, pB8, Pt
     # end to end with host buffers
     h_T_hi = torch.empty((M, N), dtype=torch.float64).pin_memory()
@@ -856,11 +859,13 @@ def run_ours(args, w):
             "roofline": {"bound": "tensor", "kernel": "slice_gemm_tc_kernel (tcgen05.mma kind::f16, bf16)",
                          "achieved": tc_tf, "peak": bf16_tf, "unit": "TFLOP/s", "frac": tc_tf / bf16_tf,
                          "peak_source": f"{peak_src} cuBLAS bf16 burst", "flops_per_launch": tc_flops,
+                         "sustained_peak": bf16_sus, "frac_of_sustained": tc_tf / bf16_sus,
                          "ms_per_launch": 1e3 * tt_gemm, "traffic": traffic_tc,
                          "traffic_over_algorithmic": traffic_tc / alg_bytes_tc if traffic_tc else None,
                          "algorithmic_bytes_per_launch": alg_bytes_tc},
             "ms_split_bf16": 1e3 * tt_split, "ms_recombine": 1e3 * tt_recomb,
             "launches_per_step": 5,
+            "clocks": tc_clock_info,  # sampled over the timed steps and the per-kernel passes
             "e2e": {"value": te2e_units / t_te2e / 1e9, "unit": UNIT, "steps": TC_STEPS,
                     "h2d_bytes_per_step": 16 * (M * K + K * N), "d2h_bytes_per_step": 16 * M * N,
                     "api": "dd_gemm_tc_host", "matches_device_result": same_t},
